@@ -1,0 +1,214 @@
+/*
+ * libmla -- Multi-head Latent Attention (DeepSeek-V2 style) decode over a
+ * paged latent KV cache, in the matrix-absorbed form, for GB300 (sm_103a).
+ *
+ * Sources for the operations (web pages; section headings as printed):
+ *   [MI17]  "mini-infer-17: MLA Attention -- from KV-cache compression to
+ *           matrix absorption" (smarter.xin)
+ *   [VLB07] "07. MLA / Mamba / MoE in vLLM source" (vLLM learning book)
+ *
+ * Shapes and names. H = num_heads; Dc = kv_lora_rank = 512; Dr =
+ * qk_rope_head_dim = 64; Dn = qk_nope_head_dim = 128; Dv = v_head_dim = 128.
+ * A cache row is [c_hat (Dc) || k_hat (Dr)] = 576 values.
+ *
+ * Conventions shared by every call.
+ *  - Every pointer is a DEVICE pointer unless stated, 16-byte aligned, and
+ *    owned by the caller. The library never allocates or frees memory.
+ *  - Every array is dense, row-major, in the layout stated.
+ *  - "dtype" tensors are float32 (MLA_F32) or bfloat16 (MLA_BF16) as set in
+ *    mla_config.dtype. Arithmetic accumulates in fp32 in every kernel.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream). Every call
+ *    only enqueues work: it returns before the GPU runs it.
+ *  - Errors the host can see (bad sizes, null or misaligned pointers, an
+ *    unsupported configuration, a small workspace) return at once and
+ *    enqueue nothing. A failed launch returns MLA_ERR_CUDA. Errors only the
+ *    GPU can see (an out-of-range block-table entry or slot, a query longer
+ *    than its sequence, a wait that ran out) set bits in a device status word
+ *    read by mla_get_device_status(); the offending row or token is skipped
+ *    (its output is zero) and no memory outside the caller's buffers is
+ *    touched.
+ *  - seq_lens[b] counts every token of sequence b in the cache, including the
+ *    ones written in this step. Query row j of sequence b (q_len_b rows,
+ *    q_len_b = query_start_loc[b+1] - query_start_loc[b]) sits at position
+ *    seq_lens[b] - q_len_b + j and attends kv positions 0..that position
+ *    (causal; [MI17] pitfall 2). A decode row (q_len 1) sees every token.
+ */
+#ifndef LIBMLA_MLA_H_
+#define LIBMLA_MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARGUMENT = 1,    /* null/misaligned pointer, bad size        */
+  MLA_ERR_UNSUPPORTED = 2,         /* configuration outside the supported set  */
+  MLA_ERR_WORKSPACE_TOO_SMALL = 3, /* ws_bytes < mla_decode_workspace_size()   */
+  MLA_ERR_CUDA = 4,                /* a CUDA runtime call or launch failed     */
+  MLA_ERR_TIMEOUT = 5,             /* device: a bounded wait ran out           */
+  MLA_ERR_BAD_BLOCK = 6,           /* device: block-table entry out of range   */
+  MLA_ERR_BAD_SEQ = 7,             /* device: q_len > seq_len, or seq_len
+                                      beyond max_blocks_per_seq * block_size   */
+  MLA_ERR_BAD_SLOT = 8             /* device: slot_mapping entry out of range  */
+} mla_status;
+
+/* Bits of the device status word (a uint32_t in device memory). */
+#define MLA_DEV_TIMEOUT   (1u << 0)
+#define MLA_DEV_BAD_BLOCK (1u << 1)
+#define MLA_DEV_BAD_SEQ   (1u << 2)
+#define MLA_DEV_BAD_SLOT  (1u << 3)
+
+typedef enum { MLA_F32 = 0, MLA_BF16 = 1 } mla_dtype;
+
+/*
+ * Model and launch configuration. Supported: kv_lora_rank 512,
+ * qk_rope_head_dim 64, qk_nope_head_dim 128, v_head_dim 128 (DeepSeek-V2-Lite,
+ * [MI17] "MLA 的数学结构"); num_heads in {16, 32, 64, 128}; block_size in
+ * {16, 32, 64}; dtype MLA_F32 or MLA_BF16. num_ctas = 0 runs the decode
+ * kernel with one CTA per SM; a positive value fixes the CTA count (the
+ * split-KV partition), e.g. to test that results do not depend on it.
+ * mla_default_config() fills the DeepSeek-V2-Lite values.
+ */
+typedef struct {
+  int32_t num_heads;
+  int32_t kv_lora_rank;
+  int32_t qk_rope_head_dim;
+  int32_t qk_nope_head_dim;
+  int32_t v_head_dim;
+  int32_t block_size;
+  float softmax_scale;   /* multiplies q_abs . row; 1/sqrt(Dn + Dr) usually  */
+  float rms_eps;         /* kv_a_layernorm epsilon                            */
+  float rope_base;       /* RoPE base (10000 for DeepSeek-V2-Lite)            */
+  int32_t dtype;         /* mla_dtype                                         */
+  int32_t num_ctas;      /* 0 = one per SM                                    */
+} mla_config;
+
+void mla_default_config(mla_config* cfg, int32_t num_heads, int32_t block_size,
+                        mla_dtype dtype);
+
+/*
+ * mla_cache_write -- kv_a_layernorm + decoupled RoPE + slot scatter.
+ * [VLB07] 2.2 (forward: write c_kv to the KV cache by slot_mapping) and 2.3
+ * (MLA cache shape (n_blocks, block, 1, latent_d + rope_d)); [MI17] "版本 1"
+ * (kv_a_layernorm before kv_b_proj), pitfall 3, and "MLA 的数学结构"
+ * (K_pe = x W_kr + RoPE, one k_pe shared by all heads).
+ *
+ * For each token t < num_tokens with slot s = slot_mapping[t] >= 0:
+ *   cache[s / block_size][s % block_size][0:512]   = RMSNorm(c_kv[t]) * rms_weight
+ *   cache[s / block_size][s % block_size][512:576] = RoPE(k_pe[t], positions[t])
+ * RMSNorm(x) = x / sqrt(mean(x^2) + rms_eps); RoPE rotates pairs
+ * (x_i, x_{i+32}) by positions[t] * rope_base^(-2i/64) (rotate-half).
+ * Statistics and rotation in fp32 (angles in fp64), one rounding to dtype.
+ *   c_kv        [num_tokens, 512] dtype      k_pe [num_tokens, 64] dtype
+ *   positions   [num_tokens] int32 (>= 0)    slot_mapping [num_tokens] int64
+ *   rms_weight  [512] dtype                  cache [num_blocks, block_size, 576] dtype
+ *   dev_status  uint32 device word or NULL; slots >= num_blocks*block_size
+ *               set MLA_DEV_BAD_SLOT and are skipped. Negative slots mean
+ *               "padding token" and are skipped silently.
+ * Bytes of the cache other than the addressed rows are never written.
+ */
+mla_status mla_cache_write(const mla_config* cfg, const void* c_kv, const void* k_pe,
+                           const int32_t* positions, const int64_t* slot_mapping,
+                           int64_t num_tokens, const void* rms_weight, void* cache,
+                           int64_t num_blocks, uint32_t* dev_status, void* stream);
+
+/*
+ * mla_absorb_q -- absorb W_uk into the query and rotate its rope part.
+ * [MI17] "版本 3: MLAAttentionAbsorbed" (_build_absorbed: W_uk per head as
+ * [Dc, Dn]); the DeepSeek-V2 report's absorption it cites.
+ *   q_abs[n,h,0:512]   = sum_d W_uk[h][c][d] * q_nope[n,h,d]   (c < 512)
+ *   q_abs[n,h,512:576] = RoPE(q_pe[n,h], q_positions[n])
+ *   q_nope [num_q, H, 128] dtype   q_pe [num_q, H, 64] dtype
+ *   q_positions [num_q] int32      W_uk [H, 512, 128] dtype
+ *   q_abs  [num_q, H, 576] dtype (output)
+ */
+mla_status mla_absorb_q(const mla_config* cfg, const void* q_nope, const void* q_pe,
+                        const int32_t* q_positions, const void* W_uk, void* q_abs,
+                        int64_t num_q, void* stream);
+
+/*
+ * Workspace for mla_decode_paged / mla_combine: a device buffer of at least
+ * mla_decode_workspace_size() bytes (it depends on the current device's SM
+ * count when cfg->num_ctas is 0). Its first 4 bytes are the device status
+ * word; call mla_workspace_init() once after allocating it.
+ */
+size_t mla_decode_workspace_size(const mla_config* cfg, int64_t num_q, int32_t batch);
+mla_status mla_workspace_init(void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * mla_decode_paged -- split-KV attention of absorbed queries over the paged
+ * latent cache, online softmax, partial results into the workspace.
+ * [MI17] "版本 3" (scores and output directly against the latent) and
+ * "设计取舍" (the nope and rope score parts summed before a hand-written
+ * softmax); [VLB07] 2.3 (block-table indirection).
+ * For each query row n, head h and every visible kv token t of its sequence:
+ *   s_t = softmax_scale * (q_abs[n,h] . row_t)      (576-wide dot product)
+ *   o_lat[n,h] = sum_t softmax(s)_t * row_t[0:512]
+ * where row_t = cache[block_table[b][t / bs]][t % bs]. The work (row, 16-head
+ * group, 64-token tile) is cut into num_ctas equal contiguous shares; each
+ * CTA writes, for every (row, head group) it touches, a normalised partial
+ * output and its log-sum-exp into the workspace. mla_combine() merges them.
+ *   q_abs [num_q, H, 576] dtype; cache [num_blocks, block_size, 576] dtype;
+ *   block_table [batch, max_blocks_per_seq] int32 (entries past a sequence's
+ *   last block are never read); seq_lens [batch] int32;
+ *   query_start_loc [batch + 1] int32 (query_start_loc[batch] == num_q).
+ * The same workspace must be passed, unchanged, to mla_combine().
+ */
+mla_status mla_decode_paged(const mla_config* cfg, const void* q_abs, const void* cache,
+                            int64_t num_blocks, const int32_t* block_table,
+                            int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                            const int32_t* query_start_loc, int32_t batch, int64_t num_q,
+                            void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * mla_combine -- merge the split partials of mla_decode_paged.
+ * For each (n, h): M = max_s lse_s, o_lat = sum_s 2^(lse_s - M) o_s /
+ * sum_s 2^(lse_s - M) (the split-softmax identity; lse is kept in base 2
+ * inside the workspace). Rows that see no token get zeros.
+ *   o_lat [num_q, H, 512] float32 (output, always fp32).
+ * cfg, batch and num_q must equal those given to mla_decode_paged.
+ */
+mla_status mla_combine(const mla_config* cfg, const void* workspace, size_t ws_bytes,
+                       int32_t batch, int64_t num_q, float* o_lat, void* stream);
+
+/*
+ * mla_out_proj -- project the latent output back to v_head_dim.
+ * [MI17] "版本 3" (W_v_absorbed [H, Dc, Dv]; attn_output = attn . (c W_v)).
+ *   out[n,h,v] = sum_c o_lat[n,h,c] * W_uv[h][c][v]
+ *   o_lat [num_q, H, 512] float32; W_uv [H, 512, 128] dtype;
+ *   out [num_q, H, 128] dtype (output).
+ */
+mla_status mla_out_proj(const mla_config* cfg, const float* o_lat, const void* W_uv,
+                        void* out, int64_t num_q, void* stream);
+
+/*
+ * mla_get_device_status -- synchronise `stream`, read the device status word
+ * at `status_word` (a workspace's first word, or the dev_status buffer given
+ * to mla_cache_write), optionally clear it, and map it to a status: the
+ * lowest set bit wins (TIMEOUT, BAD_BLOCK, BAD_SEQ, BAD_SLOT); MLA_OK if none.
+ * `mask_out` (host pointer, may be NULL) receives the raw bits.
+ */
+mla_status mla_get_device_status(const void* status_word, uint32_t* mask_out, int clear,
+                                 void* stream);
+
+/*
+ * mla_selftest_wait_timeout -- launch one CTA that waits on a shared-memory
+ * barrier nothing will ever complete, with the same bounded wait the decode
+ * pipeline uses, shortened to `timeout_ns`. It sets MLA_DEV_TIMEOUT in
+ * *status_word and returns; the context stays usable. Used to test the
+ * timeout path without hanging the GPU.
+ */
+mla_status mla_selftest_wait_timeout(uint32_t* status_word, int64_t timeout_ns, void* stream);
+
+const char* mla_status_string(mla_status s);
+int32_t mla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBMLA_MLA_H_ */

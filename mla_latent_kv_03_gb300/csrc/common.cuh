@@ -1,0 +1,218 @@
+// Internal helpers shared by the libmla kernels: constants, the workspace
+// layout, device status bits, and thin inline-PTX wrappers (mbarrier, TMA,
+// ldmatrix, warp mma). Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mla.h"
+
+namespace mla {
+
+constexpr int kDc = 512;          // kv_lora_rank
+constexpr int kDr = 64;           // qk_rope_head_dim
+constexpr int kDn = 128;          // qk_nope_head_dim
+constexpr int kDv = 128;          // v_head_dim
+constexpr int kRow = kDc + kDr;   // 576 values per cache row
+constexpr int kTile = 64;         // kv tokens per work unit
+constexpr int kHG = 16;           // heads per query tile (one m16 row block)
+constexpr uint32_t kMagic = 0x4d4c4131u;  // "MLA1"
+
+// Default bound for every spin-wait on an mbarrier (ns of %globaltimer).
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+
+// ---------------------------------------------------------------------------
+// Workspace layout (device memory owned by the caller).
+//   [0, 256)            WsHeader
+//   row_info[num_q]     int4 {seq b, query position, tiles, first unit}
+//   cta_start[C]        int4 {row n, head group g, tile k, 0}
+//   lse[S][16]          float, base-2 log-sum-exp of each partial
+//   opart[S][16][512]   float, normalised partial outputs
+// with S = C + num_q * G - 1 partial slots; slot of (CTA c, q-tile t) = c + t
+// (unique because CTA shares and q-tiles are both contiguous ranges of the
+// same ordered unit list).
+// ---------------------------------------------------------------------------
+struct WsHeader {
+  uint32_t status;      // MLA_DEV_* bits
+  uint32_t magic;
+  int32_t total_units;  // sum over rows of G * tiles(row)
+  int32_t share;        // units per CTA
+  int32_t num_ctas;
+  int32_t groups;       // G = H / 16
+  int32_t num_q;
+  int32_t batch;
+  uint32_t pad[56];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+struct WsLayout {
+  size_t row_info, cta_start, lse, opart, total;
+  int64_t slots;
+};
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline WsLayout ws_layout(int64_t num_q, int groups, int num_ctas) {
+  WsLayout L;
+  L.slots = (int64_t)num_ctas + num_q * groups;  // one spare slot
+  size_t off = sizeof(WsHeader);
+  L.row_info = off;   off = align_up(off + (size_t)num_q * 16, 256);
+  L.cta_start = off;  off = align_up(off + (size_t)num_ctas * 16, 256);
+  L.lse = off;        off = align_up(off + (size_t)L.slots * kHG * 4, 256);
+  L.opart = off;      off = align_up(off + (size_t)L.slots * kHG * kDc * 4, 256);
+  L.total = off;
+  return L;
+}
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void set_status(uint32_t* status, uint32_t bits) {
+  if (status) atomicOr(status, bits);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete; false if it did not
+// complete within timeout_ns (the caller then flags MLA_DEV_TIMEOUT and
+// leaves its loop). Never spins forever.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          uint64_t timeout_ns = kWaitTimeoutNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 15u) == 0 && globaltimer_ns() - t0 > timeout_ns) return false;
+  }
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// 2-D tiled TMA load global -> shared, completion counted on `bar` in bytes.
+// x (innermost coordinate, elements) must be a multiple of 8 for 16-bit data.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// D += A * B, m16n8k16, bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// 2^x through the PTX approximate base-2 exponential (documented max relative
+// error about 2^-22); 2^-inf = 0.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Byte offset of 16-byte chunk `chunk` of row `row` in a 128-byte-swizzled
+// tile whose rows are 128 bytes (the TMA SWIZZLE_128B pattern: chunk index
+// XOR row mod 8; the tile base must be 1024-byte aligned).
+__device__ __forceinline__ uint32_t sw128(int row, int chunk) {
+  return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+// Load / store helpers for the two storage dtypes.
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// RoPE inverse frequency and angle, in fp64 so long positions keep their
+// precision: angle = pos * base^(-2i/d).
+__device__ __forceinline__ void rope_cos_sin(int pos, int i, int d, double base, float* c,
+                                             float* s) {
+  const double inv_freq = pow(base, -2.0 * (double)i / (double)d);
+  double sd, cd;
+  sincos((double)pos * inv_freq, &sd, &cd);
+  *c = (float)cd;
+  *s = (float)sd;
+}
+
+}  // namespace mla

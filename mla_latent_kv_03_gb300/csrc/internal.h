@@ -1,0 +1,65 @@
+// Host-side launchers implemented by the kernel translation units and called
+// by the C ABI in libmla.cu. Arguments are validated before these are called.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mla.h"
+
+namespace mla {
+
+struct PlanArgs {
+  const int32_t* seq_lens;
+  const int32_t* query_start_loc;
+  int32_t batch;
+  int32_t num_q;
+  int32_t groups;
+  int32_t num_ctas;
+  int32_t block_size;
+  int32_t max_blocks_per_seq;
+  void* workspace;
+};
+
+struct DecodeArgs {
+  const void* q_abs;
+  const void* cache;
+  int64_t num_blocks;
+  const int32_t* block_table;
+  int32_t max_blocks_per_seq;
+  int32_t block_size;
+  int32_t num_heads;
+  int32_t groups;
+  int32_t num_ctas;
+  int64_t num_q;
+  float scale_log2;  // softmax_scale * log2(e)
+  void* workspace;
+};
+
+cudaError_t launch_cache_write(const mla_config& cfg, const void* c_kv, const void* k_pe,
+                               const int32_t* positions, const int64_t* slot_mapping,
+                               int64_t num_tokens, const void* rms_weight, void* cache,
+                               int64_t num_blocks, uint32_t* dev_status, cudaStream_t stream);
+
+cudaError_t launch_absorb_q(const mla_config& cfg, const void* q_nope, const void* q_pe,
+                            const int32_t* q_positions, const void* W_uk, void* q_abs,
+                            int64_t num_q, cudaStream_t stream);
+
+cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream);
+
+cudaError_t launch_decode_bf16(const DecodeArgs& a, const CUtensorMap& cache_map,
+                               const CUtensorMap& q_map, cudaStream_t stream);
+
+cudaError_t launch_decode_f32(const DecodeArgs& a, cudaStream_t stream);
+
+cudaError_t launch_combine(const void* workspace, int32_t groups, int32_t num_ctas,
+                           int64_t num_q, float* o_lat, cudaStream_t stream);
+
+cudaError_t launch_out_proj(const mla_config& cfg, const float* o_lat, const void* W_uv,
+                            void* out, int64_t num_q, cudaStream_t stream);
+
+cudaError_t launch_wait_timeout_selftest(uint32_t* status, int64_t timeout_ns,
+                                         cudaStream_t stream);
+
+}  // namespace mla

@@ -1,0 +1,264 @@
+// C ABI of libmla (declared in include/mla.h): argument validation, the
+// split-KV CTA count, TMA descriptor encoding, and kernel launches. Host
+// code only; every computation runs in the kernels of the other files.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+using namespace mla;
+
+namespace {
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+inline bool aligned(const void* p, size_t a) {
+  return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+mla_status check_cfg(const mla_config* cfg) {
+  if (!cfg) return MLA_ERR_INVALID_ARGUMENT;
+  if (cfg->kv_lora_rank != kDc || cfg->qk_rope_head_dim != kDr ||
+      cfg->qk_nope_head_dim != kDn || cfg->v_head_dim != kDv)
+    return MLA_ERR_UNSUPPORTED;
+  const int H = cfg->num_heads;
+  if (H != 16 && H != 32 && H != 64 && H != 128) return MLA_ERR_UNSUPPORTED;
+  const int bs = cfg->block_size;
+  if (bs != 16 && bs != 32 && bs != 64) return MLA_ERR_UNSUPPORTED;
+  if (cfg->dtype != MLA_F32 && cfg->dtype != MLA_BF16) return MLA_ERR_UNSUPPORTED;
+  if (cfg->num_ctas < 0 || cfg->num_ctas > 65535) return MLA_ERR_INVALID_ARGUMENT;
+  if (!std::isfinite(cfg->softmax_scale) || !(cfg->rms_eps >= 0.f) ||
+      !std::isfinite(cfg->rms_eps) || !(cfg->rope_base > 0.f) || !std::isfinite(cfg->rope_base))
+    return MLA_ERR_INVALID_ARGUMENT;
+  return MLA_OK;
+}
+
+// One CTA per SM unless the caller fixes the count. Queried on every call
+// (cheap) so a change of current device is honoured.
+int resolve_num_ctas(const mla_config* cfg) {
+  if (cfg->num_ctas > 0) return cfg->num_ctas;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  return sms;
+}
+
+constexpr int64_t kMaxRows = 48 * 1024;  // query rows one plan can hold in shared memory
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 map over rows of 576 values: box = 64 columns x box_rows rows,
+// 128-byte swizzle (the layout the decode kernel's ldmatrix addressing uses).
+bool make_row_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)kRow, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kRow * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+inline mla_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int32_t mla_version(void) { return 1; }
+
+const char* mla_status_string(mla_status s) {
+  switch (s) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case MLA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MLA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MLA_ERR_CUDA: return "CUDA error";
+    case MLA_ERR_TIMEOUT: return "device wait timed out";
+    case MLA_ERR_BAD_BLOCK: return "block table entry out of range";
+    case MLA_ERR_BAD_SEQ: return "query longer than its sequence, or sequence longer than its block table";
+    case MLA_ERR_BAD_SLOT: return "slot_mapping entry out of range";
+  }
+  return "unknown status";
+}
+
+void mla_default_config(mla_config* cfg, int32_t num_heads, int32_t block_size, mla_dtype dtype) {
+  if (!cfg) return;
+  std::memset(cfg, 0, sizeof(*cfg));
+  cfg->num_heads = num_heads;
+  cfg->kv_lora_rank = kDc;
+  cfg->qk_rope_head_dim = kDr;
+  cfg->qk_nope_head_dim = kDn;
+  cfg->v_head_dim = kDv;
+  cfg->block_size = block_size;
+  cfg->softmax_scale = 1.0f / std::sqrt((float)(kDn + kDr));
+  cfg->rms_eps = 1e-6f;
+  cfg->rope_base = 10000.0f;
+  cfg->dtype = dtype;
+  cfg->num_ctas = 0;
+}
+
+mla_status mla_cache_write(const mla_config* cfg, const void* c_kv, const void* k_pe,
+                           const int32_t* positions, const int64_t* slot_mapping,
+                           int64_t num_tokens, const void* rms_weight, void* cache,
+                           int64_t num_blocks, uint32_t* dev_status, void* stream) {
+  mla_status s = check_cfg(cfg);
+  if (s != MLA_OK) return s;
+  if (num_tokens < 0 || num_blocks < 0) return MLA_ERR_INVALID_ARGUMENT;
+  if (num_tokens == 0) return MLA_OK;
+  if (!c_kv || !k_pe || !positions || !slot_mapping || !rms_weight || !cache)
+    return MLA_ERR_INVALID_ARGUMENT;
+  if (!aligned(c_kv, 16) || !aligned(k_pe, 16) || !aligned(rms_weight, 16) ||
+      !aligned(cache, 16) || !aligned(positions, 4) || !aligned(slot_mapping, 8) ||
+      !aligned(dev_status, 4))
+    return MLA_ERR_INVALID_ARGUMENT;
+  return from_cuda(launch_cache_write(*cfg, c_kv, k_pe, positions, slot_mapping, num_tokens,
+                                      rms_weight, cache, num_blocks, dev_status,
+                                      as_stream(stream)));
+}
+
+mla_status mla_absorb_q(const mla_config* cfg, const void* q_nope, const void* q_pe,
+                        const int32_t* q_positions, const void* W_uk, void* q_abs,
+                        int64_t num_q, void* stream) {
+  mla_status s = check_cfg(cfg);
+  if (s != MLA_OK) return s;
+  if (num_q < 0 || num_q > (int64_t)1 << 24) return MLA_ERR_INVALID_ARGUMENT;
+  if (num_q == 0) return MLA_OK;
+  if (!q_nope || !q_pe || !q_positions || !W_uk || !q_abs) return MLA_ERR_INVALID_ARGUMENT;
+  if (!aligned(q_nope, 16) || !aligned(q_pe, 16) || !aligned(W_uk, 16) || !aligned(q_abs, 16) ||
+      !aligned(q_positions, 4))
+    return MLA_ERR_INVALID_ARGUMENT;
+  return from_cuda(launch_absorb_q(*cfg, q_nope, q_pe, q_positions, W_uk, q_abs, num_q,
+                                   as_stream(stream)));
+}
+
+size_t mla_decode_workspace_size(const mla_config* cfg, int64_t num_q, int32_t batch) {
+  if (check_cfg(cfg) != MLA_OK || num_q < 0 || batch < 0) return 0;
+  const int C = resolve_num_ctas(cfg);
+  if (C <= 0) return 0;
+  return ws_layout(num_q, cfg->num_heads / kHG, C).total;
+}
+
+mla_status mla_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
+  if (!workspace || ws_bytes < sizeof(WsHeader) || !aligned(workspace, 256))
+    return MLA_ERR_INVALID_ARGUMENT;
+  return from_cuda(cudaMemsetAsync(workspace, 0, sizeof(WsHeader), as_stream(stream)));
+}
+
+mla_status mla_decode_paged(const mla_config* cfg, const void* q_abs, const void* cache,
+                            int64_t num_blocks, const int32_t* block_table,
+                            int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                            const int32_t* query_start_loc, int32_t batch, int64_t num_q,
+                            void* workspace, size_t ws_bytes, void* stream) {
+  mla_status s = check_cfg(cfg);
+  if (s != MLA_OK) return s;
+  if (num_q < 0 || batch < 0 || num_blocks < 0 || max_blocks_per_seq < 0)
+    return MLA_ERR_INVALID_ARGUMENT;
+  if (num_q > kMaxRows) return MLA_ERR_UNSUPPORTED;
+  if (num_blocks * cfg->block_size > ((int64_t)1 << 31)) return MLA_ERR_UNSUPPORTED;
+  if (!workspace || !aligned(workspace, 256)) return MLA_ERR_INVALID_ARGUMENT;
+  if (num_q == 0) return MLA_OK;
+  if (!q_abs || !cache || !block_table || !seq_lens || !query_start_loc || batch == 0)
+    return MLA_ERR_INVALID_ARGUMENT;
+  if (!aligned(q_abs, 16) || !aligned(cache, 16) || !aligned(block_table, 4) ||
+      !aligned(seq_lens, 4) || !aligned(query_start_loc, 4))
+    return MLA_ERR_INVALID_ARGUMENT;
+  const int C = resolve_num_ctas(cfg);
+  if (C <= 0) return MLA_ERR_CUDA;
+  const int G = cfg->num_heads / kHG;
+  if (ws_bytes < ws_layout(num_q, G, C).total) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = as_stream(stream);
+
+  PlanArgs pa{seq_lens, query_start_loc, batch, (int32_t)num_q, G, C, cfg->block_size,
+              max_blocks_per_seq, workspace};
+  cudaError_t e = launch_plan(pa, st);
+  if (e != cudaSuccess) return MLA_ERR_CUDA;
+
+  const double log2e = 1.4426950408889634;
+  DecodeArgs da{q_abs, cache, num_blocks, block_table, max_blocks_per_seq, cfg->block_size,
+                cfg->num_heads, G, C, num_q, (float)(cfg->softmax_scale * log2e), workspace};
+  if (cfg->dtype == MLA_F32) return from_cuda(launch_decode_f32(da, st));
+  // With num_blocks == 0 every block id is rejected before any copy, so the
+  // map below is never used to read; it still needs a non-empty extent.
+  const uint64_t map_rows = num_blocks > 0 ? (uint64_t)num_blocks * cfg->block_size
+                                           : (uint64_t)cfg->block_size;
+  CUtensorMap cache_map, q_map;
+  if (!make_row_map(&cache_map, cache, map_rows,
+                    (uint32_t)cfg->block_size) ||
+      !make_row_map(&q_map, q_abs, (uint64_t)num_q * cfg->num_heads, kHG))
+    return MLA_ERR_CUDA;
+  return from_cuda(launch_decode_bf16(da, cache_map, q_map, st));
+}
+
+mla_status mla_combine(const mla_config* cfg, const void* workspace, size_t ws_bytes,
+                       int32_t batch, int64_t num_q, float* o_lat, void* stream) {
+  mla_status s = check_cfg(cfg);
+  if (s != MLA_OK) return s;
+  if (num_q < 0 || batch < 0) return MLA_ERR_INVALID_ARGUMENT;
+  if (num_q > kMaxRows) return MLA_ERR_UNSUPPORTED;
+  if (num_q == 0) return MLA_OK;
+  if (!workspace || !o_lat || !aligned(workspace, 256) || !aligned(o_lat, 16))
+    return MLA_ERR_INVALID_ARGUMENT;
+  const int C = resolve_num_ctas(cfg);
+  if (C <= 0) return MLA_ERR_CUDA;
+  const int G = cfg->num_heads / kHG;
+  if (ws_bytes < ws_layout(num_q, G, C).total) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  return from_cuda(launch_combine(workspace, G, C, num_q, o_lat, as_stream(stream)));
+}
+
+mla_status mla_out_proj(const mla_config* cfg, const float* o_lat, const void* W_uv, void* out,
+                        int64_t num_q, void* stream) {
+  mla_status s = check_cfg(cfg);
+  if (s != MLA_OK) return s;
+  if (num_q < 0 || num_q > (int64_t)1 << 24) return MLA_ERR_INVALID_ARGUMENT;
+  if (num_q == 0) return MLA_OK;
+  if (!o_lat || !W_uv || !out) return MLA_ERR_INVALID_ARGUMENT;
+  if (!aligned(o_lat, 16) || !aligned(W_uv, 16) || !aligned(out, 16)) return MLA_ERR_INVALID_ARGUMENT;
+  return from_cuda(launch_out_proj(*cfg, o_lat, W_uv, out, num_q, as_stream(stream)));
+}
+
+mla_status mla_get_device_status(const void* status_word, uint32_t* mask_out, int clear,
+                                 void* stream) {
+  if (!status_word || !aligned(status_word, 4)) return MLA_ERR_INVALID_ARGUMENT;
+  cudaStream_t st = as_stream(stream);
+  uint32_t v = 0;
+  if (cudaMemcpyAsync(&v, status_word, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  if (clear && cudaMemsetAsync(const_cast<void*>(status_word), 0, sizeof(v), st) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MLA_ERR_CUDA;
+  if (mask_out) *mask_out = v;
+  if (v & MLA_DEV_TIMEOUT) return MLA_ERR_TIMEOUT;
+  if (v & MLA_DEV_BAD_BLOCK) return MLA_ERR_BAD_BLOCK;
+  if (v & MLA_DEV_BAD_SEQ) return MLA_ERR_BAD_SEQ;
+  if (v & MLA_DEV_BAD_SLOT) return MLA_ERR_BAD_SLOT;
+  return MLA_OK;
+}
+
+mla_status mla_selftest_wait_timeout(uint32_t* status_word, int64_t timeout_ns, void* stream) {
+  if (!status_word || !aligned(status_word, 4) || timeout_ns <= 0 || timeout_ns > 10000000000ll)
+    return MLA_ERR_INVALID_ARGUMENT;
+  return from_cuda(launch_wait_timeout_selftest(status_word, timeout_ns, as_stream(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,204 @@
+// Split-KV partition (plan), the merge of split partials (combine), and the
+// bounded-wait self-test.
+//
+// Work units. Query row n of sequence b sits at position pos_n and sees
+// tiles(n) = ceil((pos_n + 1) / 64) tiles of 64 kv tokens. A q-tile is
+// (row n, head group g) with 16 heads; q-tiles are ordered t = n * G + g and
+// each owns tiles(n) consecutive units. The plan cuts the ordered unit list
+// into num_ctas equal contiguous shares (one persistent CTA per share), so a
+// ragged batch is balanced to within one unit per CTA.
+//
+// Combine follows the split-softmax identity (flash-decoding): for partials
+// o_s (normalised) with base-2 log-sum-exp lse_s,
+//   o = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M),  M = max_s lse_s.
+#include "common.cuh"
+#include "internal.h"
+
+namespace mla {
+namespace {
+
+constexpr int kPlanThreads = 1024;
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
+  extern __shared__ int s_units[];  // num_q + 1 entries: units per row, then prefix
+  __shared__ int s_warp[32];
+  const int tid = threadIdx.x;
+  uint8_t* ws = reinterpret_cast<uint8_t*>(a.workspace);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  const WsLayout L = ws_layout(a.num_q, a.groups, a.num_ctas);
+  int4* row_info = reinterpret_cast<int4*>(ws + L.row_info);
+  int4* cta_start = reinterpret_cast<int4*>(ws + L.cta_start);
+  const int Nq = a.num_q;
+
+  for (int n = tid; n < Nq; n += kPlanThreads) {
+    row_info[n] = make_int4(-1, -1, 0, 0);
+    s_units[n] = 0;
+  }
+  __syncthreads();
+  const int64_t max_len = (int64_t)a.max_blocks_per_seq * a.block_size;
+  for (int b = tid; b < a.batch; b += kPlanThreads) {
+    const int len = a.seq_lens[b];
+    const int q0 = a.query_start_loc[b], q1 = a.query_start_loc[b + 1];
+    const int ql = q1 - q0;
+    if (q0 < 0 || q1 > Nq || ql < 0) {
+      set_status(&hdr->status, MLA_DEV_BAD_SEQ);
+      continue;
+    }
+    const bool bad = ql > len || len < 0 || (int64_t)len > max_len;
+    if (bad && ql > 0) set_status(&hdr->status, MLA_DEV_BAD_SEQ);
+    for (int j = 0; j < ql; ++j) {
+      const int n = q0 + j;
+      const int pos = len - ql + j;
+      const int tiles = bad ? 0 : (pos + kTile) / kTile;  // ceil((pos + 1) / 64)
+      row_info[n] = make_int4(b, pos, tiles, 0);
+      s_units[n] = tiles * a.groups;
+    }
+  }
+  __syncthreads();
+
+  // exclusive scan of s_units[0..Nq) in place; s_units[Nq] = total
+  const int per = (Nq + kPlanThreads - 1) / kPlanThreads;
+  const int beg = min(Nq, tid * per), end = min(Nq, beg + per);
+  int local = 0;
+  for (int i = beg; i < end; ++i) local += s_units[i];
+  // block exclusive scan of `local`
+  const int lane = tid & 31, warp = tid >> 5;
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = s_warp[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += v;
+    }
+    s_warp[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  int run = incl - local + (warp > 0 ? s_warp[warp - 1] : 0);
+  const int total = s_warp[31];
+  __syncthreads();
+  for (int i = beg; i < end; ++i) {
+    const int u = s_units[i];
+    s_units[i] = run;
+    run += u;
+  }
+  if (tid == 0) s_units[Nq] = total;
+  __syncthreads();
+  for (int n = tid; n < Nq; n += kPlanThreads) row_info[n].w = s_units[n];
+
+  const int C = a.num_ctas;
+  const int share = total > 0 ? (total + C - 1) / C : 1;
+  if (tid == 0) {
+    hdr->magic = kMagic;
+    hdr->total_units = total;
+    hdr->share = share;
+    hdr->num_ctas = C;
+    hdr->groups = a.groups;
+    hdr->num_q = Nq;
+    hdr->batch = a.batch;
+  }
+  for (int c = tid; c < C; c += kPlanThreads) {
+    const int u0 = c * share;
+    if (u0 >= total) {
+      cta_start[c] = make_int4(-1, 0, 0, 0);
+      continue;
+    }
+    // last row n with start[n] <= u0 (that row has tiles > 0)
+    int lo = 0, hi = Nq;  // invariant: start[lo] <= u0 < start[hi]  (start[Nq] = total)
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_units[mid] <= u0) lo = mid; else hi = mid;
+    }
+    const int tiles = (s_units[lo + 1] - s_units[lo]) / a.groups;
+    const int off = u0 - s_units[lo];
+    cta_start[c] = make_int4(lo, off / tiles, off % tiles, 0);
+  }
+}
+
+// grid (num_q * G, 4): 16 head rows x 128 latent dims per CTA, thread = dim.
+__global__ void __launch_bounds__(128) combine_kernel(const uint8_t* __restrict__ ws, int groups,
+                                                      int num_ctas, int64_t num_q,
+                                                      float* __restrict__ o_lat) {
+  const WsHeader* hdr = reinterpret_cast<const WsHeader*>(ws);
+  const WsLayout L = ws_layout(num_q, groups, num_ctas);
+  const int4* row_info = reinterpret_cast<const int4*>(ws + L.row_info);
+  const float* lse = reinterpret_cast<const float*>(ws + L.lse);
+  const float* opart = reinterpret_cast<const float*>(ws + L.opart);
+  const int t = blockIdx.x;
+  const int n = t / groups, g = t % groups;
+  const int d = blockIdx.y * 128 + threadIdx.x;
+  const int H = groups * kHG;
+  float* out = o_lat + ((size_t)n * H + g * kHG) * kDc + d;
+  const bool match = hdr->num_q == num_q && hdr->groups == groups && hdr->num_ctas == num_ctas;
+  const int4 ri = match ? row_info[n] : make_int4(-1, -1, 0, 0);
+  const int tiles = ri.z;
+  const bool plan_ok = hdr->magic == kMagic && hdr->num_q == num_q && hdr->groups == groups &&
+                       hdr->num_ctas == num_ctas;
+  if (tiles <= 0 || !plan_ok) {
+#pragma unroll
+    for (int r = 0; r < kHG; ++r) out[(size_t)r * kDc] = 0.f;
+    return;
+  }
+  const int share = hdr->share;
+  const int U = ri.w + g * tiles;
+  const int c_first = U / share, c_last = (U + tiles - 1) / share;
+  for (int r = 0; r < kHG; ++r) {
+    float M = -INFINITY;
+    for (int c = c_first; c <= c_last; ++c) M = fmaxf(M, lse[(size_t)(c + t) * kHG + r]);
+    float den = 0.f, acc = 0.f;
+    if (M != -INFINITY) {
+      for (int c = c_first; c <= c_last; ++c) {
+        const size_t slot = (size_t)(c + t);
+        const float w = fast_exp2(lse[slot * kHG + r] - M);
+        den += w;
+        acc = fmaf(w, opart[(slot * kHG + r) * kDc + d], acc);
+      }
+    }
+    out[(size_t)r * kDc] = den > 0.f ? acc / den : 0.f;
+  }
+}
+
+__global__ void wait_timeout_selftest_kernel(uint32_t* status, uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // Nothing arrives on `bar`: the bounded wait must give up and report.
+  if (threadIdx.x == 0 && !mbar_wait(&bar, 0, timeout_ns)) set_status(status, MLA_DEV_TIMEOUT);
+}
+
+}  // namespace
+
+cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream) {
+  const size_t smem = ((size_t)a.num_q + 1) * sizeof(int);
+  cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  plan_kernel<<<1, kPlanThreads, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const void* workspace, int32_t groups, int32_t num_ctas,
+                           int64_t num_q, float* o_lat, cudaStream_t stream) {
+  if (num_q == 0) return cudaSuccess;
+  combine_kernel<<<dim3((unsigned)(num_q * groups), 4), 128, 0, stream>>>(
+      (const uint8_t*)workspace, groups, num_ctas, num_q, o_lat);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_timeout_selftest(uint32_t* status, int64_t timeout_ns,
+                                         cudaStream_t stream) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(status, (uint64_t)timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

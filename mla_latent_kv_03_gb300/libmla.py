@@ -1,0 +1,212 @@
+"""Thin ctypes binding over libmla.so (argument marshalling only).
+
+The functions carry the C names of include/mla.h and take torch tensors for
+device buffers; each one checks dtype, device and contiguity, passes raw
+pointers and the current CUDA stream to the library, and raises MlaError on a
+non-OK status. No computation happens here, and there is no fallback: if
+libmla.so cannot be loaded, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+MLA_OK = 0
+MLA_F32, MLA_BF16 = 0, 1
+STATUS_NAMES = {
+    0: "MLA_OK", 1: "MLA_ERR_INVALID_ARGUMENT", 2: "MLA_ERR_UNSUPPORTED",
+    3: "MLA_ERR_WORKSPACE_TOO_SMALL", 4: "MLA_ERR_CUDA", 5: "MLA_ERR_TIMEOUT",
+    6: "MLA_ERR_BAD_BLOCK", 7: "MLA_ERR_BAD_SEQ", 8: "MLA_ERR_BAD_SLOT",
+}
+DEV_TIMEOUT, DEV_BAD_BLOCK, DEV_BAD_SEQ, DEV_BAD_SLOT = 1, 2, 4, 8
+
+EXPORTS = (
+    "mla_default_config", "mla_cache_write", "mla_absorb_q", "mla_decode_workspace_size",
+    "mla_workspace_init", "mla_decode_paged", "mla_combine", "mla_out_proj",
+    "mla_get_device_status", "mla_selftest_wait_timeout", "mla_status_string", "mla_version",
+)
+
+
+class MlaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} "
+                         f"({_status_string(status)})")
+
+
+class MlaConfig(ctypes.Structure):
+    _fields_ = [
+        ("num_heads", ctypes.c_int32), ("kv_lora_rank", ctypes.c_int32),
+        ("qk_rope_head_dim", ctypes.c_int32), ("qk_nope_head_dim", ctypes.c_int32),
+        ("v_head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
+        ("softmax_scale", ctypes.c_float), ("rms_eps", ctypes.c_float),
+        ("rope_base", ctypes.c_float), ("dtype", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
+    ]
+
+
+_LIB: Optional[ctypes.CDLL] = None
+
+_vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+_cfgp = ctypes.POINTER(MlaConfig)
+_SIGS = {
+    "mla_default_config": (None, [_cfgp, _i32, _i32, _i32]),
+    "mla_cache_write": (_i32, [_cfgp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _i64, _vp, _vp]),
+    "mla_absorb_q": (_i32, [_cfgp, _vp, _vp, _vp, _vp, _vp, _i64, _vp]),
+    "mla_decode_workspace_size": (_sz, [_cfgp, _i64, _i32]),
+    "mla_workspace_init": (_i32, [_vp, _sz, _vp]),
+    "mla_decode_paged": (_i32, [_cfgp, _vp, _vp, _i64, _vp, _i32, _vp, _vp, _i32, _i64, _vp, _sz, _vp]),
+    "mla_combine": (_i32, [_cfgp, _vp, _sz, _i32, _i64, _vp, _vp]),
+    "mla_out_proj": (_i32, [_cfgp, _vp, _vp, _vp, _i64, _vp]),
+    "mla_get_device_status": (_i32, [_vp, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int, _vp]),
+    "mla_selftest_wait_timeout": (_i32, [_vp, _i64, _vp]),
+    "mla_status_string": (ctypes.c_char_p, [_i32]),
+    "mla_version": (_i32, []),
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libmla.so (building it first if it is missing or stale)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if build_if_missing and not _build.up_to_date():
+        _build.build()
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libmla.so not found at {path}; run build() first")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = lib
+    return lib
+
+
+def _status_string(s: int) -> str:
+    try:
+        return load().mla_status_string(s).decode()
+    except Exception:  # the library itself failed to load
+        return "?"
+
+
+def _check(status: int, where: str) -> None:
+    if status != MLA_OK:
+        raise MlaError(status, where)
+
+
+def make_config(num_heads: int, block_size: int, dtype: str, num_ctas: int = 0,
+                softmax_scale: Optional[float] = None, rms_eps: Optional[float] = None,
+                rope_base: Optional[float] = None) -> MlaConfig:
+    cfg = MlaConfig()
+    load().mla_default_config(ctypes.byref(cfg), num_heads, block_size,
+                              MLA_BF16 if dtype == "bf16" else MLA_F32)
+    cfg.num_ctas = num_ctas
+    if softmax_scale is not None:
+        cfg.softmax_scale = softmax_scale
+    if rms_eps is not None:
+        cfg.rms_eps = rms_eps
+    if rope_base is not None:
+        cfg.rope_base = rope_base
+    return cfg
+
+
+def _torch_dtype(cfg: MlaConfig):
+    return torch.bfloat16 if cfg.dtype == MLA_BF16 else torch.float32
+
+
+def _ptr(t: Optional[torch.Tensor], dtype=None, name: str = "tensor") -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def mla_cache_write(cfg: MlaConfig, c_kv, k_pe, positions, slot_mapping, rms_weight, cache,
+                    dev_status=None, stream=None) -> None:
+    dt = _torch_dtype(cfg)
+    _check(load().mla_cache_write(
+        ctypes.byref(cfg), _ptr(c_kv, dt, "c_kv"), _ptr(k_pe, dt, "k_pe"),
+        _ptr(positions, torch.int32, "positions"), _ptr(slot_mapping, torch.int64, "slot_mapping"),
+        c_kv.shape[0], _ptr(rms_weight, dt, "rms_weight"), _ptr(cache, dt, "cache"),
+        cache.shape[0], _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)),
+        "mla_cache_write")
+
+
+def mla_absorb_q(cfg: MlaConfig, q_nope, q_pe, q_positions, W_uk, q_abs, stream=None) -> None:
+    dt = _torch_dtype(cfg)
+    _check(load().mla_absorb_q(
+        ctypes.byref(cfg), _ptr(q_nope, dt, "q_nope"), _ptr(q_pe, dt, "q_pe"),
+        _ptr(q_positions, torch.int32, "q_positions"), _ptr(W_uk, dt, "W_uk"),
+        _ptr(q_abs, dt, "q_abs"), q_nope.shape[0], _stream(stream)), "mla_absorb_q")
+
+
+def mla_decode_workspace_size(cfg: MlaConfig, num_q: int, batch: int) -> int:
+    return int(load().mla_decode_workspace_size(ctypes.byref(cfg), num_q, batch))
+
+
+def mla_workspace_init(workspace, stream=None) -> None:
+    _check(load().mla_workspace_init(_ptr(workspace, None, "workspace"), workspace.numel() *
+                                     workspace.element_size(), _stream(stream)),
+           "mla_workspace_init")
+
+
+def mla_decode_paged(cfg: MlaConfig, q_abs, cache, block_table, seq_lens, query_start_loc,
+                     workspace, stream=None) -> None:
+    dt = _torch_dtype(cfg)
+    _check(load().mla_decode_paged(
+        ctypes.byref(cfg), _ptr(q_abs, dt, "q_abs"), _ptr(cache, dt, "cache"), cache.shape[0],
+        _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+        _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(query_start_loc, torch.int32, "query_start_loc"),
+        seq_lens.shape[0], q_abs.shape[0], _ptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream)), "mla_decode_paged")
+
+
+def mla_combine(cfg: MlaConfig, workspace, batch: int, o_lat, stream=None) -> None:
+    _check(load().mla_combine(
+        ctypes.byref(cfg), _ptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(), batch, o_lat.shape[0],
+        _ptr(o_lat, torch.float32, "o_lat"), _stream(stream)), "mla_combine")
+
+
+def mla_out_proj(cfg: MlaConfig, o_lat, W_uv, out, stream=None) -> None:
+    dt = _torch_dtype(cfg)
+    _check(load().mla_out_proj(
+        ctypes.byref(cfg), _ptr(o_lat, torch.float32, "o_lat"), _ptr(W_uv, dt, "W_uv"),
+        _ptr(out, dt, "out"), o_lat.shape[0], _stream(stream)), "mla_out_proj")
+
+
+def mla_get_device_status(status_word, clear: bool = True, stream=None):
+    """Returns (status, raw bits)."""
+    mask = ctypes.c_uint32(0)
+    s = load().mla_get_device_status(_ptr(status_word, None, "status_word"), ctypes.byref(mask),
+                                     int(clear), _stream(stream))
+    return int(s), int(mask.value)
+
+
+def mla_selftest_wait_timeout(status_word, timeout_ns: int, stream=None) -> None:
+    _check(load().mla_selftest_wait_timeout(_ptr(status_word, None, "status_word"), timeout_ns,
+                                            _stream(stream)), "mla_selftest_wait_timeout")

@@ -1,0 +1,115 @@
+"""Device buffers for one workload and the calls of one decode step.
+
+`MlaDecodeStep` owns torch device tensors (torch is only the allocator and
+stream provider here) and issues the libmla calls of one step:
+  mla_cache_write (new tokens) -> mla_absorb_q -> mla_decode_paged
+  -> mla_combine -> mla_out_proj.
+"""
+
+from __future__ import annotations
+
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import libmla as L
+from .workloads import Workload
+
+
+def _dev(a: np.ndarray, dtype, device) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device=device, dtype=dtype)
+
+
+class MlaDecodeStep:
+    def __init__(self, w: Workload, device: str = "cuda", num_ctas: int = 0,
+                 cache_fill: Optional[float] = None):
+        self.w = w
+        self.device = device
+        self.cfg = L.make_config(w.num_heads, w.block_size, w.dtype, num_ctas=num_ctas,
+                                 softmax_scale=w.softmax_scale, rms_eps=w.rms_eps,
+                                 rope_base=w.rope_base)
+        dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+        self.dt = dt
+        H = w.num_heads
+        self.W_uk = _dev(w.W_uk, dt, device)
+        self.W_uv = _dev(w.W_uv, dt, device)
+        self.rms_weight = _dev(w.rms_weight, dt, device)
+        self.block_table = _dev(w.block_table, torch.int32, device)
+        self.seq_lens = _dev(w.seq_lens, torch.int32, device)
+        self.query_start_loc = _dev(w.query_start_loc, torch.int32, device)
+        self.q_nope = _dev(w.q_nope, dt, device)
+        self.q_pe = _dev(w.q_pe, dt, device)
+        self.q_positions = _dev(w.q_positions, torch.int32, device)
+        # every token of every sequence (used to populate the cache)
+        self.c_kv = _dev(w.c_kv_raw, dt, device)
+        self.k_pe = _dev(w.k_pe_raw, dt, device)
+        self.kv_positions = _dev(w.kv_positions, torch.int32, device)
+        self.slot_mapping = _dev(w.slot_mapping, torch.int64, device)
+        new = np.nonzero(w.is_new)[0]
+        self.new_idx = new
+        self.c_kv_new = self.c_kv[torch.from_numpy(new).to(device)].contiguous()
+        self.k_pe_new = self.k_pe[torch.from_numpy(new).to(device)].contiguous()
+        self.pos_new = self.kv_positions[torch.from_numpy(new).to(device)].contiguous()
+        self.slot_new = self.slot_mapping[torch.from_numpy(new).to(device)].contiguous()
+        self.cache = torch.empty((w.num_blocks, w.block_size, 576), dtype=dt, device=device)
+        if cache_fill is not None:
+            self.cache.fill_(cache_fill)
+        Nq = w.num_q
+        self.q_abs = torch.empty((Nq, H, 576), dtype=dt, device=device)
+        self.o_lat = torch.empty((Nq, H, 512), dtype=torch.float32, device=device)
+        self.out = torch.empty((Nq, H, 128), dtype=dt, device=device)
+        ws_bytes = L.mla_decode_workspace_size(self.cfg, Nq, w.batch)
+        if ws_bytes == 0:
+            raise L.MlaError(L.MLA_OK + 2, "mla_decode_workspace_size")
+        self.workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+        L.mla_workspace_init(self.workspace)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    # -- cache population --------------------------------------------------
+    def populate(self, include_new: bool = True) -> None:
+        """Write every token (or every old token) into the paged cache."""
+        if include_new:
+            L.mla_cache_write(self.cfg, self.c_kv, self.k_pe, self.kv_positions,
+                              self.slot_mapping, self.rms_weight, self.cache, self.status)
+            return
+        old = torch.from_numpy(np.nonzero(~self.w.is_new)[0]).to(self.device)
+        if old.numel() == 0:
+            return
+        L.mla_cache_write(self.cfg, self.c_kv[old].contiguous(), self.k_pe[old].contiguous(),
+                          self.kv_positions[old].contiguous(), self.slot_mapping[old].contiguous(),
+                          self.rms_weight, self.cache, self.status)
+
+    def write_new(self, stream=None) -> None:
+        L.mla_cache_write(self.cfg, self.c_kv_new, self.k_pe_new, self.pos_new, self.slot_new,
+                          self.rms_weight, self.cache, self.status, stream=stream)
+
+    # -- one step ----------------------------------------------------------
+    def absorb(self, stream=None) -> None:
+        L.mla_absorb_q(self.cfg, self.q_nope, self.q_pe, self.q_positions, self.W_uk, self.q_abs,
+                       stream=stream)
+
+    def decode(self, stream=None) -> None:
+        L.mla_decode_paged(self.cfg, self.q_abs, self.cache, self.block_table, self.seq_lens,
+                           self.query_start_loc, self.workspace, stream=stream)
+
+    def combine(self, stream=None) -> None:
+        L.mla_combine(self.cfg, self.workspace, self.w.batch, self.o_lat, stream=stream)
+
+    def out_proj(self, stream=None) -> None:
+        L.mla_out_proj(self.cfg, self.o_lat, self.W_uv, self.out, stream=stream)
+
+    def step(self, write_new: bool = False, stream=None) -> torch.Tensor:
+        if write_new:
+            self.write_new(stream)
+        self.absorb(stream)
+        self.decode(stream)
+        self.combine(stream)
+        self.out_proj(stream)
+        return self.out
+
+    def device_status(self):
+        """(status, bits) of the decode workspace and of the cache-write word."""
+        s1 = L.mla_get_device_status(self.workspace)
+        s2 = L.mla_get_device_status(self.status)
+        return s1, s2

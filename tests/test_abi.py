@@ -1,0 +1,100 @@
+"""The C ABI without a GPU: the library builds and loads, exports every call
+that include/mla.h declares, and rejects bad arguments on the host before any
+CUDA work (no compute call runs here)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from mla_latent_kv_03_gb300 import libmla as L
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mla.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return L.load(build_if_missing=True)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("mla_cache_write", "mla_absorb_q", "mla_decode_paged", "mla_combine",
+                     "mla_out_proj", "mla_decode_workspace_size", "mla_get_device_status"):
+        assert required in names
+    assert set(names) == set(L.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert lib.mla_version() >= 1
+
+
+def test_status_strings(lib):
+    for code in range(9):
+        assert lib.mla_status_string(code)
+    assert lib.mla_status_string(0) == b"ok"
+
+
+def test_default_config_is_v2_lite(lib):
+    cfg = L.make_config(16, 64, "bf16")
+    assert (cfg.kv_lora_rank, cfg.qk_rope_head_dim, cfg.qk_nope_head_dim, cfg.v_head_dim) == (512, 64, 128, 128)
+    assert abs(cfg.softmax_scale - 192 ** -0.5) < 1e-7
+    assert cfg.rms_eps == pytest.approx(1e-6) and cfg.rope_base == 10000.0
+    assert cfg.dtype == L.MLA_BF16 and cfg.num_ctas == 0
+
+
+@pytest.mark.parametrize("field,value,expect", [
+    ("num_heads", 24, 2), ("num_heads", 256, 2), ("block_size", 128, 2), ("block_size", 8, 2),
+    ("kv_lora_rank", 256, 2), ("qk_rope_head_dim", 32, 2), ("dtype", 7, 2), ("num_ctas", -1, 1),
+])
+def test_unsupported_configs_are_rejected(lib, field, value, expect):
+    cfg = L.make_config(16, 64, "bf16")
+    setattr(cfg, field, value)
+    p = ctypes.c_void_p(16)  # never dereferenced: validation fails first
+    s = lib.mla_absorb_q(ctypes.byref(cfg), p, p, p, p, p, 1, None)
+    assert s == expect
+
+
+def test_null_and_misaligned_pointers_are_rejected(lib):
+    cfg = L.make_config(16, 64, "bf16")
+    p = ctypes.c_void_p(256)
+    assert lib.mla_absorb_q(None, p, p, p, p, p, 1, None) == 1
+    assert lib.mla_absorb_q(ctypes.byref(cfg), None, p, p, p, p, 1, None) == 1
+    assert lib.mla_absorb_q(ctypes.byref(cfg), ctypes.c_void_p(258), p, p, p, p, 1, None) == 1
+    assert lib.mla_out_proj(ctypes.byref(cfg), p, p, None, 1, None) == 1
+    assert lib.mla_cache_write(ctypes.byref(cfg), p, p, p, ctypes.c_void_p(260), 1, p, p, 4, None, None) == 1
+    # zero-sized work is a no-op that succeeds without touching pointers
+    assert lib.mla_absorb_q(ctypes.byref(cfg), None, None, None, None, None, 0, None) == 0
+    assert lib.mla_cache_write(ctypes.byref(cfg), None, None, None, None, 0, None, None, 0, None, None) == 0
+
+
+def test_workspace_size_with_fixed_cta_count(lib):
+    cfg = L.make_config(16, 64, "bf16", num_ctas=152)
+    n64 = lib.mla_decode_workspace_size(ctypes.byref(cfg), 64, 64)
+    # 152 CTAs + 64 q-tiles partial slots of 16 x 512 fp32 dominate
+    assert n64 >= (152 + 64) * 16 * 512 * 4
+    assert n64 < (152 + 64) * 16 * 512 * 4 + 64 * 1024
+    cfg128 = L.make_config(128, 64, "bf16", num_ctas=152)
+    n128 = lib.mla_decode_workspace_size(ctypes.byref(cfg128), 32, 32)
+    assert n128 >= (152 + 32 * 8) * 16 * 512 * 4
+    assert lib.mla_decode_workspace_size(None, 1, 1) == 0
+
+
+def test_decode_rejects_small_workspace_on_host(lib):
+    cfg = L.make_config(16, 64, "bf16", num_ctas=8)
+    p = ctypes.c_void_p(1 << 20)
+    need = lib.mla_decode_workspace_size(ctypes.byref(cfg), 4, 4)
+    s = lib.mla_decode_paged(ctypes.byref(cfg), p, p, 16, p, 4, p, p, 4, 4, p, need - 256, None)
+    assert s == 3
+    s = lib.mla_decode_paged(ctypes.byref(cfg), p, p, 16, p, 4, p, p, 4, 70000, p, 1 << 40, None)
+    assert s == 2  # more query rows than one plan holds

@@ -1,0 +1,238 @@
+"""GPU parity: every libmla call against the fp64 oracle, through the C ABI.
+
+Each step is checked in isolation (on the GPU's own inputs to that step) and
+end to end (raw inputs -> out, against the naive expanded form), on the
+workloads of the problem statement: small cases the oracle finishes in
+seconds over every row, the full-size ones on sampled sequences and heads.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from _helpers import (BF16_MAX_ABS, assert_close, bf16_ulp, errors, ref_cache_rows,
+                      ref_o_lat_from, ref_out, ref_q_abs, to_f64)
+from mla_latent_kv_03_gb300 import libmla as L
+from mla_latent_kv_03_gb300 import workloads as W
+from mla_latent_kv_03_gb300.step import MlaDecodeStep
+from oracle import mla_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    L.load()
+
+
+def _sentinel_fill(dtype):
+    return float("nan")
+
+
+# ---------------------------------------------------------------------------
+# mla_cache_write
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype,bs", [("f32", 16), ("bf16", 16), ("bf16", 32), ("bf16", 64)])
+def test_cache_write_placement_is_bit_exact(dtype, bs):
+    w = W.make("cw", [7, 33, 64, 65, 130, 1], [1] * 6, 16, bs, dtype, seed=21, extra_blocks=3)
+    s = MlaDecodeStep(w, device=DEV)
+    itype = torch.int16 if dtype == "bf16" else torch.int32
+    pattern = 0x7FC1 if dtype == "bf16" else 0x7FC00123   # a NaN bit pattern
+    s.cache.view(itype).fill_(pattern)
+    # add padding tokens (slot -1) that must write nothing
+    L.mla_cache_write(s.cfg, s.c_kv[:5].contiguous(), s.k_pe[:5].contiguous(),
+                      s.kv_positions[:5].contiguous(),
+                      torch.full((5,), -1, dtype=torch.int64, device=DEV),
+                      s.rms_weight, s.cache, s.status)
+    s.populate()
+    torch.cuda.synchronize()
+    assert L.mla_get_device_status(s.status)[0] == 0
+    bits = s.cache.view(itype).cpu().numpy().reshape(-1, 576)
+    written = np.zeros(bits.shape[0], dtype=bool)
+    written[w.slot_mapping] = True
+    assert np.all(bits[~written] == np.array(pattern).astype(bits.dtype)), "bytes outside the slots changed"
+    got = to_f64(s.cache).reshape(-1, 576)[w.slot_mapping]
+    ref = ref_cache_rows(w)
+    if dtype == "bf16":
+        assert np.all(np.abs(got - ref) <= bf16_ulp(ref)), "row values beyond 1 bf16 ulp"
+    else:
+        np.testing.assert_allclose(got, ref, rtol=1e-6, atol=1e-6)
+
+
+def test_cache_write_bad_slot_sets_status_and_writes_nothing():
+    w = W.make("cw_bad", [10], [1], 16, 16, "bf16", seed=22)
+    s = MlaDecodeStep(w, device=DEV)
+    s.cache.view(torch.int16).fill_(0x7FC1)
+    bad = torch.full((10,), w.num_blocks * 16, dtype=torch.int64, device=DEV)
+    L.mla_cache_write(s.cfg, s.c_kv, s.k_pe, s.kv_positions, bad, s.rms_weight, s.cache, s.status)
+    st, bits = L.mla_get_device_status(s.status)
+    assert st == 8 and bits & L.DEV_BAD_SLOT
+    assert torch.all(s.cache.view(torch.int16) == 0x7FC1)
+
+
+# ---------------------------------------------------------------------------
+# mla_absorb_q and mla_out_proj
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype,nq,heads", [("f32", 3, 16), ("bf16", 1, 16), ("bf16", 37, 32),
+                                            ("bf16", 600, 16), ("bf16", 5, 128)])
+def test_absorb_q(dtype, nq, heads):
+    w = W.make("aq", [40] * nq, [1] * nq, heads, 64, dtype, seed=23)
+    s = MlaDecodeStep(w, device=DEV)
+    s.absorb()
+    got = to_f64(s.q_abs)
+    ref = ref_q_abs(w)
+    if dtype == "f32":
+        np.testing.assert_allclose(got, ref, rtol=0, atol=2e-5)
+    else:
+        assert np.all(np.abs(got - ref) <= 2 * bf16_ulp(ref) + 1e-5), "q_abs beyond 2 bf16 ulp"
+
+
+@pytest.mark.parametrize("dtype,nq,heads", [("f32", 3, 16), ("bf16", 1, 16), ("bf16", 64, 16),
+                                            ("bf16", 600, 16), ("bf16", 9, 128)])
+def test_out_proj(dtype, nq, heads):
+    w = W.make("op", [8] * nq, [1] * nq, heads, 64, dtype, seed=24)
+    s = MlaDecodeStep(w, device=DEV)
+    o = torch.randn(nq, heads, 512, generator=torch.Generator().manual_seed(5)) / 20
+    s.o_lat.copy_(o)
+    s.out_proj()
+    got = to_f64(s.out)
+    ref = O.out_proj(o.double().numpy(), w.W_uv)
+    assert_close(got, ref, dtype, "out_proj")
+
+
+# ---------------------------------------------------------------------------
+# mla_decode_paged + mla_combine on the GPU's own cache rows and q_abs
+# ---------------------------------------------------------------------------
+
+SMALL = {
+    "tiny_fp32": lambda: W.tiny(),
+    "ragged_tails_bf16": lambda: W.make("ragged_tails", [1, 63, 64, 65, 127, 128, 129, 1000],
+                                        [1] * 8, 16, 64, "bf16", seed=31, extra_blocks=2),
+    "bs16_bf16": lambda: W.make("bs16", [5, 40, 200], [1] * 3, 16, 16, "bf16", seed=32),
+    "bs32_h32_bf16": lambda: W.make("bs32h32", [33, 97], [1, 1], 32, 32, "bf16", seed=33),
+    "h128_bf16": lambda: W.make("h128", [17, 300, 1], [1] * 3, 128, 64, "bf16", seed=34),
+    "h64_bf16": lambda: W.make("h64", [70, 2], [1, 1], 64, 64, "bf16", seed=35),
+    "prefill_bf16": lambda: W.make("prefill", [150, 64, 20], [40, 1, 20], 16, 64, "bf16", seed=36),
+    "empty_seq_bf16": lambda: W.make("empty", [0, 5, 0, 70], [0, 1, 0, 1], 16, 64, "bf16", seed=37),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_decode_and_combine_vs_latent_oracle(name):
+    w = SMALL[name]()
+    s = MlaDecodeStep(w, device=DEV)
+    s.populate()
+    s.absorb()
+    s.decode()
+    s.combine()
+    torch.cuda.synchronize()
+    assert s.device_status()[0][0] == 0
+    ref = ref_o_lat_from(w, to_f64(s.cache), to_f64(s.q_abs))
+    assert_close(to_f64(s.o_lat), ref, w.dtype, f"o_lat {name}")
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_end_to_end_vs_naive_oracle(name):
+    w = SMALL[name]()
+    s = MlaDecodeStep(w, device=DEV)
+    s.populate()
+    got = to_f64(s.step())
+    torch.cuda.synchronize()
+    assert s.device_status()[0][0] == 0
+    assert_close(got, ref_out(w), w.dtype, f"out {name}")
+
+
+@pytest.mark.parametrize("seq_len", [1, 256, 1024])
+def test_v2lite_decode(seq_len):
+    w = W.v2lite(seq_len)
+    s = MlaDecodeStep(w, device=DEV)
+    s.populate()
+    assert_close(to_f64(s.step()), ref_out(w), "bf16", f"v2lite L={seq_len}")
+
+
+def test_tiny_fp32_meets_page_bar():
+    w = W.tiny()
+    s = MlaDecodeStep(w, device=DEV)
+    s.populate()
+    max_abs, _ = errors(to_f64(s.step()), ref_out(w))
+    assert max_abs <= 1e-4
+
+
+def test_block_table_permutation_gives_identical_bits():
+    a = W.make("perm", [300, 129, 64], [1] * 3, 16, 64, "bf16", seed=41, extra_blocks=4)
+    b = W.make("perm", [300, 129, 64], [1] * 3, 16, 64, "bf16", seed=41, extra_blocks=4)
+    rng = np.random.default_rng(99)
+    perm = rng.permutation(b.num_blocks).astype(np.int32)
+    bt = b.block_table.copy()
+    bt[bt >= 0] = perm[bt[bt >= 0]]
+    b.block_table = bt
+    b.slot_mapping = bt[b.token_seq, b.kv_positions // 64].astype(np.int64) * 64 + b.kv_positions % 64
+    outs = []
+    for w in (a, b):
+        s = MlaDecodeStep(w, device=DEV, num_ctas=5)
+        s.populate()
+        outs.append(s.step().clone())
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+
+
+@pytest.mark.parametrize("num_ctas", [1, 3, 64, 0, 500])
+def test_split_count_does_not_change_the_result(num_ctas):
+    w = W.make("splits", [2000, 1, 333, 64], [1, 1, 1, 1], 16, 64, "bf16", seed=42)
+    s = MlaDecodeStep(w, device=DEV, num_ctas=num_ctas)
+    s.populate()
+    got = to_f64(s.step())
+    assert_close(got, ref_out(w), "bf16", f"num_ctas={num_ctas}")
+
+
+# ---------------------------------------------------------------------------
+# device-side errors: reported, skipped, no fault
+# ---------------------------------------------------------------------------
+
+def test_bad_block_entry_is_reported_and_skipped():
+    w = W.make("badblk", [200, 100], [1, 1], 16, 64, "bf16", seed=43)
+    s = MlaDecodeStep(w, device=DEV)
+    s.populate()
+    bt = s.block_table.clone()
+    s.block_table[0, 1] = w.num_blocks + 7          # out of range
+    s.step()
+    (st, bits), _ = s.device_status()
+    assert st == 6 and bits & L.DEV_BAD_BLOCK
+    got = to_f64(s.out)
+    # the untouched sequence is still exact
+    assert_close(got[1:2], ref_out(w, seqs=[1])[1:2], "bf16", "other sequence")
+    assert np.all(np.isfinite(got))
+    s.block_table.copy_(bt)
+    s.step()
+    assert s.device_status()[0][0] == 0
+
+
+def test_query_longer_than_sequence_is_reported():
+    w = W.make("badseq", [50, 60], [1, 1], 16, 64, "bf16", seed=44)
+    s = MlaDecodeStep(w, device=DEV)
+    s.populate()
+    s.seq_lens[0] = 0                                 # one query row, zero tokens
+    s.step()
+    (st, bits), _ = s.device_status()
+    assert st == 7 and bits & L.DEV_BAD_SEQ
+    out = to_f64(s.out)
+    assert np.all(out[0] == 0)
+    assert_close(out[1:2], ref_out(w, seqs=[1])[1:2], "bf16", "other sequence")
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    word = torch.zeros(1, dtype=torch.int32, device=DEV)
+    L.mla_selftest_wait_timeout(word, 20_000_000)    # 20 ms
+    st, bits = L.mla_get_device_status(word)
+    assert st == 5 and bits == L.DEV_TIMEOUT
+    w = W.tiny()
+    s = MlaDecodeStep(w, device=DEV)
+    s.populate()
+    max_abs, _ = errors(to_f64(s.step()), ref_out(w))
+    assert max_abs <= 1e-4
