@@ -165,6 +165,26 @@ mla_status mla_decode_paged(const mla_config* cfg, const void* q_abs, const void
                             void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * mla_decode_plan + mla_decode_planned -- mla_decode_paged in two calls.
+ * mla_decode_paged is exactly mla_decode_plan followed by mla_decode_planned.
+ * The plan (the split-KV partition for the given seq_lens/query_start_loc,
+ * in the workspace) depends only on the batch layout, not on the layer, so a
+ * caller decoding many layers of one step can plan once and run
+ * mla_decode_planned per layer, each with its own workspace copy of the plan
+ * or one workspace per layer planned once. mla_decode_planned reads no
+ * seq_lens: it follows the plan; a workspace planned for another num_q, head
+ * count or CTA count yields zero partials (combine then outputs zeros).
+ */
+mla_status mla_decode_plan(const mla_config* cfg, const int32_t* seq_lens,
+                           const int32_t* query_start_loc, int32_t batch, int64_t num_q,
+                           int32_t max_blocks_per_seq, void* workspace, size_t ws_bytes,
+                           void* stream);
+mla_status mla_decode_planned(const mla_config* cfg, const void* q_abs, const void* cache,
+                              int64_t num_blocks, const int32_t* block_table,
+                              int32_t max_blocks_per_seq, int64_t num_q, void* workspace,
+                              size_t ws_bytes, void* stream);
+
+/*
  * mla_combine -- merge the split partials of mla_decode_paged.
  * For each (n, h): M = max_s lse_s, o_lat = sum_s 2^(lse_s - M) o_s /
  * sum_s 2^(lse_s - M) (the split-softmax identity; lse is kept in base 2

@@ -165,6 +165,61 @@ mla_status mla_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
   return from_cuda(cudaMemsetAsync(workspace, 0, sizeof(WsHeader), as_stream(stream)));
 }
 
+mla_status mla_decode_plan(const mla_config* cfg, const int32_t* seq_lens,
+                           const int32_t* query_start_loc, int32_t batch, int64_t num_q,
+                           int32_t max_blocks_per_seq, void* workspace, size_t ws_bytes,
+                           void* stream) {
+  mla_status s = check_cfg(cfg);
+  if (s != MLA_OK) return s;
+  if (num_q < 0 || batch < 0 || max_blocks_per_seq < 0) return MLA_ERR_INVALID_ARGUMENT;
+  if (num_q > kMaxRows) return MLA_ERR_UNSUPPORTED;
+  if (!workspace || !aligned(workspace, 256)) return MLA_ERR_INVALID_ARGUMENT;
+  if (num_q == 0) return MLA_OK;
+  if (!seq_lens || !query_start_loc || batch == 0) return MLA_ERR_INVALID_ARGUMENT;
+  if (!aligned(seq_lens, 4) || !aligned(query_start_loc, 4)) return MLA_ERR_INVALID_ARGUMENT;
+  const int C = resolve_num_ctas(cfg);
+  if (C <= 0) return MLA_ERR_CUDA;
+  const int G = cfg->num_heads / kHG;
+  if (ws_bytes < ws_layout(num_q, G, C).total) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  PlanArgs pa{seq_lens, query_start_loc, batch, (int32_t)num_q, G, C, cfg->block_size,
+              max_blocks_per_seq, workspace};
+  return from_cuda(launch_plan(pa, as_stream(stream)));
+}
+
+mla_status mla_decode_planned(const mla_config* cfg, const void* q_abs, const void* cache,
+                              int64_t num_blocks, const int32_t* block_table,
+                              int32_t max_blocks_per_seq, int64_t num_q, void* workspace,
+                              size_t ws_bytes, void* stream) {
+  mla_status s = check_cfg(cfg);
+  if (s != MLA_OK) return s;
+  if (num_q < 0 || num_blocks < 0 || max_blocks_per_seq < 0) return MLA_ERR_INVALID_ARGUMENT;
+  if (num_q > kMaxRows) return MLA_ERR_UNSUPPORTED;
+  if (num_blocks * cfg->block_size > ((int64_t)1 << 31)) return MLA_ERR_UNSUPPORTED;
+  if (!workspace || !aligned(workspace, 256)) return MLA_ERR_INVALID_ARGUMENT;
+  if (num_q == 0) return MLA_OK;
+  if (!q_abs || !cache || !block_table) return MLA_ERR_INVALID_ARGUMENT;
+  if (!aligned(q_abs, 16) || !aligned(cache, 16) || !aligned(block_table, 4))
+    return MLA_ERR_INVALID_ARGUMENT;
+  const int C = resolve_num_ctas(cfg);
+  if (C <= 0) return MLA_ERR_CUDA;
+  const int G = cfg->num_heads / kHG;
+  if (ws_bytes < ws_layout(num_q, G, C).total) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = as_stream(stream);
+  const double log2e = 1.4426950408889634;
+  DecodeArgs da{q_abs, cache, num_blocks, block_table, max_blocks_per_seq, cfg->block_size,
+                cfg->num_heads, G, C, num_q, (float)(cfg->softmax_scale * log2e), workspace};
+  if (cfg->dtype == MLA_F32) return from_cuda(launch_decode_f32(da, st));
+  // With num_blocks == 0 every block id is rejected before any copy, so the
+  // map below is never used to read; it still needs a non-empty extent.
+  const uint64_t map_rows = num_blocks > 0 ? (uint64_t)num_blocks * cfg->block_size
+                                           : (uint64_t)cfg->block_size;
+  CUtensorMap cache_map, q_map;
+  if (!make_row_map(&cache_map, cache, map_rows, (uint32_t)cfg->block_size) ||
+      !make_row_map(&q_map, q_abs, (uint64_t)num_q * cfg->num_heads, kHG))
+    return MLA_ERR_CUDA;
+  return from_cuda(launch_decode_bf16(da, cache_map, q_map, st));
+}
+
 mla_status mla_decode_paged(const mla_config* cfg, const void* q_abs, const void* cache,
                             int64_t num_blocks, const int32_t* block_table,
                             int32_t max_blocks_per_seq, const int32_t* seq_lens,
@@ -180,34 +235,13 @@ mla_status mla_decode_paged(const mla_config* cfg, const void* q_abs, const void
   if (num_q == 0) return MLA_OK;
   if (!q_abs || !cache || !block_table || !seq_lens || !query_start_loc || batch == 0)
     return MLA_ERR_INVALID_ARGUMENT;
-  if (!aligned(q_abs, 16) || !aligned(cache, 16) || !aligned(block_table, 4) ||
-      !aligned(seq_lens, 4) || !aligned(query_start_loc, 4))
+  if (!aligned(q_abs, 16) || !aligned(cache, 16) || !aligned(block_table, 4))
     return MLA_ERR_INVALID_ARGUMENT;
-  const int C = resolve_num_ctas(cfg);
-  if (C <= 0) return MLA_ERR_CUDA;
-  const int G = cfg->num_heads / kHG;
-  if (ws_bytes < ws_layout(num_q, G, C).total) return MLA_ERR_WORKSPACE_TOO_SMALL;
-  cudaStream_t st = as_stream(stream);
-
-  PlanArgs pa{seq_lens, query_start_loc, batch, (int32_t)num_q, G, C, cfg->block_size,
-              max_blocks_per_seq, workspace};
-  cudaError_t e = launch_plan(pa, st);
-  if (e != cudaSuccess) return MLA_ERR_CUDA;
-
-  const double log2e = 1.4426950408889634;
-  DecodeArgs da{q_abs, cache, num_blocks, block_table, max_blocks_per_seq, cfg->block_size,
-                cfg->num_heads, G, C, num_q, (float)(cfg->softmax_scale * log2e), workspace};
-  if (cfg->dtype == MLA_F32) return from_cuda(launch_decode_f32(da, st));
-  // With num_blocks == 0 every block id is rejected before any copy, so the
-  // map below is never used to read; it still needs a non-empty extent.
-  const uint64_t map_rows = num_blocks > 0 ? (uint64_t)num_blocks * cfg->block_size
-                                           : (uint64_t)cfg->block_size;
-  CUtensorMap cache_map, q_map;
-  if (!make_row_map(&cache_map, cache, map_rows,
-                    (uint32_t)cfg->block_size) ||
-      !make_row_map(&q_map, q_abs, (uint64_t)num_q * cfg->num_heads, kHG))
-    return MLA_ERR_CUDA;
-  return from_cuda(launch_decode_bf16(da, cache_map, q_map, st));
+  s = mla_decode_plan(cfg, seq_lens, query_start_loc, batch, num_q, max_blocks_per_seq, workspace,
+                      ws_bytes, stream);
+  if (s != MLA_OK) return s;
+  return mla_decode_planned(cfg, q_abs, cache, num_blocks, block_table, max_blocks_per_seq, num_q,
+                            workspace, ws_bytes, stream);
 }
 
 mla_status mla_combine(const mla_config* cfg, const void* workspace, size_t ws_bytes,

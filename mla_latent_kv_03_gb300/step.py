@@ -93,6 +93,14 @@ class MlaDecodeStep:
         L.mla_decode_paged(self.cfg, self.q_abs, self.cache, self.block_table, self.seq_lens,
                            self.query_start_loc, self.workspace, stream=stream)
 
+    def plan(self, stream=None) -> None:
+        L.mla_decode_plan(self.cfg, self.seq_lens, self.query_start_loc, self.w.num_q,
+                          self.block_table.shape[1], self.workspace, stream=stream)
+
+    def decode_planned(self, stream=None) -> None:
+        L.mla_decode_planned(self.cfg, self.q_abs, self.cache, self.block_table, self.workspace,
+                             stream=stream)
+
     def combine(self, stream=None) -> None:
         L.mla_combine(self.cfg, self.workspace, self.w.batch, self.o_lat, stream=stream)
 
