@@ -1,0 +1,536 @@
+#!/usr/bin/env python
+"""Benchmark of the MLA paged latent decode step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload serving|ragged_h128|mixed|v2lite_1024|...]
+
+A step is one pass of the whole hot path over one batch: mla_absorb_q,
+mla_decode_plan, mla_decode_planned, mla_combine and mla_out_proj (plus
+mla_cache_write of the step's new tokens for the mixed workload). The default
+workload is the serving batch: 64 sequences x 4,096 tokens, 16 heads, bf16,
+block_size 64, a 301,989,888-byte latent cache (larger than L2, so every step
+reads it from HBM). Inputs are seeded synthetic data with the shapes of
+DeepSeek-V2-Lite's attention layer.
+
+`value` is latent-cache GB/s of the whole step (latent bytes / step time) with
+inputs resident in HBM; `e2e` repeats it through the same calls with the
+step's inputs copied from pinned host memory and the output copied back
+inside the timed region. `roofline` reports the decode kernel alone against
+the measured HBM copy bandwidth. `cpu_baseline` times the fp64 oracle on a
+bounded sample of the same workload on the host cores.
+
+Under torchrun each rank runs its own independent batch (the sequences of a
+batch are independent, so the work shards with no collective): scaling is
+weak and `value` is the sum over ranks divided by the slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MLA paged decode: latent-cache GB/s (% of HBM peak), µs/step at B=64,L=4096"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+DECODE_SOURCES = ["decode_bf16.cu", "common.cuh", "sched.cuh"]
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_bf16_serving_B64_L4096.md")
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="serving")
+    p.add_argument("--e2e-steps", type=int, default=500)
+    p.add_argument("--kernel-launches", type=int, default=1000)
+    p.add_argument("--cpu-seconds", type=float, default=15.0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# process group (one process per GPU under torchrun)
+# ---------------------------------------------------------------------------
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# peaks, clocks, profile summary
+# ---------------------------------------------------------------------------
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        return rows
+
+    @staticmethod
+    def summarise(rows, t0: float, t1: float):
+        if not rows:
+            return None
+        import datetime
+        sel = []
+        for r in rows:
+            try:
+                ts = datetime.datetime.strptime(r[0].strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except Exception:
+                continue
+            if t0 - 0.06 <= ts <= t1 + 0.06:
+                sel.append(r)
+        use = sel if sel else rows
+        sm = [float(r[2]) for r in use if r[2].strip().replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in use if r[3].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i in range(4)
+                          if len(r) > 6 + i and r[6 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(use), "samples_in_window": len(sel)}
+
+
+def decode_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in DECODE_SOURCES:
+        with open(os.path.join(ROOT, "mla_latent_kv_03_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per decode launch from the committed ncu summary, or None if
+    the decode kernel's sources changed since it was taken."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("source_sha256") != decode_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch_full_size"].replace(",", ""))
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# workloads and the CPU oracle sample
+# ---------------------------------------------------------------------------
+
+def make_workload(name: str, rank: int):
+    from mla_latent_kv_03_gb300 import workloads as W
+    if name == "serving":
+        return W.serving(seed=3 + 1000 * rank)
+    if name == "serving_b32":   # the same kernel on half the batch (151 MB > L2), for ncu
+        return W.serving(seed=3 + 1000 * rank, batch=32)
+    if name == "ragged_h128":
+        return W.ragged_h128(seed=4 + 1000 * rank)
+    if name == "mixed":
+        return W.mixed(seed=5 + 1000 * rank)
+    if name.startswith("v2lite_"):
+        return W.v2lite(int(name.split("_")[1]), seed=2 + 1000 * rank)
+    if name == "tiny":
+        return W.tiny()
+    raise SystemExit(f"unknown workload {name}")
+
+
+def step_latent_bytes(w) -> int:
+    """Latent-cache bytes one step reads: every visible row once per head group."""
+    import numpy as np
+    elem = 2 if w.dtype == "bf16" else 4
+    vis = 0
+    for b in range(w.batch):
+        qr = w.q_range(b)
+        if qr.stop > qr.start:
+            vis += int(w.seq_lens[b])   # the last row sees every token; rows share tiles
+    groups = w.num_heads // 16
+    del np
+    return vis * 576 * elem * groups
+
+
+def oracle_pair_seconds(w, pairs, prefix=None):
+    """Run the naive fp64 oracle on (sequence, head) pairs; return seconds.
+    With `prefix`, only the first `prefix` tokens of each sequence are used
+    (the query then sits at the end of that prefix)."""
+    from oracle import mla_oracle as O
+    t0 = time.perf_counter()
+    for b, h in pairs:
+        tr, qr = w.token_range(b), w.q_range(b)
+        if prefix is not None and prefix < tr.stop - tr.start:
+            tr = slice(tr.start, tr.start + prefix)
+            O.mla_sequence_naive(w.c_kv_raw[tr], w.k_pe_raw[tr], w.kv_positions[tr],
+                                 w.q_nope[qr][-1:, h:h + 1], w.q_pe[qr][-1:, h:h + 1],
+                                 [prefix - 1], w.W_uk[h:h + 1], w.W_uv[h:h + 1], w.rms_weight,
+                                 w.rms_eps, w.rope_base, w.softmax_scale)
+            continue
+        O.mla_sequence_naive(w.c_kv_raw[tr], w.k_pe_raw[tr], w.kv_positions[tr],
+                             w.q_nope[qr][:, h:h + 1], w.q_pe[qr][:, h:h + 1], w.q_positions[qr],
+                             w.W_uk[h:h + 1], w.W_uv[h:h + 1], w.rms_weight, w.rms_eps,
+                             w.rope_base, w.softmax_scale)
+    return time.perf_counter() - t0
+
+
+def pair_latent_bytes(w, pairs, prefix=None) -> float:
+    """Latent bytes a (sequence, head) pair stands for: the sequence's rows
+    divided among its heads (a step reads each row once for all heads)."""
+    elem = 2 if w.dtype == "bf16" else 4
+    rows = lambda b: min(int(w.seq_lens[b]), prefix) if prefix else int(w.seq_lens[b])  # noqa: E731
+    return sum(rows(b) * 576 * elem / w.num_heads for b, _ in pairs)
+
+
+def sample_pairs(w, seed=0):
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    seqs = [b for b in range(w.batch) if w.q_range(b).stop > w.q_range(b).start]
+    while True:
+        b = int(rng.choice(seqs))
+        yield b, int(rng.integers(w.num_heads))
+
+
+def cpu_baseline(w, seconds: float):
+    """The oracle as it stands, on a bounded sample: (sequence, head) pairs
+    drawn at random until `seconds` of host time are spent."""
+    cores = len(os.sched_getaffinity(0))
+    gen = sample_pairs(w)
+    pairs, spent = [], 0.0
+    while spent < seconds or not pairs:
+        p = [next(gen)]
+        spent += oracle_pair_seconds(w, p)
+        pairs += p
+    gbs = pair_latent_bytes(w, pairs) / spent / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{len(pairs)} random (sequence, head) pairs of {w.name}, naive fp64 form "
+                      f"(K and V expanded per head), {spent:.1f} s host time; latent bytes "
+                      f"counted as the sequence's rows / {w.num_heads} heads per pair"}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, world, rank, local):
+    import torch
+    from mla_latent_kv_03_gb300 import libmla as L
+    from mla_latent_kv_03_gb300.step import MlaDecodeStep
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU for --impl ours")
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    L.load()
+    w = make_workload(args.workload, rank)
+    mixed = bool(w.is_new.sum() > w.batch)   # a step that writes more than one token per sequence
+    s = MlaDecodeStep(w, device=dev)
+    s.populate(include_new=not mixed)
+    torch.cuda.synchronize()
+    latent = step_latent_bytes(w)
+    stream = torch.cuda.Stream(device=dev)
+
+    def one_step():
+        if mixed:
+            s.write_new()
+        s.absorb()
+        s.plan()
+        s.decode_planned()
+        s.combine()
+        s.out_proj()
+
+    launches_per_step = 5 + (1 if mixed else 0)
+    # eager warm-up (also builds the lazy state), then capture one step
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            one_step()
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        one_step()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    stream.synchronize()
+
+    # ---- timed region: K steps, inputs resident in HBM
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record(stream)
+    e1.synchronize()
+    t_wall1 = time.time()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = ClockSampler.summarise(sampler.stop(), t_wall0, t_wall1)
+    ms = e0.elapsed_time(e1)
+    ms_max = max_over_ranks(ms, world)
+    total_bytes = sum_over_ranks(float(latent) * args.steps, world)
+    value = total_bytes / (ms_max * 1e-3) / 1e9
+    ms_per_step = ms_max / args.steps
+
+    # ---- decode kernel alone: back-to-back launches, CUDA events on its stream
+    per_graph = 20
+    kgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(kgraph, stream=stream):
+        for _ in range(per_graph):
+            s.decode_planned()
+    reps = max(1, args.kernel_launches // per_graph)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            kgraph.replay()
+    stream.synchronize()
+    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        k0.record(stream)
+        for _ in range(reps):
+            kgraph.replay()
+        k1.record(stream)
+    k1.synchronize()
+    kernel_ms = k0.elapsed_time(k1) / (reps * per_graph)
+    decode_bytes = latent + int(w.block_table.size) * 4
+    peak, peak_kind = hbm_peak()
+    achieved = decode_bytes / (kernel_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
+                "kernel": "decode_bf16_kernel" if w.dtype == "bf16" else "decode_f32_kernel",
+                "kernel_us": round(kernel_ms * 1e3, 2), "algorithmic_bytes": decode_bytes,
+                "peak_kind": f"{peak_kind} HBM copy bandwidth (burst)",
+                "frac_of_nominal_8TBs": round(achieved / NOMINAL_HBM_GBS, 4)}
+
+    # ---- end to end through the same calls, host buffers, eager launches
+    e2e = run_e2e(args, s, w, stream, latent, world, mixed)
+
+    # ---- status: the timed work must not have flagged anything
+    (st1, bits1), (st2, bits2) = s.device_status()
+    if st1 != 0 or st2 != 0:
+        raise SystemExit(f"device status after bench: decode {bits1:#x}, cache write {bits2:#x}")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic (seeded; shapes of DeepSeek-V2-Lite attention)",
+            "config": {"workload": w.name, "batch": w.batch, "num_heads": w.num_heads,
+                       "seq_lens": "all 4096" if args.workload == "serving" else "see workload",
+                       "block_size": w.block_size, "latent_bytes_per_step": latent,
+                       "l2": "inputs larger than L2: the latent cache read each step exceeds 129 MB",
+                       "graph": "one step captured in a CUDA graph, replayed K times",
+                       "parallelism": f"replicas x{world} (independent batches per GPU)"},
+            "us_per_step": round(ms_per_step * 1e3, 2),
+            "tokens_per_s": round(w.num_q * world / (ms_per_step * 1e-3), 1),
+            "pct_of_nominal_8TBs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+            "pct_of_measured_hbm": round(100 * value / world / peak, 2),
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, s, w, stream, latent, world, mixed):
+    """Same step through the public calls, eager launches, with this step's
+    inputs copied from pinned host memory and the output copied back."""
+    import torch
+    ins = [s.q_nope, s.q_pe, s.q_positions, s.seq_lens, s.query_start_loc, s.block_table]
+    if mixed:
+        ins += [s.c_kv_new, s.k_pe_new, s.pos_new, s.slot_new]
+    host_in = [t.detach().cpu().pin_memory() for t in ins]
+    host_out = torch.empty(s.out.shape, dtype=s.out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+
+    def one():
+        for d, h in zip(ins, host_in):
+            d.copy_(h, non_blocking=True)
+        if mixed:
+            s.write_new()
+        s.absorb()
+        s.plan()
+        s.decode_planned()
+        s.combine()
+        s.out_proj()
+        host_out.copy_(s.out, non_blocking=True)
+
+    n = max(1, args.e2e_steps)
+    with torch.cuda.stream(stream):
+        for _ in range(5):
+            one()
+    stream.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(n):
+            one()
+        e1.record(stream)
+    e1.synchronize()
+    barrier(world)
+    ms = max_over_ranks(e0.elapsed_time(e1), world)
+    total = sum_over_ranks(float(latent) * n, world)
+    return {"value": round(total / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "us_per_step": round(ms / n * 1e3, 2), "launch": "eager (no graph)"}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the fp64 oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    w = make_workload(args.workload, 0)
+    cores = len(os.sched_getaffinity(0))
+    gen = sample_pairs(w, seed=1)
+    # size each step's sample so the whole run stays within about two minutes
+    probe = [next(gen)]
+    t_pair = oracle_pair_seconds(w, probe)
+    n_steps = args.steps + args.warmup
+    per_step = max(1, int(120.0 / max(t_pair * n_steps, 1e-9)))
+    prefix = None
+    if t_pair * n_steps > 150.0:   # even one pair per step is too long: use a token prefix
+        prefix = max(64, int(int(w.seq_lens.max()) * 150.0 / (t_pair * n_steps)))
+    for _ in range(args.warmup):
+        oracle_pair_seconds(w, [next(gen) for _ in range(per_step)], prefix)
+    spent, pairs = 0.0, []
+    for _ in range(args.steps):
+        p = [next(gen) for _ in range(per_step)]
+        spent += oracle_pair_seconds(w, p, prefix)
+        pairs += p
+    value = pair_latent_bytes(w, pairs, prefix) / spent / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(spent / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "num_heads": w.num_heads,
+                   "block_size": w.block_size},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{per_step} random (sequence, head) pair(s) per step of "
+                                   f"{w.name}, naive fp64 form"
+                                   + (f", first {prefix} tokens of each" if prefix else "")},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    world, rank, local = dist_setup()
+    if world != args.gpus and world > 1:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE {world}")
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
