@@ -6,9 +6,10 @@
 // (kv_a_layernorm before kv_b_proj), pitfall 3, and "MLA 的数学结构"
 // (K_pe = x W_kr + RoPE, shared by all heads).
 //
-// One warp per token. Lane l holds latent values [16l, 16l+16) and the RoPE
-// pair (l, l+32). HBM-bound: reads 1,152 (bf16) bytes and writes 1,152 per
-// token; 8 warps per CTA, grid-stride over tokens.
+// One warp per token. Lane l holds latent values [16l, 16l+16) (16-byte
+// vector loads and stores) and the RoPE pair (l, l+32). HBM-bound: reads and
+// writes 1,152 bytes per token (bf16); 8 warps per CTA, grid-stride.
+#include "async_copy.cuh"
 #include "common.cuh"
 #include "internal.h"
 
@@ -16,13 +17,54 @@ namespace mla {
 namespace {
 
 template <typename T>
+struct Vec16;  // 16 values of T as 16-byte vectors
+template <>
+struct Vec16<__nv_bfloat16> {
+  uint4 v[2];
+  __device__ __forceinline__ void load(const __nv_bfloat16* p) {
+    v[0] = reinterpret_cast<const uint4*>(p)[0];
+    v[1] = reinterpret_cast<const uint4*>(p)[1];
+  }
+  __device__ __forceinline__ float get(int i) const {
+    const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(v);
+    return __bfloat162float(e[i]);
+  }
+  __device__ __forceinline__ void set(int i, float x) {
+    reinterpret_cast<__nv_bfloat16*>(v)[i] = __float2bfloat16_rn(x);
+  }
+  __device__ __forceinline__ void store(__nv_bfloat16* p) const {
+    reinterpret_cast<uint4*>(p)[0] = v[0];
+    reinterpret_cast<uint4*>(p)[1] = v[1];
+  }
+};
+template <>
+struct Vec16<float> {
+  float4 v[4];
+  __device__ __forceinline__ void load(const float* p) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = reinterpret_cast<const float4*>(p)[i];
+  }
+  __device__ __forceinline__ float get(int i) const { return reinterpret_cast<const float*>(v)[i]; }
+  __device__ __forceinline__ void set(int i, float x) { reinterpret_cast<float*>(v)[i] = x; }
+  __device__ __forceinline__ void store(float* p) const {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) reinterpret_cast<float4*>(p)[i] = v[i];
+  }
+};
+
+template <typename T>
 __global__ void __launch_bounds__(256) cache_write_kernel(
     const T* __restrict__ c_kv, const T* __restrict__ k_pe, const int32_t* __restrict__ positions,
     const int64_t* __restrict__ slot_mapping, int64_t num_tokens, const T* __restrict__ w,
-    T* __restrict__ cache, int64_t num_slots, float eps, double base, uint32_t* status) {
+    T* __restrict__ cache, int64_t num_slots, float eps, RopeFreq freq, uint32_t* status) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  Vec16<T> wv;
+  wv.load(w + lane * 16);
+  const float fhi = freq.hi[lane], flo = freq.lo[lane];
   for (int64_t t = warp0; t < num_tokens; t += nwarps) {
     const int64_t slot = slot_mapping[t];
     if (slot < 0) continue;  // padding token
@@ -30,28 +72,24 @@ __global__ void __launch_bounds__(256) cache_write_kernel(
       if (lane == 0) set_status(status, MLA_DEV_BAD_SLOT);
       continue;
     }
-    // latent: 16 consecutive values per lane
-    float x[16];
-    const T* src = c_kv + t * kDc + lane * 16;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = to_f32(src[i]);
+    Vec16<T> x;
+    x.load(c_kv + t * kDc + lane * 16);
+    const T* kp = k_pe + t * kDr;
+    const float x1 = to_f32(kp[lane]), x2 = to_f32(kp[lane + 32]);
+    const int pos = positions[t];
     float ss = 0.f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) ss = fmaf(x[i], x[i], ss);
+    for (int i = 0; i < 16; ++i) ss = fmaf(x.get(i), x.get(i), ss);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     const float r = 1.0f / sqrtf(ss * (1.0f / kDc) + eps);
-    T* dst = cache + slot * kRow;
+    Vec16<T> y;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int c = lane * 16 + i;
-      dst[c] = from_f32<T>(x[i] * r * to_f32(w[c]));
-    }
-    // rope: pair (lane, lane + 32)
-    const T* kp = k_pe + t * kDr;
-    const float x1 = to_f32(kp[lane]), x2 = to_f32(kp[lane + 32]);
+    for (int i = 0; i < 16; ++i) y.set(i, x.get(i) * r * wv.get(i));
+    T* dst = cache + slot * kRow;
+    y.store(dst + lane * 16);
     float cs, sn;
-    rope_cos_sin(positions[t], lane, kDr, base, &cs, &sn);
+    rope_cos_sin(pos, fhi, flo, &cs, &sn);
     dst[kDc + lane] = from_f32<T>(x1 * cs - x2 * sn);
     dst[kDc + lane + 32] = from_f32<T>(x2 * cs + x1 * sn);
   }
@@ -68,16 +106,17 @@ cudaError_t launch_cache_write(const mla_config& cfg, const void* c_kv, const vo
   int64_t blocks = (num_tokens + 7) / 8;
   if (blocks > 4096) blocks = 4096;
   const int64_t num_slots = num_blocks * cfg.block_size;
+  const RopeFreq freq = make_rope_freq((double)cfg.rope_base);
   if (cfg.dtype == MLA_BF16) {
-    cache_write_kernel<__nv_bfloat16><<<(unsigned)blocks, threads, 0, stream>>>(
-        (const __nv_bfloat16*)c_kv, (const __nv_bfloat16*)k_pe, positions, slot_mapping,
-        num_tokens, (const __nv_bfloat16*)rms_weight, (__nv_bfloat16*)cache, num_slots,
-        cfg.rms_eps, (double)cfg.rope_base, dev_status);
+    return launch_pdl(cache_write_kernel<__nv_bfloat16>, dim3((unsigned)blocks), dim3(threads), 0,
+                      stream, (const __nv_bfloat16*)c_kv, (const __nv_bfloat16*)k_pe, positions,
+                      slot_mapping, num_tokens, (const __nv_bfloat16*)rms_weight,
+                      (__nv_bfloat16*)cache, num_slots, cfg.rms_eps, freq, dev_status);
   } else {
-    cache_write_kernel<float><<<(unsigned)blocks, threads, 0, stream>>>(
-        (const float*)c_kv, (const float*)k_pe, positions, slot_mapping, num_tokens,
-        (const float*)rms_weight, (float*)cache, num_slots, cfg.rms_eps, (double)cfg.rope_base,
-        dev_status);
+    return launch_pdl(cache_write_kernel<float>, dim3((unsigned)blocks), dim3(threads), 0, stream,
+                      (const float*)c_kv, (const float*)k_pe, positions, slot_mapping, num_tokens,
+                      (const float*)rms_weight, (float*)cache, num_slots, cfg.rms_eps, freq,
+                      dev_status);
   }
   return cudaGetLastError();
 }

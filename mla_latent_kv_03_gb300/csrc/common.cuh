@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cmath>
+
 #include "../../include/mla.h"
 
 namespace mla {
@@ -204,15 +206,38 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
   return __float2bfloat16_rn(x);
 }
 
-// RoPE inverse frequency and angle, in fp64 so long positions keep their
-// precision: angle = pos * base^(-2i/d).
-__device__ __forceinline__ void rope_cos_sin(int pos, int i, int d, double base, float* c,
-                                             float* s) {
-  const double inv_freq = pow(base, -2.0 * (double)i / (double)d);
-  double sd, cd;
-  sincos((double)pos * inv_freq, &sd, &cd);
-  *c = (float)cd;
-  *s = (float)sd;
+// RoPE inverse frequencies inv_freq_i = base^(-2i/64), i < 32, computed on
+// the host in double and passed as an unevaluated float sum hi + lo.
+struct RopeFreq {
+  float hi[32];
+  float lo[32];
+};
+
+inline RopeFreq make_rope_freq(double base) {
+  RopeFreq f;
+  for (int i = 0; i < 32; ++i) {
+    const double v = std::pow(base, -2.0 * i / 64.0);
+    f.hi[i] = (float)v;
+    f.lo[i] = (float)(v - (double)f.hi[i]);
+  }
+  return f;
+}
+
+// cos and sin of pos * inv_freq without fp64 arithmetic (GB300's fp64 rate is
+// a small fraction of fp32). The product is formed exactly as a + e + tail
+// (FMA two-product, Dekker/Kahan), then reduced modulo 2*pi by Cody-Waite
+// additive reduction with 2*pi split into two floats, so |r| <= pi with an
+// absolute error of a few 1e-7 even at positions near 2^15; sincosf finishes.
+__device__ __forceinline__ void rope_cos_sin(int pos, float hi, float lo, float* c, float* s) {
+  const float p = (float)pos;                  // exact for |pos| < 2^24
+  const float a = p * hi;
+  const float e = fmaf(p, hi, -a);             // rounding error of p * hi, exactly
+  const float tail = fmaf(p, lo, e);
+  const float k = rintf(a * 0.159154943091895336f);          // a / (2 pi)
+  float r = fmaf(-k, 6.28318548202514648f, a);               // 2 pi, leading float
+  r = fmaf(-k, -1.74845553146951715e-07f, r);                // 2 pi - leading float
+  r += tail;
+  sincosf(r, s, c);
 }
 
 }  // namespace mla

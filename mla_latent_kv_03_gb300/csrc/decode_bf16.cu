@@ -21,6 +21,7 @@
 // Every wait is bounded; a timeout sets MLA_DEV_TIMEOUT, all math warps leave
 // together, and the producer waits (bounded) for its copies in flight before
 // the CTA exits.
+#include "async_copy.cuh"
 #include "common.cuh"
 #include "internal.h"
 #include "sched.cuh"
@@ -94,7 +95,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_mbar_init();
   }
+  if (warp == kMathWarps && lane == 0) {
+    prefetch_tensormap(&cache_map);
+    prefetch_tensormap(&q_map);
+  }
   __syncthreads();
+  // the plan and q_abs come from earlier kernels
+  pdl_wait();
+  pdl_launch_dependents();
 
   SchedWalker sw;
   const bool has_work = sw.init(ws, a.num_q, a.groups, a.num_ctas, blockIdx.x);
@@ -104,8 +112,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMathWarps) {
     // ------------------------------------------------------------ producer
     if (lane != 0) return;
-    prefetch_tensormap(&cache_map);
-    prefetch_tensormap(&q_map);
     int fills[NST];
 #pragma unroll
     for (int i = 0; i < NST; ++i) fills[i] = 0;
@@ -359,8 +365,8 @@ cudaError_t launch_decode_bf16(const DecodeArgs& a, const CUtensorMap& cache_map
   cudaError_t e = cudaFuncSetAttribute(decode_bf16_kernel<NST>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  decode_bf16_kernel<NST><<<a.num_ctas, kThreads, smem, stream>>>(cache_map, q_map, a);
-  return cudaGetLastError();
+  return launch_pdl(decode_bf16_kernel<NST>, dim3(a.num_ctas), dim3(kThreads), smem, stream,
+                    cache_map, q_map, a);
 }
 
 }  // namespace mla

@@ -11,6 +11,7 @@
 // Combine follows the split-softmax identity (flash-decoding): for partials
 // o_s (normalised) with base-2 log-sum-exp lse_s,
 //   o = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M),  M = max_s lse_s.
+#include "async_copy.cuh"
 #include "common.cuh"
 #include "internal.h"
 
@@ -29,6 +30,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
   int4* row_info = reinterpret_cast<int4*>(ws + L.row_info);
   int4* cta_start = reinterpret_cast<int4*>(ws + L.cta_start);
   const int Nq = a.num_q;
+  pdl_wait();
+  pdl_launch_dependents();
 
   for (int n = tid; n < Nq; n += kPlanThreads) {
     row_info[n] = make_int4(-1, -1, 0, 0);
@@ -122,47 +125,84 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
   }
 }
 
-// grid (num_q * G, 4): 16 head rows x 128 latent dims per CTA, thread = dim.
-__global__ void __launch_bounds__(128) combine_kernel(const uint8_t* __restrict__ ws, int groups,
-                                                      int num_ctas, int64_t num_q,
-                                                      float* __restrict__ o_lat) {
+// CTA = (q-tile t = (query row n, head group g), quarter of the 512 latent
+// dims): 16 head rows x 128 dims. Threads 0-15 reduce their row's
+// log-sum-exps over the partial slots to a maximum and a reciprocal weight
+// sum; the per-(slot, row) weights are then staged in shared memory, 64 slots
+// at a time, and each thread merges 4 float4 items (row, 4 dims) with
+// independent loads over the slots.
+constexpr int kCombineThreads = 128;
+constexpr int kSlotChunk = 64;
+
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(
+    const uint8_t* __restrict__ ws, int groups, int num_ctas, int64_t num_q,
+    float* __restrict__ o_lat) {
+  __shared__ float sM[kHG], sInv[kHG];
+  __shared__ float sW[kSlotChunk][kHG];
+  pdl_wait();  // everything below reads what the decode kernel wrote
+  pdl_launch_dependents();
   const WsHeader* hdr = reinterpret_cast<const WsHeader*>(ws);
   const WsLayout L = ws_layout(num_q, groups, num_ctas);
   const int4* row_info = reinterpret_cast<const int4*>(ws + L.row_info);
   const float* lse = reinterpret_cast<const float*>(ws + L.lse);
-  const float* opart = reinterpret_cast<const float*>(ws + L.opart);
-  const int t = blockIdx.x;
+  const float4* opart = reinterpret_cast<const float4*>(ws + L.opart);
+  const int t = blockIdx.x, quarter = blockIdx.y, tid = threadIdx.x;
   const int n = t / groups, g = t % groups;
-  const int d = blockIdx.y * 128 + threadIdx.x;
   const int H = groups * kHG;
-  float* out = o_lat + ((size_t)n * H + g * kHG) * kDc + d;
-  const bool match = hdr->num_q == num_q && hdr->groups == groups && hdr->num_ctas == num_ctas;
-  const int4 ri = match ? row_info[n] : make_int4(-1, -1, 0, 0);
-  const int tiles = ri.z;
+  // item j of this thread: row (tid / 32) + 4 j, float4 column (tid % 32) of this quarter
+  const int c4 = quarter * 32 + (tid & 31);
+  float4* out = reinterpret_cast<float4*>(o_lat + ((size_t)n * H + g * kHG) * kDc);
   const bool plan_ok = hdr->magic == kMagic && hdr->num_q == num_q && hdr->groups == groups &&
                        hdr->num_ctas == num_ctas;
-  if (tiles <= 0 || !plan_ok) {
+  const int4 ri = plan_ok ? row_info[n] : make_int4(-1, -1, 0, 0);
+  const int tiles = ri.z;
+  if (tiles <= 0) {
 #pragma unroll
-    for (int r = 0; r < kHG; ++r) out[(size_t)r * kDc] = 0.f;
+    for (int j = 0; j < 4; ++j) out[((tid >> 5) + 4 * j) * (kDc / 4) + c4] = make_float4(0.f, 0.f, 0.f, 0.f);
     return;
   }
   const int share = hdr->share;
   const int U = ri.w + g * tiles;
   const int c_first = U / share, c_last = (U + tiles - 1) / share;
-  for (int r = 0; r < kHG; ++r) {
+  const int nslots = c_last - c_first + 1;
+  if (tid < kHG) {
     float M = -INFINITY;
-    for (int c = c_first; c <= c_last; ++c) M = fmaxf(M, lse[(size_t)(c + t) * kHG + r]);
-    float den = 0.f, acc = 0.f;
-    if (M != -INFINITY) {
-      for (int c = c_first; c <= c_last; ++c) {
-        const size_t slot = (size_t)(c + t);
-        const float w = fast_exp2(lse[slot * kHG + r] - M);
-        den += w;
-        acc = fmaf(w, opart[(slot * kHG + r) * kDc + d], acc);
+    for (int c = c_first; c <= c_last; ++c) M = fmaxf(M, lse[(size_t)(c + t) * kHG + tid]);
+    float den = 0.f;
+    if (M != -INFINITY)
+      for (int c = c_first; c <= c_last; ++c) den += fast_exp2(lse[(size_t)(c + t) * kHG + tid] - M);
+    sM[tid] = M;
+    sInv[tid] = den > 0.f ? 1.f / den : 0.f;
+  }
+  float4 acc[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < nslots; s0 += kSlotChunk) {
+    const int ns = min(kSlotChunk, nslots - s0);
+    __syncthreads();
+    for (int i = tid; i < ns * kHG; i += kCombineThreads) {
+      const int sl = i / kHG, r = i % kHG;
+      const float M = sM[r];
+      const size_t slot = (size_t)(c_first + s0 + sl + t);
+      sW[sl][r] = M == -INFINITY ? 0.f : fast_exp2(lse[slot * kHG + r] - M) * sInv[r];
+    }
+    __syncthreads();
+    for (int sl = 0; sl < ns; ++sl) {
+      const float4* src = opart + (size_t)(c_first + s0 + sl + t) * kHG * (kDc / 4);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = (tid >> 5) + 4 * j;
+        const float w = sW[sl][r];
+        const float4 v = src[r * (kDc / 4) + c4];
+        acc[j].x = fmaf(w, v.x, acc[j].x);
+        acc[j].y = fmaf(w, v.y, acc[j].y);
+        acc[j].z = fmaf(w, v.z, acc[j].z);
+        acc[j].w = fmaf(w, v.w, acc[j].w);
       }
     }
-    out[(size_t)r * kDc] = den > 0.f ? acc / den : 0.f;
   }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) out[((tid >> 5) + 4 * j) * (kDc / 4) + c4] = acc[j];
 }
 
 __global__ void wait_timeout_selftest_kernel(uint32_t* status, uint64_t timeout_ns) {
@@ -183,16 +223,14 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  plan_kernel<<<1, kPlanThreads, smem, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), smem, stream, a);
 }
 
 cudaError_t launch_combine(const void* workspace, int32_t groups, int32_t num_ctas,
                            int64_t num_q, float* o_lat, cudaStream_t stream) {
   if (num_q == 0) return cudaSuccess;
-  combine_kernel<<<dim3((unsigned)(num_q * groups), 4), 128, 0, stream>>>(
-      (const uint8_t*)workspace, groups, num_ctas, num_q, o_lat);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3((unsigned)(num_q * groups), 4), dim3(kCombineThreads), 0,
+                    stream, (const uint8_t*)workspace, groups, num_ctas, num_q, o_lat);
 }
 
 cudaError_t launch_wait_timeout_selftest(uint32_t* status, int64_t timeout_ns,

@@ -5,134 +5,218 @@
 // Source: "mini-infer-17: MLA Attention", section "版本 3: MLAAttentionAbsorbed"
 // (_build_absorbed gives W_k_absorbed and W_v_absorbed as [H, d_c, 128]).
 //
-// bf16: a batched-per-head GEMM on warp mma (m16n8k16, fp32 accumulate). The
-// CTA computes 16*MW query rows x 128 output columns of one head; the weight
-// is staged through shared memory 64 K-values at a time (swizzled, read with
-// ldmatrix), the activation fragments are loaded straight from global memory.
+// bf16: batched-per-head GEMMs on warp mma (m16n8k16, fp32 accumulate). They
+// are small and latency-bound, so each CTA issues all of its weight bytes as
+// cp.async copies at once and loads its activation fragments while those are
+// in flight; grids are cut into column blocks for enough CTAs.
 // fp32: plain SIMT dot products in fp32 (no tensor cores: fp32 I/O is held to
 // 1e-4 absolute).
+#include "async_copy.cuh"
 #include "common.cuh"
 #include "internal.h"
 
 namespace mla {
 namespace {
 
-// B_NMAJOR = false: B stored [n][k] (k contiguous)   -- W_uk[h][c][d], k = d
-// B_NMAJOR = true : B stored [k][n] (n contiguous)   -- W_uv[h][c][v], k = c
-template <int MW, bool A_F32, bool B_NMAJOR, bool ROPE>
-__global__ void __launch_bounds__(128) head_gemm_kernel(
-    const void* __restrict__ A_, const __nv_bfloat16* __restrict__ B, __nv_bfloat16* __restrict__ C,
-    int num_q, int H, int K, int a_stride_row, int c_stride_row, int b_ld,
-    // rope (absorb only)
-    const __nv_bfloat16* __restrict__ q_pe, const int32_t* __restrict__ q_pos, double base) {
-  constexpr int NT = 4 * MW;                // n-tiles (8 cols) per warp
+// ---------------------------------------------------------------------------
+// absorb_q, bf16. CTA = (16*MW query rows, 128 latent columns, head h).
+// The CTA's weight slice W_uk[h][col0:col0+128][0:128] (32 KB) is copied to
+// shared memory with cp.async in one go (rows of 256 B, 16-byte chunks
+// XOR-swizzled by row so ldmatrix is conflict-free); the query fragments of
+// all 8 k-steps are loaded while the copy is in flight.
+//   MW = 1: the four warps split the 128 columns (32 each).
+//   MW = 4: each warp owns 16 rows and all 128 columns.
+// ---------------------------------------------------------------------------
+template <int MW>
+__global__ void __launch_bounds__(128) absorb_bf16_kernel(
+    const __nv_bfloat16* __restrict__ q_nope, const __nv_bfloat16* __restrict__ q_pe,
+    const int32_t* __restrict__ q_pos, const __nv_bfloat16* __restrict__ W_uk,
+    __nv_bfloat16* __restrict__ q_abs, int num_q, int H, RopeFreq freq) {
+  constexpr int NT = MW == 1 ? 4 : 16;   // 8-column n-tiles per warp
   constexpr int ROWS = 16 * MW;
-  __shared__ __align__(1024) uint8_t sB[16384];
+  __shared__ __align__(1024) uint8_t sB[128 * 256];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, q = lane & 3;
-  const int h = blockIdx.z;
-  const int row0 = blockIdx.x * ROWS;
-  const int col0 = blockIdx.y * 128;
-  const int wr = warp % MW;                 // row block of this warp
-  const int wc = warp / MW;                 // column block of this warp
-  const int ncol_w = 128 / (4 / MW);        // columns per warp = 8 * NT
-  const int r_lo = row0 + wr * 16 + g, r_hi = r_lo + 8;
+  const int h = blockIdx.z, row0 = blockIdx.x * ROWS, col0 = blockIdx.y * 128;
+
+  const __nv_bfloat16* src = W_uk + ((size_t)h * kDc + col0) * kDn;
+  for (int i = tid; i < 128 * 16; i += 128) {
+    const int r = i >> 4, ch = i & 15;
+    cp_async16(sB + r * 256 + ((ch ^ (r & 7)) << 4), src + r * kDn + ch * 8);
+  }
+  cp_async_commit();
+  // the weights do not depend on earlier kernels; the query does
+  pdl_wait();
+  pdl_launch_dependents();
+
+  const int wr = MW == 1 ? 0 : warp, wc = MW == 1 ? warp : 0;
+  const int r_lo = row0 + 16 * wr + g, r_hi = r_lo + 8;
   const bool ok_lo = r_lo < num_q, ok_hi = r_hi < num_q;
+  uint32_t a[8][4];
+  const __nv_bfloat16* plo = q_nope + ((size_t)r_lo * H + h) * kDn + 2 * q;
+  const __nv_bfloat16* phi = q_nope + ((size_t)r_hi * H + h) * kDn + 2 * q;
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    a[ks][0] = ok_lo ? *reinterpret_cast<const uint32_t*>(plo + ks * 16) : 0u;
+    a[ks][1] = ok_hi ? *reinterpret_cast<const uint32_t*>(phi + ks * 16) : 0u;
+    a[ks][2] = ok_lo ? *reinterpret_cast<const uint32_t*>(plo + ks * 16 + 8) : 0u;
+    a[ks][3] = ok_hi ? *reinterpret_cast<const uint32_t*>(phi + ks * 16 + 8) : 0u;
+  }
+  cp_async_wait_all();
+  __syncthreads();
 
   float acc[NT][4];
 #pragma unroll
   for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-
-  const __nv_bfloat16* Bh = B + (size_t)h * kDc * 128;   // both weights are [H, 512, 128]
-  for (int k0 = 0; k0 < K; k0 += 64) {
-    __syncthreads();
-    // stage 16 KB of the weight
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int idx = tid + i * 128;
-      if (!B_NMAJOR) {  // rows = n (128), 64 k each = 8 chunks of 16 B
-        const int r = idx >> 3, ch = idx & 7;
-        const uint4 v = *reinterpret_cast<const uint4*>(Bh + (size_t)(col0 + r) * b_ld + k0 + ch * 8);
-        *reinterpret_cast<uint4*>(sB + sw128(r, ch)) = v;
-      } else {          // rows = k (64), 128 n each = 16 chunks of 16 B
-        const int r = idx >> 4, ch = idx & 15;
-        const uint4 v = *reinterpret_cast<const uint4*>(Bh + (size_t)(k0 + r) * b_ld + col0 + ch * 8);
-        *reinterpret_cast<uint4*>(sB + r * 256 + ((ch ^ (r & 7)) << 4)) = v;
-      }
-    }
-    __syncthreads();
+  for (int ks = 0; ks < 8; ++ks) {
 #pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      const int kk = k0 + ks * 16 + 2 * q;
-      uint32_t a0 = 0, a1 = 0, a2 = 0, a3 = 0;
-      if (A_F32) {
-        const float* A = reinterpret_cast<const float*>(A_);
-        if (ok_lo) {
-          const float* p = A + (size_t)(r_lo * H + h) * a_stride_row + kk;
-          const float2 x0 = *reinterpret_cast<const float2*>(p);
-          const float2 x1 = *reinterpret_cast<const float2*>(p + 8);
-          a0 = pack_bf16(x0.x, x0.y); a2 = pack_bf16(x1.x, x1.y);
-        }
-        if (ok_hi) {
-          const float* p = A + (size_t)(r_hi * H + h) * a_stride_row + kk;
-          const float2 x0 = *reinterpret_cast<const float2*>(p);
-          const float2 x1 = *reinterpret_cast<const float2*>(p + 8);
-          a1 = pack_bf16(x0.x, x0.y); a3 = pack_bf16(x1.x, x1.y);
-        }
-      } else {
-        const __nv_bfloat16* A = reinterpret_cast<const __nv_bfloat16*>(A_);
-        if (ok_lo) {
-          const __nv_bfloat16* p = A + (size_t)(r_lo * H + h) * a_stride_row + kk;
-          a0 = *reinterpret_cast<const uint32_t*>(p); a2 = *reinterpret_cast<const uint32_t*>(p + 8);
-        }
-        if (ok_hi) {
-          const __nv_bfloat16* p = A + (size_t)(r_hi * H + h) * a_stride_row + kk;
-          a1 = *reinterpret_cast<const uint32_t*>(p); a3 = *reinterpret_cast<const uint32_t*>(p + 8);
-        }
-      }
-#pragma unroll
-      for (int np = 0; np < NT / 2; ++np) {
-        const int cb = wc * ncol_w + np * 16;   // first column of the n-tile pair
-        uint32_t b0, b1, b2, b3;
-        if (!B_NMAJOR) {
-          // matrices: (n 0-7,k 0-7) (n 0-7,k 8-15) (n 8-15,k 0-7) (n 8-15,k 8-15)
-          const int n = cb + (lane & 7) + ((lane >> 4) << 3);
-          const int ch = ks * 2 + ((lane >> 3) & 1);
-          ldsm_x4(smem_u32(sB + sw128(n, ch)), b0, b1, b2, b3);
-        } else {
-          // matrices: (k 0-7,n c) (k 8-15,n c) (k 0-7,n c+1) (k 8-15,n c+1), transposed
-          const int kr = ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-          const int ch = (cb >> 3) + (lane >> 4);
-          ldsm_x4_t(smem_u32(sB + kr * 256 + ((ch ^ (kr & 7)) << 4)), b0, b1, b2, b3);
-        }
-        mma_16816(acc[2 * np], a0, a1, a2, a3, b0, b1);
-        mma_16816(acc[2 * np + 1], a0, a1, a2, a3, b2, b3);
-      }
+    for (int np = 0; np < NT / 2; ++np) {
+      const int n = wc * (8 * NT) + np * 16 + (lane & 7) + ((lane >> 4) << 3);
+      const int ch = ks * 2 + ((lane >> 3) & 1);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(smem_u32(sB + n * 256 + ((ch ^ (n & 7)) << 4)), b0, b1, b2, b3);
+      mma_16816(acc[2 * np], a[ks][0], a[ks][1], a[ks][2], a[ks][3], b0, b1);
+      mma_16816(acc[2 * np + 1], a[ks][0], a[ks][1], a[ks][2], a[ks][3], b2, b3);
     }
   }
-  // epilogue: bf16 pairs
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const int col = col0 + wc * ncol_w + nt * 8 + 2 * q;
+    const int col = col0 + wc * (8 * NT) + nt * 8 + 2 * q;
     if (ok_lo)
-      *reinterpret_cast<uint32_t*>(C + (size_t)(r_lo * H + h) * c_stride_row + col) =
+      *reinterpret_cast<uint32_t*>(q_abs + ((size_t)r_lo * H + h) * kRow + col) =
           pack_bf16(acc[nt][0], acc[nt][1]);
     if (ok_hi)
-      *reinterpret_cast<uint32_t*>(C + (size_t)(r_hi * H + h) * c_stride_row + col) =
+      *reinterpret_cast<uint32_t*>(q_abs + ((size_t)r_hi * H + h) * kRow + col) =
           pack_bf16(acc[nt][2], acc[nt][3]);
   }
-  if (ROPE && blockIdx.y == 0) {
+  if (blockIdx.y == 0) {
     // rotate-half RoPE of q_pe into q_abs[..., 512:576] for this CTA's rows
+    const int p = tid & 31;
+    const float fhi = freq.hi[p], flo = freq.lo[p];
     for (int i = tid; i < ROWS * 32; i += 128) {
-      const int r = row0 + i / 32, p = i % 32;
+      const int r = row0 + i / 32;
       if (r >= num_q) continue;
-      const __nv_bfloat16* x = q_pe + (size_t)(r * H + h) * kDr;
+      const __nv_bfloat16* x = q_pe + ((size_t)r * H + h) * kDr;
       const float x1 = __bfloat162float(x[p]), x2 = __bfloat162float(x[p + 32]);
       float cs, sn;
-      rope_cos_sin(q_pos[r], p, kDr, base, &cs, &sn);
-      __nv_bfloat16* o = C + (size_t)(r * H + h) * c_stride_row + kDc;
+      rope_cos_sin(q_pos[r], fhi, flo, &cs, &sn);
+      __nv_bfloat16* o = q_abs + ((size_t)r * H + h) * kRow + kDc;
       o[p] = __float2bfloat16_rn(x1 * cs - x2 * sn);
       o[p + 32] = __float2bfloat16_rn(x2 * cs + x1 * sn);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// out_proj, bf16. CTA = (16*MW query rows, 64 output columns, head h). The
+// weight slice W_uv[h][0:512][col0:col0+64] (64 KB) goes to shared memory by
+// cp.async in one go (128-byte rows, swizzled for ldmatrix.trans).
+//   MW = 1: the four warps split K = 512 into quarters (latency: the o_lat
+//           fragments of a quarter, 8 k-steps, are loaded before the wait);
+//           the four partial tiles are summed through shared memory.
+//   MW = 4: each warp owns 16 rows over all of K.
+// o_lat is fp32 and rounded to bf16 for the mma.
+// ---------------------------------------------------------------------------
+template <int MW>
+__global__ void __launch_bounds__(128) out_proj_bf16_kernel(const float* __restrict__ o_lat,
+                                                            const __nv_bfloat16* __restrict__ W_uv,
+                                                            __nv_bfloat16* __restrict__ out,
+                                                            int num_q, int H) {
+  extern __shared__ __align__(1024) uint8_t smem_op[];
+  uint8_t* sB = smem_op;                                   // 512 x 128 B
+  float* sRed = reinterpret_cast<float*>(smem_op + 512 * 128);  // [4][16][64] (MW == 1)
+  constexpr int ROWS = 16 * MW;
+  constexpr int KS = MW == 1 ? 8 : 32;                     // k-steps per warp
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, q = lane & 3;
+  const int h = blockIdx.z, row0 = blockIdx.x * ROWS, col0 = blockIdx.y * 64;
+
+  const __nv_bfloat16* src = W_uv + (size_t)h * kDc * kDv + col0;
+  for (int i = tid; i < 512 * 8; i += 128) {
+    const int r = i >> 3, ch = i & 7;
+    cp_async16(sB + sw128(r, ch), src + (size_t)r * kDv + ch * 8);
+  }
+  cp_async_commit();
+  // the weights do not depend on earlier kernels; o_lat does
+  pdl_wait();
+  pdl_launch_dependents();
+
+  const int wr = MW == 1 ? 0 : warp;
+  const int k0 = MW == 1 ? warp * 128 : 0;
+  const int r_lo = row0 + 16 * wr + g, r_hi = r_lo + 8;
+  const bool ok_lo = r_lo < num_q, ok_hi = r_hi < num_q;
+  const float* plo = o_lat + ((size_t)r_lo * H + h) * kDc + k0 + 2 * q;
+  const float* phi = o_lat + ((size_t)r_hi * H + h) * kDc + k0 + 2 * q;
+  auto load_a = [&](int ks, uint32_t* a) {
+    float2 x;
+    x = ok_lo ? *reinterpret_cast<const float2*>(plo + ks * 16) : make_float2(0.f, 0.f);
+    a[0] = pack_bf16(x.x, x.y);
+    x = ok_hi ? *reinterpret_cast<const float2*>(phi + ks * 16) : make_float2(0.f, 0.f);
+    a[1] = pack_bf16(x.x, x.y);
+    x = ok_lo ? *reinterpret_cast<const float2*>(plo + ks * 16 + 8) : make_float2(0.f, 0.f);
+    a[2] = pack_bf16(x.x, x.y);
+    x = ok_hi ? *reinterpret_cast<const float2*>(phi + ks * 16 + 8) : make_float2(0.f, 0.f);
+    a[3] = pack_bf16(x.x, x.y);
+  };
+  uint32_t apre[8][4];
+  if (MW == 1) {
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) load_a(ks, apre[ks]);
+  }
+  cp_async_wait_all();
+  __syncthreads();
+
+  float acc[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks) {
+    uint32_t a[4];
+    if (MW == 1) {
+      a[0] = apre[ks & 7][0]; a[1] = apre[ks & 7][1]; a[2] = apre[ks & 7][2]; a[3] = apre[ks & 7][3];
+    } else {
+      load_a(ks, a);
+    }
+    const int kr = k0 + ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+    for (int np = 0; np < 4; ++np) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(smem_u32(sB + sw128(kr, np * 2 + (lane >> 4))), b0, b1, b2, b3);
+      mma_16816(acc[2 * np], a[0], a[1], a[2], a[3], b0, b1);
+      mma_16816(acc[2 * np + 1], a[0], a[1], a[2], a[3], b2, b3);
+    }
+  }
+  if (MW == 1) {
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      float* d = sRed + (warp * 16 + g) * 64 + nt * 8 + 2 * q;
+      d[0] = acc[nt][0]; d[1] = acc[nt][1];
+      d[8 * 64] = acc[nt][2]; d[8 * 64 + 1] = acc[nt][3];
+    }
+    __syncthreads();
+    for (int i = tid; i < 16 * 32; i += 128) {
+      const int r = i >> 5, c = (i & 31) * 2;
+      const int row = row0 + r;
+      if (row >= num_q) continue;
+      float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        v0 += sRed[(w * 16 + r) * 64 + c];
+        v1 += sRed[(w * 16 + r) * 64 + c + 1];
+      }
+      *reinterpret_cast<uint32_t*>(out + ((size_t)row * H + h) * kDv + col0 + c) = pack_bf16(v0, v1);
+    }
+  } else {
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      const int col = col0 + nt * 8 + 2 * q;
+      if (ok_lo)
+        *reinterpret_cast<uint32_t*>(out + ((size_t)r_lo * H + h) * kDv + col) =
+            pack_bf16(acc[nt][0], acc[nt][1]);
+      if (ok_hi)
+        *reinterpret_cast<uint32_t*>(out + ((size_t)r_hi * H + h) * kDv + col) =
+            pack_bf16(acc[nt][2], acc[nt][3]);
     }
   }
 }
@@ -141,7 +225,7 @@ __global__ void __launch_bounds__(128) head_gemm_kernel(
 __global__ void __launch_bounds__(128) absorb_f32_kernel(
     const float* __restrict__ q_nope, const float* __restrict__ q_pe,
     const int32_t* __restrict__ q_pos, const float* __restrict__ W_uk, float* __restrict__ q_abs,
-    int H, double base) {
+    int H, RopeFreq freq) {
   __shared__ float sq[kDn];
   const int n = blockIdx.x, h = blockIdx.y, t = threadIdx.x;
   sq[t] = q_nope[((size_t)n * H + h) * kDn + t];
@@ -156,7 +240,7 @@ __global__ void __launch_bounds__(128) absorb_f32_kernel(
   if (t < 32) {
     const float* x = q_pe + ((size_t)n * H + h) * kDr;
     float cs, sn;
-    rope_cos_sin(q_pos[n], t, kDr, base, &cs, &sn);
+    rope_cos_sin(q_pos[n], freq.hi[t], freq.lo[t], &cs, &sn);
     out[kDc + t] = x[t] * cs - x[t + 32] * sn;
     out[kDc + t + 32] = x[t + 32] * cs + x[t] * sn;
   }
@@ -182,20 +266,23 @@ cudaError_t launch_absorb_q(const mla_config& cfg, const void* q_nope, const voi
                             int64_t num_q, cudaStream_t stream) {
   if (num_q == 0) return cudaSuccess;
   const int H = cfg.num_heads;
+  const RopeFreq freq = make_rope_freq((double)cfg.rope_base);
   if (cfg.dtype == MLA_F32) {
     absorb_f32_kernel<<<dim3((unsigned)num_q, H), 128, 0, stream>>>(
         (const float*)q_nope, (const float*)q_pe, q_positions, (const float*)W_uk, (float*)q_abs,
-        H, (double)cfg.rope_base);
+        H, freq);
     return cudaGetLastError();
   }
-  if (num_q >= 512) {
-    head_gemm_kernel<4, false, false, true><<<dim3((unsigned)((num_q + 63) / 64), 4, H), 128, 0, stream>>>(
-        q_nope, (const __nv_bfloat16*)W_uk, (__nv_bfloat16*)q_abs, (int)num_q, H, kDn, kDn, kRow,
-        kDn, (const __nv_bfloat16*)q_pe, q_positions, (double)cfg.rope_base);
+  if (num_q >= 256) {
+    return launch_pdl(absorb_bf16_kernel<4>, dim3((unsigned)((num_q + 63) / 64), 4, H), dim3(128), 0,
+                      stream, (const __nv_bfloat16*)q_nope, (const __nv_bfloat16*)q_pe,
+                      q_positions, (const __nv_bfloat16*)W_uk, (__nv_bfloat16*)q_abs, (int)num_q,
+                      H, freq);
   } else {
-    head_gemm_kernel<1, false, false, true><<<dim3((unsigned)((num_q + 15) / 16), 4, H), 128, 0, stream>>>(
-        q_nope, (const __nv_bfloat16*)W_uk, (__nv_bfloat16*)q_abs, (int)num_q, H, kDn, kDn, kRow,
-        kDn, (const __nv_bfloat16*)q_pe, q_positions, (double)cfg.rope_base);
+    return launch_pdl(absorb_bf16_kernel<1>, dim3((unsigned)((num_q + 15) / 16), 4, H), dim3(128), 0,
+                      stream, (const __nv_bfloat16*)q_nope, (const __nv_bfloat16*)q_pe,
+                      q_positions, (const __nv_bfloat16*)W_uk, (__nv_bfloat16*)q_abs, (int)num_q,
+                      H, freq);
   }
   return cudaGetLastError();
 }
@@ -209,14 +296,21 @@ cudaError_t launch_out_proj(const mla_config& cfg, const float* o_lat, const voi
                                                                    (float*)out, H);
     return cudaGetLastError();
   }
-  if (num_q >= 512) {
-    head_gemm_kernel<4, true, true, false><<<dim3((unsigned)((num_q + 63) / 64), 1, H), 128, 0, stream>>>(
-        o_lat, (const __nv_bfloat16*)W_uv, (__nv_bfloat16*)out, (int)num_q, H, kDc, kDc, kDv, kDv,
-        nullptr, nullptr, 0.0);
+  const bool big = num_q >= 256;
+  const int smem = 512 * 128 + (big ? 0 : 4 * 16 * 64 * 4);
+  cudaError_t e = big ? cudaFuncSetAttribute(out_proj_bf16_kernel<4>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
+                      : cudaFuncSetAttribute(out_proj_bf16_kernel<1>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  if (big) {
+    return launch_pdl(out_proj_bf16_kernel<4>, dim3((unsigned)((num_q + 63) / 64), 2, H), dim3(128),
+                      smem, stream, o_lat, (const __nv_bfloat16*)W_uv, (__nv_bfloat16*)out,
+                      (int)num_q, H);
   } else {
-    head_gemm_kernel<1, true, true, false><<<dim3((unsigned)((num_q + 15) / 16), 1, H), 128, 0, stream>>>(
-        o_lat, (const __nv_bfloat16*)W_uv, (__nv_bfloat16*)out, (int)num_q, H, kDc, kDc, kDv, kDv,
-        nullptr, nullptr, 0.0);
+    return launch_pdl(out_proj_bf16_kernel<1>, dim3((unsigned)((num_q + 15) / 16), 2, H), dim3(128),
+                      smem, stream, o_lat, (const __nv_bfloat16*)W_uv, (__nv_bfloat16*)out,
+                      (int)num_q, H);
   }
   return cudaGetLastError();
 }
