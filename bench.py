@@ -5,8 +5,9 @@
                     [--workload serving|ragged_h128|mixed|v2lite_1024|...]
 
 A step is one pass of the whole hot path over one batch: mla_absorb_q,
-mla_decode_plan, mla_decode_planned, mla_combine and mla_out_proj (plus
-mla_cache_write of the step's new tokens for the mixed workload). The default
+mla_decode_plan (on a side stream), mla_decode_combine (the split-KV decode
+with the split merge fused in) and mla_out_proj (plus mla_cache_write of the
+step's new tokens for the mixed workload). The default
 workload is the serving batch: 64 sequences x 4,096 tokens, 16 heads, bf16,
 block_size 64, a 301,989,888-byte latent cache (larger than L2, so every step
 reads it from HBM). Inputs are seeded synthetic data with the shapes of
@@ -336,11 +337,10 @@ def run_ours(args, world, rank, local):
             s.write_new()
         s.absorb()
         cur.wait_event(ev_join)
-        s.decode_planned()
-        s.combine()
+        s.decode_combine()       # decode + split merge in one kernel
         s.out_proj()
 
-    launches_per_step = 5 + (1 if mixed else 0)
+    launches_per_step = 4 + (1 if mixed else 0)
     # eager warm-up (also builds the lazy state), then capture one step
     with torch.cuda.stream(stream):
         for _ in range(3):
@@ -382,7 +382,7 @@ def run_ours(args, world, rank, local):
     kgraph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(kgraph, stream=stream):
         for _ in range(per_graph):
-            s.decode_planned()
+            s.decode_combine()
     reps = max(1, args.kernel_launches // per_graph)
     with torch.cuda.stream(stream):
         for _ in range(3):

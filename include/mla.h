@@ -19,6 +19,11 @@
  *    mla_config.dtype. Arithmetic accumulates in fp32 in every kernel.
  *  - `stream` is a cudaStream_t (NULL = legacy default stream). Every call
  *    only enqueues work: it returns before the GPU runs it.
+ *  - Kernels are launched with programmatic stream serialisation: a kernel
+ *    may start while the previous kernel on the stream finishes, and waits
+ *    for it before reading its outputs. The weights (W_uk, W_uv, rms_weight)
+ *    are read before that wait, so they must not be written by the kernel
+ *    launched immediately before the call on the same stream.
  *  - Errors the host can see (bad sizes, null or misaligned pointers, an
  *    unsupported configuration, a small workspace) return at once and
  *    enqueue nothing. A failed launch returns MLA_ERR_CUDA. Errors only the
@@ -183,6 +188,22 @@ mla_status mla_decode_planned(const mla_config* cfg, const void* q_abs, const vo
                               int64_t num_blocks, const int32_t* block_table,
                               int32_t max_blocks_per_seq, int64_t num_q, void* workspace,
                               size_t ws_bytes, void* stream);
+
+/*
+ * mla_decode_combine -- mla_decode_planned and mla_combine in one kernel.
+ * Same inputs as mla_decode_planned (a plan from mla_decode_plan must be in
+ * the workspace) plus o_lat [num_q, H, 512] float32, the output of
+ * mla_combine. The CTA that finishes a (row, 16-head group) last merges its
+ * split partials while they are in L2; a (row, head group) handled by one
+ * CTA is written to o_lat directly. The result equals mla_decode_planned
+ * followed by mla_combine up to fp32 rounding of the merge order. The
+ * workspace's arrival counters are left at zero, so the call can be repeated
+ * (e.g. per layer) on one plan; after a device error, plan again.
+ */
+mla_status mla_decode_combine(const mla_config* cfg, const void* q_abs, const void* cache,
+                              int64_t num_blocks, const int32_t* block_table,
+                              int32_t max_blocks_per_seq, int64_t num_q, void* workspace,
+                              size_t ws_bytes, float* o_lat, void* stream);
 
 /*
  * mla_combine -- merge the split partials of mla_decode_paged.

@@ -33,6 +33,8 @@ constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 //   cta_start[C]        int4 {row n, head group g, tile k, 0}
 //   lse[S][16]          float, base-2 log-sum-exp of each partial
 //   opart[S][16][512]   float, normalised partial outputs
+//   arrive[num_q * G]   int, CTAs done with each q-tile (fused merge only;
+//                       zeroed by the plan)
 // with S = C + num_q * G - 1 partial slots; slot of (CTA c, q-tile t) = c + t
 // (unique because CTA shares and q-tiles are both contiguous ranges of the
 // same ordered unit list).
@@ -51,7 +53,7 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
 struct WsLayout {
-  size_t row_info, cta_start, lse, opart, total;
+  size_t row_info, cta_start, lse, opart, arrive, total;
   int64_t slots;
 };
 
@@ -65,6 +67,7 @@ __host__ __device__ inline WsLayout ws_layout(int64_t num_q, int groups, int num
   L.cta_start = off;  off = align_up(off + (size_t)num_ctas * 16, 256);
   L.lse = off;        off = align_up(off + (size_t)L.slots * kHG * 4, 256);
   L.opart = off;      off = align_up(off + (size_t)L.slots * kHG * kDc * 4, 256);
+  L.arrive = off;     off = align_up(off + (size_t)num_q * groups * 4, 256);
   L.total = off;
   return L;
 }

@@ -24,6 +24,7 @@
 #include "async_copy.cuh"
 #include "common.cuh"
 #include "internal.h"
+#include "merge.cuh"
 #include "sched.cuh"
 
 namespace mla {
@@ -44,7 +45,8 @@ struct Smem {
   static constexpr int pfrag = q + 2 * kQBytes;                 // [4 warps][32 lanes] uint4
   static constexpr int smax = pfrag + kMathWarps * 32 * 16;     // [4][16] float
   static constexpr int lsum = smax + kMathWarps * 16 * 4;       // [4][16] float
-  static constexpr int info = lsum + kMathWarps * 16 * 4;       // [NST] int2
+  static constexpr int merge = lsum + kMathWarps * 16 * 4;      // fused-merge scratch
+  static constexpr int info = merge + (2 * kHG + kMergeChunk * kHG) * 4;  // [NST] int2
   static constexpr int bars = info + NST * 8;                   // full, empty, qfull, qempty
   static constexpr int bytes = bars + (2 * NST + 4) * 8;
   static constexpr int alloc = bytes + 1024;                    // alignment slack
@@ -106,6 +108,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   SchedWalker sw;
   const bool has_work = sw.init(ws, a.num_q, a.groups, a.num_ctas, blockIdx.x);
+  if (a.o_lat && warp < kMathWarps)
+    zero_unvisited_rows(sw.row_info, sw.plan_ok, a.num_q, a.num_heads, a.o_lat, tid,
+                        kMathWarps * 32);
   if (!has_work) return;
   Segment seg;
 
@@ -124,15 +129,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         set_status(status, MLA_DEV_TIMEOUT);
         break;
       }
-      mbar_arrive_expect_tx(&qfull[qb], kQBytes);
-      const int qy = seg.n * a.num_heads + seg.g * kHG;
+      auto issue_q = [&] {
+        mbar_arrive_expect_tx(&qfull[qb], kQBytes);
+        const int qy = seg.n * a.num_heads + seg.g * kHG;
 #pragma unroll 1
-      for (int j = 0; j < 9; ++j)
-        tma_load_2d(sm + S::q + qb * kQBytes + j * kQSlabBytes, &q_map, 64 * j, qy, &qfull[qb]);
-      ++qfills[qb];
+        for (int j = 0; j < 9; ++j)
+          tma_load_2d(sm + S::q + qb * kQBytes + j * kQSlabBytes, &q_map, 64 * j, qy, &qfull[qb]);
+        ++qfills[qb];
+      };
+      // the first query goes out after the first NST cache tiles
+      const int q_at = seg_i == 0 ? min(seg.k0 + NST, seg.k1) : seg.k0;
+      auto maybe_issue_q = [&](int k) {
+        if (k == q_at) issue_q();
+      };
       const int visible = seg.pos + 1;
       const int32_t* bt = a.block_table + (size_t)seg.b * a.max_blocks_per_seq;
       for (int k = seg.k0; k < seg.k1; ++k) {
+        maybe_issue_q(k);
         const int st = tile_i % NST;
         const int tstart = k * kTile;
         const int v = min(kTile, visible - tstart);
@@ -173,6 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++fills[st];
         ++tile_i;
       }
+      if (ok_run) maybe_issue_q(seg.k1);  // a first segment of fewer than NST tiles
       ++seg_i;
     }
     // never leave with copies in flight
@@ -189,6 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int g = lane >> 2, q = lane & 3;
   float* smax = reinterpret_cast<float*>(sm + S::smax);
   float* lsum = reinterpret_cast<float*>(sm + S::lsum);
+  float* merge_scratch = reinterpret_cast<float*>(sm + S::merge);
   uint4* pfrag = reinterpret_cast<uint4*>(sm + S::pfrag);
   const WsLayout L = ws_layout(a.num_q, a.groups, a.num_ctas);
   float* lse_out = reinterpret_cast<float*>(ws + L.lse);
@@ -341,16 +356,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       L1 += lsum[ww * 16 + g + 8];
     }
     const float inv0 = L0 > 0.f ? 1.f / L0 : 0.f, inv1 = L1 > 0.f ? 1.f / L1 : 0.f;
-    const int64_t slot = (int64_t)blockIdx.x + (int64_t)seg.n * a.groups + seg.g;
-    float* ob = o_out + (size_t)slot * kHG * kDc + 128 * w + 2 * q;
+    const int t = seg.n * a.groups + seg.g;
+    const int64_t slot = (int64_t)blockIdx.x + t;
+    // fused merge: which CTAs share this q-tile
+    const int u_first = seg.ustart + seg.g * seg.tiles;
+    const int c_first = u_first / sw.share, c_last = (u_first + seg.tiles - 1) / sw.share;
+    const bool direct = a.o_lat != nullptr && c_first == c_last;
+    float* ob = direct ? a.o_lat + ((size_t)seg.n * a.num_heads + seg.g * kHG) * kDc + 128 * w + 2 * q
+                       : o_out + (size_t)slot * kHG * kDc + 128 * w + 2 * q;
 #pragma unroll
     for (int nt = 0; nt < 16; ++nt) {
       *reinterpret_cast<float2*>(ob + (size_t)g * kDc + nt * 8) = make_float2(o[nt][0] * inv0, o[nt][1] * inv0);
       *reinterpret_cast<float2*>(ob + (size_t)(g + 8) * kDc + nt * 8) = make_float2(o[nt][2] * inv1, o[nt][3] * inv1);
     }
-    if (w == 0 && q == 0) {
+    if (!direct && w == 0 && q == 0) {
       lse_out[(size_t)slot * kHG + g] = L0 > 0.f ? m_run0 + log2f(L0) : -INFINITY;
       lse_out[(size_t)slot * kHG + g + 8] = L1 > 0.f ? m_run1 + log2f(L1) : -INFINITY;
+    }
+    if (a.o_lat != nullptr && !direct) {
+      // publish this part, count it, and merge if it was the last one
+      int* arrive = reinterpret_cast<int*>(ws + L.arrive);
+      __threadfence();
+      named_bar_sync(kMathBar, kMathWarps * 32);
+      int* flag = reinterpret_cast<int*>(smax);  // smax is free until the next tile
+      if (tid == 0) flag[0] = atomicAdd(&arrive[t], 1) == c_last - c_first;
+      named_bar_sync(kMathBar, kMathWarps * 32);
+      const bool last = flag[0] != 0;
+      if (last) {
+        __threadfence();
+        merge_qtile<kMathWarps * 32>(lse_out, o_out, (int64_t)c_first + t, c_last - c_first + 1,
+                                     a.o_lat + ((size_t)seg.n * a.num_heads + seg.g * kHG) * kDc, tid,
+                                     merge_scratch, [] { named_bar_sync(kMathBar, kMathWarps * 32); });
+        if (tid == 0) arrive[t] = 0;  // every part has arrived: ready for the next launch
+      }
+      named_bar_sync(kMathBar, kMathWarps * 32);
     }
     ++seg_i;
   }

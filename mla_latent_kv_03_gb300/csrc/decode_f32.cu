@@ -7,6 +7,7 @@
 // summed, then a hand-written softmax).
 #include "common.cuh"
 #include "internal.h"
+#include "merge.cuh"
 #include "sched.cuh"
 
 namespace mla {
@@ -22,6 +23,8 @@ __global__ void __launch_bounds__(256) decode_f32_kernel(DecodeArgs a) {
   float* sA = sP + kHG * kSub;                // [16] alpha
   float* sL = sA + kHG;                       // [16] final l
   float* sM = sL + kHG;                       // [16] final m
+  float* sMerge = sM + kHG;                   // fused-merge scratch
+  int* sFlag = reinterpret_cast<int*>(sMerge + 2 * kHG + kMergeChunk * kHG);
   const int tid = threadIdx.x;
   const int h = tid >> 4, j = tid & 15;       // score role: head h, token j
   const int d0 = tid * 2;                     // PV role: dims d0, d0+1 for all heads
@@ -34,7 +37,9 @@ __global__ void __launch_bounds__(256) decode_f32_kernel(DecodeArgs a) {
   const float* cache = reinterpret_cast<const float*>(a.cache);
 
   SchedWalker sw;
-  if (!sw.init(ws, a.num_q, a.groups, a.num_ctas, blockIdx.x)) return;
+  const bool has_work = sw.init(ws, a.num_q, a.groups, a.num_ctas, blockIdx.x);
+  if (a.o_lat) zero_unvisited_rows(sw.row_info, sw.plan_ok, a.num_q, a.num_heads, a.o_lat, tid, 256);
+  if (!has_work) return;
   Segment seg;
   while (sw.next(seg)) {
     const int t = seg.n * a.groups + seg.g;
@@ -109,16 +114,36 @@ __global__ void __launch_bounds__(256) decode_f32_kernel(DecodeArgs a) {
     __syncthreads();
     if (j == 0) { sL[h] = l; sM[h] = m; }
     __syncthreads();
+    const int u_first = seg.ustart + seg.g * seg.tiles;
+    const int c_first = u_first / sw.share, c_last = (u_first + seg.tiles - 1) / sw.share;
+    const bool direct = a.o_lat != nullptr && c_first == c_last;
+    float* dst = direct ? a.o_lat + ((size_t)seg.n * a.num_heads + seg.g * kHG) * kDc
+                        : o_out + (size_t)slot * kHG * kDc;
 #pragma unroll
     for (int r = 0; r < kHG; ++r) {
       const float lr = sL[r];
       const float inv = lr > 0.f ? 1.f / lr : 0.f;
       float2 v = make_float2(o[r][0] * inv, o[r][1] * inv);
-      *reinterpret_cast<float2*>(o_out + ((size_t)slot * kHG + r) * kDc + d0) = v;
+      *reinterpret_cast<float2*>(dst + (size_t)r * kDc + d0) = v;
     }
-    if (tid < kHG) {
+    if (!direct && tid < kHG) {
       const float lr = sL[tid];
       lse_out[(size_t)slot * kHG + tid] = lr > 0.f ? sM[tid] + log2f(lr) : -INFINITY;
+    }
+    if (a.o_lat != nullptr && !direct) {
+      int* arrive = reinterpret_cast<int*>(ws + L.arrive);
+      __threadfence();
+      __syncthreads();
+      if (tid == 0) sFlag[0] = atomicAdd(&arrive[t], 1) == c_last - c_first;
+      __syncthreads();
+      if (sFlag[0]) {
+        __threadfence();
+        merge_qtile<256>(lse_out, o_out, (int64_t)c_first + t, c_last - c_first + 1,
+                         a.o_lat + ((size_t)seg.n * a.num_heads + seg.g * kHG) * kDc, tid, sMerge,
+                         [] { __syncthreads(); });
+        if (tid == 0) arrive[t] = 0;  // every part has arrived: ready for the next launch
+      }
+      __syncthreads();
     }
   }
 }
@@ -126,7 +151,8 @@ __global__ void __launch_bounds__(256) decode_f32_kernel(DecodeArgs a) {
 }  // namespace
 
 cudaError_t launch_decode_f32(const DecodeArgs& a, cudaStream_t stream) {
-  const size_t smem = (size_t)(kHG * kRow + kSub * (kRow + 1) + kHG * kSub + 3 * kHG) * 4;
+  const size_t smem =
+      (size_t)(kHG * kRow + kSub * (kRow + 1) + kHG * kSub + 3 * kHG + 2 * kHG + kMergeChunk * kHG + 4) * 4;
   cudaError_t e = cudaFuncSetAttribute(decode_f32_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

@@ -35,6 +35,7 @@ struct DecodeArgs {
   int64_t num_q;
   float scale_log2;  // softmax_scale * log2(e)
   void* workspace;
+  float* o_lat;      // non-null: merge the splits in the decode kernel (fused combine)
 };
 
 cudaError_t launch_cache_write(const mla_config& cfg, const void* c_kv, const void* k_pe,

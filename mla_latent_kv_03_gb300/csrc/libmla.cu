@@ -186,10 +186,14 @@ mla_status mla_decode_plan(const mla_config* cfg, const int32_t* seq_lens,
   return from_cuda(launch_plan(pa, as_stream(stream)));
 }
 
-mla_status mla_decode_planned(const mla_config* cfg, const void* q_abs, const void* cache,
-                              int64_t num_blocks, const int32_t* block_table,
-                              int32_t max_blocks_per_seq, int64_t num_q, void* workspace,
-                              size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+mla_status decode_impl(const mla_config* cfg, const void* q_abs, const void* cache,
+                       int64_t num_blocks, const int32_t* block_table, int32_t max_blocks_per_seq,
+                       int64_t num_q, void* workspace, size_t ws_bytes, float* o_lat,
+                       void* stream) {
   mla_status s = check_cfg(cfg);
   if (s != MLA_OK) return s;
   if (num_q < 0 || num_blocks < 0 || max_blocks_per_seq < 0) return MLA_ERR_INVALID_ARGUMENT;
@@ -207,7 +211,7 @@ mla_status mla_decode_planned(const mla_config* cfg, const void* q_abs, const vo
   cudaStream_t st = as_stream(stream);
   const double log2e = 1.4426950408889634;
   DecodeArgs da{q_abs, cache, num_blocks, block_table, max_blocks_per_seq, cfg->block_size,
-                cfg->num_heads, G, C, num_q, (float)(cfg->softmax_scale * log2e), workspace};
+                cfg->num_heads, G, C, num_q, (float)(cfg->softmax_scale * log2e), workspace, o_lat};
   if (cfg->dtype == MLA_F32) return from_cuda(launch_decode_f32(da, st));
   // With num_blocks == 0 every block id is rejected before any copy, so the
   // map below is never used to read; it still needs a non-empty extent.
@@ -218,6 +222,27 @@ mla_status mla_decode_planned(const mla_config* cfg, const void* q_abs, const vo
       !make_row_map(&q_map, q_abs, (uint64_t)num_q * cfg->num_heads, kHG))
     return MLA_ERR_CUDA;
   return from_cuda(launch_decode_bf16(da, cache_map, q_map, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+mla_status mla_decode_planned(const mla_config* cfg, const void* q_abs, const void* cache,
+                              int64_t num_blocks, const int32_t* block_table,
+                              int32_t max_blocks_per_seq, int64_t num_q, void* workspace,
+                              size_t ws_bytes, void* stream) {
+  return decode_impl(cfg, q_abs, cache, num_blocks, block_table, max_blocks_per_seq, num_q,
+                     workspace, ws_bytes, nullptr, stream);
+}
+
+mla_status mla_decode_combine(const mla_config* cfg, const void* q_abs, const void* cache,
+                              int64_t num_blocks, const int32_t* block_table,
+                              int32_t max_blocks_per_seq, int64_t num_q, void* workspace,
+                              size_t ws_bytes, float* o_lat, void* stream) {
+  if (num_q > 0 && (!o_lat || !aligned(o_lat, 16))) return MLA_ERR_INVALID_ARGUMENT;
+  return decode_impl(cfg, q_abs, cache, num_blocks, block_table, max_blocks_per_seq, num_q,
+                     workspace, ws_bytes, o_lat, stream);
 }
 
 mla_status mla_decode_paged(const mla_config* cfg, const void* q_abs, const void* cache,

@@ -33,10 +33,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
   pdl_wait();
   pdl_launch_dependents();
 
+  int* arrive = reinterpret_cast<int*>(ws + L.arrive);
   for (int n = tid; n < Nq; n += kPlanThreads) {
     row_info[n] = make_int4(-1, -1, 0, 0);
     s_units[n] = 0;
   }
+  for (int i = tid; i < Nq * a.groups; i += kPlanThreads) arrive[i] = 0;
   __syncthreads();
   const int64_t max_len = (int64_t)a.max_blocks_per_seq * a.block_size;
   for (int b = tid; b < a.batch; b += kPlanThreads) {

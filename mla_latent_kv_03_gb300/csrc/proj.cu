@@ -19,7 +19,8 @@ namespace mla {
 namespace {
 
 // ---------------------------------------------------------------------------
-// absorb_q, bf16. CTA = (16*MW query rows, 128 latent columns, head h).
+// absorb_q, bf16. CTA = (16*MW query rows, 128 latent columns, head h); a
+// fifth column of CTAs (blockIdx.y == 4) does the RoPE part.
 // The CTA's weight slice W_uk[h][col0:col0+128][0:128] (32 KB) is copied to
 // shared memory with cp.async in one go (rows of 256 B, 16-byte chunks
 // XOR-swizzled by row so ldmatrix is conflict-free); the query fragments of
@@ -38,6 +39,38 @@ __global__ void __launch_bounds__(128) absorb_bf16_kernel(
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, q = lane & 3;
   const int h = blockIdx.z, row0 = blockIdx.x * ROWS, col0 = blockIdx.y * 128;
+
+  if (blockIdx.y == 4) {
+    // rotate-half RoPE of q_pe into q_abs[..., 512:576] for this CTA's rows;
+    // all loads of a thread are issued before any of them is used
+    pdl_wait();
+    pdl_launch_dependents();
+    constexpr int kPer = ROWS * 32 / 128;
+    const int p = tid & 31;
+    const float fhi = freq.hi[p], flo = freq.lo[p];
+    float x1[kPer], x2[kPer];
+    int pos[kPer];
+#pragma unroll
+    for (int it = 0; it < kPer; ++it) {
+      const int r = row0 + (tid >> 5) + 4 * it;
+      const bool ok = r < num_q;
+      const __nv_bfloat16* x = q_pe + ((size_t)r * H + h) * kDr;
+      x1[it] = ok ? __bfloat162float(x[p]) : 0.f;
+      x2[it] = ok ? __bfloat162float(x[p + 32]) : 0.f;
+      pos[it] = ok ? q_pos[r] : 0;
+    }
+#pragma unroll
+    for (int it = 0; it < kPer; ++it) {
+      const int r = row0 + (tid >> 5) + 4 * it;
+      if (r >= num_q) continue;
+      float cs, sn;
+      rope_cos_sin(pos[it], fhi, flo, &cs, &sn);
+      __nv_bfloat16* o = q_abs + ((size_t)r * H + h) * kRow + kDc;
+      o[p] = __float2bfloat16_rn(x1[it] * cs - x2[it] * sn);
+      o[p + 32] = __float2bfloat16_rn(x2[it] * cs + x1[it] * sn);
+    }
+    return;
+  }
 
   const __nv_bfloat16* src = W_uk + ((size_t)h * kDc + col0) * kDn;
   for (int i = tid; i < 128 * 16; i += 128) {
@@ -89,22 +122,6 @@ __global__ void __launch_bounds__(128) absorb_bf16_kernel(
     if (ok_hi)
       *reinterpret_cast<uint32_t*>(q_abs + ((size_t)r_hi * H + h) * kRow + col) =
           pack_bf16(acc[nt][2], acc[nt][3]);
-  }
-  if (blockIdx.y == 0) {
-    // rotate-half RoPE of q_pe into q_abs[..., 512:576] for this CTA's rows
-    const int p = tid & 31;
-    const float fhi = freq.hi[p], flo = freq.lo[p];
-    for (int i = tid; i < ROWS * 32; i += 128) {
-      const int r = row0 + i / 32;
-      if (r >= num_q) continue;
-      const __nv_bfloat16* x = q_pe + ((size_t)r * H + h) * kDr;
-      const float x1 = __bfloat162float(x[p]), x2 = __bfloat162float(x[p + 32]);
-      float cs, sn;
-      rope_cos_sin(q_pos[r], fhi, flo, &cs, &sn);
-      __nv_bfloat16* o = q_abs + ((size_t)r * H + h) * kRow + kDc;
-      o[p] = __float2bfloat16_rn(x1 * cs - x2 * sn);
-      o[p + 32] = __float2bfloat16_rn(x2 * cs + x1 * sn);
-    }
   }
 }
 
@@ -274,12 +291,12 @@ cudaError_t launch_absorb_q(const mla_config& cfg, const void* q_nope, const voi
     return cudaGetLastError();
   }
   if (num_q >= 256) {
-    return launch_pdl(absorb_bf16_kernel<4>, dim3((unsigned)((num_q + 63) / 64), 4, H), dim3(128), 0,
+    return launch_pdl(absorb_bf16_kernel<4>, dim3((unsigned)((num_q + 63) / 64), 5, H), dim3(128), 0,
                       stream, (const __nv_bfloat16*)q_nope, (const __nv_bfloat16*)q_pe,
                       q_positions, (const __nv_bfloat16*)W_uk, (__nv_bfloat16*)q_abs, (int)num_q,
                       H, freq);
   } else {
-    return launch_pdl(absorb_bf16_kernel<1>, dim3((unsigned)((num_q + 15) / 16), 4, H), dim3(128), 0,
+    return launch_pdl(absorb_bf16_kernel<1>, dim3((unsigned)((num_q + 15) / 16), 5, H), dim3(128), 0,
                       stream, (const __nv_bfloat16*)q_nope, (const __nv_bfloat16*)q_pe,
                       q_positions, (const __nv_bfloat16*)W_uk, (__nv_bfloat16*)q_abs, (int)num_q,
                       H, freq);

@@ -14,24 +14,28 @@ struct Segment {
   int k0, k1;  // tiles [k0, k1) of this row's causal range
   int b;       // sequence
   int pos;     // query position: tokens 0..pos are visible
+  int tiles;   // tiles of this row's causal range
+  int ustart;  // first unit of the row in the ordered unit list
 };
 
 struct SchedWalker {
   const int4* row_info;
-  int u, u_end, n, g, k, G;
+  int u, u_end, n, g, k, G, share;
+  bool plan_ok;  // the workspace holds a plan for this launch
 
   // false if this CTA has no work (or the workspace holds no plan)
   __device__ __forceinline__ bool init(const uint8_t* ws, int64_t num_q, int groups, int num_ctas,
                                        int c) {
     const WsHeader* hdr = reinterpret_cast<const WsHeader*>(ws);
-    // the plan must describe this launch (same rows, head groups, CTAs)
-    if (hdr->magic != kMagic || hdr->num_q != num_q || hdr->groups != groups ||
-        hdr->num_ctas != num_ctas)
-      return false;
     const WsLayout L = ws_layout(num_q, groups, num_ctas);
     row_info = reinterpret_cast<const int4*>(ws + L.row_info);
+    // the plan must describe this launch (same rows, head groups, CTAs)
+    plan_ok = hdr->magic == kMagic && hdr->num_q == num_q && hdr->groups == groups &&
+              hdr->num_ctas == num_ctas;
+    if (!plan_ok) return false;
     const int4* cta_start = reinterpret_cast<const int4*>(ws + L.cta_start);
-    const int share = hdr->share, total = hdr->total_units;
+    share = hdr->share;
+    const int total = hdr->total_units;
     G = groups;
     u = c * share;
     u_end = min(u + share, total);
@@ -50,6 +54,7 @@ struct SchedWalker {
     }
     const int take = min(ri.z - k, u_end - u);
     s.n = n; s.g = g; s.k0 = k; s.k1 = k + take; s.b = ri.x; s.pos = ri.y;
+    s.tiles = ri.z; s.ustart = ri.w;
     u += take;
     k += take;
     if (k == ri.z) {

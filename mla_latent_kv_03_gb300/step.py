@@ -101,6 +101,10 @@ class MlaDecodeStep:
         L.mla_decode_planned(self.cfg, self.q_abs, self.cache, self.block_table, self.workspace,
                              stream=stream)
 
+    def decode_combine(self, stream=None) -> None:
+        L.mla_decode_combine(self.cfg, self.q_abs, self.cache, self.block_table, self.workspace,
+                             self.o_lat, stream=stream)
+
     def combine(self, stream=None) -> None:
         L.mla_combine(self.cfg, self.workspace, self.w.batch, self.o_lat, stream=stream)
 

@@ -236,3 +236,61 @@ def test_bounded_wait_times_out_and_context_survives():
     s.populate()
     max_abs, _ = errors(to_f64(s.step()), ref_out(w))
     assert max_abs <= 1e-4
+
+
+# ---------------------------------------------------------------------------
+# mla_decode_combine: the decode kernel merging its own splits
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+@pytest.mark.parametrize("num_ctas", [0, 7, 500])
+def test_fused_decode_combine_matches_oracle_and_unfused(name, num_ctas):
+    w = SMALL[name]()
+    s = MlaDecodeStep(w, device=DEV, num_ctas=num_ctas)
+    s.populate()
+    s.absorb()
+    s.plan()
+    s.o_lat.fill_(float("nan"))                      # rows nobody visits must become 0
+    s.decode_combine()
+    torch.cuda.synchronize()
+    assert s.device_status()[0][0] == 0
+    fused = to_f64(s.o_lat)
+    ref = ref_o_lat_from(w, to_f64(s.cache), to_f64(s.q_abs))
+    empty = np.isnan(ref).all(axis=(1, 2))
+    assert np.all(fused[empty] == 0)
+    assert_close(fused, ref, w.dtype, f"fused o_lat {name}")
+    s.decode_planned()
+    s.combine()
+    unfused = to_f64(s.o_lat)
+    tol = 1e-6 if w.dtype == "f32" else 1e-5
+    np.testing.assert_allclose(fused, unfused, rtol=0, atol=tol)
+
+
+def test_fused_merge_of_many_splits():
+    # one 2,000-token row over 500 CTAs: 32 single-tile parts, more than one
+    # chunk of staged merge weights
+    w = W.make("many", [2000, 1, 333, 64], [1, 1, 1, 1], 16, 64, "bf16", seed=45)
+    s = MlaDecodeStep(w, device=DEV, num_ctas=500)
+    s.populate()
+    s.absorb()
+    s.plan()
+    s.decode_combine()
+    s.out_proj()
+    assert_close(to_f64(s.out), ref_out(w), "bf16", "fused, 500 CTAs")
+
+
+def test_fused_decode_combine_repeats_on_one_plan():
+    w = W.make("repeat", [700, 1, 129], [1, 1, 1], 16, 64, "bf16", seed=46)
+    s = MlaDecodeStep(w, device=DEV, num_ctas=9)
+    s.populate()
+    s.absorb()
+    s.plan()
+    outs = []
+    for _ in range(3):
+        s.o_lat.fill_(float("nan"))
+        s.decode_combine()
+        outs.append(s.o_lat.clone())
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+    ref = ref_o_lat_from(w, to_f64(s.cache), to_f64(s.q_abs))
+    assert_close(to_f64(outs[2]), ref, "bf16", "third launch on one plan")
