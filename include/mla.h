@@ -227,6 +227,33 @@ mla_status mla_out_proj(const mla_config* cfg, const float* o_lat, const void* W
                         void* out, int64_t num_q, void* stream);
 
 /*
+ * mla_decode_paged_noalloc -- mla_decode_paged followed by mla_combine for
+ * callers that cannot allocate device memory (a step callback with a fixed
+ * memory budget, a real-time loop where cudaMalloc would stall or fail, a
+ * plugin that must not allocate). The pages have no counterpart of this
+ * call; it exists for such callers only.
+ * The caller passes the same inputs as mla_decode_paged and the output
+ * o_lat [num_q, H, 512] float32 of mla_combine; the workspace is instead a
+ * 16 MiB array built into the library, which every GPU that loads the
+ * library keeps until the process exits. A launch whose workspace
+ * (mla_decode_workspace_size) exceeds 16 MiB returns
+ * MLA_ERR_WORKSPACE_TOO_SMALL and enqueues nothing.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture. Every call on a device shares the array and leaves its contents
+ * for the next one: each call clears the status word and plan header itself,
+ * and calls whose GPU work overlaps (other streams or host threads) race on
+ * the array and must not be issued. dev_status (device word, may be NULL)
+ * receives the call's device status bits (MLA_DEV_*). Nothing is allocated:
+ * no cudaMalloc, cudaFree or allocating library routine is called.
+ */
+mla_status mla_decode_paged_noalloc(const mla_config* cfg, const void* q_abs, const void* cache,
+                                    int64_t num_blocks, const int32_t* block_table,
+                                    int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                    const int32_t* query_start_loc, int32_t batch, int64_t num_q,
+                                    float* o_lat, uint32_t* dev_status, void* stream);
+
+/*
  * mla_get_device_status -- synchronise `stream`, read the device status word
  * at `status_word` (a workspace's first word, or the dev_status buffer given
  * to mla_cache_write), optionally clear it, and map it to a status: the

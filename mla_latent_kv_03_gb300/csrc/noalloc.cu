@@ -1,0 +1,86 @@
+// mla_decode_paged_noalloc: the paged decode (plan, split-KV attention and
+// the merge of the splits) for callers that cannot allocate device memory.
+//
+// Some callers cannot call cudaMalloc at the point where they decode: code
+// that runs inside a host framework's per-step callback with a fixed device
+// memory budget, a real-time serving loop where an allocation would
+// synchronise the device or fail under fragmentation, or a plugin whose
+// contract forbids allocating. They still own and pass every input and the
+// output; only the scratch the decode needs (the split plan, the per-split
+// partial outputs and the device status word) comes from a fixed array built
+// into this library.
+//
+// The array is file-scope device memory of kScratchBytes. Every GPU that
+// loads the library holds it until the process exits. All calls on a device
+// share it: calls whose GPU work overlaps (two streams, or two host threads)
+// race on it and must not be issued. Each call clears the part that has to
+// start at zero (the status word and plan header) and rebuilds the rest.
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace {
+
+constexpr size_t kScratchBytes = 16u << 20;  // 16 MiB
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) uint8_t g_scratch[kScratchBytes];
+
+// The host-side name g_scratch is only a stand-in for the device array; the
+// kernels get its device address, resolved once per device.
+void* g_scratch_ptr[kMaxDevices] = {};
+std::mutex g_scratch_mu;
+
+cudaError_t scratch_for_current_device(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" {
+
+mla_status mla_decode_paged_noalloc(const mla_config* cfg, const void* q_abs, const void* cache,
+                                    int64_t num_blocks, const int32_t* block_table,
+                                    int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                    const int32_t* query_start_loc, int32_t batch, int64_t num_q,
+                                    float* o_lat, uint32_t* dev_status, void* stream) {
+  if (num_q < 0) return MLA_ERR_INVALID_ARGUMENT;
+  if (num_q == 0) return MLA_OK;
+  if (!o_lat || (reinterpret_cast<uintptr_t>(o_lat) & 15) != 0) return MLA_ERR_INVALID_ARGUMENT;
+  if (dev_status && (reinterpret_cast<uintptr_t>(dev_status) & 3) != 0)
+    return MLA_ERR_INVALID_ARGUMENT;
+  // the scratch must hold this launch's workspace
+  const size_t need = mla_decode_workspace_size(cfg, num_q, batch);
+  if (need == 0) return cfg ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARGUMENT;
+  if (need > kScratchBytes) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  void* ws = nullptr;
+  if (scratch_for_current_device(&ws) != cudaSuccess) return MLA_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // status word and plan header start at zero on every call
+  if (cudaMemsetAsync(ws, 0, sizeof(mla::WsHeader), st) != cudaSuccess) return MLA_ERR_CUDA;
+  mla_status s = mla_decode_paged(cfg, q_abs, cache, num_blocks, block_table, max_blocks_per_seq,
+                                  seq_lens, query_start_loc, batch, num_q, ws, kScratchBytes,
+                                  stream);
+  if (s != MLA_OK) return s;
+  s = mla_combine(cfg, ws, kScratchBytes, batch, num_q, o_lat, stream);
+  if (s != MLA_OK) return s;
+  if (dev_status &&
+      cudaMemcpyAsync(dev_status, ws, sizeof(uint32_t), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+}  // extern "C"

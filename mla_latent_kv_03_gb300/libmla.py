@@ -29,7 +29,7 @@ DEV_TIMEOUT, DEV_BAD_BLOCK, DEV_BAD_SEQ, DEV_BAD_SLOT = 1, 2, 4, 8
 EXPORTS = (
     "mla_default_config", "mla_cache_write", "mla_absorb_q", "mla_decode_workspace_size",
     "mla_workspace_init", "mla_decode_paged", "mla_decode_plan", "mla_decode_planned",
-    "mla_decode_combine",
+    "mla_decode_combine", "mla_decode_paged_noalloc",
     "mla_combine", "mla_out_proj",
     "mla_get_device_status", "mla_selftest_wait_timeout", "mla_status_string", "mla_version",
 )
@@ -66,6 +66,8 @@ _SIGS = {
     "mla_decode_plan": (_i32, [_cfgp, _vp, _vp, _i32, _i64, _i32, _vp, _sz, _vp]),
     "mla_decode_planned": (_i32, [_cfgp, _vp, _vp, _i64, _vp, _i32, _i64, _vp, _sz, _vp]),
     "mla_decode_combine": (_i32, [_cfgp, _vp, _vp, _i64, _vp, _i32, _i64, _vp, _sz, _vp, _vp]),
+    "mla_decode_paged_noalloc": (_i32, [_cfgp, _vp, _vp, _i64, _vp, _i32, _vp, _vp, _i32, _i64,
+                                        _vp, _vp, _vp]),
     "mla_combine": (_i32, [_cfgp, _vp, _sz, _i32, _i64, _vp, _vp]),
     "mla_out_proj": (_i32, [_cfgp, _vp, _vp, _vp, _i64, _vp]),
     "mla_get_device_status": (_i32, [_vp, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int, _vp]),
@@ -216,6 +218,18 @@ def mla_decode_combine(cfg: MlaConfig, q_abs, cache, block_table, workspace, o_l
         _ptr(block_table, torch.int32, "block_table"), block_table.shape[1], q_abs.shape[0],
         _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
         _ptr(o_lat, torch.float32, "o_lat"), _stream(stream)), "mla_decode_combine")
+
+
+def mla_decode_paged_noalloc(cfg: MlaConfig, q_abs, cache, block_table, seq_lens,
+                             query_start_loc, o_lat, dev_status=None, stream=None) -> None:
+    """Decode + merge with the library's built-in scratch instead of a workspace."""
+    dt = _torch_dtype(cfg)
+    _check(load().mla_decode_paged_noalloc(
+        ctypes.byref(cfg), _ptr(q_abs, dt, "q_abs"), _ptr(cache, dt, "cache"), cache.shape[0],
+        _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+        _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(query_start_loc, torch.int32, "query_start_loc"),
+        seq_lens.shape[0], q_abs.shape[0], _ptr(o_lat, torch.float32, "o_lat"),
+        _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)), "mla_decode_paged_noalloc")
 
 
 def mla_combine(cfg: MlaConfig, workspace, batch: int, o_lat, stream=None) -> None:
