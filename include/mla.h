@@ -196,7 +196,10 @@ mla_status mla_decode_planned(const mla_config* cfg, const void* q_abs, const vo
  * mla_combine. The CTA that finishes a (row, 16-head group) last merges its
  * split partials while they are in L2; a (row, head group) handled by one
  * CTA is written to o_lat directly. The result equals mla_decode_planned
- * followed by mla_combine up to fp32 rounding of the merge order. The
+ * followed by mla_combine up to fp32 rounding of the merge order. When
+ * there are fewer than num_ctas / 4 (row, head group) tiles, the splits of
+ * each tile are many, and the call runs the decode kernel and then the merge
+ * kernel of mla_combine instead (same result). The
  * workspace's arrival counters are left at zero, so the call can be repeated
  * (e.g. per layer) on one plan; after a device error, plan again.
  */
@@ -252,6 +255,20 @@ mla_status mla_decode_paged_noalloc(const mla_config* cfg, const void* q_abs, co
                                     int32_t max_blocks_per_seq, const int32_t* seq_lens,
                                     const int32_t* query_start_loc, int32_t batch, int64_t num_q,
                                     float* o_lat, uint32_t* dev_status, void* stream);
+
+/*
+ * mla_combine_out_proj -- mla_combine followed by mla_out_proj without
+ * writing o_lat: the split partials that mla_decode_paged / mla_decode_planned
+ * left in the workspace are merged (split-softmax identity) while the mma
+ * fragments of the output projection are built.
+ *   out[n,h,v] = sum_c merge(n,h)[c] * W_uv[h][c][v]
+ *   W_uv [H, 512, 128] dtype; out [num_q, H, 128] dtype (output).
+ * cfg, batch and num_q must equal those of the decode call. Rows that see no
+ * token give zeros.
+ */
+mla_status mla_combine_out_proj(const mla_config* cfg, const void* workspace, size_t ws_bytes,
+                                int32_t batch, int64_t num_q, const void* W_uv, void* out,
+                                void* stream);
 
 /*
  * mla_get_device_status -- synchronise `stream`, read the device status word

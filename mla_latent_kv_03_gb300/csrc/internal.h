@@ -60,6 +60,10 @@ cudaError_t launch_combine(const void* workspace, int32_t groups, int32_t num_ct
 cudaError_t launch_out_proj(const mla_config& cfg, const float* o_lat, const void* W_uv,
                             void* out, int64_t num_q, cudaStream_t stream);
 
+cudaError_t launch_combine_out_proj(const mla_config& cfg, const void* workspace, int32_t groups,
+                                   int32_t num_ctas, int64_t num_q, const void* W_uv, void* out,
+                                   cudaStream_t stream);
+
 cudaError_t launch_wait_timeout_selftest(uint32_t* status, int64_t timeout_ns,
                                          cudaStream_t stream);
 

@@ -241,6 +241,20 @@ mla_status mla_decode_combine(const mla_config* cfg, const void* q_abs, const vo
                               int32_t max_blocks_per_seq, int64_t num_q, void* workspace,
                               size_t ws_bytes, float* o_lat, void* stream) {
   if (num_q > 0 && (!o_lat || !aligned(o_lat, 16))) return MLA_ERR_INVALID_ARGUMENT;
+  mla_status s = check_cfg(cfg);
+  if (s != MLA_OK) return s;
+  // With few (row, head group) tiles per CTA each tile is cut into many
+  // splits, and one CTA merging all of them at the end of the decode is slower
+  // than the merge kernel, which spreads that work over more CTAs.
+  const int C = resolve_num_ctas(cfg);
+  const int64_t qtiles = num_q * (cfg->num_heads / kHG);
+  if (C > 0 && qtiles * 4 < C) {
+    s = decode_impl(cfg, q_abs, cache, num_blocks, block_table, max_blocks_per_seq, num_q,
+                    workspace, ws_bytes, nullptr, stream);
+    if (s != MLA_OK) return s;
+    return from_cuda(launch_combine(workspace, cfg->num_heads / kHG, C, num_q, o_lat,
+                                    as_stream(stream)));
+  }
   return decode_impl(cfg, q_abs, cache, num_blocks, block_table, max_blocks_per_seq, num_q,
                      workspace, ws_bytes, o_lat, stream);
 }
@@ -283,6 +297,25 @@ mla_status mla_combine(const mla_config* cfg, const void* workspace, size_t ws_b
   const int G = cfg->num_heads / kHG;
   if (ws_bytes < ws_layout(num_q, G, C).total) return MLA_ERR_WORKSPACE_TOO_SMALL;
   return from_cuda(launch_combine(workspace, G, C, num_q, o_lat, as_stream(stream)));
+}
+
+mla_status mla_combine_out_proj(const mla_config* cfg, const void* workspace, size_t ws_bytes,
+                                int32_t batch, int64_t num_q, const void* W_uv, void* out,
+                                void* stream) {
+  mla_status s = check_cfg(cfg);
+  if (s != MLA_OK) return s;
+  if (num_q < 0 || batch < 0) return MLA_ERR_INVALID_ARGUMENT;
+  if (num_q > kMaxRows) return MLA_ERR_UNSUPPORTED;
+  if (num_q == 0) return MLA_OK;
+  if (!workspace || !W_uv || !out || !aligned(workspace, 256) || !aligned(W_uv, 16) ||
+      !aligned(out, 16))
+    return MLA_ERR_INVALID_ARGUMENT;
+  const int C = resolve_num_ctas(cfg);
+  if (C <= 0) return MLA_ERR_CUDA;
+  const int G = cfg->num_heads / kHG;
+  if (ws_bytes < ws_layout(num_q, G, C).total) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  return from_cuda(launch_combine_out_proj(*cfg, workspace, G, C, num_q, W_uv, out,
+                                           as_stream(stream)));
 }
 
 mla_status mla_out_proj(const mla_config* cfg, const float* o_lat, const void* W_uv, void* out,

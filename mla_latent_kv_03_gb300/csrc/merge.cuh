@@ -18,6 +18,8 @@ constexpr int kMergeChunk = 16;  // slots whose weights are staged at a time
 
 // Scratch: 32 + kMergeChunk * 16 floats of shared memory.
 // `sync` synchronises the `nthreads` participating threads (tid in [0, nthreads)).
+// All (slot, row) log-sum-exps of a chunk are fetched in one parallel round
+// trip; the partial rows of two slots are in flight at a time.
 template <int NTHREADS, typename Sync>
 __device__ __forceinline__ void merge_qtile(const float* __restrict__ lse,
                                             const float* __restrict__ opart, int64_t slot0,
@@ -27,15 +29,29 @@ __device__ __forceinline__ void merge_qtile(const float* __restrict__ lse,
   float* sM = scratch;
   float* sInv = scratch + kHG;
   float* sW = scratch + 2 * kHG;
-  if (tid < kHG) {
-    float M = -INFINITY;
-    for (int s = 0; s < nslots; ++s) M = fmaxf(M, lse[(slot0 + s) * kHG + tid]);
-    float den = 0.f;
-    if (M != -INFINITY)
-      for (int s = 0; s < nslots; ++s) den += fast_exp2(lse[(slot0 + s) * kHG + tid] - M);
-    sM[tid] = M;
-    sInv[tid] = den > 0.f ? 1.f / den : 0.f;
+  // pass 1: per-row maximum and weight sum over all slots (online over chunks)
+  if (tid < kHG) { sM[tid] = -INFINITY; sInv[tid] = 0.f; }
+  for (int s0 = 0; s0 < nslots; s0 += kMergeChunk) {
+    const int ns = min(kMergeChunk, nslots - s0);
+    sync();
+    for (int i = tid; i < ns * kHG; i += NTHREADS) sW[i] = lse[(slot0 + s0) * kHG + i];
+    sync();
+    if (tid < kHG) {
+      const float Mold = sM[tid];
+      float M = Mold;
+      for (int s = 0; s < ns; ++s) M = fmaxf(M, sW[s * kHG + tid]);
+      float den = 0.f;
+      if (M != -INFINITY) {
+        den = Mold == -INFINITY ? 0.f : sInv[tid] * fast_exp2(Mold - M);
+        for (int s = 0; s < ns; ++s) den += fast_exp2(sW[s * kHG + tid] - M);
+      }
+      sM[tid] = M;
+      sInv[tid] = den;  // running sum; inverted below
+    }
   }
+  sync();
+  if (tid < kHG) sInv[tid] = sInv[tid] > 0.f ? 1.f / sInv[tid] : 0.f;
+  // pass 2: weighted sum of the partial rows
   float4 acc[kItems];
 #pragma unroll
   for (int j = 0; j < kItems; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -46,20 +62,28 @@ __device__ __forceinline__ void merge_qtile(const float* __restrict__ lse,
     for (int i = tid; i < ns * kHG; i += NTHREADS) {
       const int r = i % kHG;
       const float M = sM[r];
-      sW[i] = M == -INFINITY ? 0.f : fast_exp2(lse[(slot0 + s0 + i / kHG) * kHG + r] - M) * sInv[r];
+      sW[i] = M == -INFINITY ? 0.f : fast_exp2(lse[(slot0 + s0) * kHG + i] - M) * sInv[r];
     }
     sync();
-    for (int s = 0; s < ns; ++s) {
-      const float4* src = op + (slot0 + s0 + s) * (kHG * kDc / 4);
+    for (int s = 0; s < ns; s += 2) {
+      const bool two = s + 1 < ns;
+      const float4* src0 = op + (slot0 + s0 + s) * (kHG * kDc / 4);
+      const float4* src1 = two ? src0 + kHG * kDc / 4 : src0;
+      float4 v0[kItems], v1[kItems];
 #pragma unroll
       for (int j = 0; j < kItems; ++j) {
-        const int item = tid + j * NTHREADS;
-        const float w = sW[s * kHG + item / (kDc / 4)];
-        const float4 v = src[item];
-        acc[j].x = fmaf(w, v.x, acc[j].x);
-        acc[j].y = fmaf(w, v.y, acc[j].y);
-        acc[j].z = fmaf(w, v.z, acc[j].z);
-        acc[j].w = fmaf(w, v.w, acc[j].w);
+        v0[j] = src0[tid + j * NTHREADS];
+        v1[j] = src1[tid + j * NTHREADS];
+      }
+#pragma unroll
+      for (int j = 0; j < kItems; ++j) {
+        const int row = (tid + j * NTHREADS) / (kDc / 4);
+        const float w0 = sW[s * kHG + row];
+        const float w1 = two ? sW[(s + 1) * kHG + row] : 0.f;
+        acc[j].x = fmaf(w1, v1[j].x, fmaf(w0, v0[j].x, acc[j].x));
+        acc[j].y = fmaf(w1, v1[j].y, fmaf(w0, v0[j].y, acc[j].y));
+        acc[j].z = fmaf(w1, v1[j].z, fmaf(w0, v0[j].z, acc[j].z));
+        acc[j].w = fmaf(w1, v1[j].w, fmaf(w0, v0[j].w, acc[j].w));
       }
     }
   }

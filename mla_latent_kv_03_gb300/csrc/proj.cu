@@ -238,6 +238,214 @@ __global__ void __launch_bounds__(128) out_proj_bf16_kernel(const float* __restr
   }
 }
 
+// ---------------------------------------------------------------------------
+// combine + out_proj, bf16: out[n,h,:] = merge_s(partials of (n, h)) @ W_uv[h].
+// Same tiling as out_proj; the A fragments are merged on the fly from the
+// decode's split partials (split-softmax identity, base-2 lse) instead of
+// being read from o_lat, which is never materialised. Per CTA row r the merge
+// parameters (first slot, number of slots, max lse, 1 / weight sum) are
+// computed once into shared memory.
+// ---------------------------------------------------------------------------
+struct MergeRow {
+  int slot0, nslots;
+  float M, inv;
+};
+
+template <int MW>
+__global__ void __launch_bounds__(128) combine_out_proj_bf16_kernel(
+    const uint8_t* __restrict__ ws, int groups, int num_ctas, int num_q,
+    const __nv_bfloat16* __restrict__ W_uv, __nv_bfloat16* __restrict__ out, int H) {
+  extern __shared__ __align__(1024) uint8_t smem_cp[];
+  constexpr int ROWS = 16 * MW;
+  constexpr int KS = MW == 1 ? 8 : 32;
+  uint8_t* sB = smem_cp;                                          // 512 x 128 B
+  float* sRed = reinterpret_cast<float*>(smem_cp + 512 * 128);    // [4][16][64] (MW == 1)
+  MergeRow* sRow = reinterpret_cast<MergeRow*>(smem_cp + 512 * 128 + (MW == 1 ? 4 * 16 * 64 * 4 : 0));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, q = lane & 3;
+  const int h = blockIdx.z, row0 = blockIdx.x * ROWS, col0 = blockIdx.y * 64;
+
+  const __nv_bfloat16* src = W_uv + (size_t)h * kDc * kDv + col0;
+  for (int i = tid; i < 512 * 8; i += 128) {
+    const int r = i >> 3, ch = i & 7;
+    cp_async16(sB + sw128(r, ch), src + (size_t)r * kDv + ch * 8);
+  }
+  cp_async_commit();
+  // the weights do not depend on earlier kernels; the partials do
+  pdl_wait();
+  pdl_launch_dependents();
+
+  const WsHeader* hdr = reinterpret_cast<const WsHeader*>(ws);
+  const WsLayout L = ws_layout(num_q, groups, num_ctas);
+  const int4* row_info = reinterpret_cast<const int4*>(ws + L.row_info);
+  const float* lse = reinterpret_cast<const float*>(ws + L.lse);
+  const float* opart = reinterpret_cast<const float*>(ws + L.opart);
+  const bool plan_ok = hdr->magic == kMagic && hdr->num_q == num_q && hdr->groups == groups &&
+                       hdr->num_ctas == num_ctas;
+  const int hg = h / kHG, hr = h % kHG;
+  for (int r = tid; r < ROWS; r += 128) {
+    const int n = row0 + r;
+    MergeRow mr{0, 0, 0.f, 0.f};
+    const int4 ri = (plan_ok && n < num_q) ? row_info[n] : make_int4(-1, -1, 0, 0);
+    if (ri.z > 0) {
+      const int share = hdr->share;
+      const int t = n * groups + hg;
+      const int U = ri.w + hg * ri.z;
+      const int cf = U / share, cl = (U + ri.z - 1) / share;
+      mr.slot0 = cf + t;
+      mr.nslots = cl - cf + 1;
+      float M = -INFINITY;
+      for (int s = 0; s < mr.nslots; ++s) M = fmaxf(M, lse[(size_t)(mr.slot0 + s) * kHG + hr]);
+      float den = 0.f;
+      if (M != -INFINITY)
+        for (int s = 0; s < mr.nslots; ++s) den += fast_exp2(lse[(size_t)(mr.slot0 + s) * kHG + hr] - M);
+      mr.M = M;
+      mr.inv = den > 0.f ? 1.f / den : 0.f;
+      if (M == -INFINITY) mr.nslots = 0;
+    }
+    sRow[r] = mr;
+  }
+  __syncthreads();
+
+  const int wr = MW == 1 ? 0 : warp;
+  const int k0 = MW == 1 ? warp * 128 : 0;
+  const int rl_lo = 16 * wr + g, rl_hi = rl_lo + 8;
+  const MergeRow m_lo = sRow[rl_lo], m_hi = sRow[rl_hi];
+  // merged (o_lat) value pair at column k of a local row
+  auto merged2 = [&](const MergeRow& m, int k) {
+    float2 acc = make_float2(0.f, 0.f);
+    for (int s = 0; s < m.nslots; ++s) {
+      const size_t slot = (size_t)(m.slot0 + s);
+      const float w = fast_exp2(lse[slot * kHG + hr] - m.M) * m.inv;
+      const float2 v = *reinterpret_cast<const float2*>(opart + (slot * kHG + hr) * kDc + k);
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+    }
+    return acc;
+  };
+  auto load_a = [&](int ks, uint32_t* a) {
+    const int k = k0 + ks * 16 + 2 * q;
+    float2 x;
+    x = merged2(m_lo, k);     a[0] = pack_bf16(x.x, x.y);
+    x = merged2(m_hi, k);     a[1] = pack_bf16(x.x, x.y);
+    x = merged2(m_lo, k + 8); a[2] = pack_bf16(x.x, x.y);
+    x = merged2(m_hi, k + 8); a[3] = pack_bf16(x.x, x.y);
+  };
+  uint32_t apre[8][4];
+  if (MW == 1) {
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) load_a(ks, apre[ks]);
+  }
+  cp_async_wait_all();
+  __syncthreads();
+
+  float acc[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks) {
+    uint32_t a[4];
+    if (MW == 1) {
+      a[0] = apre[ks & 7][0]; a[1] = apre[ks & 7][1]; a[2] = apre[ks & 7][2]; a[3] = apre[ks & 7][3];
+    } else {
+      load_a(ks, a);
+    }
+    const int kr = k0 + ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+    for (int np = 0; np < 4; ++np) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(smem_u32(sB + sw128(kr, np * 2 + (lane >> 4))), b0, b1, b2, b3);
+      mma_16816(acc[2 * np], a[0], a[1], a[2], a[3], b0, b1);
+      mma_16816(acc[2 * np + 1], a[0], a[1], a[2], a[3], b2, b3);
+    }
+  }
+  const int r_lo = row0 + rl_lo, r_hi = row0 + rl_hi;
+  if (MW == 1) {
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      float* d = sRed + (warp * 16 + g) * 64 + nt * 8 + 2 * q;
+      d[0] = acc[nt][0]; d[1] = acc[nt][1];
+      d[8 * 64] = acc[nt][2]; d[8 * 64 + 1] = acc[nt][3];
+    }
+    __syncthreads();
+    for (int i = tid; i < 16 * 32; i += 128) {
+      const int r = i >> 5, c = (i & 31) * 2;
+      const int row = row0 + r;
+      if (row >= num_q) continue;
+      float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        v0 += sRed[(w * 16 + r) * 64 + c];
+        v1 += sRed[(w * 16 + r) * 64 + c + 1];
+      }
+      *reinterpret_cast<uint32_t*>(out + ((size_t)row * H + h) * kDv + col0 + c) = pack_bf16(v0, v1);
+    }
+  } else {
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      const int col = col0 + nt * 8 + 2 * q;
+      if (r_lo < num_q)
+        *reinterpret_cast<uint32_t*>(out + ((size_t)r_lo * H + h) * kDv + col) =
+            pack_bf16(acc[nt][0], acc[nt][1]);
+      if (r_hi < num_q)
+        *reinterpret_cast<uint32_t*>(out + ((size_t)r_hi * H + h) * kDv + col) =
+            pack_bf16(acc[nt][2], acc[nt][3]);
+    }
+  }
+}
+
+// combine + out_proj, fp32: one CTA per (row n, head h); the merged latent
+// row goes to shared memory, then 128 threads take one output column each.
+__global__ void __launch_bounds__(128) combine_out_proj_f32_kernel(
+    const uint8_t* __restrict__ ws, int groups, int num_ctas, int num_q,
+    const float* __restrict__ W_uv, float* __restrict__ out, int H) {
+  __shared__ float so[kDc];
+  __shared__ MergeRow sr;
+  const int n = blockIdx.x, h = blockIdx.y, t0 = threadIdx.x;
+  const WsHeader* hdr = reinterpret_cast<const WsHeader*>(ws);
+  const WsLayout L = ws_layout(num_q, groups, num_ctas);
+  const int4* row_info = reinterpret_cast<const int4*>(ws + L.row_info);
+  const float* lse = reinterpret_cast<const float*>(ws + L.lse);
+  const float* opart = reinterpret_cast<const float*>(ws + L.opart);
+  const int hg = h / kHG, hr = h % kHG;
+  if (t0 == 0) {
+    const bool plan_ok = hdr->magic == kMagic && hdr->num_q == num_q && hdr->groups == groups &&
+                         hdr->num_ctas == num_ctas;
+    MergeRow mr{0, 0, 0.f, 0.f};
+    const int4 ri = plan_ok ? row_info[n] : make_int4(-1, -1, 0, 0);
+    if (ri.z > 0) {
+      const int t = n * groups + hg, U = ri.w + hg * ri.z, share = hdr->share;
+      const int cf = U / share, cl = (U + ri.z - 1) / share;
+      mr.slot0 = cf + t;
+      mr.nslots = cl - cf + 1;
+      float M = -INFINITY;
+      for (int s = 0; s < mr.nslots; ++s) M = fmaxf(M, lse[(size_t)(mr.slot0 + s) * kHG + hr]);
+      float den = 0.f;
+      if (M != -INFINITY)
+        for (int s = 0; s < mr.nslots; ++s) den += fast_exp2(lse[(size_t)(mr.slot0 + s) * kHG + hr] - M);
+      mr.M = M;
+      mr.inv = den > 0.f ? 1.f / den : 0.f;
+      if (M == -INFINITY) mr.nslots = 0;
+    }
+    sr = mr;
+  }
+  __syncthreads();
+  const MergeRow mr = sr;
+  for (int c = t0; c < kDc; c += 128) {
+    float acc = 0.f;
+    for (int s = 0; s < mr.nslots; ++s) {
+      const size_t slot = (size_t)(mr.slot0 + s);
+      acc = fmaf(fast_exp2(lse[slot * kHG + hr] - mr.M) * mr.inv, opart[(slot * kHG + hr) * kDc + c], acc);
+    }
+    so[c] = acc;
+  }
+  __syncthreads();
+  const float* w = W_uv + (size_t)h * kDc * kDv + t0;
+  float s = 0.f;
+  for (int c = 0; c < kDc; ++c) s = fmaf(so[c], w[(size_t)c * kDv], s);
+  out[((size_t)n * H + h) * kDv + t0] = s;
+}
+
 // fp32 SIMT: one CTA per (row n, head h).
 __global__ void __launch_bounds__(128) absorb_f32_kernel(
     const float* __restrict__ q_nope, const float* __restrict__ q_pe,
@@ -330,6 +538,32 @@ cudaError_t launch_out_proj(const mla_config& cfg, const float* o_lat, const voi
                       (int)num_q, H);
   }
   return cudaGetLastError();
+}
+
+cudaError_t launch_combine_out_proj(const mla_config& cfg, const void* workspace, int32_t groups,
+                                   int32_t num_ctas, int64_t num_q, const void* W_uv, void* out,
+                                   cudaStream_t stream) {
+  if (num_q == 0) return cudaSuccess;
+  const int H = cfg.num_heads;
+  const uint8_t* ws = (const uint8_t*)workspace;
+  if (cfg.dtype == MLA_F32) {
+    return launch_pdl(combine_out_proj_f32_kernel, dim3((unsigned)num_q, H), dim3(128), 0, stream,
+                      ws, groups, num_ctas, (int)num_q, (const float*)W_uv, (float*)out, H);
+  }
+  const bool big = num_q >= 256;
+  const int smem = 512 * 128 + (big ? 0 : 4 * 16 * 64 * 4) + (big ? 64 : 16) * (int)sizeof(MergeRow);
+  cudaError_t e = big ? cudaFuncSetAttribute(combine_out_proj_bf16_kernel<4>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
+                      : cudaFuncSetAttribute(combine_out_proj_bf16_kernel<1>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  if (big)
+    return launch_pdl(combine_out_proj_bf16_kernel<4>, dim3((unsigned)((num_q + 63) / 64), 2, H),
+                      dim3(128), smem, stream, ws, groups, num_ctas, (int)num_q,
+                      (const __nv_bfloat16*)W_uv, (__nv_bfloat16*)out, H);
+  return launch_pdl(combine_out_proj_bf16_kernel<1>, dim3((unsigned)((num_q + 15) / 16), 2, H),
+                    dim3(128), smem, stream, ws, groups, num_ctas, (int)num_q,
+                    (const __nv_bfloat16*)W_uv, (__nv_bfloat16*)out, H);
 }
 
 }  // namespace mla

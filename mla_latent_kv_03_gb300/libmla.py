@@ -29,7 +29,7 @@ DEV_TIMEOUT, DEV_BAD_BLOCK, DEV_BAD_SEQ, DEV_BAD_SLOT = 1, 2, 4, 8
 EXPORTS = (
     "mla_default_config", "mla_cache_write", "mla_absorb_q", "mla_decode_workspace_size",
     "mla_workspace_init", "mla_decode_paged", "mla_decode_plan", "mla_decode_planned",
-    "mla_decode_combine", "mla_decode_paged_noalloc",
+    "mla_decode_combine", "mla_decode_paged_noalloc", "mla_combine_out_proj",
     "mla_combine", "mla_out_proj",
     "mla_get_device_status", "mla_selftest_wait_timeout", "mla_status_string", "mla_version",
 )
@@ -69,6 +69,7 @@ _SIGS = {
     "mla_decode_paged_noalloc": (_i32, [_cfgp, _vp, _vp, _i64, _vp, _i32, _vp, _vp, _i32, _i64,
                                         _vp, _vp, _vp]),
     "mla_combine": (_i32, [_cfgp, _vp, _sz, _i32, _i64, _vp, _vp]),
+    "mla_combine_out_proj": (_i32, [_cfgp, _vp, _sz, _i32, _i64, _vp, _vp, _vp]),
     "mla_out_proj": (_i32, [_cfgp, _vp, _vp, _vp, _i64, _vp]),
     "mla_get_device_status": (_i32, [_vp, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int, _vp]),
     "mla_selftest_wait_timeout": (_i32, [_vp, _i64, _vp]),
@@ -237,6 +238,15 @@ def mla_combine(cfg: MlaConfig, workspace, batch: int, o_lat, stream=None) -> No
         ctypes.byref(cfg), _ptr(workspace, None, "workspace"),
         workspace.numel() * workspace.element_size(), batch, o_lat.shape[0],
         _ptr(o_lat, torch.float32, "o_lat"), _stream(stream)), "mla_combine")
+
+
+def mla_combine_out_proj(cfg: MlaConfig, workspace, batch: int, num_q: int, W_uv, out,
+                         stream=None) -> None:
+    dt = _torch_dtype(cfg)
+    _check(load().mla_combine_out_proj(
+        ctypes.byref(cfg), _ptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(), batch, num_q, _ptr(W_uv, dt, "W_uv"),
+        _ptr(out, dt, "out"), _stream(stream)), "mla_combine_out_proj")
 
 
 def mla_out_proj(cfg: MlaConfig, o_lat, W_uv, out, stream=None) -> None:

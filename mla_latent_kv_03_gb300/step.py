@@ -108,6 +108,10 @@ class MlaDecodeStep:
     def combine(self, stream=None) -> None:
         L.mla_combine(self.cfg, self.workspace, self.w.batch, self.o_lat, stream=stream)
 
+    def combine_out_proj(self, stream=None) -> None:
+        L.mla_combine_out_proj(self.cfg, self.workspace, self.w.batch, self.w.num_q, self.W_uv,
+                               self.out, stream=stream)
+
     def out_proj(self, stream=None) -> None:
         L.mla_out_proj(self.cfg, self.o_lat, self.W_uv, self.out, stream=stream)
 

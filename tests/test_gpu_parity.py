@@ -267,10 +267,12 @@ def test_fused_decode_combine_matches_oracle_and_unfused(name, num_ctas):
 
 
 def test_fused_merge_of_many_splits():
-    # one 2,000-token row over 500 CTAs: 32 single-tile parts, more than one
-    # chunk of staged merge weights
-    w = W.make("many", [2000, 1, 333, 64], [1, 1, 1, 1], 16, 64, "bf16", seed=45)
-    s = MlaDecodeStep(w, device=DEV, num_ctas=500)
+    # 12 q-tiles over 40 CTAs keeps the merge inside the decode kernel; the
+    # 3,000-token row (47 tiles, 2 per CTA) is cut into 24 parts, more than
+    # one chunk of staged merge weights
+    lens = [3000] + [1] * 9 + [333, 64]
+    w = W.make("many", lens, [1] * len(lens), 16, 64, "bf16", seed=45)
+    s = MlaDecodeStep(w, device=DEV, num_ctas=40)
     s.populate()
     s.absorb()
     s.plan()
@@ -294,3 +296,37 @@ def test_fused_decode_combine_repeats_on_one_plan():
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
     ref = ref_o_lat_from(w, to_f64(s.cache), to_f64(s.q_abs))
     assert_close(to_f64(outs[2]), ref, "bf16", "third launch on one plan")
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+@pytest.mark.parametrize("num_ctas", [0, 7, 500])
+def test_combine_out_proj_matches_separate_calls_and_oracle(name, num_ctas):
+    w = SMALL[name]()
+    s = MlaDecodeStep(w, device=DEV, num_ctas=num_ctas)
+    s.populate()
+    s.absorb()
+    s.plan()
+    s.decode_planned()
+    s.out.fill_(float("nan"))
+    s.combine_out_proj()
+    torch.cuda.synchronize()
+    fused = to_f64(s.out)
+    assert_close(fused, ref_out(w), w.dtype, f"combine_out_proj {name}")
+    s.combine()
+    s.out_proj()
+    sep = to_f64(s.out)
+    if w.dtype == "f32":
+        np.testing.assert_allclose(fused, sep, rtol=0, atol=1e-6)
+    else:  # both round the merged row to bf16 for the mma; the merge order differs
+        assert np.max(np.abs(fused - sep)) <= 2e-3
+
+
+def test_combine_out_proj_many_rows():
+    w = W.make("cop_big", [300] * 3 + [1] * 300, [100] * 3 + [1] * 300, 16, 64, "bf16", seed=47)
+    s = MlaDecodeStep(w, device=DEV)
+    s.populate()
+    s.absorb()
+    s.plan()
+    s.decode_planned()
+    s.combine_out_proj()
+    assert_close(to_f64(s.out), ref_out(w), "bf16", "combine_out_proj, 600 rows")
