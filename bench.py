@@ -44,6 +44,7 @@ if ROOT not in sys.path:
 METRIC = "MLA paged decode: latent-cache GB/s (% of HBM peak), µs/step at B=64,L=4096"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 DECODE_SOURCES = ["decode_bf16.cu", "common.cuh", "sched.cuh", "merge.cuh", "async_copy.cuh"]
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_bf16_serving_B64_L4096.md")
 
@@ -109,6 +110,15 @@ def sum_over_ranks(x: float, world: int) -> float:
 # ---------------------------------------------------------------------------
 # peaks, clocks, profile summary
 # ---------------------------------------------------------------------------
+
+def tensor_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
 
 def hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -223,6 +233,8 @@ def make_workload(name: str, rank: int):
         return W.serving(seed=3 + 1000 * rank, batch=48)
     if name == "ragged_h128":
         return W.ragged_h128(seed=4 + 1000 * rank)
+    if name == "ragged_h128_b8":   # 8 of the ragged many-head rows (> L2), for ncu
+        return W.ragged_h128(seed=4 + 1000 * rank, batch=8)
     if name == "mixed":
         return W.mixed(seed=5 + 1000 * rank)
     if name.startswith("v2lite_"):
@@ -406,9 +418,22 @@ def run_ours(args, world, rank, local):
     decode_bytes = latent + int(w.block_table.size) * 4
     peak, peak_kind = hbm_peak()
     achieved = decode_bytes / (kernel_ms * 1e-3) / 1e9
+    mode = s.decode_mode()
+    # (row, head) x visible token pairs, each a 576-wide score and a 512-wide
+    # accumulation: the tensor-core work the attention needs at the least
+    attn_flops = int(w.num_heads) * int(sum(int(p) + 1 for p in w.q_positions)) * (576 + 512) * 2
+    tpeak, _ = tensor_peak()
+    kernel = ("decode_f32_kernel" if w.dtype != "bf16" else
+              "decode_tc_kernel" if mode == 1 else "decode_bf16_kernel")
+    # the committed DRAM figure belongs to the warp-mma kernel on the serving batch
+    traffic = profiled_traffic() if (kernel == "decode_bf16_kernel" and
+                                     args.workload == "serving") else None
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
-                "kernel": "decode_bf16_kernel" if w.dtype == "bf16" else "decode_f32_kernel",
+                "frac": round(achieved / peak, 4), "traffic": traffic,
+                "kernel": kernel,
+                "attention_tflops": round(attn_flops / (kernel_ms * 1e-3) / 1e12, 1),
+                "attention_tensor_frac": round(attn_flops / (kernel_ms * 1e-3) / 1e12 / tpeak, 4),
+                "attention_flops": attn_flops,
                 "kernel_us": round(kernel_ms * 1e3, 2), "algorithmic_bytes": decode_bytes,
                 "peak_kind": f"{peak_kind} HBM copy bandwidth (burst)",
                 "frac_of_nominal_8TBs": round(achieved / NOMINAL_HBM_GBS, 4)}

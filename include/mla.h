@@ -162,6 +162,11 @@ mla_status mla_workspace_init(void* workspace, size_t ws_bytes, void* stream);
  *   last block are never read); seq_lens [batch] int32;
  *   query_start_loc [batch + 1] int32 (query_start_loc[batch] == num_q).
  * The same workspace must be passed, unchanged, to mla_combine().
+ * Kernel choice (the same for every call given cfg, num_q and batch): with
+ * bf16 and either num_heads >= 64 or num_q >= 4 * batch (prefill chunks),
+ * tiles are 128 (row, head) rows on tcgen05 tensor cores with the
+ * accumulator in TMEM (one query row of 128 heads, or 8 rows of 16 heads);
+ * otherwise tiles are one row x 16 heads on warp mma.
  */
 mla_status mla_decode_paged(const mla_config* cfg, const void* q_abs, const void* cache,
                             int64_t num_blocks, const int32_t* block_table,
@@ -186,8 +191,8 @@ mla_status mla_decode_plan(const mla_config* cfg, const int32_t* seq_lens,
                            void* stream);
 mla_status mla_decode_planned(const mla_config* cfg, const void* q_abs, const void* cache,
                               int64_t num_blocks, const int32_t* block_table,
-                              int32_t max_blocks_per_seq, int64_t num_q, void* workspace,
-                              size_t ws_bytes, void* stream);
+                              int32_t max_blocks_per_seq, int32_t batch, int64_t num_q,
+                              void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * mla_decode_combine -- mla_decode_planned and mla_combine in one kernel.
@@ -205,8 +210,8 @@ mla_status mla_decode_planned(const mla_config* cfg, const void* q_abs, const vo
  */
 mla_status mla_decode_combine(const mla_config* cfg, const void* q_abs, const void* cache,
                               int64_t num_blocks, const int32_t* block_table,
-                              int32_t max_blocks_per_seq, int64_t num_q, void* workspace,
-                              size_t ws_bytes, float* o_lat, void* stream);
+                              int32_t max_blocks_per_seq, int32_t batch, int64_t num_q,
+                              void* workspace, size_t ws_bytes, float* o_lat, void* stream);
 
 /*
  * mla_combine -- merge the split partials of mla_decode_paged.
@@ -238,8 +243,11 @@ mla_status mla_out_proj(const mla_config* cfg, const float* o_lat, const void* W
  * The caller passes the same inputs as mla_decode_paged and the output
  * o_lat [num_q, H, 512] float32 of mla_combine; the workspace is instead a
  * 16 MiB array built into the library, which every GPU that loads the
- * library keeps until the process exits. A launch whose workspace
- * (mla_decode_workspace_size) exceeds 16 MiB returns
+ * library keeps until the process exits. With cfg->num_ctas = 0 and a
+ * workspace (mla_decode_workspace_size) above 16 MiB at the default count,
+ * the call uses the largest CTA count c below the SM count for which
+ * mla_decode_workspace_size with num_ctas = c fits. A launch that does not
+ * fit even so, or with the caller's fixed num_ctas, returns
  * MLA_ERR_WORKSPACE_TOO_SMALL and enqueues nothing.
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream

@@ -48,7 +48,9 @@ struct WsHeader {
   int32_t groups;       // G = H / 16
   int32_t num_q;
   int32_t batch;
-  uint32_t pad[56];
+  int32_t mode;         // 0: units per (row, 16-head group); 1: per 128-row q-block
+  int32_t qblocks;      // mode 1: number of q-blocks
+  uint32_t pad[54];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -70,6 +72,89 @@ __host__ __device__ inline WsLayout ws_layout(int64_t num_q, int groups, int num
   L.arrive = off;     off = align_up(off + (size_t)num_q * groups * 4, 256);
   L.total = off;
   return L;
+}
+
+// Mode-1 workspace (the tensor-core kernel for many heads or prefill rows).
+// A q-block is 8 consecutive q-tiles (128 consecutive (row, head) rows of
+// q_abs) of one sequence; work units are (q-block, 64-token tile); each share
+// of units is processed by two CTAs, one per 256-column half of the output.
+//   [0, 256)              WsHeader (mode = 1)
+//   row_info[num_q]       int4 {seq b, query position, tiles, 0}
+//   seq_info[batch]       int4 {first q-tile, first q-block, end q-tile, 0}
+//   qblock[QB]            int4 {seq b, first q-tile, tiles, first unit}
+//   cta_start[shares]     int4 {q-block, tile, 0, 0}
+//   lse[S][128]           float (base 2)
+//   opart[S][128][512]    float
+//   arrive[QB][2]         int (fused merge, per output half)
+// with QB = ceil(num_q * G / 8) + batch and S = shares + QB; the slot of
+// (share c, q-block qb) is c + qb. Rows [16 sub, 16 sub + 16) of a slot are
+// q-tile (first q-tile + sub), so in units of 16-row groups the q-tile's
+// partials sit at (c + qb) * 8 + sub, stride 8 between shares.
+constexpr int kQBlockTiles = 8;
+constexpr int kQBlockRows = kQBlockTiles * kHG;  // 128
+
+struct WsLayoutTc {
+  size_t row_info, seq_info, qblock, cta_start, lse, opart, arrive, total;
+  int64_t qblocks_max, slots;
+};
+
+__host__ __device__ inline WsLayoutTc ws_layout_tc(int64_t num_q, int groups, int shares,
+                                                   int batch) {
+  WsLayoutTc L;
+  L.qblocks_max = (num_q * groups + kQBlockTiles - 1) / kQBlockTiles + batch;
+  L.slots = (int64_t)shares + L.qblocks_max;
+  size_t off = sizeof(WsHeader);
+  L.row_info = off;  off = align_up(off + (size_t)num_q * 16, 256);
+  L.seq_info = off;  off = align_up(off + (size_t)batch * 16, 256);
+  L.qblock = off;    off = align_up(off + (size_t)L.qblocks_max * 16, 256);
+  L.cta_start = off; off = align_up(off + (size_t)shares * 16, 256);
+  L.lse = off;       off = align_up(off + (size_t)L.slots * kQBlockRows * 4, 256);
+  L.opart = off;     off = align_up(off + (size_t)L.slots * kQBlockRows * kDc * 4, 256);
+  L.arrive = off;    off = align_up(off + (size_t)L.qblocks_max * 2 * 4, 256);
+  L.total = off;
+  return L;
+}
+
+// Where the split partials of q-tile t (query row n, head group g) live, in
+// units of 16-row x 512 groups of the partial buffer: `count` groups starting
+// at `first`, `stride` apart. count = 0: the q-tile saw no token.
+struct QtileParts {
+  int64_t first;
+  int stride, count;
+};
+
+__device__ __forceinline__ QtileParts locate_qtile(const uint8_t* ws, int64_t num_q, int groups,
+                                                   int num_ctas, int batch, int n, int g) {
+  const WsHeader* hdr = reinterpret_cast<const WsHeader*>(ws);
+  QtileParts r{0, 1, 0};
+  if (hdr->magic != kMagic || hdr->num_q != num_q || hdr->groups != groups ||
+      hdr->num_ctas != num_ctas)
+    return r;
+  const int share = hdr->share;
+  const int t = n * groups + g;
+  if (hdr->mode == 0) {
+    const WsLayout L = ws_layout(num_q, groups, num_ctas);
+    const int4 ri = reinterpret_cast<const int4*>(ws + L.row_info)[n];
+    if (ri.z <= 0) return r;
+    const int U = ri.w + g * ri.z;
+    const int cf = U / share, cl = (U + ri.z - 1) / share;
+    r.first = (int64_t)cf + t;
+    r.count = cl - cf + 1;
+    return r;
+  }
+  const WsLayoutTc L = ws_layout_tc(num_q, groups, num_ctas / 2, batch);
+  const int4 ri = reinterpret_cast<const int4*>(ws + L.row_info)[n];
+  if (ri.z <= 0 || ri.x < 0 || ri.x >= batch) return r;
+  const int4 si = reinterpret_cast<const int4*>(ws + L.seq_info)[ri.x];
+  const int li = t - si.x;
+  const int qb = si.y + li / kQBlockTiles, sub = li % kQBlockTiles;
+  if (li < 0 || qb < 0 || qb >= hdr->qblocks) return r;
+  const int4 bi = reinterpret_cast<const int4*>(ws + L.qblock)[qb];
+  const int cf = bi.w / share, cl = (bi.w + bi.z - 1) / share;
+  r.first = ((int64_t)cf + qb) * kQBlockTiles + sub;
+  r.stride = kQBlockTiles;
+  r.count = cl - cf + 1;
+  return r;
 }
 
 // ---------------------------------------------------------------------------

@@ -384,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool last = flag[0] != 0;
       if (last) {
         __threadfence();
-        merge_qtile<kMathWarps * 32>(lse_out, o_out, (int64_t)c_first + t, c_last - c_first + 1,
+        merge_qtile<kMathWarps * 32>(lse_out, o_out, (int64_t)c_first + t, c_last - c_first + 1, 1,
                                      a.o_lat + ((size_t)seg.n * a.num_heads + seg.g * kHG) * kDc, tid,
                                      merge_scratch, [] { named_bar_sync(kMathBar, kMathWarps * 32); });
         if (tid == 0) arrive[t] = 0;  // every part has arrived: ready for the next launch

@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(256) decode_f32_kernel(DecodeArgs a) {
       __syncthreads();
       if (sFlag[0]) {
         __threadfence();
-        merge_qtile<256>(lse_out, o_out, (int64_t)c_first + t, c_last - c_first + 1,
+        merge_qtile<256>(lse_out, o_out, (int64_t)c_first + t, c_last - c_first + 1, 1,
                          a.o_lat + ((size_t)seg.n * a.num_heads + seg.g * kHG) * kDc, tid, sMerge,
                          [] { __syncthreads(); });
         if (tid == 0) arrive[t] = 0;  // every part has arrived: ready for the next launch

@@ -48,21 +48,25 @@ cudaError_t launch_absorb_q(const mla_config& cfg, const void* q_nope, const voi
                             int64_t num_q, cudaStream_t stream);
 
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream);
+cudaError_t launch_plan_tc(const PlanArgs& a, cudaStream_t stream);
 
 cudaError_t launch_decode_bf16(const DecodeArgs& a, const CUtensorMap& cache_map,
                                const CUtensorMap& q_map, cudaStream_t stream);
 
 cudaError_t launch_decode_f32(const DecodeArgs& a, cudaStream_t stream);
 
+cudaError_t launch_decode_tc(const DecodeArgs& a, int32_t batch, const CUtensorMap& cache_map,
+                             const CUtensorMap& q_map, cudaStream_t stream);
+
 cudaError_t launch_combine(const void* workspace, int32_t groups, int32_t num_ctas,
-                           int64_t num_q, float* o_lat, cudaStream_t stream);
+                           int64_t num_q, int32_t batch, float* o_lat, cudaStream_t stream);
 
 cudaError_t launch_out_proj(const mla_config& cfg, const float* o_lat, const void* W_uv,
                             void* out, int64_t num_q, cudaStream_t stream);
 
 cudaError_t launch_combine_out_proj(const mla_config& cfg, const void* workspace, int32_t groups,
-                                   int32_t num_ctas, int64_t num_q, const void* W_uv, void* out,
-                                   cudaStream_t stream);
+                                   int32_t num_ctas, int64_t num_q, int32_t batch, const void* W_uv,
+                                   void* out, cudaStream_t stream);
 
 cudaError_t launch_wait_timeout_selftest(uint32_t* status, int64_t timeout_ns,
                                          cudaStream_t stream);

@@ -49,6 +49,26 @@ int resolve_num_ctas(const mla_config* cfg) {
 
 constexpr int64_t kMaxRows = 48 * 1024;  // query rows one plan can hold in shared memory
 
+// Tiles of 128 (row, head) rows on tcgen05 when a 16-head tile would waste
+// the cache stream: many heads, or prefill chunks (several query rows per
+// sequence on average). Plain decode with 16 or 32 heads uses warp mma.
+bool use_tc(const mla_config* cfg, int64_t num_q, int32_t batch) {
+  return cfg->dtype == MLA_BF16 && (cfg->num_heads >= 64 || num_q >= 4 * (int64_t)batch);
+}
+
+// CTA count of the decode launch: one per SM (or the caller's), even in
+// tensor-core mode, where two CTAs share each split (one per output half).
+int decode_ctas(const mla_config* cfg, bool tc) {
+  const int C = resolve_num_ctas(cfg);
+  if (C <= 0 || !tc) return C;
+  return C >= 2 ? (C & ~1) : 2;
+}
+
+size_t ws_bytes_needed(const mla_config* cfg, int64_t num_q, int32_t batch, bool tc, int C) {
+  const int G = cfg->num_heads / kHG;
+  return tc ? ws_layout_tc(num_q, G, C / 2, batch).total : ws_layout(num_q, G, C).total;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -154,9 +174,10 @@ mla_status mla_absorb_q(const mla_config* cfg, const void* q_nope, const void* q
 
 size_t mla_decode_workspace_size(const mla_config* cfg, int64_t num_q, int32_t batch) {
   if (check_cfg(cfg) != MLA_OK || num_q < 0 || batch < 0) return 0;
-  const int C = resolve_num_ctas(cfg);
+  const bool tc = use_tc(cfg, num_q, batch);
+  const int C = decode_ctas(cfg, tc);
   if (C <= 0) return 0;
-  return ws_layout(num_q, cfg->num_heads / kHG, C).total;
+  return ws_bytes_needed(cfg, num_q, batch, tc, C);
 }
 
 mla_status mla_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
@@ -177,13 +198,14 @@ mla_status mla_decode_plan(const mla_config* cfg, const int32_t* seq_lens,
   if (num_q == 0) return MLA_OK;
   if (!seq_lens || !query_start_loc || batch == 0) return MLA_ERR_INVALID_ARGUMENT;
   if (!aligned(seq_lens, 4) || !aligned(query_start_loc, 4)) return MLA_ERR_INVALID_ARGUMENT;
-  const int C = resolve_num_ctas(cfg);
+  const bool tc = use_tc(cfg, num_q, batch);
+  const int C = decode_ctas(cfg, tc);
   if (C <= 0) return MLA_ERR_CUDA;
   const int G = cfg->num_heads / kHG;
-  if (ws_bytes < ws_layout(num_q, G, C).total) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  if (ws_bytes < ws_bytes_needed(cfg, num_q, batch, tc, C)) return MLA_ERR_WORKSPACE_TOO_SMALL;
   PlanArgs pa{seq_lens, query_start_loc, batch, (int32_t)num_q, G, C, cfg->block_size,
               max_blocks_per_seq, workspace};
-  return from_cuda(launch_plan(pa, as_stream(stream)));
+  return from_cuda(tc ? launch_plan_tc(pa, as_stream(stream)) : launch_plan(pa, as_stream(stream)));
 }
 
 }  // extern "C"
@@ -192,11 +214,12 @@ namespace {
 
 mla_status decode_impl(const mla_config* cfg, const void* q_abs, const void* cache,
                        int64_t num_blocks, const int32_t* block_table, int32_t max_blocks_per_seq,
-                       int64_t num_q, void* workspace, size_t ws_bytes, float* o_lat,
+                       int32_t batch, int64_t num_q, void* workspace, size_t ws_bytes, float* o_lat,
                        void* stream) {
   mla_status s = check_cfg(cfg);
   if (s != MLA_OK) return s;
-  if (num_q < 0 || num_blocks < 0 || max_blocks_per_seq < 0) return MLA_ERR_INVALID_ARGUMENT;
+  if (num_q < 0 || batch < 0 || num_blocks < 0 || max_blocks_per_seq < 0)
+    return MLA_ERR_INVALID_ARGUMENT;
   if (num_q > kMaxRows) return MLA_ERR_UNSUPPORTED;
   if (num_blocks * cfg->block_size > ((int64_t)1 << 31)) return MLA_ERR_UNSUPPORTED;
   if (!workspace || !aligned(workspace, 256)) return MLA_ERR_INVALID_ARGUMENT;
@@ -204,10 +227,11 @@ mla_status decode_impl(const mla_config* cfg, const void* q_abs, const void* cac
   if (!q_abs || !cache || !block_table) return MLA_ERR_INVALID_ARGUMENT;
   if (!aligned(q_abs, 16) || !aligned(cache, 16) || !aligned(block_table, 4))
     return MLA_ERR_INVALID_ARGUMENT;
-  const int C = resolve_num_ctas(cfg);
+  const bool tc = use_tc(cfg, num_q, batch);
+  const int C = decode_ctas(cfg, tc);
   if (C <= 0) return MLA_ERR_CUDA;
   const int G = cfg->num_heads / kHG;
-  if (ws_bytes < ws_layout(num_q, G, C).total) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  if (ws_bytes < ws_bytes_needed(cfg, num_q, batch, tc, C)) return MLA_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t st = as_stream(stream);
   const double log2e = 1.4426950408889634;
   DecodeArgs da{q_abs, cache, num_blocks, block_table, max_blocks_per_seq, cfg->block_size,
@@ -218,6 +242,14 @@ mla_status decode_impl(const mla_config* cfg, const void* q_abs, const void* cac
   const uint64_t map_rows = num_blocks > 0 ? (uint64_t)num_blocks * cfg->block_size
                                            : (uint64_t)cfg->block_size;
   CUtensorMap cache_map, q_map;
+  if (tc) {
+    // boxes: 32-token half pages (or whole pages below 32 tokens), 128-row q-blocks
+    const uint32_t box_rows = cfg->block_size < 32 ? (uint32_t)cfg->block_size : 32u;
+    if (!make_row_map(&cache_map, cache, map_rows, box_rows) ||
+        !make_row_map(&q_map, q_abs, (uint64_t)num_q * cfg->num_heads, kQBlockRows))
+      return MLA_ERR_CUDA;
+    return from_cuda(launch_decode_tc(da, batch, cache_map, q_map, st));
+  }
   if (!make_row_map(&cache_map, cache, map_rows, (uint32_t)cfg->block_size) ||
       !make_row_map(&q_map, q_abs, (uint64_t)num_q * cfg->num_heads, kHG))
     return MLA_ERR_CUDA;
@@ -230,32 +262,33 @@ extern "C" {
 
 mla_status mla_decode_planned(const mla_config* cfg, const void* q_abs, const void* cache,
                               int64_t num_blocks, const int32_t* block_table,
-                              int32_t max_blocks_per_seq, int64_t num_q, void* workspace,
-                              size_t ws_bytes, void* stream) {
-  return decode_impl(cfg, q_abs, cache, num_blocks, block_table, max_blocks_per_seq, num_q,
+                              int32_t max_blocks_per_seq, int32_t batch, int64_t num_q,
+                              void* workspace, size_t ws_bytes, void* stream) {
+  return decode_impl(cfg, q_abs, cache, num_blocks, block_table, max_blocks_per_seq, batch, num_q,
                      workspace, ws_bytes, nullptr, stream);
 }
 
 mla_status mla_decode_combine(const mla_config* cfg, const void* q_abs, const void* cache,
                               int64_t num_blocks, const int32_t* block_table,
-                              int32_t max_blocks_per_seq, int64_t num_q, void* workspace,
-                              size_t ws_bytes, float* o_lat, void* stream) {
+                              int32_t max_blocks_per_seq, int32_t batch, int64_t num_q,
+                              void* workspace, size_t ws_bytes, float* o_lat, void* stream) {
   if (num_q > 0 && (!o_lat || !aligned(o_lat, 16))) return MLA_ERR_INVALID_ARGUMENT;
   mla_status s = check_cfg(cfg);
   if (s != MLA_OK) return s;
+  const bool tc = use_tc(cfg, num_q, batch);
   // With few (row, head group) tiles per CTA each tile is cut into many
   // splits, and one CTA merging all of them at the end of the decode is slower
   // than the merge kernel, which spreads that work over more CTAs.
-  const int C = resolve_num_ctas(cfg);
+  const int C = decode_ctas(cfg, tc);
   const int64_t qtiles = num_q * (cfg->num_heads / kHG);
-  if (C > 0 && qtiles * 4 < C) {
-    s = decode_impl(cfg, q_abs, cache, num_blocks, block_table, max_blocks_per_seq, num_q,
+  if (!tc && C > 0 && qtiles * 4 < C) {
+    s = decode_impl(cfg, q_abs, cache, num_blocks, block_table, max_blocks_per_seq, batch, num_q,
                     workspace, ws_bytes, nullptr, stream);
     if (s != MLA_OK) return s;
-    return from_cuda(launch_combine(workspace, cfg->num_heads / kHG, C, num_q, o_lat,
+    return from_cuda(launch_combine(workspace, cfg->num_heads / kHG, C, num_q, batch, o_lat,
                                     as_stream(stream)));
   }
-  return decode_impl(cfg, q_abs, cache, num_blocks, block_table, max_blocks_per_seq, num_q,
+  return decode_impl(cfg, q_abs, cache, num_blocks, block_table, max_blocks_per_seq, batch, num_q,
                      workspace, ws_bytes, o_lat, stream);
 }
 
@@ -279,8 +312,8 @@ mla_status mla_decode_paged(const mla_config* cfg, const void* q_abs, const void
   s = mla_decode_plan(cfg, seq_lens, query_start_loc, batch, num_q, max_blocks_per_seq, workspace,
                       ws_bytes, stream);
   if (s != MLA_OK) return s;
-  return mla_decode_planned(cfg, q_abs, cache, num_blocks, block_table, max_blocks_per_seq, num_q,
-                            workspace, ws_bytes, stream);
+  return mla_decode_planned(cfg, q_abs, cache, num_blocks, block_table, max_blocks_per_seq, batch,
+                            num_q, workspace, ws_bytes, stream);
 }
 
 mla_status mla_combine(const mla_config* cfg, const void* workspace, size_t ws_bytes,
@@ -292,11 +325,12 @@ mla_status mla_combine(const mla_config* cfg, const void* workspace, size_t ws_b
   if (num_q == 0) return MLA_OK;
   if (!workspace || !o_lat || !aligned(workspace, 256) || !aligned(o_lat, 16))
     return MLA_ERR_INVALID_ARGUMENT;
-  const int C = resolve_num_ctas(cfg);
+  const bool tc = use_tc(cfg, num_q, batch);
+  const int C = decode_ctas(cfg, tc);
   if (C <= 0) return MLA_ERR_CUDA;
   const int G = cfg->num_heads / kHG;
-  if (ws_bytes < ws_layout(num_q, G, C).total) return MLA_ERR_WORKSPACE_TOO_SMALL;
-  return from_cuda(launch_combine(workspace, G, C, num_q, o_lat, as_stream(stream)));
+  if (ws_bytes < ws_bytes_needed(cfg, num_q, batch, tc, C)) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  return from_cuda(launch_combine(workspace, G, C, num_q, batch, o_lat, as_stream(stream)));
 }
 
 mla_status mla_combine_out_proj(const mla_config* cfg, const void* workspace, size_t ws_bytes,
@@ -310,11 +344,12 @@ mla_status mla_combine_out_proj(const mla_config* cfg, const void* workspace, si
   if (!workspace || !W_uv || !out || !aligned(workspace, 256) || !aligned(W_uv, 16) ||
       !aligned(out, 16))
     return MLA_ERR_INVALID_ARGUMENT;
-  const int C = resolve_num_ctas(cfg);
+  const bool tc = use_tc(cfg, num_q, batch);
+  const int C = decode_ctas(cfg, tc);
   if (C <= 0) return MLA_ERR_CUDA;
   const int G = cfg->num_heads / kHG;
-  if (ws_bytes < ws_layout(num_q, G, C).total) return MLA_ERR_WORKSPACE_TOO_SMALL;
-  return from_cuda(launch_combine_out_proj(*cfg, workspace, G, C, num_q, W_uv, out,
+  if (ws_bytes < ws_bytes_needed(cfg, num_q, batch, tc, C)) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  return from_cuda(launch_combine_out_proj(*cfg, workspace, G, C, num_q, batch, W_uv, out,
                                            as_stream(stream)));
 }
 

@@ -16,6 +16,7 @@ namespace mla {
 
 constexpr int kMergeChunk = 16;  // slots whose weights are staged at a time
 
+// The parts are 16-row groups slot0, slot0 + stride, ... of the partial buffer.
 // Scratch: 32 + kMergeChunk * 16 floats of shared memory.
 // `sync` synchronises the `nthreads` participating threads (tid in [0, nthreads)).
 // All (slot, row) log-sum-exps of a chunk are fetched in one parallel round
@@ -23,8 +24,8 @@ constexpr int kMergeChunk = 16;  // slots whose weights are staged at a time
 template <int NTHREADS, typename Sync>
 __device__ __forceinline__ void merge_qtile(const float* __restrict__ lse,
                                             const float* __restrict__ opart, int64_t slot0,
-                                            int nslots, float* __restrict__ out, int tid,
-                                            float* scratch, Sync sync) {
+                                            int nslots, int stride, float* __restrict__ out,
+                                            int tid, float* scratch, Sync sync) {
   constexpr int kItems = kHG * kDc / 4 / NTHREADS;  // float4 items per thread
   float* sM = scratch;
   float* sInv = scratch + kHG;
@@ -34,7 +35,8 @@ __device__ __forceinline__ void merge_qtile(const float* __restrict__ lse,
   for (int s0 = 0; s0 < nslots; s0 += kMergeChunk) {
     const int ns = min(kMergeChunk, nslots - s0);
     sync();
-    for (int i = tid; i < ns * kHG; i += NTHREADS) sW[i] = lse[(slot0 + s0) * kHG + i];
+    for (int i = tid; i < ns * kHG; i += NTHREADS)
+      sW[i] = lse[(slot0 + (int64_t)(s0 + i / kHG) * stride) * kHG + i % kHG];
     sync();
     if (tid < kHG) {
       const float Mold = sM[tid];
@@ -62,13 +64,15 @@ __device__ __forceinline__ void merge_qtile(const float* __restrict__ lse,
     for (int i = tid; i < ns * kHG; i += NTHREADS) {
       const int r = i % kHG;
       const float M = sM[r];
-      sW[i] = M == -INFINITY ? 0.f : fast_exp2(lse[(slot0 + s0) * kHG + i] - M) * sInv[r];
+      sW[i] = M == -INFINITY
+                  ? 0.f
+                  : fast_exp2(lse[(slot0 + (int64_t)(s0 + i / kHG) * stride) * kHG + r] - M) * sInv[r];
     }
     sync();
     for (int s = 0; s < ns; s += 2) {
       const bool two = s + 1 < ns;
-      const float4* src0 = op + (slot0 + s0 + s) * (kHG * kDc / 4);
-      const float4* src1 = two ? src0 + kHG * kDc / 4 : src0;
+      const float4* src0 = op + (slot0 + (int64_t)(s0 + s) * stride) * (kHG * kDc / 4);
+      const float4* src1 = two ? src0 + (int64_t)stride * (kHG * kDc / 4) : src0;
       float4 v0[kItems], v1[kItems];
 #pragma unroll
       for (int j = 0; j < kItems; ++j) {

@@ -65,17 +65,34 @@ mla_status mla_decode_paged_noalloc(const mla_config* cfg, const void* q_abs, co
   // the scratch must hold this launch's workspace
   const size_t need = mla_decode_workspace_size(cfg, num_q, batch);
   if (need == 0) return cfg ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARGUMENT;
-  if (need > kScratchBytes) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  mla_config fit = *cfg;
+  if (need > kScratchBytes) {
+    if (cfg->num_ctas > 0) return MLA_ERR_WORKSPACE_TOO_SMALL;
+    // default CTA count: take the largest count below it whose workspace fits
+    // (the size does not decrease with the count, so bisect)
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MLA_ERR_CUDA;
+    int lo = 0, hi = sms;  // size(lo) fits (lo > 0) or lo == 0; size(hi) does not
+    while (hi - lo > 1) {
+      const int mid = lo + (hi - lo) / 2;
+      fit.num_ctas = mid;
+      if (mla_decode_workspace_size(&fit, num_q, batch) <= kScratchBytes) lo = mid; else hi = mid;
+    }
+    if (lo == 0) return MLA_ERR_WORKSPACE_TOO_SMALL;
+    fit.num_ctas = lo;
+  }
   void* ws = nullptr;
   if (scratch_for_current_device(&ws) != cudaSuccess) return MLA_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // status word and plan header start at zero on every call
   if (cudaMemsetAsync(ws, 0, sizeof(mla::WsHeader), st) != cudaSuccess) return MLA_ERR_CUDA;
-  mla_status s = mla_decode_paged(cfg, q_abs, cache, num_blocks, block_table, max_blocks_per_seq,
+  mla_status s = mla_decode_paged(&fit, q_abs, cache, num_blocks, block_table, max_blocks_per_seq,
                                   seq_lens, query_start_loc, batch, num_q, ws, kScratchBytes,
                                   stream);
   if (s != MLA_OK) return s;
-  s = mla_combine(cfg, ws, kScratchBytes, batch, num_q, o_lat, stream);
+  s = mla_combine(&fit, ws, kScratchBytes, batch, num_q, o_lat, stream);
   if (s != MLA_OK) return s;
   if (dev_status &&
       cudaMemcpyAsync(dev_status, ws, sizeof(uint32_t), cudaMemcpyDeviceToDevice, st) != cudaSuccess)

@@ -102,6 +102,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
   const int share = total > 0 ? (total + C - 1) / C : 1;
   if (tid == 0) {
     hdr->magic = kMagic;
+    hdr->mode = 0;
+    hdr->qblocks = 0;
     hdr->total_units = total;
     hdr->share = share;
     hdr->num_ctas = C;
@@ -127,6 +129,142 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
   }
 }
 
+// Block-wide exclusive scan of data[0..n) in place (kPlanThreads threads);
+// returns the total. `scratch` holds 32 ints.
+__device__ int block_exclusive_scan(int* data, int n, int* scratch) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (n + kPlanThreads - 1) / kPlanThreads;
+  const int beg = min(n, tid * per), end = min(n, beg + per);
+  int local = 0;
+  for (int i = beg; i < end; ++i) local += data[i];
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  __syncthreads();
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = scratch[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += v;
+    }
+    scratch[lane] = w;
+  }
+  __syncthreads();
+  int run = incl - local + (warp > 0 ? scratch[warp - 1] : 0);
+  const int total = scratch[31];
+  for (int i = beg; i < end; ++i) {
+    const int u = data[i];
+    data[i] = run;
+    run += u;
+  }
+  __syncthreads();
+  return total;
+}
+
+// Plan for the tensor-core kernel (mode 1): q-blocks of 8 consecutive q-tiles
+// of one sequence; units = (q-block, 64-token tile), a q-block owning the tiles
+// its last row sees; `shares` equal contiguous shares of the unit list.
+__global__ void __launch_bounds__(kPlanThreads) plan_tc_kernel(PlanArgs a) {
+  extern __shared__ int s_tc[];  // [batch + 1] blocks per sequence, then [qb_max + 1] units
+  __shared__ int s_scan[32];
+  const int tid = threadIdx.x;
+  pdl_wait();
+  pdl_launch_dependents();
+  uint8_t* ws = reinterpret_cast<uint8_t*>(a.workspace);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  const int shares = a.num_ctas / 2;
+  const int G = a.groups, B = a.batch, Nq = a.num_q;
+  const WsLayoutTc L = ws_layout_tc(Nq, G, shares, B);
+  int4* row_info = reinterpret_cast<int4*>(ws + L.row_info);
+  int4* seq_info = reinterpret_cast<int4*>(ws + L.seq_info);
+  int4* qblock = reinterpret_cast<int4*>(ws + L.qblock);
+  int4* cta_start = reinterpret_cast<int4*>(ws + L.cta_start);
+  int* arrive = reinterpret_cast<int*>(ws + L.arrive);
+  int* s_nb = s_tc;
+  int* s_units = s_tc + B + 1;
+  const int qb_max = (int)L.qblocks_max;
+
+  for (int n = tid; n < Nq; n += kPlanThreads) row_info[n] = make_int4(-1, -1, 0, 0);
+  for (int i = tid; i < qb_max * 2; i += kPlanThreads) arrive[i] = 0;
+  __syncthreads();
+  const int64_t max_len = (int64_t)a.max_blocks_per_seq * a.block_size;
+  for (int b = tid; b < B; b += kPlanThreads) {
+    const int len = a.seq_lens[b];
+    const int q0 = a.query_start_loc[b], q1 = a.query_start_loc[b + 1];
+    const int ql = q1 - q0;
+    int nb = 0;
+    if (q0 < 0 || q1 > Nq || ql < 0) {
+      set_status(&hdr->status, MLA_DEV_BAD_SEQ);
+    } else {
+      const bool bad = ql > len || len < 0 || (int64_t)len > max_len;
+      if (bad && ql > 0) set_status(&hdr->status, MLA_DEV_BAD_SEQ);
+      if (!bad) {
+        for (int j = 0; j < ql; ++j) {
+          const int pos = len - ql + j;
+          row_info[q0 + j] = make_int4(b, pos, (pos + kTile) / kTile, 0);
+        }
+        nb = (ql * G + kQBlockTiles - 1) / kQBlockTiles;
+      }
+    }
+    s_nb[b] = nb;
+  }
+  __syncthreads();
+  int total_blocks = block_exclusive_scan(s_nb, B, s_scan);   // s_nb[b] = first q-block of b
+  if (total_blocks > qb_max) {  // overlapping query ranges: more blocks than the layout holds
+    if (tid == 0) set_status(&hdr->status, MLA_DEV_BAD_SEQ);
+    total_blocks = 0;
+  }
+  for (int b = tid; b < B && total_blocks > 0; b += kPlanThreads) {
+    const int q0 = a.query_start_loc[b], q1 = a.query_start_loc[b + 1];
+    const int nb = (b + 1 < B ? s_nb[b + 1] : total_blocks) - s_nb[b];
+    const int t0 = q0 * G, t_end = q1 * G;
+    seq_info[b] = make_int4(t0, s_nb[b], t_end, 0);
+    for (int k = 0; k < nb; ++k) {
+      const int t_first = t0 + k * kQBlockTiles;
+      const int t_last = min(t_first + kQBlockTiles, t_end) - 1;
+      const int tiles = row_info[t_last / G].z;   // the block's last row sees the most tokens
+      qblock[s_nb[b] + k] = make_int4(b, t_first, tiles, 0);
+      s_units[s_nb[b] + k] = tiles;
+    }
+  }
+  __syncthreads();
+  const int total = block_exclusive_scan(s_units, total_blocks, s_scan);
+  for (int qb = tid; qb < total_blocks; qb += kPlanThreads) qblock[qb].w = s_units[qb];
+  if (tid == 0) s_units[total_blocks] = total;
+  __syncthreads();
+  const int share = total > 0 ? (total + shares - 1) / shares : 1;
+  if (tid == 0) {
+    hdr->magic = kMagic;
+    hdr->mode = 1;
+    hdr->qblocks = total_blocks;
+    hdr->total_units = total;
+    hdr->share = share;
+    hdr->num_ctas = a.num_ctas;
+    hdr->groups = G;
+    hdr->num_q = Nq;
+    hdr->batch = B;
+  }
+  for (int c = tid; c < shares; c += kPlanThreads) {
+    const int u0 = c * share;
+    if (u0 >= total) {
+      cta_start[c] = make_int4(-1, 0, 0, 0);
+      continue;
+    }
+    int lo = 0, hi = total_blocks;  // start[lo] <= u0 < start[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_units[mid] <= u0) lo = mid; else hi = mid;
+    }
+    cta_start[c] = make_int4(lo, u0 - s_units[lo], 0, 0);
+  }
+}
+
 // CTA = (q-tile t = (query row n, head group g), quarter of the 512 latent
 // dims): 16 head rows x 128 dims. Threads 0-15 reduce their row's
 // log-sum-exps over the partial slots to a maximum and a reciprocal weight
@@ -137,42 +275,39 @@ constexpr int kCombineThreads = 128;
 constexpr int kSlotChunk = 64;
 
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
-    const uint8_t* __restrict__ ws, int groups, int num_ctas, int64_t num_q,
+    const uint8_t* __restrict__ ws, int groups, int num_ctas, int64_t num_q, int batch,
     float* __restrict__ o_lat) {
   __shared__ float sM[kHG], sInv[kHG];
   __shared__ float sW[kSlotChunk][kHG];
   pdl_wait();  // everything below reads what the decode kernel wrote
   pdl_launch_dependents();
   const WsHeader* hdr = reinterpret_cast<const WsHeader*>(ws);
-  const WsLayout L = ws_layout(num_q, groups, num_ctas);
-  const int4* row_info = reinterpret_cast<const int4*>(ws + L.row_info);
-  const float* lse = reinterpret_cast<const float*>(ws + L.lse);
-  const float4* opart = reinterpret_cast<const float4*>(ws + L.opart);
+  const size_t lse_off = hdr->mode == 0 ? ws_layout(num_q, groups, num_ctas).lse
+                                        : ws_layout_tc(num_q, groups, num_ctas / 2, batch).lse;
+  const size_t op_off = hdr->mode == 0 ? ws_layout(num_q, groups, num_ctas).opart
+                                       : ws_layout_tc(num_q, groups, num_ctas / 2, batch).opart;
+  const float* lse = reinterpret_cast<const float*>(ws + lse_off);
+  const float4* opart = reinterpret_cast<const float4*>(ws + op_off);
   const int t = blockIdx.x, quarter = blockIdx.y, tid = threadIdx.x;
   const int n = t / groups, g = t % groups;
   const int H = groups * kHG;
   // item j of this thread: row (tid / 32) + 4 j, float4 column (tid % 32) of this quarter
   const int c4 = quarter * 32 + (tid & 31);
   float4* out = reinterpret_cast<float4*>(o_lat + ((size_t)n * H + g * kHG) * kDc);
-  const bool plan_ok = hdr->magic == kMagic && hdr->num_q == num_q && hdr->groups == groups &&
-                       hdr->num_ctas == num_ctas;
-  const int4 ri = plan_ok ? row_info[n] : make_int4(-1, -1, 0, 0);
-  const int tiles = ri.z;
-  if (tiles <= 0) {
+  const QtileParts qp = locate_qtile(ws, num_q, groups, num_ctas, batch, n, g);
+  if (qp.count <= 0) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) out[((tid >> 5) + 4 * j) * (kDc / 4) + c4] = make_float4(0.f, 0.f, 0.f, 0.f);
     return;
   }
-  const int share = hdr->share;
-  const int U = ri.w + g * tiles;
-  const int c_first = U / share, c_last = (U + tiles - 1) / share;
-  const int nslots = c_last - c_first + 1;
+  const int nslots = qp.count;
+  auto grp = [&](int s) { return qp.first + (int64_t)s * qp.stride; };
   if (tid < kHG) {
     float M = -INFINITY;
-    for (int c = c_first; c <= c_last; ++c) M = fmaxf(M, lse[(size_t)(c + t) * kHG + tid]);
+    for (int s = 0; s < nslots; ++s) M = fmaxf(M, lse[grp(s) * kHG + tid]);
     float den = 0.f;
     if (M != -INFINITY)
-      for (int c = c_first; c <= c_last; ++c) den += fast_exp2(lse[(size_t)(c + t) * kHG + tid] - M);
+      for (int s = 0; s < nslots; ++s) den += fast_exp2(lse[grp(s) * kHG + tid] - M);
     sM[tid] = M;
     sInv[tid] = den > 0.f ? 1.f / den : 0.f;
   }
@@ -185,12 +320,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
     for (int i = tid; i < ns * kHG; i += kCombineThreads) {
       const int sl = i / kHG, r = i % kHG;
       const float M = sM[r];
-      const size_t slot = (size_t)(c_first + s0 + sl + t);
-      sW[sl][r] = M == -INFINITY ? 0.f : fast_exp2(lse[slot * kHG + r] - M) * sInv[r];
+      sW[sl][r] = M == -INFINITY ? 0.f : fast_exp2(lse[grp(s0 + sl) * kHG + r] - M) * sInv[r];
     }
     __syncthreads();
     for (int sl = 0; sl < ns; ++sl) {
-      const float4* src = opart + (size_t)(c_first + s0 + sl + t) * kHG * (kDc / 4);
+      const float4* src = opart + grp(s0 + sl) * kHG * (kDc / 4);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int r = (tid >> 5) + 4 * j;
@@ -220,6 +354,15 @@ __global__ void wait_timeout_selftest_kernel(uint32_t* status, uint64_t timeout_
 
 }  // namespace
 
+cudaError_t launch_plan_tc(const PlanArgs& a, cudaStream_t stream) {
+  const int64_t qb_max = ws_layout_tc(a.num_q, a.groups, a.num_ctas / 2, a.batch).qblocks_max;
+  const size_t smem = ((size_t)a.batch + 1 + (size_t)qb_max + 1) * sizeof(int);
+  cudaError_t e = cudaFuncSetAttribute(plan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(plan_tc_kernel, dim3(1), dim3(kPlanThreads), smem, stream, a);
+}
+
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream) {
   const size_t smem = ((size_t)a.num_q + 1) * sizeof(int);
   cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -229,10 +372,10 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream) {
 }
 
 cudaError_t launch_combine(const void* workspace, int32_t groups, int32_t num_ctas,
-                           int64_t num_q, float* o_lat, cudaStream_t stream) {
+                           int64_t num_q, int32_t batch, float* o_lat, cudaStream_t stream) {
   if (num_q == 0) return cudaSuccess;
   return launch_pdl(combine_kernel, dim3((unsigned)(num_q * groups), 4), dim3(kCombineThreads), 0,
-                    stream, (const uint8_t*)workspace, groups, num_ctas, num_q, o_lat);
+                    stream, (const uint8_t*)workspace, groups, num_ctas, num_q, (int)batch, o_lat);
 }
 
 cudaError_t launch_wait_timeout_selftest(uint32_t* status, int64_t timeout_ns,

@@ -247,13 +247,52 @@ __global__ void __launch_bounds__(128) out_proj_bf16_kernel(const float* __restr
 // computed once into shared memory.
 // ---------------------------------------------------------------------------
 struct MergeRow {
-  int slot0, nslots;
+  int64_t slot0;   // first 16-row partial group
+  int stride, nslots;
   float M, inv;
 };
 
+// Merge parameters of (query row n, head h): where its parts are, the max
+// base-2 log-sum-exp and 1 / the weight sum. nslots = 0: a zero row.
+__device__ __forceinline__ MergeRow merge_row(const uint8_t* ws, const float* lse, int64_t num_q,
+                                              int groups, int num_ctas, int batch, int n, int h) {
+  MergeRow mr{0, 1, 0, 0.f, 0.f};
+  if (n >= num_q) return mr;
+  const QtileParts qp = locate_qtile(ws, num_q, groups, num_ctas, batch, n, h / kHG);
+  if (qp.count <= 0) return mr;
+  const int hr = h % kHG;
+  float M = -INFINITY;
+  for (int s = 0; s < qp.count; ++s) M = fmaxf(M, lse[(qp.first + (int64_t)s * qp.stride) * kHG + hr]);
+  float den = 0.f;
+  if (M != -INFINITY)
+    for (int s = 0; s < qp.count; ++s)
+      den += fast_exp2(lse[(qp.first + (int64_t)s * qp.stride) * kHG + hr] - M);
+  if (M == -INFINITY) return mr;
+  mr.slot0 = qp.first;
+  mr.stride = qp.stride;
+  mr.nslots = qp.count;
+  mr.M = M;
+  mr.inv = den > 0.f ? 1.f / den : 0.f;
+  return mr;
+}
+
+__device__ __forceinline__ void ws_parts(const uint8_t* ws, int64_t num_q, int groups, int num_ctas,
+                                         int batch, const float** lse, const float** opart) {
+  const WsHeader* hdr = reinterpret_cast<const WsHeader*>(ws);
+  if (hdr->mode == 0) {
+    const WsLayout L = ws_layout(num_q, groups, num_ctas);
+    *lse = reinterpret_cast<const float*>(ws + L.lse);
+    *opart = reinterpret_cast<const float*>(ws + L.opart);
+  } else {
+    const WsLayoutTc L = ws_layout_tc(num_q, groups, num_ctas / 2, batch);
+    *lse = reinterpret_cast<const float*>(ws + L.lse);
+    *opart = reinterpret_cast<const float*>(ws + L.opart);
+  }
+}
+
 template <int MW>
 __global__ void __launch_bounds__(128) combine_out_proj_bf16_kernel(
-    const uint8_t* __restrict__ ws, int groups, int num_ctas, int num_q,
+    const uint8_t* __restrict__ ws, int groups, int num_ctas, int num_q, int batch,
     const __nv_bfloat16* __restrict__ W_uv, __nv_bfloat16* __restrict__ out, int H) {
   extern __shared__ __align__(1024) uint8_t smem_cp[];
   constexpr int ROWS = 16 * MW;
@@ -275,36 +314,12 @@ __global__ void __launch_bounds__(128) combine_out_proj_bf16_kernel(
   pdl_wait();
   pdl_launch_dependents();
 
-  const WsHeader* hdr = reinterpret_cast<const WsHeader*>(ws);
-  const WsLayout L = ws_layout(num_q, groups, num_ctas);
-  const int4* row_info = reinterpret_cast<const int4*>(ws + L.row_info);
-  const float* lse = reinterpret_cast<const float*>(ws + L.lse);
-  const float* opart = reinterpret_cast<const float*>(ws + L.opart);
-  const bool plan_ok = hdr->magic == kMagic && hdr->num_q == num_q && hdr->groups == groups &&
-                       hdr->num_ctas == num_ctas;
-  const int hg = h / kHG, hr = h % kHG;
-  for (int r = tid; r < ROWS; r += 128) {
-    const int n = row0 + r;
-    MergeRow mr{0, 0, 0.f, 0.f};
-    const int4 ri = (plan_ok && n < num_q) ? row_info[n] : make_int4(-1, -1, 0, 0);
-    if (ri.z > 0) {
-      const int share = hdr->share;
-      const int t = n * groups + hg;
-      const int U = ri.w + hg * ri.z;
-      const int cf = U / share, cl = (U + ri.z - 1) / share;
-      mr.slot0 = cf + t;
-      mr.nslots = cl - cf + 1;
-      float M = -INFINITY;
-      for (int s = 0; s < mr.nslots; ++s) M = fmaxf(M, lse[(size_t)(mr.slot0 + s) * kHG + hr]);
-      float den = 0.f;
-      if (M != -INFINITY)
-        for (int s = 0; s < mr.nslots; ++s) den += fast_exp2(lse[(size_t)(mr.slot0 + s) * kHG + hr] - M);
-      mr.M = M;
-      mr.inv = den > 0.f ? 1.f / den : 0.f;
-      if (M == -INFINITY) mr.nslots = 0;
-    }
-    sRow[r] = mr;
-  }
+  const float* lse;
+  const float* opart;
+  ws_parts(ws, num_q, groups, num_ctas, batch, &lse, &opart);
+  const int hr = h % kHG;
+  for (int r = tid; r < ROWS; r += 128)
+    sRow[r] = merge_row(ws, lse, num_q, groups, num_ctas, batch, row0 + r, h);
   __syncthreads();
 
   const int wr = MW == 1 ? 0 : warp;
@@ -315,7 +330,7 @@ __global__ void __launch_bounds__(128) combine_out_proj_bf16_kernel(
   auto merged2 = [&](const MergeRow& m, int k) {
     float2 acc = make_float2(0.f, 0.f);
     for (int s = 0; s < m.nslots; ++s) {
-      const size_t slot = (size_t)(m.slot0 + s);
+      const size_t slot = (size_t)(m.slot0 + (int64_t)s * m.stride);
       const float w = fast_exp2(lse[slot * kHG + hr] - m.M) * m.inv;
       const float2 v = *reinterpret_cast<const float2*>(opart + (slot * kHG + hr) * kDc + k);
       acc.x = fmaf(w, v.x, acc.x);
@@ -397,44 +412,24 @@ __global__ void __launch_bounds__(128) combine_out_proj_bf16_kernel(
 // combine + out_proj, fp32: one CTA per (row n, head h); the merged latent
 // row goes to shared memory, then 128 threads take one output column each.
 __global__ void __launch_bounds__(128) combine_out_proj_f32_kernel(
-    const uint8_t* __restrict__ ws, int groups, int num_ctas, int num_q,
+    const uint8_t* __restrict__ ws, int groups, int num_ctas, int num_q, int batch,
     const float* __restrict__ W_uv, float* __restrict__ out, int H) {
   __shared__ float so[kDc];
   __shared__ MergeRow sr;
+  pdl_wait();
+  pdl_launch_dependents();
   const int n = blockIdx.x, h = blockIdx.y, t0 = threadIdx.x;
-  const WsHeader* hdr = reinterpret_cast<const WsHeader*>(ws);
-  const WsLayout L = ws_layout(num_q, groups, num_ctas);
-  const int4* row_info = reinterpret_cast<const int4*>(ws + L.row_info);
-  const float* lse = reinterpret_cast<const float*>(ws + L.lse);
-  const float* opart = reinterpret_cast<const float*>(ws + L.opart);
-  const int hg = h / kHG, hr = h % kHG;
-  if (t0 == 0) {
-    const bool plan_ok = hdr->magic == kMagic && hdr->num_q == num_q && hdr->groups == groups &&
-                         hdr->num_ctas == num_ctas;
-    MergeRow mr{0, 0, 0.f, 0.f};
-    const int4 ri = plan_ok ? row_info[n] : make_int4(-1, -1, 0, 0);
-    if (ri.z > 0) {
-      const int t = n * groups + hg, U = ri.w + hg * ri.z, share = hdr->share;
-      const int cf = U / share, cl = (U + ri.z - 1) / share;
-      mr.slot0 = cf + t;
-      mr.nslots = cl - cf + 1;
-      float M = -INFINITY;
-      for (int s = 0; s < mr.nslots; ++s) M = fmaxf(M, lse[(size_t)(mr.slot0 + s) * kHG + hr]);
-      float den = 0.f;
-      if (M != -INFINITY)
-        for (int s = 0; s < mr.nslots; ++s) den += fast_exp2(lse[(size_t)(mr.slot0 + s) * kHG + hr] - M);
-      mr.M = M;
-      mr.inv = den > 0.f ? 1.f / den : 0.f;
-      if (M == -INFINITY) mr.nslots = 0;
-    }
-    sr = mr;
-  }
+  const float* lse;
+  const float* opart;
+  ws_parts(ws, num_q, groups, num_ctas, batch, &lse, &opart);
+  const int hr = h % kHG;
+  if (t0 == 0) sr = merge_row(ws, lse, num_q, groups, num_ctas, batch, n, h);
   __syncthreads();
   const MergeRow mr = sr;
   for (int c = t0; c < kDc; c += 128) {
     float acc = 0.f;
     for (int s = 0; s < mr.nslots; ++s) {
-      const size_t slot = (size_t)(mr.slot0 + s);
+      const size_t slot = (size_t)(mr.slot0 + (int64_t)s * mr.stride);
       acc = fmaf(fast_exp2(lse[slot * kHG + hr] - mr.M) * mr.inv, opart[(slot * kHG + hr) * kDc + c], acc);
     }
     so[c] = acc;
@@ -541,14 +536,14 @@ cudaError_t launch_out_proj(const mla_config& cfg, const float* o_lat, const voi
 }
 
 cudaError_t launch_combine_out_proj(const mla_config& cfg, const void* workspace, int32_t groups,
-                                   int32_t num_ctas, int64_t num_q, const void* W_uv, void* out,
-                                   cudaStream_t stream) {
+                                   int32_t num_ctas, int64_t num_q, int32_t batch, const void* W_uv,
+                                   void* out, cudaStream_t stream) {
   if (num_q == 0) return cudaSuccess;
   const int H = cfg.num_heads;
   const uint8_t* ws = (const uint8_t*)workspace;
   if (cfg.dtype == MLA_F32) {
     return launch_pdl(combine_out_proj_f32_kernel, dim3((unsigned)num_q, H), dim3(128), 0, stream,
-                      ws, groups, num_ctas, (int)num_q, (const float*)W_uv, (float*)out, H);
+                      ws, groups, num_ctas, (int)num_q, (int)batch, (const float*)W_uv, (float*)out, H);
   }
   const bool big = num_q >= 256;
   const int smem = 512 * 128 + (big ? 0 : 4 * 16 * 64 * 4) + (big ? 64 : 16) * (int)sizeof(MergeRow);
@@ -559,10 +554,10 @@ cudaError_t launch_combine_out_proj(const mla_config& cfg, const void* workspace
   if (e != cudaSuccess) return e;
   if (big)
     return launch_pdl(combine_out_proj_bf16_kernel<4>, dim3((unsigned)((num_q + 63) / 64), 2, H),
-                      dim3(128), smem, stream, ws, groups, num_ctas, (int)num_q,
+                      dim3(128), smem, stream, ws, groups, num_ctas, (int)num_q, (int)batch,
                       (const __nv_bfloat16*)W_uv, (__nv_bfloat16*)out, H);
   return launch_pdl(combine_out_proj_bf16_kernel<1>, dim3((unsigned)((num_q + 15) / 16), 2, H),
-                    dim3(128), smem, stream, ws, groups, num_ctas, (int)num_q,
+                    dim3(128), smem, stream, ws, groups, num_ctas, (int)num_q, (int)batch,
                     (const __nv_bfloat16*)W_uv, (__nv_bfloat16*)out, H);
 }
 

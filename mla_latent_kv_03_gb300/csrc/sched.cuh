@@ -30,8 +30,8 @@ struct SchedWalker {
     const WsLayout L = ws_layout(num_q, groups, num_ctas);
     row_info = reinterpret_cast<const int4*>(ws + L.row_info);
     // the plan must describe this launch (same rows, head groups, CTAs)
-    plan_ok = hdr->magic == kMagic && hdr->num_q == num_q && hdr->groups == groups &&
-              hdr->num_ctas == num_ctas;
+    plan_ok = hdr->magic == kMagic && hdr->mode == 0 && hdr->num_q == num_q &&
+              hdr->groups == groups && hdr->num_ctas == num_ctas;
     if (!plan_ok) return false;
     const int4* cta_start = reinterpret_cast<const int4*>(ws + L.cta_start);
     share = hdr->share;

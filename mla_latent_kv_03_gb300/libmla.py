@@ -64,8 +64,8 @@ _SIGS = {
     "mla_workspace_init": (_i32, [_vp, _sz, _vp]),
     "mla_decode_paged": (_i32, [_cfgp, _vp, _vp, _i64, _vp, _i32, _vp, _vp, _i32, _i64, _vp, _sz, _vp]),
     "mla_decode_plan": (_i32, [_cfgp, _vp, _vp, _i32, _i64, _i32, _vp, _sz, _vp]),
-    "mla_decode_planned": (_i32, [_cfgp, _vp, _vp, _i64, _vp, _i32, _i64, _vp, _sz, _vp]),
-    "mla_decode_combine": (_i32, [_cfgp, _vp, _vp, _i64, _vp, _i32, _i64, _vp, _sz, _vp, _vp]),
+    "mla_decode_planned": (_i32, [_cfgp, _vp, _vp, _i64, _vp, _i32, _i32, _i64, _vp, _sz, _vp]),
+    "mla_decode_combine": (_i32, [_cfgp, _vp, _vp, _i64, _vp, _i32, _i32, _i64, _vp, _sz, _vp, _vp]),
     "mla_decode_paged_noalloc": (_i32, [_cfgp, _vp, _vp, _i64, _vp, _i32, _vp, _vp, _i32, _i64,
                                         _vp, _vp, _vp]),
     "mla_combine": (_i32, [_cfgp, _vp, _sz, _i32, _i64, _vp, _vp]),
@@ -202,21 +202,22 @@ def mla_decode_plan(cfg: MlaConfig, seq_lens, query_start_loc, num_q: int,
         workspace.numel() * workspace.element_size(), _stream(stream)), "mla_decode_plan")
 
 
-def mla_decode_planned(cfg: MlaConfig, q_abs, cache, block_table, workspace, stream=None) -> None:
+def mla_decode_planned(cfg: MlaConfig, q_abs, cache, block_table, batch: int, workspace,
+                       stream=None) -> None:
     dt = _torch_dtype(cfg)
     _check(load().mla_decode_planned(
         ctypes.byref(cfg), _ptr(q_abs, dt, "q_abs"), _ptr(cache, dt, "cache"), cache.shape[0],
-        _ptr(block_table, torch.int32, "block_table"), block_table.shape[1], q_abs.shape[0],
+        _ptr(block_table, torch.int32, "block_table"), block_table.shape[1], batch, q_abs.shape[0],
         _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
         _stream(stream)), "mla_decode_planned")
 
 
-def mla_decode_combine(cfg: MlaConfig, q_abs, cache, block_table, workspace, o_lat,
+def mla_decode_combine(cfg: MlaConfig, q_abs, cache, block_table, batch: int, workspace, o_lat,
                        stream=None) -> None:
     dt = _torch_dtype(cfg)
     _check(load().mla_decode_combine(
         ctypes.byref(cfg), _ptr(q_abs, dt, "q_abs"), _ptr(cache, dt, "cache"), cache.shape[0],
-        _ptr(block_table, torch.int32, "block_table"), block_table.shape[1], q_abs.shape[0],
+        _ptr(block_table, torch.int32, "block_table"), block_table.shape[1], batch, q_abs.shape[0],
         _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
         _ptr(o_lat, torch.float32, "o_lat"), _stream(stream)), "mla_decode_combine")
 

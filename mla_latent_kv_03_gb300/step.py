@@ -98,12 +98,12 @@ class MlaDecodeStep:
                           self.block_table.shape[1], self.workspace, stream=stream)
 
     def decode_planned(self, stream=None) -> None:
-        L.mla_decode_planned(self.cfg, self.q_abs, self.cache, self.block_table, self.workspace,
-                             stream=stream)
+        L.mla_decode_planned(self.cfg, self.q_abs, self.cache, self.block_table, self.w.batch,
+                             self.workspace, stream=stream)
 
     def decode_combine(self, stream=None) -> None:
-        L.mla_decode_combine(self.cfg, self.q_abs, self.cache, self.block_table, self.workspace,
-                             self.o_lat, stream=stream)
+        L.mla_decode_combine(self.cfg, self.q_abs, self.cache, self.block_table, self.w.batch,
+                             self.workspace, self.o_lat, stream=stream)
 
     def combine(self, stream=None) -> None:
         L.mla_combine(self.cfg, self.workspace, self.w.batch, self.o_lat, stream=stream)
@@ -129,3 +129,8 @@ class MlaDecodeStep:
         s1 = L.mla_get_device_status(self.workspace)
         s2 = L.mla_get_device_status(self.status)
         return s1, s2
+
+    def decode_mode(self) -> int:
+        """Kernel family the last plan chose: 0 = warp-mma tiles of 16 heads,
+        1 = tensor-core tiles of 128 (row, head) rows. Synchronises."""
+        return int(self.workspace[32:36].view(torch.int32).item())

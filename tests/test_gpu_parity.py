@@ -330,3 +330,41 @@ def test_combine_out_proj_many_rows():
     s.decode_planned()
     s.combine_out_proj()
     assert_close(to_f64(s.out), ref_out(w), "bf16", "combine_out_proj, 600 rows")
+
+
+# ---------------------------------------------------------------------------
+# tensor-core tiles of 128 (row, head) rows: 128 heads, or prefill chunks
+# ---------------------------------------------------------------------------
+
+TC_CASES = {
+    "h128_bs64": lambda: W.make("tc_h128", [1, 31, 32, 33, 64, 65, 200], [1] * 7, 128, 64, "bf16", seed=61),
+    "h128_bs16": lambda: W.make("tc_h128_16", [5, 40, 129], [1] * 3, 128, 16, "bf16", seed=62),
+    "h64_bs32": lambda: W.make("tc_h64_32", [70, 2, 97], [1] * 3, 64, 32, "bf16", seed=63),
+    "prefill_h16": lambda: W.make("tc_pf16", [300, 77, 40], [120, 9, 40], 16, 64, "bf16", seed=64),
+    "prefill_h32_mixed": lambda: W.make("tc_pf32", [150, 10, 64, 1], [37, 10, 1, 1], 32, 64, "bf16", seed=65),
+    "bad_and_empty": lambda: W.make("tc_empty", [0, 90, 0, 3], [0, 12, 0, 3], 16, 64, "bf16", seed=66),
+}
+
+
+@pytest.mark.parametrize("name", sorted(TC_CASES))
+@pytest.mark.parametrize("num_ctas", [2, 7, 0, 500])
+def test_tensor_core_tiles(name, num_ctas):
+    w = TC_CASES[name]()
+    s = MlaDecodeStep(w, device=DEV, num_ctas=num_ctas)
+    s.populate()
+    s.absorb()
+    s.plan()
+    s.o_lat.fill_(float("nan"))
+    s.decode_combine()                                  # fused merge
+    torch.cuda.synchronize()
+    assert s.device_status()[0][0] == 0
+    fused = to_f64(s.o_lat)
+    ref = ref_o_lat_from(w, to_f64(s.cache), to_f64(s.q_abs))
+    empty = np.isnan(ref).all(axis=(1, 2))
+    assert np.all(fused[empty] == 0)
+    assert_close(fused, ref, "bf16", f"tc fused o_lat {name}")
+    s.decode_planned()                                  # partials + merge kernel
+    s.combine()
+    np.testing.assert_allclose(to_f64(s.o_lat), fused, rtol=0, atol=1e-5)
+    s.combine_out_proj()                                # merge inside the projection
+    assert_close(to_f64(s.out), ref_out(w), "bf16", f"tc out {name}")
