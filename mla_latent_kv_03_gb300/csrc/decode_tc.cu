@@ -7,34 +7,47 @@
 // (paged layout).
 //
 // Work units are (q-block, 64-token tile); each equal share of the unit list
-// is processed by a pair of CTAs, CTA 2c + h computing output columns
-// [256h, 256h + 256) (the 128 x 512 fp32 accumulator would fill all of TMEM).
-// TMEM (512 columns): O half [0, 256), two score buffers S [256, 320), two
-// probability buffers P [320, 352) (bf16 pairs), query columns 256..575 of
-// the q-block [352, 512) (bf16 pairs). Shared memory: query columns 0..255
-// (64 KB) and a ring of four 32-token cache stages (36 KB each, SWIZZLE_128B).
+// is processed by a cluster of two CTAs. CTA h of the pair owns cache columns
+// [256h, 256h + 256 + 64h) -- 256 latent columns for h = 0, 256 latent plus
+// the 64 rope columns for h = 1 -- and the same query columns:
+//   S_h = Q[:, cols_h] . K[:, cols_h]^T   (partial scores, K = 256 or 320)
+//   S   = S_0 + S_1                       (each CTA sends its partial to the
+//                                           peer's shared memory, two stages
+//                                           ahead of their use)
+//   O_h += P . V[:, 256h : 256h + 256]    (each CTA half of the output)
+// so each CTA streams only its own columns of every cache row, and both CTAs
+// run the same softmax on the same sums (S_0 + S_1 == S_1 + S_0 in fp32),
+// giving identical probabilities and log-sum-exps.
+//
+// TMEM (512 columns): O half [0, 256), two score buffers [256, 320), two
+// probability buffers [320, 352) (bf16 pairs), this CTA's query columns
+// [352, 512) (bf16 pairs, the A operand of the score MMAs). Shared memory: a
+// ring of five 32-token cache stages of this CTA's columns (SWIZZLE_128B slabs
+// of 64 columns), four buffers of the peer's partial scores, three of this
+// CTA's own (the source of the bulk copies to the peer), and merge weights.
 // Per CTA (256 threads):
-//   warp 0 (TMA producer): the q-block's shared-memory query columns and the
-//     cache stages, guarded by full / empty mbarriers; every block id is
-//     bounds-checked.
-//   warp 1 (MMA issuer; the warp owns the TMEM allocation and issues from one
-//     elected lane): S[i%2] = Q . K_i^T as 36 tcgen05.mma (M 128, N 32, K 16;
-//     A from shared memory for columns < 256, from TMEM above), one stage
-//     ahead of O += P[i%2] . V_i (2 tcgen05.mma, M 128, N 256, A = P in TMEM,
-//     V MN-major from the stage), so the scores of stage i + 1 run while the
-//     softmax of stage i does.
-//   warps 4-7 (softmax): thread r owns row r: it loads the q-block's upper
-//     query columns into TMEM, then per stage loads its 32 scores, masks
-//     (sequence end, causal position, rejected blocks), keeps the running
-//     maximum, rescales the warp's O rows in TMEM only when some row's maximum
-//     grows by more than 2^8 (probabilities stay below 256), and stores bf16 P
-//     to TMEM. At the end of a segment it normalises its O row into the
-//     partial buffer (and, when o_lat is given, the last CTA of a q-block's
-//     half merges the splits while they are in L2).
-// Every wait is bounded; on a timeout the roles leave their loops, the MMA
-// warp waits for its last MMAs and the producer for its copies before TMEM
-// is freed.
+//   warp 0 (TMA producer): cache stages under full / empty mbarriers; every
+//     block id is bounds-checked.
+//   warp 1 (P.V issuer; owns the TMEM allocation): O += P . V per stage
+//     (2 tcgen05.mma, M 128, N 256, K 16, A = P in TMEM, V MN-major).
+//   warp 2 (score issuer): the partial scores of a stage as soon as its score
+//     buffer is free (16 or 20 tcgen05.mma, M 128, N 32, K 16, A from TMEM).
+//   warps 4-7 (softmax): thread r owns row r. Per stage it sends its partial
+//     scores of two stages ahead to the peer, adds the peer's partial scores
+//     of this one to its own, masks (sequence end, causal position, rejected
+//     blocks), keeps the running maximum, rescales the warp's O rows in TMEM
+//     only when some row's maximum grows by more than 2^8 (probabilities stay
+//     below 256), and stores bf16 P to TMEM. At the end of a segment it
+//     normalises its O row: straight into o_lat when the q-block lies in this
+//     share and the merge is fused, else into the partial buffer, and the
+//     last CTA of a split q-block's half merges the parts while they are in L2.
+// The MMA warps issue from one elected lane. Every wait is bounded; on a
+// timeout the roles leave their loops, the MMA warps wait for their last
+// MMAs and the producer for its copies before TMEM is freed, and the pair
+// meets at a final cluster barrier so neither exits while the other may still
+// write into its shared memory.
 #include "async_copy.cuh"
+#include "cluster.cuh"
 #include "common.cuh"
 #include "internal.h"
 #include "merge.cuh"
@@ -45,40 +58,46 @@ namespace {
 
 constexpr int kTok = 32;                       // tokens per stage
 constexpr int kSlab = kTok * 128;              // 32 rows x 64 bf16 columns
-constexpr int kStage = 9 * kSlab;              // 36 KB
-constexpr int kStages = 4;                     // cache stages in the ring
-constexpr int kQSlab = kQBlockRows * 128;      // 128 rows x 64 columns
-constexpr int kQSmemSlabs = 4;                 // query columns [0, 256) in shared memory
-constexpr int kQSmemBytes = kQSmemSlabs * kQSlab;            // 64 KB
-constexpr int kQTmemWords = (kRow - 64 * kQSmemSlabs) / 2;   // 160: columns [256, 576)
+constexpr int kMaxSlabs = 5;                   // column slabs of one CTA (64 columns each)
+constexpr int kStage = kMaxSlabs * kSlab;      // 20 KB
+constexpr int kStages = 5;                     // cache stages in the ring
+constexpr int kXRecv = 4;                      // buffers of the peer's partial scores
+constexpr int kXSend = 3;                      // buffers of this CTA's partial scores
 constexpr int kThreads = 256;
 constexpr int kSoftWarp0 = 4;
-constexpr int kSoftBar = 2;                    // named barrier of the softmax warps
+constexpr int kSoftBar = 2;                    // named barriers of the softmax warps
+constexpr int kXBar = 3;
 constexpr uint32_t kOCol = 0, kSCol = 256, kPCol = 320, kQCol = 352, kTmemCols = 512;
-static_assert(kQCol + kQTmemWords <= kTmemCols, "TMEM budget");
 constexpr float kRescaleLog2 = 8.f;            // lazy rescale threshold (2^8)
+constexpr int kXBytes = kQBlockRows * kTok * 4;  // one stage of partial scores
+constexpr int kMergeSlots = 16;                // parts merged by the one-pass merge
+static_assert(kQCol + 32 * kMaxSlabs <= kTmemCols, "TMEM budget");
 
 enum {
   kFull0 = 0,
   kEmpty0 = kFull0 + kStages,
-  kSFull0 = kEmpty0 + kStages,   // [2] scores of stage i in S[i % 2]
-  kPFull0 = kSFull0 + 2,         // [2] probabilities of stage i in P[i % 2] (128 arrivals)
-  kQFull = kPFull0 + 2,          // shared-memory query columns landed
-  kQtReady,                      // TMEM query columns stored (128 arrivals)
+  kSFull0 = kEmpty0 + kStages,   // [2] partial scores of stage i in S[i % 2]
+  kSFree0 = kSFull0 + 2,         // [2] S[i % 2] read out (128 arrivals)
+  kXFull0 = kSFull0 + 4,         // [kXRecv] the peer's partial scores (bytes from the peer)
+  kPFull0 = kXFull0 + kXRecv,    // [2] probabilities of stage i in P[i % 2] (128 arrivals)
+  kPVDone0 = kPFull0 + 2,        // [2] O += P[i % 2] . V_i done
+  kQtReady = kPVDone0 + 2,       // query columns stored in TMEM (128 arrivals)
   kQEmpty,                       // every score MMA of the segment done
-  kPVDone,                       // the latest O += P . V done
-  kODone,                        // every MMA of the segment done
+  kODone,                        // every P.V MMA of the segment done
   kOFree,                        // O read out by the epilogue (128 arrivals)
-  kFinal,
+  kFinalS,                       // the score warp's last MMAs done
+  kFinalP,                       // the P.V warp's last MMAs done
   kNumBars
 };
 
 struct Smem {
-  static constexpr int q = 0;
-  static constexpr int stage = q + kQSmemBytes;
-  static constexpr int info = stage + kStages * kStage;  // [kStages] int2
+  static constexpr int stage = 0;
+  static constexpr int x = stage + kStages * kStage;           // [kXRecv] peer partial scores
+  static constexpr int xs = x + kXRecv * kXBytes;              // [kXSend] own partial scores
+  static constexpr int w = xs + kXSend * kXBytes;              // merge weights [16][128]
+  static constexpr int info = w + kMergeSlots * kQBlockRows * 4;  // [kStages] int2
   static constexpr int bars = info + kStages * 8;
-  static constexpr int misc = bars + kNumBars * 8;       // tmem base, abort flag, merge flag
+  static constexpr int misc = bars + kNumBars * 8;             // tmem base, abort flag, merge flag
   static constexpr int bytes = misc + 16;
   static constexpr int alloc = bytes + 1024;
 };
@@ -146,6 +165,55 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   }
 }
 
+// The same for a barrier that a peer CTA arrives on (cluster-scope acquire).
+__device__ __forceinline__ bool wait_or_abort_cluster(uint64_t* bar, uint32_t parity,
+                                                      volatile int* abort_flag) {
+  if (cl::try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (cl::try_wait_cluster(bar, parity)) return true;
+    if ((i & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+    }
+  }
+}
+
+// Four barriers polled together (their latencies overlap); parity 2 means
+// "no wait". The first is waited with cluster-scope acquire.
+__device__ __forceinline__ bool wait4_or_abort(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1,
+                                               uint64_t* b2, uint32_t p2, uint64_t* b3, uint32_t p3,
+                                               volatile int* abort_flag) {
+  auto poll = [&]() {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred q0, q1, q2, q3;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 q0, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 q1, [%3], %4;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 q2, [%5], %6;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 q3, [%7], %8;\n\t"
+        "and.pred q0, q0, q1;\n\tand.pred q2, q2, q3;\n\tand.pred q0, q0, q2;\n\t"
+        "selp.u32 %0, 1, 0, q0;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(b0)), "r"(p0), "r"(smem_u32(b1)), "r"(p1), "r"(smem_u32(b2)), "r"(p2 & 1),
+          "r"(smem_u32(b3)), "r"(p3 & 1)
+        : "memory");
+    return done != 0;
+  };
+  // a barrier that needs no wait is replaced by a copy of the second
+  if (p2 > 1) b2 = b1, p2 = p1;
+  if (p3 > 1) b3 = b1, p3 = p1;
+  if (poll()) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (poll()) return true;
+    if ((i & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+    }
+  }
+}
+
 __device__ __forceinline__ bool soft_red_or(bool v) {
   uint32_t r;
   asm volatile(
@@ -166,24 +234,27 @@ __device__ __forceinline__ int seg_stages(const TcSeg& s) {
   return span <= 0 ? 0 : min((span + kTok - 1) / kTok, 2 * (s.k1 - s.k0));
 }
 
-// Query columns [256, 576) of q-block row `qrow` into this thread's TMEM lane
-// (rows past the last query row are zero). Warp-collective.
+// This CTA's query columns [col0, col0 + 8 * nvec) of q-block row `qrow` into
+// its TMEM lane (rows past the last query row are zero). Warp-collective.
+template <int NVEC>
 __device__ __forceinline__ void load_q_tmem(const uint16_t* q_abs, int64_t qrow, int64_t qrows,
-                                            uint32_t taddr) {
-  const uint4* src = reinterpret_cast<const uint4*>(q_abs + (size_t)qrow * kRow + 64 * kQSmemSlabs);
+                                            int col0, uint32_t taddr) {
+  static_assert(NVEC % 8 == 0, "whole x16 stores per batch");
+  const uint4* src = reinterpret_cast<const uint4*>(q_abs + (size_t)qrow * kRow + col0);
   const bool live = qrow < qrows;
+  constexpr int kHalf = NVEC / 2;   // vectors per batch (registers)
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    uint4 buf[20];
+  for (int hb = 0; hb < 2; ++hb) {
+    uint4 buf[kHalf];
     if (live) {
 #pragma unroll
-      for (int i = 0; i < 20; ++i) buf[i] = __ldg(src + 20 * h + i);
+      for (int i = 0; i < kHalf; ++i) buf[i] = __ldg(src + kHalf * hb + i);
     } else {
 #pragma unroll
-      for (int i = 0; i < 20; ++i) buf[i] = make_uint4(0, 0, 0, 0);
+      for (int i = 0; i < kHalf; ++i) buf[i] = make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
-    for (int c = 0; c < 5; ++c) {
+    for (int c = 0; c < kHalf / 4; ++c) {
       uint32_t w[16];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -192,14 +263,21 @@ __device__ __forceinline__ void load_q_tmem(const uint16_t* q_abs, int64_t qrow,
         w[4 * k + 2] = buf[4 * c + k].z;
         w[4 * k + 3] = buf[4 * c + k].w;
       }
-      tc::st16(taddr + kQCol + 80 * h + 16 * c, w);
+      tc::st16(taddr + kQCol + 4 * kHalf * hb + 16 * c, w);
     }
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-    decode_tc_kernel(const __grid_constant__ CUtensorMap cache_map,
-                     const __grid_constant__ CUtensorMap q_map, DecodeArgs a, int batch) {
+__device__ __forceinline__ void load_q_cta(int h, const uint16_t* q_abs, int64_t qrow,
+                                           int64_t qrows, uint32_t trow) {
+  if (h == 0)
+    load_q_tmem<32>(q_abs, qrow, qrows, 0, trow);      // columns [0, 256)
+  else
+    load_q_tmem<40>(q_abs, qrow, qrows, 256, trow);    // columns [256, 576)
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap cache_map, DecodeArgs a, int batch) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -208,11 +286,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Smem::misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Smem::misc + 4);
   int* merge_flag = reinterpret_cast<int*>(sm + Smem::misc + 8);
-  uint8_t* sQ = sm + Smem::q;
   uint8_t* sStage = sm + Smem::stage;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int share_idx = blockIdx.x >> 1, half = blockIdx.x & 1;
+  const int h = (int)cl::rank();                    // column half of this CTA
+  const int share_idx = blockIdx.x >> 1;
+  const int slab0 = 4 * h, nslab = 4 + h;          // cache column slabs [slab0, slab0 + nslab)
   uint8_t* ws = reinterpret_cast<uint8_t*>(a.workspace);
   uint32_t* status = &reinterpret_cast<WsHeader*>(ws)->status;
   const int bs = a.block_size;
@@ -223,19 +302,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int i = 0; i < kNumBars; ++i) {
-      const bool many = i == kPFull0 || i == kPFull0 + 1 || i == kQtReady || i == kOFree;
+      const bool many = (i >= kSFree0 && i < kSFree0 + 2) || (i >= kPFull0 && i < kPFull0 + 2) ||
+                        i == kQtReady || i == kOFree;
       mbar_init(&bars[i], many ? 128 : 1);
     }
+    // the peer's partial scores of the first kXRecv stages are expected
+    for (int i = 0; i < kXRecv; ++i) mbar_arrive_expect_tx(&bars[kXFull0 + i], kXBytes);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) tc::alloc(tmem_slot, kTmemCols);
-  if (warp == 0 && lane == 0) {
-    prefetch_tensormap(&cache_map);
-    prefetch_tensormap(&q_map);
-  }
+  if (warp == 0 && lane == 0) prefetch_tensormap(&cache_map);
   tc::fence_before_sync();
-  __syncthreads();
+  cl::sync();  // both CTAs' barriers exist before either copies into the other
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   pdl_wait();  // the plan and q_abs come from earlier kernels
@@ -243,32 +322,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   TcWalker sw;
   const bool has_work = sw.init(ws, a.num_q, a.groups, a.num_ctas, batch, share_idx);
-  if (a.o_lat && warp >= kSoftWarp0)
+  if (a.o_lat && warp >= kSoftWarp0 && h == 0)
     zero_unvisited_rows(sw.row_info, sw.plan_ok, a.num_q, a.num_heads, a.o_lat, tid - 128, 128);
   TcSeg seg;
+  auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, wait_or_abort(bar, parity, abort_flag));
+  };
 
   if (has_work && warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int stage_i = 0, seg_i = 0;
+      int stage_i = 0;
       bool ok = true;
       while (ok && sw.next(seg)) {
-        if (seg_i > 0 && !wait_or_abort(&bars[kQEmpty], (seg_i - 1) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(&bars[kQFull], kQSmemBytes);
-#pragma unroll 1
-        for (int j = 0; j < kQSmemSlabs; ++j)
-          tma_load_2d(sQ + j * kQSlab, &q_map, 64 * j, kHG * seg.t_first, &bars[kQFull]);
-        ++seg_i;
         const int32_t* bt = a.block_table + (size_t)seg.b * a.max_blocks_per_seq;
         const int n = seg_stages(seg);
 #pragma unroll 1
         for (int t = 0; t < n; ++t) {
           const int tstart = seg.k0 * kTile + t * kTok;
           const int v = min(kTok, seg.vis - tstart);
-          const int slot = stage_i & (kStages - 1);
+          const int slot = stage_i % kStages;
           int blk[2], okmask = 0, nload = 0;
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
@@ -292,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           info[slot] = make_int2(v, okmask);
-          mbar_arrive_expect_tx(&bars[kFull0 + slot], (uint32_t)nload * 9u * (uint32_t)bsr * 128u);
+          mbar_arrive_expect_tx(&bars[kFull0 + slot], (uint32_t)(nload * nslab * bsr * 128));
           uint8_t* dst = sStage + slot * kStage;
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
@@ -300,9 +373,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int tok = tstart + (i << bsr_shift);
               const int y = blk[i] * bs + (tok % bs);
 #pragma unroll 1
-              for (int j = 0; j < 9; ++j)
-                tma_load_2d(dst + j * kSlab + (i << bsr_shift) * 128, &cache_map, 64 * j, y,
-                            &bars[kFull0 + slot]);
+              for (int j = 0; j < nslab; ++j)
+                tma_load_2d(dst + j * kSlab + (i << bsr_shift) * 128, &cache_map,
+                            64 * (slab0 + j), y, &bars[kFull0 + slot]);
             }
           }
           ++stage_i;
@@ -318,103 +391,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (fills > 0 && !mbar_wait(&bars[kFull0 + slot], (fills - 1) & 1))
           set_status(status, MLA_DEV_TIMEOUT);
       }
-      if (seg_i > 0 && !mbar_wait(&bars[kQFull], (seg_i - 1) & 1)) set_status(status, MLA_DEV_TIMEOUT);
     }
     __syncwarp();
   } else if (has_work && warp == 1) {
-    // --------------------------------------------------------- MMA issuer
-    constexpr uint32_t kIdS = tc::idesc_bf16(128, kTok, false, false);
+    // ------------------------------------------------------ P.V issuer
     constexpr uint32_t kIdO = tc::idesc_bf16(128, 256, false, true);
-    // descriptors of the first slab; others differ only in the start address
-    const uint64_t qdesc = tc::smem_desc(smem_u32(sQ), 16, 1024, tc::kSwizzle128);
-    const uint64_t kdesc = tc::smem_desc(smem_u32(sStage), 16, 1024, tc::kSwizzle128);
-    const uint64_t vdesc =
-        tc::smem_desc(smem_u32(sStage) + 4 * half * kSlab, kSlab, 1024, tc::kSwizzle128);
+    // V: this CTA's first four slabs of the stage, MN-major
+    const uint64_t vdesc = tc::smem_desc(smem_u32(sStage), kSlab, 1024, tc::kSwizzle128);
     const bool leader = tc::elect_one();
-    auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
-      return __all_sync(0xffffffffu, wait_or_abort(bar, parity, abort_flag));
-    };
-    // S[i % 2] = Q . K_i^T over the 576 columns (9 slabs x 4 k-steps)
-    auto issue_score = [&](int i) {
-      const int slot = i & (kStages - 1);
-      const uint32_t d = tmem + kSCol + (uint32_t)(i & 1) * kTok;
-      if (leader) {
-#pragma unroll
-        for (int kk = 0; kk < 36; ++kk) {
-          const int j = kk >> 2, c = kk & 3;
-          const uint64_t b = kdesc + (uint64_t)((slot * kStage + j * kSlab + c * 32) >> 4);
-          if (j < kQSmemSlabs)
-            tc::mma_bf16(d, qdesc + (uint64_t)((j * kQSlab + c * 32) >> 4), b, kIdS, kk > 0);
-          else
-            tc::mma_bf16_tmem_a(d, tmem + kQCol + (uint32_t)((j - kQSmemSlabs) * 32 + c * 8), b,
-                                kIdS, kk > 0);
-        }
-        tc::commit(&bars[kSFull0 + (i & 1)]);
-      }
-      __syncwarp();
-    };
-    // O += P[i % 2] . V_i (this CTA's 256 latent columns of the stage)
-    auto issue_pv = [&](int i, bool first) {
-      const int slot = i & (kStages - 1);
-      if (leader) {
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks)
-          tc::mma_bf16_tmem_a(tmem + kOCol, tmem + kPCol + (uint32_t)((i & 1) * 16 + ks * 8),
-                              vdesc + (uint64_t)((slot * kStage + ks * 16 * 128) >> 4), kIdO,
-                              !(first && ks == 0));
-        tc::commit(&bars[kEmpty0 + slot]);
-        tc::commit(&bars[kPVDone]);
-      }
-      __syncwarp();
-    };
     int stage_i = 0, seg_i = 0;
     bool ok = true;
     while (ok && sw.next(seg)) {
       const int n = seg_stages(seg);
-      if (!warp_wait(&bars[kQFull], seg_i & 1) || !warp_wait(&bars[kQtReady], seg_i & 1)) {
-        ok = false;
-        break;
-      }
-      tc::fence_after_sync();
-      if (n > 0) {
-        if (!warp_wait(&bars[kFull0 + (stage_i & (kStages - 1))], (stage_i / kStages) & 1)) {
-          ok = false;
-          break;
-        }
-        tc::fence_after_sync();
-        issue_score(stage_i);
-      }
 #pragma unroll 1
       for (int t = 0; t < n; ++t) {
-        const int i = stage_i + t;
-        if (t + 1 < n) {
-          // scores of the next stage while the softmax works on this one
-          if (!warp_wait(&bars[kFull0 + ((i + 1) & (kStages - 1))], ((i + 1) / kStages) & 1)) {
-            ok = false;
-            break;
-          }
-          tc::fence_after_sync();
-          issue_score(i + 1);
-        } else {
-          if (leader) tc::commit(&bars[kQEmpty]);  // the query may be replaced
-          __syncwarp();
-        }
-        if (!warp_wait(&bars[kPFull0 + (i & 1)], (i >> 1) & 1)) {
-          ok = false;
-          break;
-        }
-        if (t == 0 && seg_i > 0 && !warp_wait(&bars[kOFree], (seg_i - 1) & 1)) {
-          ok = false;
-          break;
-        }
+        const int i = stage_i + t, slot = i % kStages;
+        if (!warp_wait(&bars[kPFull0 + (i & 1)], (i >> 1) & 1)) { ok = false; break; }
+        if (t == 0 && seg_i > 0 && !warp_wait(&bars[kOFree], (seg_i - 1) & 1)) { ok = false; break; }
         tc::fence_after_sync();
-        issue_pv(i, t == 0);
+        if (leader) {
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks)
+            tc::mma_bf16_tmem_a(tmem + kOCol, tmem + kPCol + (uint32_t)((i & 1) * 16 + ks * 8),
+                                vdesc + (uint64_t)((slot * kStage + ks * 16 * 128) >> 4), kIdO,
+                                !(t == 0 && ks == 0));
+          tc::commit(&bars[kEmpty0 + slot]);
+          tc::commit(&bars[kPVDone0 + (i & 1)]);
+        }
+        __syncwarp();
       }
       if (!ok) break;
-      if (leader) {
-        if (n == 0) tc::commit(&bars[kQEmpty]);
-        tc::commit(&bars[kODone]);
-      }
+      if (leader) tc::commit(&bars[kODone]);
       __syncwarp();
       stage_i += n;
       ++seg_i;
@@ -424,9 +431,57 @@ __global__ void __launch_bounds__(kThreads, 1)
       *abort_flag = 1;
     }
     // every MMA issued so far must finish before TMEM is freed
-    if (leader) tc::commit(&bars[kFinal]);
+    if (leader) tc::commit(&bars[kFinalP]);
     __syncwarp();
-    if (!mbar_wait(&bars[kFinal], 0) && leader) set_status(status, MLA_DEV_TIMEOUT);
+    if (!mbar_wait(&bars[kFinalP], 0) && leader) set_status(status, MLA_DEV_TIMEOUT);
+    __syncwarp();
+  } else if (has_work && warp == 2) {
+    // ----------------------------------------------------- score issuer
+    constexpr uint32_t kIdS = tc::idesc_bf16(128, kTok, false, false);
+    const uint64_t kdesc = tc::smem_desc(smem_u32(sStage), 16, 1024, tc::kSwizzle128);
+    const bool leader = tc::elect_one();
+    const int ksteps = 4 * nslab;
+    int stage_i = 0, seg_i = 0;
+    bool ok = true;
+    while (ok && sw.next(seg)) {
+      const int n = seg_stages(seg);
+      if (!warp_wait(&bars[kQtReady], seg_i & 1)) { ok = false; break; }
+      tc::fence_after_sync();
+#pragma unroll 1
+      for (int t = 0; t < n; ++t) {
+        const int i = stage_i + t, slot = i % kStages;
+        // S[i % 2] was read out (stage i - 2) and the stage has landed
+        if (i >= 2 && !warp_wait(&bars[kSFree0 + (i & 1)], ((i - 2) >> 1) & 1)) { ok = false; break; }
+        if (!warp_wait(&bars[kFull0 + slot], (i / kStages) & 1)) { ok = false; break; }
+        tc::fence_after_sync();
+        if (leader) {
+          const uint32_t d = tmem + kSCol + (uint32_t)(i & 1) * kTok;
+#pragma unroll
+          for (int kk = 0; kk < 4 * kMaxSlabs; ++kk) {
+            if (kk < ksteps) {
+              const int j = kk >> 2, c = kk & 3;
+              tc::mma_bf16_tmem_a(d, tmem + kQCol + (uint32_t)(j * 32 + c * 8),
+                                  kdesc + (uint64_t)((slot * kStage + j * kSlab + c * 32) >> 4),
+                                  kIdS, kk > 0);
+            }
+          }
+          tc::commit(&bars[kSFull0 + (i & 1)]);
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (leader) tc::commit(&bars[kQEmpty]);  // the query may be replaced
+      __syncwarp();
+      stage_i += n;
+      ++seg_i;
+    }
+    if (!ok && leader) {
+      set_status(status, MLA_DEV_TIMEOUT);
+      *abort_flag = 1;
+    }
+    if (leader) tc::commit(&bars[kFinalS]);
+    __syncwarp();
+    if (!mbar_wait(&bars[kFinalS], 0) && leader) set_status(status, MLA_DEV_TIMEOUT);
     __syncwarp();
   } else if (has_work && warp >= kSoftWarp0) {
     // ----------------------------------------------------------- softmax
@@ -439,11 +494,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint16_t* q_abs = reinterpret_cast<const uint16_t*>(a.q_abs);
     const int64_t qrows = a.num_q * a.num_heads;
     const float scale = a.scale_log2;
+    const uint32_t peer = (uint32_t)(h ^ 1);
+    const uint32_t x_peer0 = cl::map(smem_u32(sm + Smem::x), peer);
+    const uint32_t xbar_peer0 = cl::map(smem_u32(&bars[kXFull0]), peer);
+    float* wsm = reinterpret_cast<float*>(sm + Smem::w);
     int stage_i = 0, seg_i = 0;
     bool aborted = false, fail = false;
+    // partial scores of stage j: TMEM -> own buffer j % kXSend -> one bulk copy
+    // into the peer's buffer j % kXRecv, counted on the peer's barrier
+    auto send_scores = [&](int j) {
+      uint32_t sv[32];
+      tc::ld32(trow + kSCol + (uint32_t)(j & 1) * kTok, sv);
+      tc::wait_ld();
+      tc::fence_before_sync();
+      mbar_arrive(&bars[kSFree0 + (j & 1)]);
+      // the copy of stage j - kXSend read this buffer; at most kXSend - 1 newer remain
+      if (r == 0) cl::bulk_wait_read<kXSend - 1>();
+      named_bar_sync(kXBar, 128);
+      uint8_t* xs = sm + Smem::xs + (j % kXSend) * kXBytes + r * 128;
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        *reinterpret_cast<uint4*>(xs + ((k ^ (r & 7)) << 4)) =
+            make_uint4(sv[4 * k], sv[4 * k + 1], sv[4 * k + 2], sv[4 * k + 3]);
+      fence_proxy_async_smem();
+      named_bar_sync(kXBar, 128);
+      if (r == 0) {
+        cl::bulk_to_peer(x_peer0 + (uint32_t)(j % kXRecv) * kXBytes,
+                         smem_u32(sm + Smem::xs) + (uint32_t)(j % kXSend) * kXBytes, kXBytes,
+                         xbar_peer0 + (uint32_t)(j % kXRecv) * 8);
+        cl::bulk_commit();
+      }
+    };
     bool have = sw.next(seg);
     if (have) {
-      load_q_tmem(q_abs, (int64_t)kHG * seg.t_first + r, qrows, trow);
+      load_q_cta(h, q_abs, (int64_t)kHG * seg.t_first + r, qrows, trow);
       tc::wait_st();
       tc::fence_before_sync();
       mbar_arrive(&bars[kQtReady]);
@@ -454,32 +538,58 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid_row = t < seg.t_end;
       const int pos = valid_row ? sw.row_info[t / sw.G].y : -1;
       float m_used = -INFINITY, l = 0.f;
+      // the first two stages' partial scores go out before any is used
+#pragma unroll 1
+      for (int tt = 0; tt < n && tt < 2; ++tt) {
+        const int j = stage_i + tt;
+        const bool oks = wait_or_abort(&bars[kSFull0 + (j & 1)], (j >> 1) & 1, abort_flag);
+        if (soft_red_or(!oks || fail)) { aborted = true; break; }
+        tc::fence_after_sync();
+        send_scores(j);
+      }
+      if (aborted) break;
 #pragma unroll 1
       for (int tt = 0; tt < n; ++tt) {
-        const int i = stage_i + tt, slot = i & (kStages - 1), b = i & 1;
-        bool okw = wait_or_abort(&bars[kFull0 + slot], (i / kStages) & 1, abort_flag);
-        okw = okw && wait_or_abort(&bars[kSFull0 + b], (i >> 1) & 1, abort_flag);
+        const int i = stage_i + tt, slot = i % kStages, b = i & 1, xb = i % kXRecv;
+        const bool ahead = tt + 2 < n;
+        // the peer's partial scores of stage i, the stage (for its info), the
+        // scores of stage i + 2, and P[i % 2] free (O += P . V of stage i - 2)
+        const bool okw = wait4_or_abort(&bars[kXFull0 + xb], (i / kXRecv) & 1,
+                                        &bars[kFull0 + slot], (i / kStages) & 1,
+                                        &bars[kSFull0 + b], ahead ? ((i + 2) >> 1) & 1 : 2u,
+                                        &bars[kPVDone0 + b], i >= 2 ? ((i - 2) >> 1) & 1 : 2u,
+                                        abort_flag);
         if (soft_red_or(!okw || fail)) { aborted = true; break; }
         tc::fence_after_sync();
-        uint32_t sr[32];
-        tc::ld32(trow + kSCol + (uint32_t)b * kTok, sr);
-        tc::wait_ld();
         const int tstart = seg.k0 * kTile + tt * kTok;
         const int2 inf = info[slot];
         const int v = inf.x, okmask = inf.y;
         // live tokens: a prefix (sequence end, causal position) minus rejected blocks
         const int lim = min(v, pos - tstart + 1);
+        // S = own partial + the peer's partial (both swizzled the same way)
         float x[32];
-        if (lim >= kTok && okmask == full_mask) {
+        {
+          const uint8_t* xo = sm + Smem::xs + (i % kXSend) * kXBytes + r * 128;
+          const uint8_t* xp = sm + Smem::x + xb * kXBytes + r * 128;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(sr[j]);
-        } else {
+          for (int k = 0; k < 8; ++k) {
+            const float4 u = *reinterpret_cast<const float4*>(xo + ((k ^ (r & 7)) << 4));
+            const float4 w = *reinterpret_cast<const float4*>(xp + ((k ^ (r & 7)) << 4));
+            x[4 * k] = u.x + w.x; x[4 * k + 1] = u.y + w.y;
+            x[4 * k + 2] = u.z + w.z; x[4 * k + 3] = u.w + w.w;
+          }
+        }
+        if (!(lim >= kTok && okmask == full_mask)) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const bool live = j < lim && ((okmask >> (j >> bsr_shift)) & 1);
-            x[j] = live ? __uint_as_float(sr[j]) : -INFINITY;
+            if (!live) x[j] = -INFINITY;
           }
         }
+        // the peer writes this buffer again for stage i + kXRecv only after this
+        // CTA has sent stage i + 2 (below), i.e. after every load above
+        if (r == 0) mbar_arrive_expect_tx(&bars[kXFull0 + xb], kXBytes);
+        if (ahead) send_scores(i + 2);
         float mx[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) mx[j] = fmaxf(x[j], x[j + 16]);
@@ -500,7 +610,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (__any_sync(0xffffffffu, rescale_o)) {
           // this warp's O rows: the previous O += P . V must have landed
-          const bool okp = __all_sync(0xffffffffu, wait_or_abort(&bars[kPVDone], (i - 1) & 1, abort_flag));
+          const bool okp = __all_sync(
+              0xffffffffu, wait_or_abort(&bars[kPVDone0 + ((i - 1) & 1)], ((i - 1) >> 1) & 1, abort_flag));
           if (okp) {
             tc::fence_after_sync();
 #pragma unroll 1
@@ -534,10 +645,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         l += ps[0];
         if (v < kTok || okmask != full_mask) {
           // cache rows past the sequence's last token or in a rejected block may
-          // hold anything (NaN): zero this half's latent columns so P = 0 stays 0
+          // hold anything (NaN): zero the latent columns so P = 0 stays 0
           uint8_t* stg = sStage + slot * kStage;
           for (int e = r; e < kTok * 4 * 8; e += 128) {
-            const int row = e >> 5, sl = 4 * half + ((e >> 3) & 3), ch = e & 7;
+            const int row = e >> 5, sl = (e >> 3) & 3, ch = e & 7;
             const bool live = row < v && ((okmask >> (row >> bsr_shift)) & 1);
             if (!live) *reinterpret_cast<uint4*>(stg + sl * kSlab + sw128(row, ch)) = make_uint4(0, 0, 0, 0);
           }
@@ -549,113 +660,171 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (aborted) break;
       stage_i += n;
-      // the next segment's upper query columns, while this one's last
-      // products finish (its scores are all done once QEmpty completes)
+      // the next segment's query columns, while this one's last products
+      // finish (its scores are all done once QEmpty completes)
       TcSeg nxt;
-      const bool more = sw.next(nxt);
-      if (more) {
+      const bool more_seg = sw.next(nxt);
+      if (more_seg) {
         const bool okq = wait_or_abort(&bars[kQEmpty], seg_i & 1, abort_flag);
         if (soft_red_or(!okq || fail)) { aborted = true; break; }
         tc::fence_after_sync();
-        load_q_tmem(q_abs, (int64_t)kHG * nxt.t_first + r, qrows, trow);
+        load_q_cta(h, q_abs, (int64_t)kHG * nxt.t_first + r, qrows, trow);
         tc::wait_st();
         tc::fence_before_sync();
         mbar_arrive(&bars[kQtReady]);
       }
-      // ---- epilogue: normalise the O row half into the partial buffer
+      // ---- epilogue: normalise this CTA's half of the O row
       const bool okd = wait_or_abort(&bars[kODone], seg_i & 1, abort_flag);
       if (soft_red_or(!okd || fail)) { aborted = true; break; }
       tc::fence_after_sync();
+      const int c_first = seg.ustart / sw.share;
+      const int c_last = (seg.ustart + seg.tiles - 1) / sw.share;
+      const bool direct = a.o_lat != nullptr && c_first == c_last;   // the q-block is this share's alone
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const int64_t slot = (int64_t)share_idx + seg.qb;
-      float4* dst = reinterpret_cast<float4*>(o_out + ((size_t)slot * kQBlockRows + r) * kDc + 256 * half);
+      float4* dst;
+      if (direct)
+        dst = reinterpret_cast<float4*>(a.o_lat + ((size_t)kHG * seg.t_first + r) * kDc + 256 * h);
+      else
+        dst = reinterpret_cast<float4*>(o_out + ((size_t)slot * kQBlockRows + r) * kDc + 256 * h);
+      const bool store = !direct || valid_row;
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
         uint32_t o[32];
         tc::ld32(trow + kOCol + 32 * c, o);
         tc::wait_ld();
+        if (store) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          dst[8 * c + k] = make_float4(__uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
-                                       __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
+          for (int k = 0; k < 8; ++k)
+            dst[8 * c + k] = make_float4(__uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
+                                         __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
+        }
       }
-      // both halves see the same scores, so both write the same lse
-      lse_out[slot * kQBlockRows + r] = l > 0.f ? m_used + log2f(l) : -INFINITY;
+      // both CTAs of the pair see the same scores and write the same lse
+      if (!direct) lse_out[slot * kQBlockRows + r] = l > 0.f ? m_used + log2f(l) : -INFINITY;
       tc::fence_before_sync();
       mbar_arrive(&bars[kOFree]);
-      if (a.o_lat != nullptr) {
+      if (a.o_lat != nullptr && !direct) {
         // count this part; the last part of this half merges the q-block
-        const int c_first = seg.ustart / sw.share;
-        const int c_last = (seg.ustart + seg.tiles - 1) / sw.share;
         __threadfence();
         named_bar_sync(kSoftBar, 128);
-        if (r == 0) *merge_flag = atomicAdd(&arrive[seg.qb * 2 + half], 1) == c_last - c_first;
+        if (r == 0) *merge_flag = atomicAdd(&arrive[seg.qb * 2 + h], 1) == c_last - c_first;
         named_bar_sync(kSoftBar, 128);
         if (*merge_flag) {
           __threadfence();
-          if (valid_row) {
-            const int ns = c_last - c_first + 1;
-            const int64_t s0 = (int64_t)c_first + seg.qb;
-            float M = -INFINITY;
-            for (int s = 0; s < ns; ++s) M = fmaxf(M, lse_out[(s0 + s) * kQBlockRows + r]);
-            float den = 0.f;
-            if (M != -INFINITY)
-              for (int s = 0; s < ns; ++s) den += fast_exp2(lse_out[(s0 + s) * kQBlockRows + r] - M);
-            const float dinv = den > 0.f ? 1.f / den : 0.f;
-            float4* orow = reinterpret_cast<float4*>(a.o_lat + ((size_t)kHG * seg.t_first + r) * kDc + 256 * half);
+          const int ns = c_last - c_first + 1;
+          const int64_t s0 = (int64_t)c_first + seg.qb;
+          // row r's max lse and 1 / weight sum over its parts
+          float M = -INFINITY;
+          for (int s = 0; s < ns; ++s) M = fmaxf(M, lse_out[(s0 + s) * kQBlockRows + r]);
+          float den = 0.f;
+          if (M != -INFINITY)
+            for (int s = 0; s < ns; ++s) den += fast_exp2(lse_out[(s0 + s) * kQBlockRows + r] - M);
+          const float dinv = den > 0.f ? 1.f / den : 0.f;
+          const int rows_valid = min(kQBlockRows, (seg.t_end - seg.t_first) * kHG);
+          const float4* op4 = reinterpret_cast<const float4*>(o_out) + 64 * h;
+          float4* ol4 = reinterpret_cast<float4*>(a.o_lat + (size_t)kHG * seg.t_first * kDc) + 64 * h;
+          if (ns <= kMergeSlots) {
+            // weights w[s][row] to shared memory, then rows 2k + (tid / 64) with
+            // float4 column tid % 64 of the half: coalesced, 16 rows per pass
+            for (int s = 0; s < ns; ++s)
+              wsm[s * kQBlockRows + r] =
+                  M == -INFINITY ? 0.f : fast_exp2(lse_out[(s0 + s) * kQBlockRows + r] - M) * dinv;
+            named_bar_sync(kSoftBar, 128);
+            const int c4 = r & 63, rsub = r >> 6;
 #pragma unroll 1
-            for (int c = 0; c < 8; ++c) {
-              float4 acc[8];
+            for (int k0 = 0; k0 < kQBlockRows / 2; k0 += 16) {
+              float4 acc[16];
 #pragma unroll
-              for (int k = 0; k < 8; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+              for (int u = 0; u < 16; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
               for (int s = 0; s < ns; ++s) {
-                const float lv = lse_out[(s0 + s) * kQBlockRows + r];
-                const float wgt = M == -INFINITY ? 0.f : fast_exp2(lv - M) * dinv;
-                const float4* src = reinterpret_cast<const float4*>(
-                    o_out + ((size_t)(s0 + s) * kQBlockRows + r) * kDc + 256 * half) + 8 * c;
+                const float4* src = op4 + (size_t)(s0 + s) * kQBlockRows * (kDc / 4) + c4;
+                float4 vv[16];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                  const float4 xv = src[k];
-                  acc[k].x = fmaf(wgt, xv.x, acc[k].x);
-                  acc[k].y = fmaf(wgt, xv.y, acc[k].y);
-                  acc[k].z = fmaf(wgt, xv.z, acc[k].z);
-                  acc[k].w = fmaf(wgt, xv.w, acc[k].w);
+                for (int u = 0; u < 16; ++u) vv[u] = src[(size_t)(rsub + 2 * (k0 + u)) * (kDc / 4)];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                  const float wgt = wsm[s * kQBlockRows + rsub + 2 * (k0 + u)];
+                  acc[u].x = fmaf(wgt, vv[u].x, acc[u].x);
+                  acc[u].y = fmaf(wgt, vv[u].y, acc[u].y);
+                  acc[u].z = fmaf(wgt, vv[u].z, acc[u].z);
+                  acc[u].w = fmaf(wgt, vv[u].w, acc[u].w);
                 }
               }
 #pragma unroll
-              for (int k = 0; k < 8; ++k) orow[8 * c + k] = acc[k];
+              for (int u = 0; u < 16; ++u) {
+                const int row = rsub + 2 * (k0 + u);
+                if (row < rows_valid) ol4[(size_t)row * (kDc / 4) + c4] = acc[u];
+              }
+            }
+            named_bar_sync(kSoftBar, 128);   // the weights may be overwritten after this
+          } else if (valid_row) {
+            // many parts (tiny shares): row r by thread r
+#pragma unroll 1
+            for (int c = 0; c < 64; ++c) {
+              float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+              for (int s = 0; s < ns; ++s) {
+                const float wgt = M == -INFINITY ? 0.f : fast_exp2(lse_out[(s0 + s) * kQBlockRows + r] - M) * dinv;
+                const float4 xv = op4[((size_t)(s0 + s) * kQBlockRows + r) * (kDc / 4) + c];
+                acc.x = fmaf(wgt, xv.x, acc.x);
+                acc.y = fmaf(wgt, xv.y, acc.y);
+                acc.z = fmaf(wgt, xv.z, acc.z);
+                acc.w = fmaf(wgt, xv.w, acc.w);
+              }
+              ol4[(size_t)r * (kDc / 4) + c] = acc;
             }
           }
-          if (r == 0) arrive[seg.qb * 2 + half] = 0;  // ready for the next launch
+          if (r == 0) arrive[seg.qb * 2 + h] = 0;  // ready for the next launch
         }
         named_bar_sync(kSoftBar, 128);
       }
       seg = nxt;
-      have = more;
+      have = more_seg;
       ++seg_i;
     }
     if (aborted && r == 0) {
       set_status(status, MLA_DEV_TIMEOUT);
       *abort_flag = 1;
     }
+    if (r == 0) cl::bulk_wait_read<0>();   // no copy still reads this CTA's staging buffers
   }
 
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   if (warp == 1) tc::dealloc(tmem, kTmemCols);
+  cl::sync();  // the peer no longer writes into this CTA's shared memory
 }
 
 }  // namespace
 
+int decode_tc_max_clusters() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev] > 0) return cached[dev];
+  if (cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Smem::alloc) != cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(2);
+  lc.blockDim = dim3(kThreads);
+  lc.dynamicSmemBytes = Smem::alloc;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel, &lc) != cudaSuccess) return 0;
+  cached[dev] = n;
+  return n;
+}
+
 cudaError_t launch_decode_tc(const DecodeArgs& a, int32_t batch, const CUtensorMap& cache_map,
-                             const CUtensorMap& q_map, cudaStream_t stream) {
+                             cudaStream_t stream) {
   const int smem = Smem::alloc;
   cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(decode_tc_kernel, dim3(a.num_ctas), dim3(kThreads), smem, stream, cache_map,
-                    q_map, a, (int)batch);
+  return launch_pdl(decode_tc_kernel, dim3(a.num_ctas), dim3(kThreads), smem, stream, cache_map, a,
+                    (int)batch);
 }
 
 }  // namespace mla

@@ -55,8 +55,13 @@ cudaError_t launch_decode_bf16(const DecodeArgs& a, const CUtensorMap& cache_map
 
 cudaError_t launch_decode_f32(const DecodeArgs& a, cudaStream_t stream);
 
+// Tensor-core decode (CTA pairs as clusters); num_ctas must be even.
 cudaError_t launch_decode_tc(const DecodeArgs& a, int32_t batch, const CUtensorMap& cache_map,
-                             const CUtensorMap& q_map, cudaStream_t stream);
+                             cudaStream_t stream);
+
+// CTA pairs of the tensor-core decode that fit on the current device at once
+// (0 if the query fails).
+int decode_tc_max_clusters();
 
 cudaError_t launch_combine(const void* workspace, int32_t groups, int32_t num_ctas,
                            int64_t num_q, int32_t batch, float* o_lat, cudaStream_t stream);

@@ -56,9 +56,14 @@ bool use_tc(const mla_config* cfg, int64_t num_q, int32_t batch) {
   return cfg->dtype == MLA_BF16 && (cfg->num_heads >= 64 || num_q >= 4 * (int64_t)batch);
 }
 
-// CTA count of the decode launch: one per SM (or the caller's), even in
-// tensor-core mode, where two CTAs share each split (one per output half).
+// CTA count of the decode launch: one per SM (or the caller's). In
+// tensor-core mode two CTAs (a cluster) share each split, so the count is
+// even, and by default it is the number of pairs the device holds at once.
 int decode_ctas(const mla_config* cfg, bool tc) {
+  if (tc && cfg->num_ctas <= 0) {
+    const int pairs = decode_tc_max_clusters();
+    if (pairs > 0) return 2 * pairs;
+  }
   const int C = resolve_num_ctas(cfg);
   if (C <= 0 || !tc) return C;
   return C >= 2 ? (C & ~1) : 2;
@@ -243,12 +248,10 @@ mla_status decode_impl(const mla_config* cfg, const void* q_abs, const void* cac
                                            : (uint64_t)cfg->block_size;
   CUtensorMap cache_map, q_map;
   if (tc) {
-    // boxes: 32-token half pages (or whole pages below 32 tokens), 128-row q-blocks
+    // boxes: 32-token half pages (or whole pages below 32 tokens)
     const uint32_t box_rows = cfg->block_size < 32 ? (uint32_t)cfg->block_size : 32u;
-    if (!make_row_map(&cache_map, cache, map_rows, box_rows) ||
-        !make_row_map(&q_map, q_abs, (uint64_t)num_q * cfg->num_heads, kQBlockRows))
-      return MLA_ERR_CUDA;
-    return from_cuda(launch_decode_tc(da, batch, cache_map, q_map, st));
+    if (!make_row_map(&cache_map, cache, map_rows, box_rows)) return MLA_ERR_CUDA;
+    return from_cuda(launch_decode_tc(da, batch, cache_map, st));
   }
   if (!make_row_map(&cache_map, cache, map_rows, (uint32_t)cfg->block_size) ||
       !make_row_map(&q_map, q_abs, (uint64_t)num_q * cfg->num_heads, kHG))

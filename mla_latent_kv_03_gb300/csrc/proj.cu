@@ -409,6 +409,153 @@ __global__ void __launch_bounds__(128) combine_out_proj_bf16_kernel(
   }
 }
 
+// combine + out_proj, bf16, up to 16 query rows per CTA (decode batches):
+// the CTA first merges its 16 latent rows of head h into shared memory as
+// bf16 -- per row one warp reduces the max log-sum-exp and the weight sum over
+// the parts, then 8 threads per row accumulate the weighted partial rows, one
+// round trip per part -- and then projects them as out_proj does.
+constexpr int kMergedStride = kDc * 2 + 16;  // bytes per merged row (padded against bank conflicts)
+
+__global__ void __launch_bounds__(128) combine_out_proj_rows16_kernel(
+    const uint8_t* __restrict__ ws, int groups, int num_ctas, int num_q, int batch,
+    const __nv_bfloat16* __restrict__ W_uv, __nv_bfloat16* __restrict__ out, int H) {
+  extern __shared__ __align__(1024) uint8_t smem_cr[];
+  uint8_t* sB = smem_cr;                                               // 512 x 128 B
+  float* sRed = reinterpret_cast<float*>(smem_cr + 512 * 128);         // [4][16][64]
+  uint8_t* sA = smem_cr + 512 * 128 + 4 * 16 * 64 * 4;                 // [16] merged rows, bf16
+  int64_t* sFirst = reinterpret_cast<int64_t*>(sA + 16 * kMergedStride);
+  int* sStride = reinterpret_cast<int*>(sFirst + 16);
+  int* sCount = sStride + 16;
+  float* sM = reinterpret_cast<float*>(sCount + 16);
+  float* sInv = sM + 16;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, q = lane & 3;
+  const int h = blockIdx.z, row0 = blockIdx.x * 16, col0 = blockIdx.y * 64;
+  const int hr = h % kHG;
+
+  const __nv_bfloat16* src = W_uv + (size_t)h * kDc * kDv + col0;
+  for (int i = tid; i < 512 * 8; i += 128) {
+    const int r = i >> 3, ch = i & 7;
+    cp_async16(sB + sw128(r, ch), src + (size_t)r * kDv + ch * 8);
+  }
+  cp_async_commit();
+  // the weights do not depend on earlier kernels; the partials do
+  pdl_wait();
+  pdl_launch_dependents();
+
+  const float* lse;
+  const float* opart;
+  ws_parts(ws, num_q, groups, num_ctas, batch, &lse, &opart);
+  if (tid < 16) {
+    const int n = row0 + tid;
+    QtileParts qp{0, 1, 0};
+    if (n < num_q) qp = locate_qtile(ws, num_q, groups, num_ctas, batch, n, h / kHG);
+    sFirst[tid] = qp.first;
+    sStride[tid] = qp.stride;
+    sCount[tid] = qp.count > 0 ? qp.count : 0;
+  }
+  __syncthreads();
+  // per row: max base-2 lse and 1 / weight sum over its parts (one warp per row)
+#pragma unroll 1
+  for (int r = warp; r < 16; r += 4) {
+    const int cnt = sCount[r];
+    const int64_t f = sFirst[r];
+    const int st = sStride[r];
+    float M = -INFINITY;
+    for (int s = lane; s < cnt; s += 32) M = fmaxf(M, lse[(f + (int64_t)s * st) * kHG + hr]);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float den = 0.f;
+    if (M != -INFINITY)
+      for (int s = lane; s < cnt; s += 32) den += fast_exp2(lse[(f + (int64_t)s * st) * kHG + hr] - M);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    if (lane == 0) {
+      sM[r] = M;
+      sInv[r] = (M != -INFINITY && den > 0.f) ? 1.f / den : 0.f;
+    }
+  }
+  __syncthreads();
+  // merged rows: 8 threads per row, float4 j + 8 m of the row (m < 16)
+  {
+    const int r = tid >> 3, j = tid & 7;
+    const int cnt = sCount[r];
+    const int64_t f = sFirst[r];
+    const int st = sStride[r];
+    const float M = sM[r], inv = sInv[r];
+    float4 acc[16];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
+#pragma unroll 1
+      for (int s = 0; s < cnt; ++s) {
+        const int64_t slot = f + (int64_t)s * st;
+        const float4* srcp = reinterpret_cast<const float4*>(opart + (slot * kHG + hr) * kDc) + j;
+        float4 v[16];
+#pragma unroll
+        for (int m = 0; m < 16; ++m) v[m] = srcp[8 * m];
+        const float w = fast_exp2(lse[slot * kHG + hr] - M) * inv;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+          acc[m].x = fmaf(w, v[m].x, acc[m].x);
+          acc[m].y = fmaf(w, v[m].y, acc[m].y);
+          acc[m].z = fmaf(w, v[m].z, acc[m].z);
+          acc[m].w = fmaf(w, v[m].w, acc[m].w);
+        }
+      }
+    }
+    uint8_t* dstrow = sA + r * kMergedStride;
+#pragma unroll
+    for (int m = 0; m < 16; ++m)
+      *reinterpret_cast<uint2*>(dstrow + (j + 8 * m) * 8) =
+          make_uint2(pack_bf16(acc[m].x, acc[m].y), pack_bf16(acc[m].z, acc[m].w));
+  }
+  cp_async_wait_all();
+  __syncthreads();
+
+  // out[16 rows x 64 cols] over this warp's quarter of K, summed through sRed
+  const int k0 = warp * 128;
+  float acc[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    const int k = k0 + ks * 16 + 2 * q;
+    uint32_t a[4];
+    a[0] = *reinterpret_cast<const uint32_t*>(sA + g * kMergedStride + k * 2);
+    a[1] = *reinterpret_cast<const uint32_t*>(sA + (g + 8) * kMergedStride + k * 2);
+    a[2] = *reinterpret_cast<const uint32_t*>(sA + g * kMergedStride + (k + 8) * 2);
+    a[3] = *reinterpret_cast<const uint32_t*>(sA + (g + 8) * kMergedStride + (k + 8) * 2);
+    const int kr = k0 + ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+    for (int np = 0; np < 4; ++np) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(smem_u32(sB + sw128(kr, np * 2 + (lane >> 4))), b0, b1, b2, b3);
+      mma_16816(acc[2 * np], a[0], a[1], a[2], a[3], b0, b1);
+      mma_16816(acc[2 * np + 1], a[0], a[1], a[2], a[3], b2, b3);
+    }
+  }
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt) {
+    float* d = sRed + (warp * 16 + g) * 64 + nt * 8 + 2 * q;
+    d[0] = acc[nt][0]; d[1] = acc[nt][1];
+    d[8 * 64] = acc[nt][2]; d[8 * 64 + 1] = acc[nt][3];
+  }
+  __syncthreads();
+  for (int i = tid; i < 16 * 32; i += 128) {
+    const int r = i >> 5, c = (i & 31) * 2;
+    const int row = row0 + r;
+    if (row >= num_q) continue;
+    float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      v0 += sRed[(w * 16 + r) * 64 + c];
+      v1 += sRed[(w * 16 + r) * 64 + c + 1];
+    }
+    *reinterpret_cast<uint32_t*>(out + ((size_t)row * H + h) * kDv + col0 + c) = pack_bf16(v0, v1);
+  }
+}
+
 // combine + out_proj, fp32: one CTA per (row n, head h); the merged latent
 // row goes to shared memory, then 128 threads take one output column each.
 __global__ void __launch_bounds__(128) combine_out_proj_f32_kernel(
@@ -545,18 +692,20 @@ cudaError_t launch_combine_out_proj(const mla_config& cfg, const void* workspace
     return launch_pdl(combine_out_proj_f32_kernel, dim3((unsigned)num_q, H), dim3(128), 0, stream,
                       ws, groups, num_ctas, (int)num_q, (int)batch, (const float*)W_uv, (float*)out, H);
   }
-  const bool big = num_q >= 256;
-  const int smem = 512 * 128 + (big ? 0 : 4 * 16 * 64 * 4) + (big ? 64 : 16) * (int)sizeof(MergeRow);
-  cudaError_t e = big ? cudaFuncSetAttribute(combine_out_proj_bf16_kernel<4>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
-                      : cudaFuncSetAttribute(combine_out_proj_bf16_kernel<1>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  if (big)
+  if (num_q >= 256) {
+    const int smem = 512 * 128 + 64 * (int)sizeof(MergeRow);
+    cudaError_t e = cudaFuncSetAttribute(combine_out_proj_bf16_kernel<4>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
     return launch_pdl(combine_out_proj_bf16_kernel<4>, dim3((unsigned)((num_q + 63) / 64), 2, H),
                       dim3(128), smem, stream, ws, groups, num_ctas, (int)num_q, (int)batch,
                       (const __nv_bfloat16*)W_uv, (__nv_bfloat16*)out, H);
-  return launch_pdl(combine_out_proj_bf16_kernel<1>, dim3((unsigned)((num_q + 15) / 16), 2, H),
+  }
+  const int smem = 512 * 128 + 4 * 16 * 64 * 4 + 16 * kMergedStride + 16 * (8 + 4 + 4 + 4 + 4);
+  cudaError_t e = cudaFuncSetAttribute(combine_out_proj_rows16_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(combine_out_proj_rows16_kernel, dim3((unsigned)((num_q + 15) / 16), 2, H),
                     dim3(128), smem, stream, ws, groups, num_ctas, (int)num_q, (int)batch,
                     (const __nv_bfloat16*)W_uv, (__nv_bfloat16*)out, H);
 }
