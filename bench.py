@@ -45,8 +45,16 @@ METRIC = "MLA paged decode: latent-cache GB/s (% of HBM peak), µs/step at B=64,
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-DECODE_SOURCES = ["decode_bf16.cu", "common.cuh", "sched.cuh", "merge.cuh", "async_copy.cuh"]
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_bf16_serving_B64_L4096.md")
+# Committed ncu summaries: (decode kernel, workload) -> (file, the sources
+# whose hash the summary records; its DRAM figure is void once they change)
+PROFILES = {
+    ("decode_bf16_kernel", "serving"): (
+        "decode_bf16_serving_B64_L4096.md",
+        ["decode_bf16.cu", "common.cuh", "sched.cuh", "merge.cuh", "async_copy.cuh"]),
+    ("decode_tc_kernel", "ragged_h128"): (
+        "decode_tc_ragged_B32_H128.md",
+        ["decode_tc.cu", "common.cuh", "cluster.cuh", "tcgen05.cuh", "merge.cuh", "async_copy.cuh"]),
+}
 
 
 def parse_args(argv=None):
@@ -191,19 +199,24 @@ class ClockSampler:
                 "samples": len(use), "samples_in_window": len(sel)}
 
 
-def decode_source_hash() -> str:
+def source_hash(names) -> str:
     h = hashlib.sha256()
-    for name in DECODE_SOURCES:
+    for name in names:
         with open(os.path.join(ROOT, "mla_latent_kv_03_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per decode launch from the committed ncu summary, or None if
-    the decode kernel's sources changed since it was taken."""
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary of this
+    kernel on this workload, or None if there is none or the kernel's sources
+    changed since it was taken."""
+    entry = PROFILES.get((kernel, workload))
+    if entry is None:
+        return None
+    fname, sources = entry
     try:
-        text = open(PROFILE_SUMMARY).read()
+        text = open(os.path.join(ROOT, "profiles", fname)).read()
     except OSError:
         return None
     vals = {}
@@ -211,7 +224,7 @@ def profiled_traffic():
         if ":" in line and line.strip().startswith("- "):
             k, v = line.strip()[2:].split(":", 1)
             vals[k.strip()] = v.strip().strip("`")
-    if vals.get("source_sha256") != decode_source_hash():
+    if vals.get("source_sha256") != source_hash(sources):
         return None
     try:
         return float(vals["dram_bytes_per_launch_full_size"].replace(",", ""))
@@ -233,8 +246,10 @@ def make_workload(name: str, rank: int):
         return W.serving(seed=3 + 1000 * rank, batch=48)
     if name == "ragged_h128":
         return W.ragged_h128(seed=4 + 1000 * rank)
-    if name == "ragged_h128_b8":   # 8 of the ragged many-head rows (> L2), for ncu
+    if name == "ragged_h128_b8":   # 8 of the ragged many-head rows (92 MB), for ncu
         return W.ragged_h128(seed=4 + 1000 * rank, batch=8)
+    if name == "ragged_h128_b16":  # 16 of the ragged many-head rows (> L2), for ncu
+        return W.ragged_h128(seed=4 + 1000 * rank, batch=16)
     if name == "mixed":
         return W.mixed(seed=5 + 1000 * rank)
     if name.startswith("v2lite_"):
@@ -425,9 +440,7 @@ def run_ours(args, world, rank, local):
     tpeak, _ = tensor_peak()
     kernel = ("decode_f32_kernel" if w.dtype != "bf16" else
               "decode_tc_kernel" if mode == 1 else "decode_bf16_kernel")
-    # the committed DRAM figure belongs to the warp-mma kernel on the serving batch
-    traffic = profiled_traffic() if (kernel == "decode_bf16_kernel" and
-                                     args.workload == "serving") else None
+    traffic = profiled_traffic(kernel, args.workload)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "kernel": kernel,
