@@ -61,6 +61,14 @@ __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 
+// Arrive (relaxed, cluster scope) on an mbarrier given by its cluster address:
+// no fence. For signalling that this thread's earlier shared-memory reads --
+// whose values it has already used -- are done.
+__device__ __forceinline__ void arrive_remote_relaxed(uint32_t bar_caddr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_caddr)
+               : "memory");
+}
+
 // Arrive (release, cluster scope) on an mbarrier given by its cluster address.
 __device__ __forceinline__ void arrive_remote(uint32_t bar_caddr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_caddr)

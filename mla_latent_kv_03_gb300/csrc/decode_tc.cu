@@ -12,8 +12,7 @@
 // the 64 rope columns for h = 1 -- and the same query columns:
 //   S_h = Q[:, cols_h] . K[:, cols_h]^T   (partial scores, K = 256 or 320)
 //   S   = S_0 + S_1                       (each CTA sends its partial to the
-//                                           peer's shared memory, two stages
-//                                           ahead of their use)
+//                                           peer's shared memory ahead of use)
 //   O_h += P . V[:, 256h : 256h + 256]    (each CTA half of the output)
 // so each CTA streams only its own columns of every cache row, and both CTAs
 // run the same softmax on the same sums (S_0 + S_1 == S_1 + S_0 in fp32),
@@ -25,22 +24,25 @@
 // ring of five 32-token cache stages of this CTA's columns (SWIZZLE_128B slabs
 // of 64 columns), four buffers of the peer's partial scores, three of this
 // CTA's own (the source of the bulk copies to the peer), and merge weights.
-// Per CTA (256 threads):
+// Per CTA (384 threads):
 //   warp 0 (TMA producer): cache stages under full / empty mbarriers; every
 //     block id is bounds-checked.
 //   warp 1 (P.V issuer; owns the TMEM allocation): O += P . V per stage
 //     (2 tcgen05.mma, M 128, N 256, K 16, A = P in TMEM, V MN-major).
 //   warp 2 (score issuer): the partial scores of a stage as soon as its score
 //     buffer is free (16 or 20 tcgen05.mma, M 128, N 32, K 16, A from TMEM).
-//   warps 4-7 (softmax): thread r owns row r. Per stage it sends its partial
-//     scores of two stages ahead to the peer, adds the peer's partial scores
-//     of this one to its own, masks (sequence end, causal position, rejected
-//     blocks), keeps the running maximum, rescales the warp's O rows in TMEM
-//     only when some row's maximum grows by more than 2^8 (probabilities stay
-//     below 256), and stores bf16 P to TMEM. At the end of a segment it
-//     normalises its O row: straight into o_lat when the q-block lies in this
-//     share and the merge is fused, else into the partial buffer, and the
-//     last CTA of a split q-block's half merges the parts while they are in L2.
+//   warps 8-11 (senders): each stage's partial scores from TMEM to a staging
+//     buffer and, by one bulk copy, into the peer's shared memory, up to three
+//     stages ahead of their use.
+//   warps 4-7 (softmax): thread r owns row r. Per stage it adds the peer's
+//     partial scores to its own, masks (sequence end, causal position,
+//     rejected blocks), keeps the running maximum, rescales the warp's O rows
+//     in TMEM only when some row's maximum grows by more than 2^8
+//     (probabilities stay below 256), and stores bf16 P to TMEM. At the end of
+//     a segment it normalises its O row: straight into o_lat when the q-block
+//     lies in this share and the merge is fused, else into the partial buffer,
+//     and the last CTA of a split q-block's half merges the parts while they
+//     are in L2.
 // The MMA warps issue from one elected lane. Every wait is bounded; on a
 // timeout the roles leave their loops, the MMA warps wait for their last
 // MMAs and the producer for its copies before TMEM is freed, and the pair
@@ -63,10 +65,11 @@ constexpr int kStage = kMaxSlabs * kSlab;      // 20 KB
 constexpr int kStages = 5;                     // cache stages in the ring
 constexpr int kXRecv = 4;                      // buffers of the peer's partial scores
 constexpr int kXSend = 3;                      // buffers of this CTA's partial scores
-constexpr int kThreads = 256;
-constexpr int kSoftWarp0 = 4;
-constexpr int kSoftBar = 2;                    // named barriers of the softmax warps
-constexpr int kXBar = 3;
+constexpr int kThreads = 384;
+constexpr int kSoftWarp0 = 4;                  // warps 4-7: softmax
+constexpr int kSendWarp0 = 8;                  // warps 8-11: partial-score senders
+constexpr int kSoftBar = 2;                    // named barrier of the softmax warps
+constexpr int kXBar = 3;                       // named barrier of the sender warps
 constexpr uint32_t kOCol = 0, kSCol = 256, kPCol = 320, kQCol = 352, kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.f;            // lazy rescale threshold (2^8)
 constexpr int kXBytes = kQBlockRows * kTok * 4;  // one stage of partial scores
@@ -81,7 +84,10 @@ enum {
   kXFull0 = kSFull0 + 4,         // [kXRecv] the peer's partial scores (bytes from the peer)
   kPFull0 = kXFull0 + kXRecv,    // [2] probabilities of stage i in P[i % 2] (128 arrivals)
   kPVDone0 = kPFull0 + 2,        // [2] O += P[i % 2] . V_i done
-  kQtReady = kPVDone0 + 2,       // query columns stored in TMEM (128 arrivals)
+  kXSReady0 = kPVDone0 + 2,      // [kXSend] own partial scores of stage i staged (1 arrival)
+  kXSFree0 = kXSReady0 + kXSend, // [kXSend] ... and read by the softmax (1 arrival)
+  kPeerFree0 = kXSFree0 + kXSend,// [kXRecv] the peer's softmax read its buffer (1 remote arrival)
+  kQtReady = kPeerFree0 + kXRecv,// query columns stored in TMEM (128 arrivals)
   kQEmpty,                       // every score MMA of the segment done
   kODone,                        // every P.V MMA of the segment done
   kOFree,                        // O read out by the epilogue (128 arrivals)
@@ -165,20 +171,6 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   }
 }
 
-// The same for a barrier that a peer CTA arrives on (cluster-scope acquire).
-__device__ __forceinline__ bool wait_or_abort_cluster(uint64_t* bar, uint32_t parity,
-                                                      volatile int* abort_flag) {
-  if (cl::try_wait_cluster(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (cl::try_wait_cluster(bar, parity)) return true;
-    if ((i & 15u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
-    }
-  }
-}
-
 // Four barriers polled together (their latencies overlap); parity 2 means
 // "no wait". The first is waited with cluster-scope acquire.
 __device__ __forceinline__ bool wait4_or_abort(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1,
@@ -223,6 +215,19 @@ __device__ __forceinline__ bool soft_red_or(bool v) {
       "selp.u32 %0, 1, 0, po;\n\t}"
       : "=r"(r)
       : "r"((uint32_t)v), "r"(kSoftBar)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ bool send_red_or(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "barrier.red.or.pred po, %2, 128, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(kXBar)
       : "memory");
   return r != 0;
 }
@@ -322,7 +327,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   TcWalker sw;
   const bool has_work = sw.init(ws, a.num_q, a.groups, a.num_ctas, batch, share_idx);
-  if (a.o_lat && warp >= kSoftWarp0 && h == 0)
+  if (a.o_lat && warp >= kSoftWarp0 && warp < kSendWarp0 && h == 0)
     zero_unvisited_rows(sw.row_info, sw.plan_ok, a.num_q, a.num_heads, a.o_lat, tid - 128, 128);
   TcSeg seg;
   auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
@@ -483,6 +488,66 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncwarp();
     if (!mbar_wait(&bars[kFinalS], 0) && leader) set_status(status, MLA_DEV_TIMEOUT);
     __syncwarp();
+  } else if (has_work && warp >= kSendWarp0) {
+    // ------------------------------------------------------------ senders
+    // Partial scores of every stage, in order: TMEM -> own staging buffer
+    // j % kXSend -> one bulk copy into the peer's buffer j % kXRecv, counted
+    // on the peer's barrier. Runs up to kXSend stages ahead of the softmax.
+    const int r = tid - kSendWarp0 * 32;
+    const uint32_t trow = tmem + ((uint32_t)((warp - kSendWarp0) * 32) << 16);
+    const uint32_t peer = (uint32_t)(h ^ 1);
+    const uint32_t x_peer0 = cl::map(smem_u32(sm + Smem::x), peer);
+    const uint32_t xbar_peer0 = cl::map(smem_u32(&bars[kXFull0]), peer);
+    int stage_i = 0;
+    bool aborted = false;
+    while (!aborted && sw.next(seg)) {
+      const int n = seg_stages(seg);
+#pragma unroll 1
+      for (int tt = 0; tt < n; ++tt) {
+        const int j = stage_i + tt, b = j & 1, xs = j % kXSend;
+        // the scores, and the staging buffer read by the softmax (stage j - kXSend)
+        bool ok = wait_or_abort(&bars[kSFull0 + b], (j >> 1) & 1, abort_flag);
+        if (j >= kXSend) ok = ok && wait_or_abort(&bars[kXSFree0 + xs], ((j - kXSend) / kXSend) & 1, abort_flag);
+        if (send_red_or(!ok)) { aborted = true; break; }
+        tc::fence_after_sync();
+        uint32_t sv[32];
+        tc::ld32(trow + kSCol + (uint32_t)b * kTok, sv);
+        tc::wait_ld();
+        tc::fence_before_sync();
+        mbar_arrive(&bars[kSFree0 + b]);
+        // the copy of stage j - kXSend read this buffer; at most kXSend - 1 newer remain
+        if (r == 0) cl::bulk_wait_read<kXSend - 1>();
+        named_bar_sync(kXBar, 128);
+        uint8_t* dst = sm + Smem::xs + xs * kXBytes + r * 128;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          *reinterpret_cast<uint4*>(dst + ((k ^ (r & 7)) << 4)) =
+              make_uint4(sv[4 * k], sv[4 * k + 1], sv[4 * k + 2], sv[4 * k + 3]);
+        fence_proxy_async_smem();
+        named_bar_sync(kXBar, 128);
+        if (r == 0) {
+          // the peer's softmax has read its buffer for stage j - kXRecv
+          const int xr = j % kXRecv;
+          if (j < kXRecv ||
+              wait_or_abort(&bars[kPeerFree0 + xr], ((j - kXRecv) / kXRecv) & 1, abort_flag)) {
+            cl::bulk_to_peer(x_peer0 + (uint32_t)xr * kXBytes,
+                             smem_u32(sm + Smem::xs) + (uint32_t)xs * kXBytes, kXBytes,
+                             xbar_peer0 + (uint32_t)xr * 8);
+            cl::bulk_commit();
+          } else {
+            set_status(status, MLA_DEV_TIMEOUT);
+            *abort_flag = 1;
+          }
+          mbar_arrive(&bars[kXSReady0 + xs]);
+        }
+      }
+      stage_i += n;
+    }
+    if (aborted && r == 0) {
+      set_status(status, MLA_DEV_TIMEOUT);
+      *abort_flag = 1;
+    }
+    if (r == 0) cl::bulk_wait_read<0>();   // no copy still reads the staging buffers
   } else if (has_work && warp >= kSoftWarp0) {
     // ----------------------------------------------------------- softmax
     const int r = tid - kSoftWarp0 * 32;                 // row of the q-block
@@ -495,34 +560,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int64_t qrows = a.num_q * a.num_heads;
     const float scale = a.scale_log2;
     const uint32_t peer = (uint32_t)(h ^ 1);
-    const uint32_t x_peer0 = cl::map(smem_u32(sm + Smem::x), peer);
-    const uint32_t xbar_peer0 = cl::map(smem_u32(&bars[kXFull0]), peer);
+    const uint32_t pfree_peer0 = cl::map(smem_u32(&bars[kPeerFree0]), peer);
     float* wsm = reinterpret_cast<float*>(sm + Smem::w);
     int stage_i = 0, seg_i = 0;
     bool aborted = false, fail = false;
-    // partial scores of stage j: TMEM -> own buffer j % kXSend -> one bulk copy
-    // into the peer's buffer j % kXRecv, counted on the peer's barrier
-    auto send_scores = [&](int j) {
-      uint32_t sv[32];
-      tc::ld32(trow + kSCol + (uint32_t)(j & 1) * kTok, sv);
-      tc::wait_ld();
-      tc::fence_before_sync();
-      mbar_arrive(&bars[kSFree0 + (j & 1)]);
-      // the copy of stage j - kXSend read this buffer; at most kXSend - 1 newer remain
-      if (r == 0) cl::bulk_wait_read<kXSend - 1>();
-      named_bar_sync(kXBar, 128);
-      uint8_t* xs = sm + Smem::xs + (j % kXSend) * kXBytes + r * 128;
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-        *reinterpret_cast<uint4*>(xs + ((k ^ (r & 7)) << 4)) =
-            make_uint4(sv[4 * k], sv[4 * k + 1], sv[4 * k + 2], sv[4 * k + 3]);
-      fence_proxy_async_smem();
-      named_bar_sync(kXBar, 128);
-      if (r == 0) {
-        cl::bulk_to_peer(x_peer0 + (uint32_t)(j % kXRecv) * kXBytes,
-                         smem_u32(sm + Smem::xs) + (uint32_t)(j % kXSend) * kXBytes, kXBytes,
-                         xbar_peer0 + (uint32_t)(j % kXRecv) * 8);
-        cl::bulk_commit();
+    // After an agreement over all 128 threads at stage i, every thread has
+    // finished with stage i - 1: its own staging buffer is free for the
+    // senders and its receive buffer for the peer (re-armed for stage i - 1 + kXRecv).
+    auto release_prev = [&](int i) {
+      if (r == 0 && i >= 1) {
+        const int p = i - 1;
+        mbar_arrive(&bars[kXSFree0 + p % kXSend]);
+        mbar_arrive_expect_tx(&bars[kXFull0 + p % kXRecv], kXBytes);
+        // relaxed: the loads of stage i - 1's buffer returned long ago (their
+        // sums fed that stage's softmax), and a release here would stall
+        cl::arrive_remote_relaxed(pfree_peer0 + (uint32_t)(p % kXRecv) * 8);
       }
     };
     bool have = sw.next(seg);
@@ -538,28 +590,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const bool valid_row = t < seg.t_end;
       const int pos = valid_row ? sw.row_info[t / sw.G].y : -1;
       float m_used = -INFINITY, l = 0.f;
-      // the first two stages' partial scores go out before any is used
-#pragma unroll 1
-      for (int tt = 0; tt < n && tt < 2; ++tt) {
-        const int j = stage_i + tt;
-        const bool oks = wait_or_abort(&bars[kSFull0 + (j & 1)], (j >> 1) & 1, abort_flag);
-        if (soft_red_or(!oks || fail)) { aborted = true; break; }
-        tc::fence_after_sync();
-        send_scores(j);
-      }
-      if (aborted) break;
 #pragma unroll 1
       for (int tt = 0; tt < n; ++tt) {
-        const int i = stage_i + tt, slot = i % kStages, b = i & 1, xb = i % kXRecv;
-        const bool ahead = tt + 2 < n;
-        // the peer's partial scores of stage i, the stage (for its info), the
-        // scores of stage i + 2, and P[i % 2] free (O += P . V of stage i - 2)
+        const int i = stage_i + tt, slot = i % kStages, b = i & 1, xb = i % kXRecv,
+                  xs = i % kXSend;
+        // the peer's partial scores of stage i, the stage (for its info), this
+        // CTA's partial scores staged, and P[i % 2] free (P.V of stage i - 2)
         const bool okw = wait4_or_abort(&bars[kXFull0 + xb], (i / kXRecv) & 1,
                                         &bars[kFull0 + slot], (i / kStages) & 1,
-                                        &bars[kSFull0 + b], ahead ? ((i + 2) >> 1) & 1 : 2u,
+                                        &bars[kXSReady0 + xs], (i / kXSend) & 1,
                                         &bars[kPVDone0 + b], i >= 2 ? ((i - 2) >> 1) & 1 : 2u,
                                         abort_flag);
         if (soft_red_or(!okw || fail)) { aborted = true; break; }
+        release_prev(i);
         tc::fence_after_sync();
         const int tstart = seg.k0 * kTile + tt * kTok;
         const int2 inf = info[slot];
@@ -569,7 +612,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // S = own partial + the peer's partial (both swizzled the same way)
         float x[32];
         {
-          const uint8_t* xo = sm + Smem::xs + (i % kXSend) * kXBytes + r * 128;
+          const uint8_t* xo = sm + Smem::xs + xs * kXBytes + r * 128;
           const uint8_t* xp = sm + Smem::x + xb * kXBytes + r * 128;
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
@@ -586,10 +629,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (!live) x[j] = -INFINITY;
           }
         }
-        // the peer writes this buffer again for stage i + kXRecv only after this
-        // CTA has sent stage i + 2 (below), i.e. after every load above
-        if (r == 0) mbar_arrive_expect_tx(&bars[kXFull0 + xb], kXBytes);
-        if (ahead) send_scores(i + 2);
         float mx[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) mx[j] = fmaxf(x[j], x[j + 16]);
@@ -787,7 +826,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       set_status(status, MLA_DEV_TIMEOUT);
       *abort_flag = 1;
     }
-    if (r == 0) cl::bulk_wait_read<0>();   // no copy still reads this CTA's staging buffers
   }
 
   tc::fence_before_sync();
