@@ -1,6 +1,6 @@
 // Thread-block-cluster helpers (inline PTX): the CTA's rank in its cluster,
-// addresses in a peer CTA's shared memory, stores and mbarrier arrivals
-// there, cluster-scope acquire waits and the cluster-wide barrier.
+// addresses in a peer CTA's shared memory, bulk copies and mbarrier arrivals
+// into it, and the cluster-wide barrier.
 #pragma once
 
 #include <stdint.h>
@@ -24,28 +24,10 @@ __device__ __forceinline__ uint32_t map(uint32_t saddr, uint32_t peer) {
   return r;
 }
 
-__device__ __forceinline__ void st_v4(uint32_t caddr, uint32_t a, uint32_t b, uint32_t c,
-                                      uint32_t d) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(caddr), "r"(a), "r"(b),
-               "r"(c), "r"(d)
-               : "memory");
-}
-
-// Asynchronous 16-byte store into a peer CTA's shared memory that counts its
-// bytes on the peer's mbarrier (complete_tx): the peer sees the data once the
-// barrier phase, armed there with expect_tx, completes.
-__device__ __forceinline__ void st_async_v4(uint32_t caddr, uint32_t a, uint32_t b, uint32_t c,
-                                            uint32_t d, uint32_t bar_caddr) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
-          caddr),
-      "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar_caddr)
-      : "memory");
-}
-
 // Bulk copy (TMA engine) of `bytes` from this CTA's shared memory to a peer
-// CTA's, counted on the peer's mbarrier (complete_tx). One thread issues it;
-// `commit` groups it for wait_read.
+// CTA's, counted on the peer's mbarrier (complete_tx): the peer sees the data
+// once that barrier's phase, armed there with expect_tx, completes. One
+// thread issues it; `bulk_commit` groups it for `bulk_wait_read`.
 __device__ __forceinline__ void bulk_to_peer(uint32_t dst_caddr, uint32_t src_saddr,
                                              uint32_t bytes, uint32_t bar_caddr) {
   asm volatile(
@@ -67,26 +49,6 @@ __device__ __forceinline__ void bulk_wait_read() {
 __device__ __forceinline__ void arrive_remote_relaxed(uint32_t bar_caddr) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_caddr)
                : "memory");
-}
-
-// Arrive (release, cluster scope) on an mbarrier given by its cluster address.
-__device__ __forceinline__ void arrive_remote(uint32_t bar_caddr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_caddr)
-               : "memory");
-}
-
-// try_wait with cluster-scope acquire: data a peer CTA stored before its
-// release arrival is visible once this returns true.
-__device__ __forceinline__ bool try_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
 }
 
 // Every thread of every CTA of the cluster (release / acquire).

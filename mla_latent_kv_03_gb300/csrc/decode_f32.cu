@@ -25,6 +25,7 @@ __global__ void __launch_bounds__(256) decode_f32_kernel(DecodeArgs a) {
   float* sM = sL + kHG;                       // [16] final m
   float* sMerge = sM + kHG;                   // fused-merge scratch
   int* sFlag = reinterpret_cast<int*>(sMerge + 2 * kHG + kMergeChunk * kHG);
+  int64_t* sOff = reinterpret_cast<int64_t*>(sFlag + 2);   // [kSub] cache offsets (8-aligned)
   const int tid = threadIdx.x;
   const int h = tid >> 4, j = tid & 15;       // score role: head h, token j
   const int d0 = tid * 2;                     // PV role: dims d0, d0+1 for all heads
@@ -57,30 +58,52 @@ __global__ void __launch_bounds__(256) decode_f32_kernel(DecodeArgs a) {
         const int tok0 = k * kTile + sub * kSub;
         if (tok0 >= visible) break;
         __syncthreads();
-        // stage 16 rows; rows that are not visible or not mapped become 0
-        for (int i = tid; i < kSub * kRow; i += 256) {
-          const int r = i / kRow, c = i % kRow;
-          const int tok = tok0 + r;
-          float v = 0.f;
+        // stage 16 rows; rows that are not visible or not mapped become 0.
+        // The rows' cache offsets are looked up once, then every float4 of
+        // the 16 rows is loaded in one round trip.
+        if (tid < kSub) {
+          const int tok = tok0 + tid;
+          int64_t off = -1;
           if (tok < visible) {
             const int blk = a.block_table[(size_t)seg.b * a.max_blocks_per_seq + tok / a.block_size];
             if (blk >= 0 && blk < a.num_blocks)
-              v = cache[((size_t)blk * a.block_size + tok % a.block_size) * kRow + c];
+              off = ((int64_t)blk * a.block_size + tok % a.block_size) * kRow;
           }
-          sK[r * (kRow + 1) + c] = v;
+          sOff[tid] = off;
+        }
+        __syncthreads();
+        {
+          constexpr int kVec = kSub * (kRow / 4) / 256;   // float4 per thread (9)
+          float4 v[kVec];
+#pragma unroll
+          for (int u = 0; u < kVec; ++u) {
+            const int i = tid + 256 * u, r = i / (kRow / 4), c4 = i % (kRow / 4);
+            const int64_t off = sOff[r];
+            v[u] = off >= 0 ? *reinterpret_cast<const float4*>(cache + off + 4 * c4)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int u = 0; u < kVec; ++u) {
+            const int i = tid + 256 * u, r = i / (kRow / 4), c4 = i % (kRow / 4);
+            float* d = sK + r * (kRow + 1) + 4 * c4;
+            d[0] = v[u].x; d[1] = v[u].y; d[2] = v[u].z; d[3] = v[u].w;
+          }
         }
         __syncthreads();
         const int tok = tok0 + j;
         bool live = tok < visible;
-        if (live) {
-          const int blk = a.block_table[(size_t)seg.b * a.max_blocks_per_seq + tok / a.block_size];
-          if (blk < 0 || blk >= a.num_blocks) {
-            live = false;
-            if (h == 0) set_status(&hdr->status, MLA_DEV_BAD_BLOCK);
-          }
+        if (live && sOff[j] < 0) {
+          live = false;
+          if (h == 0) set_status(&hdr->status, MLA_DEV_BAD_BLOCK);
         }
-        float s = 0.f;
-        for (int c = 0; c < kRow; ++c) s = fmaf(sQ[h * kRow + c], sK[j * (kRow + 1) + c], s);
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+        for (int c = 0; c < kRow; c += 4) {
+          s0 = fmaf(sQ[h * kRow + c], sK[j * (kRow + 1) + c], s0);
+          s1 = fmaf(sQ[h * kRow + c + 1], sK[j * (kRow + 1) + c + 1], s1);
+          s2 = fmaf(sQ[h * kRow + c + 2], sK[j * (kRow + 1) + c + 2], s2);
+          s3 = fmaf(sQ[h * kRow + c + 3], sK[j * (kRow + 1) + c + 3], s3);
+        }
+        float s = (s0 + s1) + (s2 + s3);
         s = live ? s * a.scale_log2 : -INFINITY;
         float mx = s;
 #pragma unroll
@@ -152,7 +175,8 @@ __global__ void __launch_bounds__(256) decode_f32_kernel(DecodeArgs a) {
 
 cudaError_t launch_decode_f32(const DecodeArgs& a, cudaStream_t stream) {
   const size_t smem =
-      (size_t)(kHG * kRow + kSub * (kRow + 1) + kHG * kSub + 3 * kHG + 2 * kHG + kMergeChunk * kHG + 4) * 4;
+      (size_t)(kHG * kRow + kSub * (kRow + 1) + kHG * kSub + 3 * kHG + 2 * kHG + kMergeChunk * kHG + 2) * 4 +
+      kSub * 8;
   cudaError_t e = cudaFuncSetAttribute(decode_f32_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

@@ -266,13 +266,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_tc_kernel(PlanArgs a) {
 }
 
 // CTA = (q-tile t = (query row n, head group g), quarter of the 512 latent
-// dims): 16 head rows x 128 dims. Threads 0-15 reduce their row's
-// log-sum-exps over the partial slots to a maximum and a reciprocal weight
-// sum; the per-(slot, row) weights are then staged in shared memory, 64 slots
-// at a time, and each thread merges 4 float4 items (row, 4 dims) with
-// independent loads over the slots.
+// dims): 16 head rows x 128 dims. The slots' log-sum-exps go to shared memory
+// 64 slots at a time, all (slot, row) values of a chunk loaded at once; threads
+// 0-15 fold each chunk into their row's running maximum and weight sum. The
+// per-(slot, row) weights are then staged the same way, and each thread merges
+// 4 float4 items (row, 4 dims), with the loads of 4 slots in flight together.
 constexpr int kCombineThreads = 128;
 constexpr int kSlotChunk = 64;
+constexpr int kSlotsInFlight = 4;
 
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
     const uint8_t* __restrict__ ws, int groups, int num_ctas, int64_t num_q, int batch,
@@ -302,15 +303,30 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
   }
   const int nslots = qp.count;
   auto grp = [&](int s) { return qp.first + (int64_t)s * qp.stride; };
-  if (tid < kHG) {
-    float M = -INFINITY;
-    for (int s = 0; s < nslots; ++s) M = fmaxf(M, lse[grp(s) * kHG + tid]);
-    float den = 0.f;
-    if (M != -INFINITY)
-      for (int s = 0; s < nslots; ++s) den += fast_exp2(lse[grp(s) * kHG + tid] - M);
-    sM[tid] = M;
-    sInv[tid] = den > 0.f ? 1.f / den : 0.f;
+  // pass 1: per-row maximum and weight sum, online over chunks of slots
+  if (tid < kHG) { sM[tid] = -INFINITY; sInv[tid] = 0.f; }
+  for (int s0 = 0; s0 < nslots; s0 += kSlotChunk) {
+    const int ns = min(kSlotChunk, nslots - s0);
+    __syncthreads();
+    for (int i = tid; i < ns * kHG; i += kCombineThreads)
+      sW[i / kHG][i % kHG] = lse[grp(s0 + i / kHG) * kHG + i % kHG];
+    __syncthreads();
+    if (tid < kHG) {
+      const float Mold = sM[tid];
+      float M = Mold;
+      for (int sl = 0; sl < ns; ++sl) M = fmaxf(M, sW[sl][tid]);
+      float den = 0.f;
+      if (M != -INFINITY) {
+        den = Mold == -INFINITY ? 0.f : sInv[tid] * fast_exp2(Mold - M);
+        for (int sl = 0; sl < ns; ++sl) den += fast_exp2(sW[sl][tid] - M);
+      }
+      sM[tid] = M;
+      sInv[tid] = den;   // a running sum; inverted below
+    }
   }
+  __syncthreads();
+  if (tid < kHG) sInv[tid] = sInv[tid] > 0.f ? 1.f / sInv[tid] : 0.f;
+  // pass 2: weighted sum of the partial rows
   float4 acc[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -323,17 +339,28 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
       sW[sl][r] = M == -INFINITY ? 0.f : fast_exp2(lse[grp(s0 + sl) * kHG + r] - M) * sInv[r];
     }
     __syncthreads();
-    for (int sl = 0; sl < ns; ++sl) {
-      const float4* src = opart + grp(s0 + sl) * kHG * (kDc / 4);
+    for (int sl0 = 0; sl0 < ns; sl0 += kSlotsInFlight) {
+      float4 v[kSlotsInFlight][4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int r = (tid >> 5) + 4 * j;
-        const float w = sW[sl][r];
-        const float4 v = src[r * (kDc / 4) + c4];
-        acc[j].x = fmaf(w, v.x, acc[j].x);
-        acc[j].y = fmaf(w, v.y, acc[j].y);
-        acc[j].z = fmaf(w, v.z, acc[j].z);
-        acc[j].w = fmaf(w, v.w, acc[j].w);
+      for (int u = 0; u < kSlotsInFlight; ++u) {
+        if (sl0 + u < ns) {
+          const float4* src = opart + grp(s0 + sl0 + u) * kHG * (kDc / 4);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) v[u][j] = src[((tid >> 5) + 4 * j) * (kDc / 4) + c4];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kSlotsInFlight; ++u) {
+        if (sl0 + u < ns) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float w = sW[sl0 + u][(tid >> 5) + 4 * j];
+            acc[j].x = fmaf(w, v[u][j].x, acc[j].x);
+            acc[j].y = fmaf(w, v[u][j].y, acc[j].y);
+            acc[j].z = fmaf(w, v[u][j].z, acc[j].z);
+            acc[j].w = fmaf(w, v[u][j].w, acc[j].w);
+          }
+        }
       }
     }
   }

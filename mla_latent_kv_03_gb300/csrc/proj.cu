@@ -589,41 +589,92 @@ __global__ void __launch_bounds__(128) combine_out_proj_f32_kernel(
 }
 
 // fp32 SIMT: one CTA per (row n, head h).
-__global__ void __launch_bounds__(128) absorb_f32_kernel(
+// absorb_q, fp32 (the fp32 configuration: a handful of rows). CTA = (head h,
+// 64 latent rows c); each of its 8 warps holds 8 rows of W_uk[h] in registers
+// (lane l: columns 4l..4l+3, coalesced float4 loads, all in flight at once)
+// and, for every query row n, reduces the 8 dot products over its lanes. A
+// ninth CTA column does the RoPE part.
+constexpr int kAbsorbF32Rows = 64;
+
+__global__ void __launch_bounds__(256) absorb_f32_kernel(
     const float* __restrict__ q_nope, const float* __restrict__ q_pe,
     const int32_t* __restrict__ q_pos, const float* __restrict__ W_uk, float* __restrict__ q_abs,
-    int H, RopeFreq freq) {
-  __shared__ float sq[kDn];
-  const int n = blockIdx.x, h = blockIdx.y, t = threadIdx.x;
-  sq[t] = q_nope[((size_t)n * H + h) * kDn + t];
-  __syncthreads();
-  float* out = q_abs + ((size_t)n * H + h) * kRow;
-  for (int c = t; c < kDc; c += 128) {
-    const float* w = W_uk + ((size_t)h * kDc + c) * kDn;
-    float s = 0.f;
-    for (int d = 0; d < kDn; ++d) s = fmaf(w[d], sq[d], s);
-    out[c] = s;
+    int num_q, int H, RopeFreq freq) {
+  const int h = blockIdx.x, chunk = blockIdx.y, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  if (chunk == kDc / kAbsorbF32Rows) {
+    // rotate-half RoPE of q_pe into q_abs[..., 512:576]
+    for (int i = tid; i < num_q * 32; i += 256) {
+      const int n = i >> 5, p = i & 31;
+      const float* x = q_pe + ((size_t)n * H + h) * kDr;
+      float cs, sn;
+      rope_cos_sin(q_pos[n], freq.hi[p], freq.lo[p], &cs, &sn);
+      float* out = q_abs + ((size_t)n * H + h) * kRow + kDc;
+      out[p] = x[p] * cs - x[p + 32] * sn;
+      out[p + 32] = x[p + 32] * cs + x[p] * sn;
+    }
+    return;
   }
-  if (t < 32) {
-    const float* x = q_pe + ((size_t)n * H + h) * kDr;
-    float cs, sn;
-    rope_cos_sin(q_pos[n], freq.hi[t], freq.lo[t], &cs, &sn);
-    out[kDc + t] = x[t] * cs - x[t + 32] * sn;
-    out[kDc + t + 32] = x[t + 32] * cs + x[t] * sn;
+  const int c0 = chunk * kAbsorbF32Rows + warp * 8;
+  float4 w[8];
+#pragma unroll
+  for (int r = 0; r < 8; ++r)
+    w[r] = *reinterpret_cast<const float4*>(W_uk + ((size_t)h * kDc + c0 + r) * kDn + 4 * lane);
+  for (int n = 0; n < num_q; ++n) {
+    const float4 q = *reinterpret_cast<const float4*>(q_nope + ((size_t)n * H + h) * kDn + 4 * lane);
+    float d[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) d[r] = fmaf(w[r].x, q.x, fmaf(w[r].y, q.y, fmaf(w[r].z, q.z, w[r].w * q.w)));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1)
+#pragma unroll
+      for (int r = 0; r < 8; ++r) d[r] += __shfl_xor_sync(0xffffffffu, d[r], o);
+    if (lane < 8) {
+      float v = d[0];
+#pragma unroll
+      for (int r = 1; r < 8; ++r) v = lane == r ? d[r] : v;
+      q_abs[((size_t)n * H + h) * kRow + c0 + lane] = v;
+    }
   }
 }
 
-__global__ void __launch_bounds__(128) out_proj_f32_kernel(const float* __restrict__ o_lat,
+// out_proj, fp32. CTA = (head h, 32 output columns); warp w holds rows
+// [64 w, 64 w + 64) of W_uv[h] for its lane's column in registers (coalesced,
+// all loads in flight at once), and for every query row n the 8 warps' partial
+// sums meet in shared memory.
+__global__ void __launch_bounds__(256) out_proj_f32_kernel(const float* __restrict__ o_lat,
                                                            const float* __restrict__ W_uv,
-                                                           float* __restrict__ out, int H) {
+                                                           float* __restrict__ out, int num_q,
+                                                           int H) {
   __shared__ float so[kDc];
-  const int n = blockIdx.x, h = blockIdx.y, t = threadIdx.x;
-  for (int c = t; c < kDc; c += 128) so[c] = o_lat[((size_t)n * H + h) * kDc + c];
-  __syncthreads();
-  const float* w = W_uv + (size_t)h * kDc * kDv + t;
-  float s = 0.f;
-  for (int c = 0; c < kDc; ++c) s = fmaf(so[c], w[(size_t)c * kDv], s);
-  out[((size_t)n * H + h) * kDv + t] = s;
+  __shared__ float sred[8][32];
+  const int h = blockIdx.x, v0 = blockIdx.y * 32, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  float w[64];
+  const float* wp = W_uv + ((size_t)h * kDc + warp * 64) * kDv + v0 + lane;
+#pragma unroll
+  for (int c = 0; c < 64; ++c) w[c] = wp[(size_t)c * kDv];
+  for (int n = 0; n < num_q; ++n) {
+    __syncthreads();
+    for (int c = tid; c < kDc; c += 256) so[c] = o_lat[((size_t)n * H + h) * kDc + c];
+    __syncthreads();
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+    for (int c = 0; c < 64; c += 4) {
+      a0 = fmaf(so[warp * 64 + c], w[c], a0);
+      a1 = fmaf(so[warp * 64 + c + 1], w[c + 1], a1);
+      a2 = fmaf(so[warp * 64 + c + 2], w[c + 2], a2);
+      a3 = fmaf(so[warp * 64 + c + 3], w[c + 3], a3);
+    }
+    sred[warp][lane] = (a0 + a1) + (a2 + a3);
+    __syncthreads();
+    if (warp == 0) {
+      float t = 0.f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) t += sred[k][lane];
+      out[((size_t)n * H + h) * kDv + v0 + lane] = t;
+    }
+  }
 }
 
 }  // namespace
@@ -635,9 +686,9 @@ cudaError_t launch_absorb_q(const mla_config& cfg, const void* q_nope, const voi
   const int H = cfg.num_heads;
   const RopeFreq freq = make_rope_freq((double)cfg.rope_base);
   if (cfg.dtype == MLA_F32) {
-    absorb_f32_kernel<<<dim3((unsigned)num_q, H), 128, 0, stream>>>(
+    absorb_f32_kernel<<<dim3(H, kDc / kAbsorbF32Rows + 1), 256, 0, stream>>>(
         (const float*)q_nope, (const float*)q_pe, q_positions, (const float*)W_uk, (float*)q_abs,
-        H, freq);
+        (int)num_q, H, freq);
     return cudaGetLastError();
   }
   if (num_q >= 256) {
@@ -659,8 +710,8 @@ cudaError_t launch_out_proj(const mla_config& cfg, const float* o_lat, const voi
   if (num_q == 0) return cudaSuccess;
   const int H = cfg.num_heads;
   if (cfg.dtype == MLA_F32) {
-    out_proj_f32_kernel<<<dim3((unsigned)num_q, H), 128, 0, stream>>>(o_lat, (const float*)W_uv,
-                                                                   (float*)out, H);
+    out_proj_f32_kernel<<<dim3(H, kDv / 32), 256, 0, stream>>>(o_lat, (const float*)W_uv,
+                                                              (float*)out, (int)num_q, H);
     return cudaGetLastError();
   }
   const bool big = num_q >= 256;

@@ -1,5 +1,5 @@
 // Thin inline-PTX wrappers for the 5th-generation tensor core (tcgen05):
-// TMEM allocation, MMA issue with shared-memory operand descriptors,
+// TMEM allocation, MMA issue (A from TMEM, B by shared-memory descriptor),
 // completion through mbarriers, and TMEM loads / stores.
 #pragma once
 
@@ -10,9 +10,8 @@ namespace tc {
 
 // Shared-memory matrix descriptor: start address, leading / stride byte
 // offsets (16-byte units), descriptor version 1, swizzle layout
-// (2 = 128-byte swizzle, 4 = 64-byte swizzle).
+// (2 = 128-byte swizzle).
 constexpr uint32_t kSwizzle128 = 2;
-constexpr uint32_t kSwizzle64 = 4;
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
                                               uint32_t layout) {
@@ -32,18 +31,9 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
          ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem] * B[smem]; issued by one thread.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                         bool accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)accumulate)
-      : "memory");
-}
-
-// The same with A (M x K, K-major) read from TMEM: lane i holds row i, each
-// 32-bit column two consecutive k (the lower k in the low half).
+// D[tmem] (+)= A[tmem] * B[smem], issued by one thread. A (M x K, K-major)
+// is read from TMEM: lane i holds row i, each 32-bit column two consecutive k
+// (the lower k in the low half).
 __device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
                                                 uint32_t idesc, bool accumulate) {
   asm volatile(
