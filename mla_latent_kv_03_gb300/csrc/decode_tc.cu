@@ -80,13 +80,11 @@ enum {
   kFull0 = 0,
   kEmpty0 = kFull0 + kStages,
   kSFull0 = kEmpty0 + kStages,   // [2] partial scores of stage i in S[i % 2]
-  kSFree0 = kSFull0 + 2,         // [2] S[i % 2] read out (128 arrivals)
+  kSFree0 = kSFull0 + 2,         // [2] S[i % 2] read out by senders and softmax (256 arrivals)
   kXFull0 = kSFull0 + 4,         // [kXRecv] the peer's partial scores (bytes from the peer)
   kPFull0 = kXFull0 + kXRecv,    // [2] probabilities of stage i in P[i % 2] (128 arrivals)
   kPVDone0 = kPFull0 + 2,        // [2] O += P[i % 2] . V_i done
-  kXSReady0 = kPVDone0 + 2,      // [kXSend] own partial scores of stage i staged (1 arrival)
-  kXSFree0 = kXSReady0 + kXSend, // [kXSend] ... and read by the softmax (1 arrival)
-  kPeerFree0 = kXSFree0 + kXSend,// [kXRecv] the peer's softmax read its buffer (1 remote arrival)
+  kPeerFree0 = kPVDone0 + 2,     // [kXRecv] the peer's softmax read its buffer (1 remote arrival)
   kQtReady = kPeerFree0 + kXRecv,// query columns stored in TMEM (128 arrivals)
   kQEmpty,                       // every score MMA of the segment done
   kODone,                        // every P.V MMA of the segment done
@@ -307,9 +305,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int i = 0; i < kNumBars; ++i) {
-      const bool many = (i >= kSFree0 && i < kSFree0 + 2) || (i >= kPFull0 && i < kPFull0 + 2) ||
-                        i == kQtReady || i == kOFree;
-      mbar_init(&bars[i], many ? 128 : 1);
+      const bool sfree = i >= kSFree0 && i < kSFree0 + 2;
+      const bool many = (i >= kPFull0 && i < kPFull0 + 2) || i == kQtReady || i == kOFree;
+      mbar_init(&bars[i], sfree ? 256 : many ? 128 : 1);
     }
     // the peer's partial scores of the first kXRecv stages are expected
     for (int i = 0; i < kXRecv; ++i) mbar_arrive_expect_tx(&bars[kXFull0 + i], kXBytes);
@@ -505,9 +503,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int tt = 0; tt < n; ++tt) {
         const int j = stage_i + tt, b = j & 1, xs = j % kXSend;
-        // the scores, and the staging buffer read by the softmax (stage j - kXSend)
-        bool ok = wait_or_abort(&bars[kSFull0 + b], (j >> 1) & 1, abort_flag);
-        if (j >= kXSend) ok = ok && wait_or_abort(&bars[kXSFree0 + xs], ((j - kXSend) / kXSend) & 1, abort_flag);
+        const bool ok = wait_or_abort(&bars[kSFull0 + b], (j >> 1) & 1, abort_flag);
         if (send_red_or(!ok)) { aborted = true; break; }
         tc::fence_after_sync();
         uint32_t sv[32];
@@ -538,7 +534,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             set_status(status, MLA_DEV_TIMEOUT);
             *abort_flag = 1;
           }
-          mbar_arrive(&bars[kXSReady0 + xs]);
         }
       }
       stage_i += n;
@@ -565,12 +560,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int stage_i = 0, seg_i = 0;
     bool aborted = false, fail = false;
     // After an agreement over all 128 threads at stage i, every thread has
-    // finished with stage i - 1: its own staging buffer is free for the
-    // senders and its receive buffer for the peer (re-armed for stage i - 1 + kXRecv).
+    // finished with stage i - 1: its receive buffer is free for the peer
+    // (re-armed for stage i - 1 + kXRecv).
     auto release_prev = [&](int i) {
       if (r == 0 && i >= 1) {
         const int p = i - 1;
-        mbar_arrive(&bars[kXSFree0 + p % kXSend]);
         mbar_arrive_expect_tx(&bars[kXFull0 + p % kXRecv], kXBytes);
         // relaxed: the loads of stage i - 1's buffer returned long ago (their
         // sums fed that stage's softmax), and a release here would stall
@@ -592,34 +586,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       float m_used = -INFINITY, l = 0.f;
 #pragma unroll 1
       for (int tt = 0; tt < n; ++tt) {
-        const int i = stage_i + tt, slot = i % kStages, b = i & 1, xb = i % kXRecv,
-                  xs = i % kXSend;
+        const int i = stage_i + tt, slot = i % kStages, b = i & 1, xb = i % kXRecv;
         // the peer's partial scores of stage i, the stage (for its info), this
-        // CTA's partial scores staged, and P[i % 2] free (P.V of stage i - 2)
+        // CTA's partial scores in TMEM, and P[i % 2] free (P.V of stage i - 2)
         const bool okw = wait4_or_abort(&bars[kXFull0 + xb], (i / kXRecv) & 1,
                                         &bars[kFull0 + slot], (i / kStages) & 1,
-                                        &bars[kXSReady0 + xs], (i / kXSend) & 1,
+                                        &bars[kSFull0 + b], (i >> 1) & 1,
                                         &bars[kPVDone0 + b], i >= 2 ? ((i - 2) >> 1) & 1 : 2u,
                                         abort_flag);
         if (soft_red_or(!okw || fail)) { aborted = true; break; }
-        release_prev(i);
         tc::fence_after_sync();
+        uint32_t sown[32];
+        tc::ld32(trow + kSCol + (uint32_t)b * kTok, sown);
+        release_prev(i);
         const int tstart = seg.k0 * kTile + tt * kTok;
         const int2 inf = info[slot];
         const int v = inf.x, okmask = inf.y;
         // live tokens: a prefix (sequence end, causal position) minus rejected blocks
         const int lim = min(v, pos - tstart + 1);
-        // S = own partial + the peer's partial (both swizzled the same way)
+        // S = own partial (TMEM) + the peer's partial (shared memory, swizzled)
         float x[32];
         {
-          const uint8_t* xo = sm + Smem::xs + xs * kXBytes + r * 128;
           const uint8_t* xp = sm + Smem::x + xb * kXBytes + r * 128;
+          float4 pw[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) pw[k] = *reinterpret_cast<const float4*>(xp + ((k ^ (r & 7)) << 4));
+          tc::wait_ld();
+          tc::fence_before_sync();
+          mbar_arrive(&bars[kSFree0 + b]);   // S[i % 2] may take stage i + 2's scores
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const float4 u = *reinterpret_cast<const float4*>(xo + ((k ^ (r & 7)) << 4));
-            const float4 w = *reinterpret_cast<const float4*>(xp + ((k ^ (r & 7)) << 4));
-            x[4 * k] = u.x + w.x; x[4 * k + 1] = u.y + w.y;
-            x[4 * k + 2] = u.z + w.z; x[4 * k + 3] = u.w + w.w;
+            x[4 * k] = __uint_as_float(sown[4 * k]) + pw[k].x;
+            x[4 * k + 1] = __uint_as_float(sown[4 * k + 1]) + pw[k].y;
+            x[4 * k + 2] = __uint_as_float(sown[4 * k + 2]) + pw[k].z;
+            x[4 * k + 3] = __uint_as_float(sown[4 * k + 3]) + pw[k].w;
           }
         }
         if (!(lim >= kTok && okmask == full_mask)) {
