@@ -69,6 +69,18 @@ cudaError_t launch_combine(const void* workspace, int32_t groups, int32_t num_ct
 cudaError_t launch_out_proj(const mla_config& cfg, const float* o_lat, const void* W_uv,
                             void* out, int64_t num_q, cudaStream_t stream);
 
+// Query absorption on tcgen05 for bf16 and many rows; q_map views q_nope as
+// (128 dims, H, num_q) with (64, 1, 128) boxes, w_map views W_uk as
+// [H * 512 rows, 128 columns] with 64 x 256 boxes, both with the 128-byte swizzle.
+cudaError_t launch_absorb_tc(const CUtensorMap& q_map, const CUtensorMap& w_map,
+                             const mla_config& cfg, const void* q_pe, const int32_t* q_positions,
+                             void* q_abs, int64_t num_q, cudaStream_t stream);
+
+// Output projection on tcgen05 for bf16 and many rows; w_map views W_uv as
+// [H * 512 rows, 128 columns] with 64 x 64 boxes and the 128-byte swizzle.
+cudaError_t launch_out_proj_tc(const CUtensorMap& w_map, const float* o_lat, void* out,
+                               int64_t num_q, int H, cudaStream_t stream);
+
 cudaError_t launch_combine_out_proj(const mla_config& cfg, const void* workspace, int32_t groups,
                                    int32_t num_ctas, int64_t num_q, int32_t batch, const void* W_uv,
                                    void* out, cudaStream_t stream);

@@ -104,6 +104,44 @@ bool make_row_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t bo
   return r == CUDA_SUCCESS;
 }
 
+// 2-D bf16 map over a row-major [rows, cols] matrix: box = box_cols x
+// box_rows, 128-byte swizzle.
+bool make_map_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                 uint32_t box_cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 3-D bf16 map over (d, head, row) of a [rows, heads, dims] tensor: box =
+// (box_d, 1, box_rows), 128-byte swizzle.
+bool make_map_heads(CUtensorMap* map, const void* base, uint64_t dims, uint64_t heads,
+                    uint64_t rows, uint32_t box_d, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t gdim[3] = {(cuuint64_t)dims, (cuuint64_t)heads, (cuuint64_t)rows};
+  const cuuint64_t strides[2] = {(cuuint64_t)dims * 2, (cuuint64_t)dims * heads * 2};
+  const cuuint32_t box[3] = {box_d, 1, box_rows};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), gdim,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Rows from which the projections run on tcgen05 (below, the latency-bound
+// warp-mma kernels are faster).
+constexpr int64_t kTcProjRows = 256;
+
 inline mla_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
 
 }  // namespace
@@ -173,6 +211,14 @@ mla_status mla_absorb_q(const mla_config* cfg, const void* q_nope, const void* q
   if (!aligned(q_nope, 16) || !aligned(q_pe, 16) || !aligned(W_uk, 16) || !aligned(q_abs, 16) ||
       !aligned(q_positions, 4))
     return MLA_ERR_INVALID_ARGUMENT;
+  if (cfg->dtype == MLA_BF16 && num_q >= kTcProjRows) {
+    CUtensorMap q_map, w_map;
+    if (!make_map_heads(&q_map, q_nope, kDn, (uint64_t)cfg->num_heads, (uint64_t)num_q, 64, 128) ||
+        !make_map_2d(&w_map, W_uk, kDn, (uint64_t)cfg->num_heads * kDc, 64, 256))
+      return MLA_ERR_CUDA;
+    return from_cuda(launch_absorb_tc(q_map, w_map, *cfg, q_pe, q_positions, q_abs, num_q,
+                                      as_stream(stream)));
+  }
   return from_cuda(launch_absorb_q(*cfg, q_nope, q_pe, q_positions, W_uk, q_abs, num_q,
                                    as_stream(stream)));
 }
@@ -364,6 +410,11 @@ mla_status mla_out_proj(const mla_config* cfg, const float* o_lat, const void* W
   if (num_q == 0) return MLA_OK;
   if (!o_lat || !W_uv || !out) return MLA_ERR_INVALID_ARGUMENT;
   if (!aligned(o_lat, 16) || !aligned(W_uv, 16) || !aligned(out, 16)) return MLA_ERR_INVALID_ARGUMENT;
+  if (cfg->dtype == MLA_BF16 && num_q >= kTcProjRows) {
+    CUtensorMap w_map;
+    if (!make_map_2d(&w_map, W_uv, kDv, (uint64_t)cfg->num_heads * kDc, 64, 64)) return MLA_ERR_CUDA;
+    return from_cuda(launch_out_proj_tc(w_map, o_lat, out, num_q, cfg->num_heads, as_stream(stream)));
+  }
   return from_cuda(launch_out_proj(*cfg, o_lat, W_uv, out, num_q, as_stream(stream)));
 }
 

@@ -1,5 +1,5 @@
 // Thin inline-PTX wrappers for the 5th-generation tensor core (tcgen05):
-// TMEM allocation, MMA issue (A from TMEM, B by shared-memory descriptor),
+// TMEM allocation, MMA issue (A from shared memory or TMEM, B by descriptor),
 // completion through mbarriers, and TMEM loads / stores.
 #pragma once
 
@@ -29,6 +29,16 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
          ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem], issued by one thread.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
 }
 
 // D[tmem] (+)= A[tmem] * B[smem], issued by one thread. A (M x K, K-major)

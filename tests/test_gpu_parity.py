@@ -368,3 +368,38 @@ def test_tensor_core_tiles(name, num_ctas):
     np.testing.assert_allclose(to_f64(s.o_lat), fused, rtol=0, atol=1e-5)
     s.combine_out_proj()                                # merge inside the projection
     assert_close(to_f64(s.out), ref_out(w), "bf16", f"tc out {name}")
+
+
+# ---------------------------------------------------------------------------
+# projections for many rows (tcgen05 kernels from 256 rows on)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("rows,heads", [(255, 16), (256, 16), (300, 16), (1000, 32), (257, 128)])
+def test_out_proj_many_rows(rows, heads):
+    rng = np.random.default_rng(800 + rows + heads)
+    cfg = L.make_config(heads, 64, "bf16")
+    # latent outputs are convex combinations of normalised rows: |o| well below 1
+    o_lat = torch.from_numpy(0.25 * rng.standard_normal((rows, heads, 512)).astype(np.float32)).to(DEV)
+    w = W.round_to_dtype(rng.standard_normal((heads, 512, 128)).astype(np.float32) / np.sqrt(512), "bf16")
+    W_uv = torch.from_numpy(w).to(DEV).to(torch.bfloat16)
+    out = torch.full((rows, heads, 128), float("nan"), dtype=torch.bfloat16, device=DEV)
+    L.mla_out_proj(cfg, o_lat, W_uv, out)
+    torch.cuda.synchronize()
+    ref = O.out_proj(to_f64(o_lat), w.astype(np.float64))
+    assert_close(to_f64(out), ref, "bf16", f"out_proj {rows} rows x {heads} heads")
+
+
+@pytest.mark.parametrize("rows,heads", [(255, 16), (256, 16), (300, 16), (1000, 32), (257, 128)])
+def test_absorb_many_rows(rows, heads):
+    rng = np.random.default_rng(900 + rows + heads)
+    cfg = L.make_config(heads, 64, "bf16")
+    qn = W.round_to_dtype(rng.standard_normal((rows, heads, 128)).astype(np.float32), "bf16")
+    qp = W.round_to_dtype(rng.standard_normal((rows, heads, 64)).astype(np.float32), "bf16")
+    wk = W.round_to_dtype(rng.standard_normal((heads, 512, 128)).astype(np.float32) / np.sqrt(512), "bf16")
+    pos = rng.integers(0, 32768, size=rows).astype(np.int32)
+    t = lambda a: torch.from_numpy(a).to(DEV).to(torch.bfloat16)
+    q_abs = torch.full((rows, heads, 576), float("nan"), dtype=torch.bfloat16, device=DEV)
+    L.mla_absorb_q(cfg, t(qn), t(qp), torch.from_numpy(pos).to(DEV), t(wk), q_abs)
+    torch.cuda.synchronize()
+    ref = O.absorb_q(qn, qp, pos, wk, cfg.rope_base)
+    assert_close(to_f64(q_abs), ref, "bf16", f"absorb {rows} rows x {heads} heads")
