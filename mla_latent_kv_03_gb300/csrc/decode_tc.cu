@@ -32,8 +32,8 @@
 //   warp 2 (score issuer): the partial scores of a stage as soon as its score
 //     buffer is free (16 or 20 tcgen05.mma, M 128, N 32, K 16, A from TMEM).
 //   warps 8-11 (senders): each stage's partial scores from TMEM to a staging
-//     buffer and, by one bulk copy, into the peer's shared memory, up to three
-//     stages ahead of their use.
+//     buffer and, by one bulk copy per warp (its 32 rows), into the peer's
+//     shared memory, up to three stages ahead of their use.
 //   warps 4-7 (softmax): thread r owns row r. Per stage it adds the peer's
 //     partial scores to its own, masks (sequence end, causal position,
 //     rejected blocks), keeps the running maximum, rescales the warp's O rows
@@ -62,17 +62,18 @@ constexpr int kTok = 32;                       // tokens per stage
 constexpr int kSlab = kTok * 128;              // 32 rows x 64 bf16 columns
 constexpr int kMaxSlabs = 5;                   // column slabs of one CTA (64 columns each)
 constexpr int kStage = kMaxSlabs * kSlab;      // 20 KB
-constexpr int kStages = 5;                     // cache stages in the ring
+constexpr int kStages = 7;                     // cache stages in the ring
 constexpr int kXRecv = 4;                      // buffers of the peer's partial scores
-constexpr int kXSend = 3;                      // buffers of this CTA's partial scores
+constexpr int kXSend = 4;                      // buffers of this CTA's partial scores
 constexpr int kThreads = 384;
 constexpr int kSoftWarp0 = 4;                  // warps 4-7: softmax
 constexpr int kSendWarp0 = 8;                  // warps 8-11: partial-score senders
 constexpr int kSoftBar = 2;                    // named barrier of the softmax warps
-constexpr int kXBar = 3;                       // named barrier of the sender warps
 constexpr uint32_t kOCol = 0, kSCol = 256, kPCol = 320, kQCol = 352, kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.f;            // lazy rescale threshold (2^8)
-constexpr int kXBytes = kQBlockRows * kTok * 4;  // one stage of partial scores
+constexpr int kXRow = kTok * 2;                // one row of a stage's partial scores (bf16)
+constexpr int kXBytes = kQBlockRows * kXRow;   // one stage of partial scores
+constexpr int kXWarpBytes = kXBytes / 4;       // the 32 rows of one sender warp
 constexpr int kMergeSlots = 16;                // parts merged by the one-pass merge
 static_assert(kQCol + 32 * kMaxSlabs <= kTmemCols, "TMEM budget");
 
@@ -80,12 +81,14 @@ enum {
   kFull0 = 0,
   kEmpty0 = kFull0 + kStages,
   kSFull0 = kEmpty0 + kStages,   // [2] partial scores of stage i in S[i % 2]
-  kSFree0 = kSFull0 + 2,         // [2] S[i % 2] read out by senders and softmax (256 arrivals)
+  kSFree0 = kSFull0 + 2,         // [2] S[i % 2] read out by the senders (128 arrivals)
   kXFull0 = kSFull0 + 4,         // [kXRecv] the peer's partial scores (bytes from the peer)
   kPFull0 = kXFull0 + kXRecv,    // [2] probabilities of stage i in P[i % 2] (128 arrivals)
   kPVDone0 = kPFull0 + 2,        // [2] O += P[i % 2] . V_i done
   kPeerFree0 = kPVDone0 + 2,     // [kXRecv] the peer's softmax read its buffer (1 remote arrival)
-  kQtReady = kPeerFree0 + kXRecv,// query columns stored in TMEM (128 arrivals)
+  kXsFull0 = kPeerFree0 + kXRecv,// [kXSend] own partial scores staged (128 arrivals)
+  kXsFree0 = kXsFull0 + kXSend,  // [kXSend] own staged partial read by the softmax
+  kQtReady = kXsFree0 + kXSend,  // query columns stored in TMEM (128 arrivals)
   kQEmpty,                       // every score MMA of the segment done
   kODone,                        // every P.V MMA of the segment done
   kOFree,                        // O read out by the epilogue (128 arrivals)
@@ -217,19 +220,6 @@ __device__ __forceinline__ bool soft_red_or(bool v) {
   return r != 0;
 }
 
-__device__ __forceinline__ bool send_red_or(bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred pi, po;\n\t"
-      "setp.ne.u32 pi, %1, 0;\n\t"
-      "barrier.red.or.pred po, %2, 128, pi;\n\t"
-      "selp.u32 %0, 1, 0, po;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)v), "r"(kXBar)
-      : "memory");
-  return r != 0;
-}
-
 // Stages (32 tokens) of a segment that hold a token its last row sees: they
 // form a prefix of the segment's tiles. Stage t starts at token k0 * 64 + 32 t.
 __device__ __forceinline__ int seg_stages(const TcSeg& s) {
@@ -305,9 +295,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int i = 0; i < kNumBars; ++i) {
-      const bool sfree = i >= kSFree0 && i < kSFree0 + 2;
-      const bool many = (i >= kPFull0 && i < kPFull0 + 2) || i == kQtReady || i == kOFree;
-      mbar_init(&bars[i], sfree ? 256 : many ? 128 : 1);
+      const bool many = (i >= kSFree0 && i < kSFree0 + 2) || (i >= kPFull0 && i < kPFull0 + 2) ||
+                        (i >= kXsFull0 && i < kXsFull0 + kXSend) || i == kQtReady || i == kOFree;
+      mbar_init(&bars[i], many ? 128 : 1);
     }
     // the peer's partial scores of the first kXRecv stages are expected
     for (int i = 0; i < kXRecv; ++i) mbar_arrive_expect_tx(&bars[kXFull0 + i], kXBytes);
@@ -334,28 +324,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (has_work && warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int stage_i = 0;
-      bool ok = true;
-      while (ok && sw.next(seg)) {
-        const int32_t* bt = a.block_table + (size_t)seg.b * a.max_blocks_per_seq;
-        const int n = seg_stages(seg);
+    // The whole warp walks the stages; lane 0 issues the copies. Block ids
+    // come from the block table 32 at a time (one per lane, handed out by
+    // shuffles), so a stage never waits on a dependent global load.
+    int stage_i = 0;
+    bool ok = true;
+    while (ok && sw.next(seg)) {
+      const int32_t* bt = a.block_table + (size_t)seg.b * a.max_blocks_per_seq;
+      const int n = seg_stages(seg);
+      int cache_base = -(1 << 30), cached = -1;   // lane l holds bt[cache_base + l]
 #pragma unroll 1
-        for (int t = 0; t < n; ++t) {
-          const int tstart = seg.k0 * kTile + t * kTok;
-          const int v = min(kTok, seg.vis - tstart);
-          const int slot = stage_i % kStages;
-          int blk[2], okmask = 0, nload = 0;
+      for (int t = 0; t < n; ++t) {
+        const int tstart = seg.k0 * kTile + t * kTok;
+        const int v = min(kTok, seg.vis - tstart);
+        const int slot = stage_i % kStages;
+        int blk[2];
 #pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            blk[i] = -1;
-            if (i < ppst && (i << bsr_shift) < v) blk[i] = bt[(tstart + (i << bsr_shift)) / bs];
+        for (int i = 0; i < 2; ++i) {
+          blk[i] = -1;
+          if (i < ppst && (i << bsr_shift) < v) {   // warp-uniform
+            const int bi = (tstart + (i << bsr_shift)) / bs;
+            if (bi - cache_base >= 32 || bi < cache_base) {
+              cache_base = bi;
+              cached = bi + lane < a.max_blocks_per_seq ? bt[bi + lane] : -1;
+            }
+            blk[i] = __shfl_sync(0xffffffffu, cached, bi - cache_base);
           }
-          if (stage_i >= kStages &&
-              !wait_or_abort(&bars[kEmpty0 + slot], ((stage_i / kStages) - 1) & 1, abort_flag)) {
-            ok = false;
-            break;
-          }
+        }
+        if (stage_i >= kStages &&
+            !__all_sync(0xffffffffu, wait_or_abort(&bars[kEmpty0 + slot],
+                                                  ((stage_i / kStages) - 1) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          int okmask = 0, nload = 0;
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
             if (i < ppst && (i << bsr_shift) < v) {
@@ -381,9 +384,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             64 * (slab0 + j), y, &bars[kFull0 + slot]);
             }
           }
-          ++stage_i;
         }
+        __syncwarp();
+        ++stage_i;
       }
+    }
+    if (lane == 0) {
       if (!ok) {
         set_status(status, MLA_DEV_TIMEOUT);
         *abort_flag = 1;
@@ -488,61 +494,76 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (has_work && warp >= kSendWarp0) {
     // ------------------------------------------------------------ senders
-    // Partial scores of every stage, in order: TMEM -> own staging buffer
-    // j % kXSend -> one bulk copy into the peer's buffer j % kXRecv, counted
-    // on the peer's barrier. Runs up to kXSend stages ahead of the softmax.
+    // Partial scores of every stage, in order: TMEM -> bf16 -> own staging
+    // buffer j % kXSend, which this CTA's softmax reads, and from which each
+    // warp's bulk copy moves its 32 rows into the peer's buffer j % kXRecv,
+    // counted on the peer's barrier. The score buffer is free as soon as the
+    // senders have read it, so the next scores never wait for the softmax.
     const int r = tid - kSendWarp0 * 32;
-    const uint32_t trow = tmem + ((uint32_t)((warp - kSendWarp0) * 32) << 16);
+    const int wl = warp - kSendWarp0;                  // rows [32 wl, 32 wl + 32)
+    const uint32_t trow = tmem + ((uint32_t)(wl * 32) << 16);
     const uint32_t peer = (uint32_t)(h ^ 1);
-    const uint32_t x_peer0 = cl::map(smem_u32(sm + Smem::x), peer);
+    const uint32_t x_peer0 = cl::map(smem_u32(sm + Smem::x), peer) + (uint32_t)wl * kXWarpBytes;
     const uint32_t xbar_peer0 = cl::map(smem_u32(&bars[kXFull0]), peer);
+    const uint32_t xs_src0 = smem_u32(sm + Smem::xs) + (uint32_t)wl * kXWarpBytes;
+    const int sw4 = (r >> 1) & 3;                      // 16-byte chunk swizzle of row r
     int stage_i = 0;
     bool aborted = false;
     while (!aborted && sw.next(seg)) {
       const int n = seg_stages(seg);
 #pragma unroll 1
       for (int tt = 0; tt < n; ++tt) {
-        const int j = stage_i + tt, b = j & 1, xs = j % kXSend;
-        const bool ok = wait_or_abort(&bars[kSFull0 + b], (j >> 1) & 1, abort_flag);
-        if (send_red_or(!ok)) { aborted = true; break; }
+        const int j = stage_i + tt, b = j & 1, xs = j % kXSend, xr = j % kXRecv;
+        if (!__all_sync(0xffffffffu, wait_or_abort(&bars[kSFull0 + b], (j >> 1) & 1, abort_flag))) {
+          aborted = true;
+          break;
+        }
         tc::fence_after_sync();
         uint32_t sv[32];
         tc::ld32(trow + kSCol + (uint32_t)b * kTok, sv);
         tc::wait_ld();
         tc::fence_before_sync();
-        mbar_arrive(&bars[kSFree0 + b]);
-        // the copy of stage j - kXSend read this buffer; at most kXSend - 1 newer remain
-        if (r == 0) cl::bulk_wait_read<kXSend - 1>();
-        named_bar_sync(kXBar, 128);
-        uint8_t* dst = sm + Smem::xs + xs * kXBytes + r * 128;
+        mbar_arrive(&bars[kSFree0 + b]);   // S[j % 2] may take stage j + 2's scores
+        uint32_t pk[16];
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          *reinterpret_cast<uint4*>(dst + ((k ^ (r & 7)) << 4)) =
-              make_uint4(sv[4 * k], sv[4 * k + 1], sv[4 * k + 2], sv[4 * k + 3]);
+        for (int k = 0; k < 16; ++k) pk[k] = pack_bf16(__uint_as_float(sv[2 * k]), __uint_as_float(sv[2 * k + 1]));
+        // staging buffer xs: this CTA's softmax has read stage j - kXSend from
+        // it, and this warp's copy of that stage has read its rows
+        const bool okf = j < kXSend ||
+                         wait_or_abort(&bars[kXsFree0 + xs], ((j - kXSend) / kXSend) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, okf)) { aborted = true; break; }
+        if (lane == 0) cl::bulk_wait_read<kXSend - 1>();
+        __syncwarp();
+        uint8_t* dst = sm + Smem::xs + xs * kXBytes + r * kXRow;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          *reinterpret_cast<uint4*>(dst + ((k ^ sw4) << 4)) =
+              make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
         fence_proxy_async_smem();
-        named_bar_sync(kXBar, 128);
-        if (r == 0) {
+        mbar_arrive(&bars[kXsFull0 + xs]);
+        __syncwarp();
+        int sent = 1;
+        if (lane == 0) {
           // the peer's softmax has read its buffer for stage j - kXRecv
-          const int xr = j % kXRecv;
           if (j < kXRecv ||
               wait_or_abort(&bars[kPeerFree0 + xr], ((j - kXRecv) / kXRecv) & 1, abort_flag)) {
             cl::bulk_to_peer(x_peer0 + (uint32_t)xr * kXBytes,
-                             smem_u32(sm + Smem::xs) + (uint32_t)xs * kXBytes, kXBytes,
+                             xs_src0 + (uint32_t)xs * kXBytes, kXWarpBytes,
                              xbar_peer0 + (uint32_t)xr * 8);
             cl::bulk_commit();
           } else {
-            set_status(status, MLA_DEV_TIMEOUT);
-            *abort_flag = 1;
+            sent = 0;
           }
         }
+        if (__shfl_sync(0xffffffffu, sent, 0) == 0) { aborted = true; break; }
       }
       stage_i += n;
     }
-    if (aborted && r == 0) {
+    if (aborted && lane == 0) {
       set_status(status, MLA_DEV_TIMEOUT);
       *abort_flag = 1;
     }
-    if (r == 0) cl::bulk_wait_read<0>();   // no copy still reads the staging buffers
+    if (lane == 0) cl::bulk_wait_read<0>();   // no copy still reads the staging buffers
   } else if (has_work && warp >= kSoftWarp0) {
     // ----------------------------------------------------------- softmax
     const int r = tid - kSoftWarp0 * 32;                 // row of the q-block
@@ -561,10 +582,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool aborted = false, fail = false;
     // After an agreement over all 128 threads at stage i, every thread has
     // finished with stage i - 1: its receive buffer is free for the peer
-    // (re-armed for stage i - 1 + kXRecv).
+    // (re-armed for stage i - 1 + kXRecv), its staging buffer for the senders.
     auto release_prev = [&](int i) {
       if (r == 0 && i >= 1) {
         const int p = i - 1;
+        mbar_arrive(&bars[kXsFree0 + p % kXSend]);
         mbar_arrive_expect_tx(&bars[kXFull0 + p % kXRecv], kXBytes);
         // relaxed: the loads of stage i - 1's buffer returned long ago (their
         // sums fed that stage's softmax), and a release here would stall
@@ -586,40 +608,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       float m_used = -INFINITY, l = 0.f;
 #pragma unroll 1
       for (int tt = 0; tt < n; ++tt) {
-        const int i = stage_i + tt, slot = i % kStages, b = i & 1, xb = i % kXRecv;
-        // the peer's partial scores of stage i, the stage (for its info), this
-        // CTA's partial scores in TMEM, and P[i % 2] free (P.V of stage i - 2)
+        const int i = stage_i + tt, slot = i % kStages, b = i & 1, xb = i % kXRecv, xsb = i % kXSend;
+        // the peer's partial scores of stage i, this CTA's (staged by the
+        // senders), the stage (for its info), and P[i % 2] free (P.V of stage i - 2)
         const bool okw = wait4_or_abort(&bars[kXFull0 + xb], (i / kXRecv) & 1,
+                                        &bars[kXsFull0 + xsb], (i / kXSend) & 1,
                                         &bars[kFull0 + slot], (i / kStages) & 1,
-                                        &bars[kSFull0 + b], (i >> 1) & 1,
                                         &bars[kPVDone0 + b], i >= 2 ? ((i - 2) >> 1) & 1 : 2u,
                                         abort_flag);
         if (soft_red_or(!okw || fail)) { aborted = true; break; }
-        tc::fence_after_sync();
-        uint32_t sown[32];
-        tc::ld32(trow + kSCol + (uint32_t)b * kTok, sown);
         release_prev(i);
         const int tstart = seg.k0 * kTile + tt * kTok;
         const int2 inf = info[slot];
         const int v = inf.x, okmask = inf.y;
         // live tokens: a prefix (sequence end, causal position) minus rejected blocks
         const int lim = min(v, pos - tstart + 1);
-        // S = own partial (TMEM) + the peer's partial (shared memory, swizzled)
+        // S = own partial + the peer's partial, both as the senders rounded
+        // them to bf16 (so both CTAs add the same two values), read from the
+        // staging and receive buffers (16-byte chunks swizzled by the row)
         float x[32];
         {
-          const uint8_t* xp = sm + Smem::x + xb * kXBytes + r * 128;
-          float4 pw[8];
+          const int sw4 = (r >> 1) & 3;
+          const uint8_t* xp = sm + Smem::x + xb * kXBytes + r * kXRow;
+          const uint8_t* op = sm + Smem::xs + xsb * kXBytes + r * kXRow;
+          uint4 pv[4], ov[4];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) pw[k] = *reinterpret_cast<const float4*>(xp + ((k ^ (r & 7)) << 4));
-          tc::wait_ld();
-          tc::fence_before_sync();
-          mbar_arrive(&bars[kSFree0 + b]);   // S[i % 2] may take stage i + 2's scores
+          for (int k = 0; k < 4; ++k) {
+            pv[k] = *reinterpret_cast<const uint4*>(xp + ((k ^ sw4) << 4));
+            ov[k] = *reinterpret_cast<const uint4*>(op + ((k ^ sw4) << 4));
+          }
+          auto add2 = [&](int j, uint32_t a, uint32_t c) {
+            x[j] = __uint_as_float(a << 16) + __uint_as_float(c << 16);
+            x[j + 1] = __uint_as_float(a & 0xffff0000u) + __uint_as_float(c & 0xffff0000u);
+          };
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            x[4 * k] = __uint_as_float(sown[4 * k]) + pw[k].x;
-            x[4 * k + 1] = __uint_as_float(sown[4 * k + 1]) + pw[k].y;
-            x[4 * k + 2] = __uint_as_float(sown[4 * k + 2]) + pw[k].z;
-            x[4 * k + 3] = __uint_as_float(sown[4 * k + 3]) + pw[k].w;
+          for (int k = 0; k < 4; ++k) {
+            add2(8 * k, ov[k].x, pv[k].x);
+            add2(8 * k + 2, ov[k].y, pv[k].y);
+            add2(8 * k + 4, ov[k].z, pv[k].z);
+            add2(8 * k + 6, ov[k].w, pv[k].w);
           }
         }
         if (!(lim >= kTok && okmask == full_mask)) {

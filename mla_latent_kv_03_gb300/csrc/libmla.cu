@@ -325,12 +325,15 @@ mla_status mla_decode_combine(const mla_config* cfg, const void* q_abs, const vo
   mla_status s = check_cfg(cfg);
   if (s != MLA_OK) return s;
   const bool tc = use_tc(cfg, num_q, batch);
-  // With few (row, head group) tiles per CTA each tile is cut into many
+  // With few tiles per CTA (row x head group tiles of 16 rows; 128-row
+  // q-blocks per CTA pair on the tensor cores) each tile is cut into many
   // splits, and one CTA merging all of them at the end of the decode is slower
-  // than the merge kernel, which spreads that work over more CTAs.
+  // than the merge kernel, which spreads that work over all SMs.
   const int C = decode_ctas(cfg, tc);
   const int64_t qtiles = num_q * (cfg->num_heads / kHG);
-  if (!tc && C > 0 && qtiles * 4 < C) {
+  const int64_t qblocks = num_q * cfg->num_heads / kQBlockRows;
+  const bool split_heavy = tc ? qblocks < C / 2 : qtiles * 4 < C;
+  if (C > 0 && split_heavy) {
     s = decode_impl(cfg, q_abs, cache, num_blocks, block_table, max_blocks_per_seq, batch, num_q,
                     workspace, ws_bytes, nullptr, stream);
     if (s != MLA_OK) return s;

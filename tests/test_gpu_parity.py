@@ -370,6 +370,28 @@ def test_tensor_core_tiles(name, num_ctas):
     assert_close(to_f64(s.out), ref_out(w), "bf16", f"tc out {name}")
 
 
+def test_tensor_core_merge_of_many_splits():
+    # 41 q-blocks over 40 CTA pairs keeps the merge inside the decode kernel;
+    # the 32,000-token row (500 tiles, ~14 per pair) is cut into ~37 parts,
+    # more than one pass of staged merge weights
+    lens = [32000] + [1] * 38 + [100, 64]
+    w = W.make("tc_many", lens, [1] * len(lens), 128, 64, "bf16", seed=67)
+    s = MlaDecodeStep(w, device=DEV, num_ctas=80)
+    s.populate()
+    s.absorb()
+    s.plan()
+    s.o_lat.fill_(float("nan"))
+    s.decode_combine()
+    torch.cuda.synchronize()
+    assert s.device_status()[0][0] == 0
+    fused = to_f64(s.o_lat)
+    ref = ref_o_lat_from(w, to_f64(s.cache), to_f64(s.q_abs))
+    assert_close(fused, ref, "bf16", "tc fused o_lat, 37 parts")
+    s.decode_planned()
+    s.combine()
+    np.testing.assert_allclose(to_f64(s.o_lat), fused, rtol=0, atol=1e-5)
+
+
 # ---------------------------------------------------------------------------
 # projections for many rows (tcgen05 kernels from 256 rows on)
 # ---------------------------------------------------------------------------
