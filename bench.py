@@ -4,10 +4,13 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload serving|ragged_h128|mixed|v2lite_1024|...]
 
-A step is one pass of the whole hot path over one batch: mla_absorb_q,
-mla_decode_plan (on a side stream), mla_decode_combine (the split-KV decode
-with the split merge fused in) and mla_out_proj (plus mla_cache_write of the
-step's new tokens for the mixed workload). The default
+A step is one pass of the whole hot path over one batch: mla_absorb_q, the
+split plan, the split-KV decode with its split merge, and mla_out_proj (plus
+mla_cache_write of the step's new tokens for the mixed workload). On the
+16-head warp-mma path the middle three are one kernel
+(mla_decode_paged_combine); on the tensor-core path mla_decode_plan runs on a
+side stream beside the cache write and the absorption, then
+mla_decode_combine. The default
 workload is the serving batch: 64 sequences x 4,096 tokens, 16 heads, bf16,
 block_size 64, a 301,989,888-byte latent cache (larger than L2, so every step
 reads it from HBM). Inputs are seeded synthetic data with the shapes of
@@ -328,6 +331,23 @@ def cpu_baseline(w, seconds: float):
 # our arm
 # ---------------------------------------------------------------------------
 
+def decode_call_launches(w, props):
+    """(self-planned, kernel launches) of one mla_decode_paged_combine call,
+    following the library's choice: the 16-head warp-mma path plans inside
+    its kernel for up to 256 rows; with fewer than num_ctas / 4 tiles (16-head
+    tiles, or 128-row q-blocks per CTA pair on the tensor cores) the merge runs
+    as its own kernel."""
+    sms = props.multi_processor_count
+    tc = w.dtype == "bf16" and (w.num_heads >= 64 or w.num_q >= 4 * w.batch)
+    self_planned = w.dtype == "bf16" and not tc and w.num_q <= 256
+    if tc:
+        split_heavy = w.num_q * w.num_heads // 128 < sms // 2
+    else:
+        split_heavy = w.num_q * (w.num_heads // 16) * 4 < sms
+    launches = (1 if self_planned else 2) + (1 if split_heavy else 0)
+    return self_planned, launches
+
+
 def run_ours(args, world, rank, local):
     import torch
     from mla_latent_kv_03_gb300 import libmla as L
@@ -347,8 +367,16 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.Stream(device=dev)
     side = torch.cuda.Stream(device=dev)
     ev_fork, ev_join = torch.cuda.Event(), torch.cuda.Event()
+    self_planned, decode_launches = decode_call_launches(w, torch.cuda.get_device_properties(dev))
 
     def one_step():
+        if self_planned:
+            # one kernel plans, decodes and merges; it starts its cache stream
+            # while the absorption finishes
+            s.absorb()
+            s.decode_paged_combine()
+            s.out_proj()
+            return
         # the split plan depends only on the batch layout: it runs on a side
         # stream, concurrently with the cache write and the query absorption
         cur = torch.cuda.current_stream()
@@ -361,10 +389,10 @@ def run_ours(args, world, rank, local):
             s.write_new()
         s.absorb()
         cur.wait_event(ev_join)
-        s.decode_combine()       # decode + split merge in one kernel
+        s.decode_combine()         # decode + split merge
         s.out_proj()
 
-    launches_per_step = 4 + (1 if mixed else 0)
+    launches_per_step = 2 + decode_launches + (1 if mixed else 0)
     # eager warm-up (also builds the lazy state), then capture one step
     with torch.cuda.stream(stream):
         for _ in range(3):
@@ -414,9 +442,12 @@ def run_ours(args, world, rank, local):
     # ---- decode kernel alone: back-to-back launches, CUDA events on its stream
     per_graph = 20
     kgraph = torch.cuda.CUDAGraph()
+    # the decode kernel of the step: the self-planned one on the warp-mma
+    # path, else the planned decode (the plan is in the workspace by now)
+    decode_alone = s.decode_paged_combine if self_planned else s.decode_combine
     with torch.cuda.graph(kgraph, stream=stream):
         for _ in range(per_graph):
-            s.decode_combine()
+            decode_alone()
     reps = max(1, args.kernel_launches // per_graph)
     with torch.cuda.stream(stream):
         for _ in range(3):
@@ -473,8 +504,8 @@ def run_ours(args, world, rank, local):
                        "seq_lens": "all 4096" if args.workload == "serving" else "see workload",
                        "block_size": w.block_size, "latent_bytes_per_step": latent,
                        "l2": "inputs larger than L2: the latent cache read each step exceeds 129 MB",
-                       "graph": "steps captured in CUDA graphs of 10 (plan forked onto a side "
-                                "stream, joined before the decode); exactly K steps replayed",
+                       "graph": "steps captured in CUDA graphs of 10; exactly K steps replayed"
+                                + ("" if self_planned else " (plan forked onto a side stream)"),
                        "parallelism": f"replicas x{world} (independent batches per GPU)"},
             "us_per_step": round(ms_per_step * 1e3, 2),
             "tokens_per_s": round(w.num_q * world / (ms_per_step * 1e-3), 1),

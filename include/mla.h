@@ -139,7 +139,9 @@ mla_status mla_absorb_q(const mla_config* cfg, const void* q_nope, const void* q
  * Workspace for mla_decode_paged / mla_combine: a device buffer of at least
  * mla_decode_workspace_size() bytes (it depends on the current device's SM
  * count when cfg->num_ctas is 0). Its first 4 bytes are the device status
- * word; call mla_workspace_init() once after allocating it.
+ * word; call mla_workspace_init() once after allocating it (it zeroes the
+ * status word, the plan header and the fused merge's arrival counters), and
+ * again after any call that reported a device error.
  */
 size_t mla_decode_workspace_size(const mla_config* cfg, int64_t num_q, int32_t batch);
 mla_status mla_workspace_init(void* workspace, size_t ws_bytes, void* stream);
@@ -159,14 +161,19 @@ mla_status mla_workspace_init(void* workspace, size_t ws_bytes, void* stream);
  * output and its log-sum-exp into the workspace. mla_combine() merges them.
  *   q_abs [num_q, H, 576] dtype; cache [num_blocks, block_size, 576] dtype;
  *   block_table [batch, max_blocks_per_seq] int32 (entries past a sequence's
- *   last block are never read); seq_lens [batch] int32;
+ *   last block are never used as block ids; they may be read, within the
+ *   row); seq_lens [batch] int32;
  *   query_start_loc [batch + 1] int32 (query_start_loc[batch] == num_q).
  * The same workspace must be passed, unchanged, to mla_combine().
  * Kernel choice (the same for every call given cfg, num_q and batch): with
  * bf16 and either num_heads >= 64 or num_q >= 4 * batch (prefill chunks),
  * tiles are 128 (row, head) rows on tcgen05 tensor cores with the
  * accumulator in TMEM (one query row of 128 heads, or 8 rows of 16 heads);
- * otherwise tiles are one row x 16 heads on warp mma.
+ * otherwise tiles are one row x 16 heads on warp mma. On that warp-mma path
+ * with num_q <= 256 the call is a single kernel launch: each CTA derives the
+ * split plan from seq_lens / query_start_loc itself and the kernel writes the
+ * plan to the workspace; otherwise it is mla_decode_plan followed by
+ * mla_decode_planned (two launches). The workspace contents are the same.
  */
 mla_status mla_decode_paged(const mla_config* cfg, const void* q_abs, const void* cache,
                             int64_t num_blocks, const int32_t* block_table,
@@ -212,6 +219,30 @@ mla_status mla_decode_combine(const mla_config* cfg, const void* q_abs, const vo
                               int64_t num_blocks, const int32_t* block_table,
                               int32_t max_blocks_per_seq, int32_t batch, int64_t num_q,
                               void* workspace, size_t ws_bytes, float* o_lat, void* stream);
+
+/*
+ * mla_decode_paged_combine -- mla_decode_paged and mla_combine in one call:
+ * same inputs as mla_decode_paged plus o_lat [num_q, H, 512] float32, the
+ * output of mla_combine. On the warp-mma path with num_q <= 256 this is one
+ * kernel launch that plans, decodes and merges (the CTA that finishes a
+ * (row, 16-head group) last merges its parts); with fewer than num_ctas / 4
+ * (row, head group) tiles it is that kernel without the merge followed by the
+ * merge kernel. Elsewhere it is mla_decode_plan + mla_decode_combine.
+ * Ordering: the kernel may start reading the cache and block_table before
+ * the kernel launched just before it on the stream has finished (programmatic
+ * dependent launch, as every libmla kernel uses); q_abs, seq_lens and
+ * query_start_loc are read, and the workspace and o_lat written, only after
+ * it has finished. So the kernel immediately before this call must not write
+ * the cache or the block table: in a layer step it is mla_absorb_q, with
+ * mla_cache_write before it. Rows that see no token get zeros. The result
+ * equals mla_decode_paged followed by mla_combine up to fp32 rounding of the
+ * merge order. The arrival counters are left at zero after a successful call.
+ */
+mla_status mla_decode_paged_combine(const mla_config* cfg, const void* q_abs, const void* cache,
+                                    int64_t num_blocks, const int32_t* block_table,
+                                    int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                    const int32_t* query_start_loc, int32_t batch, int64_t num_q,
+                                    void* workspace, size_t ws_bytes, float* o_lat, void* stream);
 
 /*
  * mla_combine -- merge the split partials of mla_decode_paged.

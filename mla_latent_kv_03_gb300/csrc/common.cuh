@@ -29,12 +29,16 @@ constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 // ---------------------------------------------------------------------------
 // Workspace layout (device memory owned by the caller).
 //   [0, 256)            WsHeader
+//   counters[512]       int, CTAs done with each q-tile of the fused merge when
+//                       num_q * G <= 512 (a fixed region: no layout puts
+//                       anything else there, mla_workspace_init zeroes it, and
+//                       the CTA that merges a q-tile resets its counter to 0)
 //   row_info[num_q]     int4 {seq b, query position, tiles, first unit}
 //   cta_start[C]        int4 {row n, head group g, tile k, 0}
 //   lse[S][16]          float, base-2 log-sum-exp of each partial
 //   opart[S][16][512]   float, normalised partial outputs
-//   arrive[num_q * G]   int, CTAs done with each q-tile (fused merge only;
-//                       zeroed by the plan)
+//   arrive[num_q * G]   int, the fused merge's counters when num_q * G > 512
+//                       (zeroed by the plan)
 // with S = C + num_q * G - 1 partial slots; slot of (CTA c, q-tile t) = c + t
 // (unique because CTA shares and q-tiles are both contiguous ranges of the
 // same ordered unit list).
@@ -61,15 +65,27 @@ struct WsLayout {
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Query rows up to which the bf16 warp-mma decode plans its own split.
+constexpr int kSelfMaxRows = 256;
+
+// Fused-merge counters kept at a fixed place right after the header.
+constexpr int kFixedCounters = 512;
+constexpr size_t kFixedCountersOff = 256;
+constexpr size_t kLayoutStart = kFixedCountersOff + kFixedCounters * 4;  // 2,304
+
 __host__ __device__ inline WsLayout ws_layout(int64_t num_q, int groups, int num_ctas) {
   WsLayout L;
   L.slots = (int64_t)num_ctas + num_q * groups;  // one spare slot
-  size_t off = sizeof(WsHeader);
+  size_t off = kLayoutStart;
   L.row_info = off;   off = align_up(off + (size_t)num_q * 16, 256);
   L.cta_start = off;  off = align_up(off + (size_t)num_ctas * 16, 256);
   L.lse = off;        off = align_up(off + (size_t)L.slots * kHG * 4, 256);
   L.opart = off;      off = align_up(off + (size_t)L.slots * kHG * kDc * 4, 256);
-  L.arrive = off;     off = align_up(off + (size_t)num_q * groups * 4, 256);
+  if (num_q * groups <= kFixedCounters) {
+    L.arrive = kFixedCountersOff;
+  } else {
+    L.arrive = off;   off = align_up(off + (size_t)num_q * groups * 4, 256);
+  }
   L.total = off;
   return L;
 }
@@ -103,7 +119,7 @@ __host__ __device__ inline WsLayoutTc ws_layout_tc(int64_t num_q, int groups, in
   WsLayoutTc L;
   L.qblocks_max = (num_q * groups + kQBlockTiles - 1) / kQBlockTiles + batch;
   L.slots = (int64_t)shares + L.qblocks_max;
-  size_t off = sizeof(WsHeader);
+  size_t off = kLayoutStart;  // the fixed counters belong to the 16-row layout
   L.row_info = off;  off = align_up(off + (size_t)num_q * 16, 256);
   L.seq_info = off;  off = align_up(off + (size_t)batch * 16, 256);
   L.qblock = off;    off = align_up(off + (size_t)L.qblocks_max * 16, 256);
@@ -234,6 +250,25 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// L2 policy for data read once per step (the latent cache stream): its lines
+// are evicted first, so the weights and the small per-step tensors stay in L2
+// from one step to the next.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// tma_load_2d with an L2 cache policy (from createpolicy).
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, int x, int y,
+                                                 uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
 

@@ -21,6 +21,19 @@
 // Every wait is bounded; a timeout sets MLA_DEV_TIMEOUT, all math warps leave
 // together, and the producer waits (bounded) for its copies in flight before
 // the CTA exits.
+//
+// Self-planned launches (SELF): every CTA computes the split plan from
+// seq_lens / query_start_loc itself (no plan kernel) and the math warps write
+// it to the workspace for a later merge kernel. With early streaming the
+// producer issues its first cache tiles before the preceding kernel in the
+// stream has finished (programmatic dependent launch); only the query copy
+// and every global write wait for it.
+//
+// Fused merge: a (row, head group) cut into parts is merged by the CTA that
+// finishes its part last. Parts are published in the math threads' fragment
+// order (thread i's 16 float4 at [slot][nt][i]), so each thread of the
+// merging CTA reads exactly the values it adds, coalesced, two parts per round
+// trip with their log-sum-exps in the same round trip, in CTA order.
 #include "async_copy.cuh"
 #include "common.cuh"
 #include "internal.h"
@@ -38,17 +51,17 @@ constexpr int kMathWarps = 4;
 constexpr int kThreads = (kMathWarps + 1) * 32;
 constexpr int kMathBar = 1;
 
-template <int NST>
+template <int NST, bool SELF>
 struct Smem {
   static constexpr int stage = 0;
   static constexpr int q = NST * kStageBytes;
   static constexpr int pfrag = q + 2 * kQBytes;                 // [4 warps][32 lanes] uint4
   static constexpr int smax = pfrag + kMathWarps * 32 * 16;     // [4][16] float
   static constexpr int lsum = smax + kMathWarps * 16 * 4;       // [4][16] float
-  static constexpr int merge = lsum + kMathWarps * 16 * 4;      // fused-merge scratch
-  static constexpr int info = merge + (2 * kHG + kMergeChunk * kHG) * 4;  // [NST] int2
+  static constexpr int info = lsum + kMathWarps * 16 * 4;       // [NST] int2
   static constexpr int bars = info + NST * 8;                   // full, empty, qfull, qempty
-  static constexpr int bytes = bars + (2 * NST + 4) * 8;
+  static constexpr int rows = (bars + (2 * NST + 4) * 8 + 15) / 16 * 16;  // SELF: plan
+  static constexpr int bytes = rows + (SELF ? kSelfMaxRows * 16 + 64 : 0);
   static constexpr int alloc = bytes + 1024;                    // alignment slack
 };
 
@@ -65,11 +78,11 @@ __device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool v) {
   return r != 0;
 }
 
-template <int NST>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int NST, bool SELF>
+__global__ void __maxnreg__(168)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap cache_map,
                        const __grid_constant__ CUtensorMap q_map, DecodeArgs a) {
-  using S = Smem<NST>;
+  using S = Smem<NST, SELF>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -102,12 +115,61 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&q_map);
   }
   __syncthreads();
-  // the plan and q_abs come from earlier kernels
-  pdl_wait();
+  // early: only the cache stream may start before the preceding kernel ends
+  const bool early = SELF && a.self_plan == 2;
+  if (!early) pdl_wait();  // the plan and q_abs come from earlier kernels
+  // The next kernel may launch now: its CTAs (the output projection's take
+  // 36 KB of shared memory and 168 registers a thread) fit beside a decode CTA
+  // and stage their weights while the decode runs.
   pdl_launch_dependents();
 
   SchedWalker sw;
-  const bool has_work = sw.init(ws, a.num_q, a.groups, a.num_ctas, blockIdx.x);
+  bool has_work;
+  if constexpr (SELF) {
+    int4* rows = reinterpret_cast<int4*>(sm + S::rows);
+    int* scratch = reinterpret_cast<int*>(sm + S::rows + kSelfMaxRows * 16);
+    const int total = self_plan<kThreads>(a.seq_lens, a.query_start_loc, a.batch, (int)a.num_q,
+                                          a.groups, (int64_t)a.max_blocks_per_seq * bs, rows,
+                                          scratch, status, tid);
+    has_work = sw.init_rows(rows, (int)a.num_q, a.groups, total, a.num_ctas, blockIdx.x);
+    if (warp < kMathWarps) {
+      // the workspace and o_lat may still be read by earlier kernels
+      pdl_wait();
+      if (tid == 0 && has_work) {
+        // the first query tile, as soon as q_abs is complete (the producer is
+        // busy starting the cache stream)
+        mbar_arrive_expect_tx(&qfull[0], kQBytes);
+        const int qy = sw.n * a.num_heads + sw.g * kHG;
+#pragma unroll 1
+        for (int j = 0; j < 9; ++j)
+          tma_load_2d(sm + S::q + j * kQSlabBytes, &q_map, 64 * j, qy, &qfull[0]);
+      }
+      // publish the plan (what plan_kernel would have written) for a later
+      // mla_combine or mla_decode_planned on this workspace
+      const WsLayout L = ws_layout(a.num_q, a.groups, a.num_ctas);
+      int4* cta_start = reinterpret_cast<int4*>(ws + L.cta_start);
+      if (tid == 0)
+        cta_start[blockIdx.x] = has_work ? make_int4(sw.n, sw.g, sw.k, 0) : make_int4(-1, 0, 0, 0);
+      if (blockIdx.x == 0) {
+        int4* row_info = reinterpret_cast<int4*>(ws + L.row_info);
+        for (int n = tid; n < (int)a.num_q; n += kMathWarps * 32) row_info[n] = rows[n];
+        if (tid == 0) {
+          WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+          hdr->magic = kMagic;
+          hdr->mode = 0;
+          hdr->qblocks = 0;
+          hdr->total_units = total;
+          hdr->share = sw.share;
+          hdr->num_ctas = a.num_ctas;
+          hdr->groups = a.groups;
+          hdr->num_q = (int32_t)a.num_q;
+          hdr->batch = a.batch;
+        }
+      }
+    }
+  } else {
+    has_work = sw.init(ws, a.num_q, a.groups, a.num_ctas, blockIdx.x);
+  }
   if (a.o_lat && warp < kMathWarps)
     zero_unvisited_rows(sw.row_info, sw.plan_ok, a.num_q, a.num_heads, a.o_lat, tid,
                         kMathWarps * 32);
@@ -116,7 +178,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kMathWarps) {
     // ------------------------------------------------------------ producer
-    if (lane != 0) return;
+    // The whole warp walks the schedule; lane 0 issues the copies. Block ids
+    // come from the block table 32 at a time (lane l holds entry base + l and
+    // hands it out by shuffle), so a tile never waits on a dependent load.
+    const bool leader = lane == 0;
+    const uint64_t policy = l2_evict_first_policy();
     int fills[NST];
 #pragma unroll
     for (int i = 0; i < NST; ++i) fills[i] = 0;
@@ -125,16 +191,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok_run = true;
     while (ok_run && sw.next(seg)) {
       const int qb = seg_i & 1;
-      if (seg_i >= 2 && !mbar_wait(&qempty[qb], ((seg_i >> 1) - 1) & 1)) {
-        set_status(status, MLA_DEV_TIMEOUT);
+      if (seg_i >= 2 &&
+          !__all_sync(0xffffffffu, mbar_wait(&qempty[qb], ((seg_i >> 1) - 1) & 1))) {
+        if (leader) set_status(status, MLA_DEV_TIMEOUT);
         break;
       }
       auto issue_q = [&] {
-        mbar_arrive_expect_tx(&qfull[qb], kQBytes);
-        const int qy = seg.n * a.num_heads + seg.g * kHG;
+        // (self-planned: a math thread issued the first one)
+        if (leader && !(SELF && seg_i == 0)) {
+          if (early) pdl_wait();  // q_abs comes from the preceding kernel
+          mbar_arrive_expect_tx(&qfull[qb], kQBytes);
+          const int qy = seg.n * a.num_heads + seg.g * kHG;
 #pragma unroll 1
-        for (int j = 0; j < 9; ++j)
-          tma_load_2d(sm + S::q + qb * kQBytes + j * kQSlabBytes, &q_map, 64 * j, qy, &qfull[qb]);
+          for (int j = 0; j < 9; ++j)
+            tma_load_2d(sm + S::q + qb * kQBytes + j * kQSlabBytes, &q_map, 64 * j, qy, &qfull[qb]);
+        }
         ++qfills[qb];
       };
       // the first query goes out after the first NST cache tiles
@@ -144,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       const int visible = seg.pos + 1;
       const int32_t* bt = a.block_table + (size_t)seg.b * a.max_blocks_per_seq;
+      int cache_base = -(1 << 30), cached = -1;
       for (int k = seg.k0; k < seg.k1; ++k) {
         maybe_issue_q(k);
         const int st = tile_i % NST;
@@ -151,44 +223,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int v = min(kTile, visible - tstart);
         int blk[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          blk[i] = (i < ppt && (i << bs_shift) < v) ? bt[(tstart >> bs_shift) + i] : -1;
-        if (tile_i >= NST && !mbar_wait(&empty[st], ((tile_i / NST) - 1) & 1)) {
-          set_status(status, MLA_DEV_TIMEOUT);
+        for (int i = 0; i < 4; ++i) {
+          blk[i] = -1;
+          if (i < ppt && (i << bs_shift) < v) {  // warp-uniform
+            const int bi = (tstart >> bs_shift) + i;
+            if (bi < cache_base || bi - cache_base >= 32) {
+              cache_base = bi;
+              cached = bi + lane < a.max_blocks_per_seq ? bt[bi + lane] : -1;
+            }
+            blk[i] = __shfl_sync(0xffffffffu, cached, bi - cache_base);
+          }
+        }
+        if (tile_i >= NST &&
+            !__all_sync(0xffffffffu, mbar_wait(&empty[st], ((tile_i / NST) - 1) & 1))) {
+          if (leader) set_status(status, MLA_DEV_TIMEOUT);
           ok_run = false;
           break;
         }
-        int okmask = 0;
-        uint32_t bytes = 0;
+        if (leader) {
+          int okmask = 0;
+          uint32_t bytes = 0;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          if (i < ppt && (i << bs_shift) < v) {
-            if (blk[i] >= 0 && blk[i] < a.num_blocks) {
-              okmask |= 1 << i;
-              bytes += 9u * (uint32_t)bs * 128u;
-            } else {
-              set_status(status, MLA_DEV_BAD_BLOCK);
+          for (int i = 0; i < 4; ++i) {
+            if (i < ppt && (i << bs_shift) < v) {
+              if (blk[i] >= 0 && blk[i] < a.num_blocks) {
+                okmask |= 1 << i;
+                bytes += 9u * (uint32_t)bs * 128u;
+              } else {
+                set_status(status, MLA_DEV_BAD_BLOCK);
+              }
+            }
+          }
+          info[st] = make_int2(v, okmask);
+          mbar_arrive_expect_tx(&full[st], bytes);
+          uint8_t* dst = sm + S::stage + st * kStageBytes;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (okmask & (1 << i)) {
+#pragma unroll 1
+              for (int j = 0; j < 9; ++j)
+                tma_load_2d_hint(dst + j * kSlabBytes + (i << bs_shift) * 128, &cache_map, 64 * j,
+                                 blk[i] << bs_shift, &full[st], policy);
             }
           }
         }
-        info[st] = make_int2(v, okmask);
-        mbar_arrive_expect_tx(&full[st], bytes);
-        uint8_t* dst = sm + S::stage + st * kStageBytes;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          if (okmask & (1 << i)) {
-#pragma unroll 1
-            for (int j = 0; j < 9; ++j)
-              tma_load_2d(dst + j * kSlabBytes + (i << bs_shift) * 128, &cache_map, 64 * j,
-                          blk[i] << bs_shift, &full[st]);
-          }
-        }
+        __syncwarp();
         ++fills[st];
         ++tile_i;
       }
       if (ok_run) maybe_issue_q(seg.k1);  // a first segment of fewer than NST tiles
       ++seg_i;
     }
+    if (!leader) return;
     // never leave with copies in flight
 #pragma unroll
     for (int i = 0; i < NST; ++i)
@@ -203,7 +289,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int g = lane >> 2, q = lane & 3;
   float* smax = reinterpret_cast<float*>(sm + S::smax);
   float* lsum = reinterpret_cast<float*>(sm + S::lsum);
-  float* merge_scratch = reinterpret_cast<float*>(sm + S::merge);
   uint4* pfrag = reinterpret_cast<uint4*>(sm + S::pfrag);
   const WsLayout L = ws_layout(a.num_q, a.groups, a.num_ctas);
   float* lse_out = reinterpret_cast<float*>(ws + L.lse);
@@ -356,37 +441,104 @@ __global__ void __launch_bounds__(kThreads, 1)
       L1 += lsum[ww * 16 + g + 8];
     }
     const float inv0 = L0 > 0.f ? 1.f / L0 : 0.f, inv1 = L1 > 0.f ? 1.f / L1 : 0.f;
-    const int t = seg.n * a.groups + seg.g;
-    const int64_t slot = (int64_t)blockIdx.x + t;
-    // fused merge: which CTAs share this q-tile
-    const int u_first = seg.ustart + seg.g * seg.tiles;
-    const int c_first = u_first / sw.share, c_last = (u_first + seg.tiles - 1) / sw.share;
-    const bool direct = a.o_lat != nullptr && c_first == c_last;
-    float* ob = direct ? a.o_lat + ((size_t)seg.n * a.num_heads + seg.g * kHG) * kDc + 128 * w + 2 * q
-                       : o_out + (size_t)slot * kHG * kDc + 128 * w + 2 * q;
+    const float lse0 = L0 > 0.f ? m_run0 + log2f(L0) : -INFINITY;
+    const float lse1 = L1 > 0.f ? m_run1 + log2f(L1) : -INFINITY;
 #pragma unroll
     for (int nt = 0; nt < 16; ++nt) {
-      *reinterpret_cast<float2*>(ob + (size_t)g * kDc + nt * 8) = make_float2(o[nt][0] * inv0, o[nt][1] * inv0);
-      *reinterpret_cast<float2*>(ob + (size_t)(g + 8) * kDc + nt * 8) = make_float2(o[nt][2] * inv1, o[nt][3] * inv1);
+      o[nt][0] *= inv0; o[nt][1] *= inv0;
+      o[nt][2] *= inv1; o[nt][3] *= inv1;
     }
-    if (!direct && w == 0 && q == 0) {
-      lse_out[(size_t)slot * kHG + g] = L0 > 0.f ? m_run0 + log2f(L0) : -INFINITY;
-      lse_out[(size_t)slot * kHG + g + 8] = L1 > 0.f ? m_run1 + log2f(L1) : -INFINITY;
-    }
-    if (a.o_lat != nullptr && !direct) {
-      // publish this part, count it, and merge if it was the last one
+    const int t = seg.n * a.groups + seg.g;
+    const int64_t slot = (int64_t)blockIdx.x + t;
+    // the CTAs that share this q-tile
+    const int u_first = seg.ustart + seg.g * seg.tiles;
+    const int c_first = u_first / sw.share, c_last = (u_first + seg.tiles - 1) / sw.share;
+    float* o_tile = a.o_lat ? a.o_lat + ((size_t)seg.n * a.num_heads + seg.g * kHG) * kDc : nullptr;
+    auto store_rows = [&](float* base) {  // 16 x 512 fp32 rows, row stride kDc
+      float* ob = base + 128 * w + 2 * q;
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        *reinterpret_cast<float2*>(ob + (size_t)g * kDc + nt * 8) = make_float2(o[nt][0], o[nt][1]);
+        *reinterpret_cast<float2*>(ob + (size_t)(g + 8) * kDc + nt * 8) = make_float2(o[nt][2], o[nt][3]);
+      }
+    };
+    if (o_tile == nullptr || c_first == c_last) {
+      // partial for the merge kernel, or the whole q-tile straight into o_lat
+      store_rows(o_tile ? o_tile : o_out + (size_t)slot * kHG * kDc);
+      if (!o_tile && w == 0 && q == 0) {
+        lse_out[(size_t)slot * kHG + g] = lse0;
+        lse_out[(size_t)slot * kHG + g + 8] = lse1;
+      }
+    } else {
+      // publish this part in fragment order, count it, merge if it was the last
+      float4* of = reinterpret_cast<float4*>(o_out) + (size_t)slot * 16 * 128 + tid;
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) of[nt * 128] = make_float4(o[nt][0], o[nt][1], o[nt][2], o[nt][3]);
+      if (w == 0 && q == 0) {
+        lse_out[(size_t)slot * kHG + g] = lse0;
+        lse_out[(size_t)slot * kHG + g + 8] = lse1;
+      }
+      // every thread's part is written (barrier), one thread publishes them
+      // (fence, count) and, if it counted last, orders the reads that follow
       int* arrive = reinterpret_cast<int*>(ws + L.arrive);
-      __threadfence();
       named_bar_sync(kMathBar, kMathWarps * 32);
       int* flag = reinterpret_cast<int*>(smax);  // smax is free until the next tile
-      if (tid == 0) flag[0] = atomicAdd(&arrive[t], 1) == c_last - c_first;
-      named_bar_sync(kMathBar, kMathWarps * 32);
-      const bool last = flag[0] != 0;
-      if (last) {
+      if (tid == 0) {
         __threadfence();
-        merge_qtile<kMathWarps * 32>(lse_out, o_out, (int64_t)c_first + t, c_last - c_first + 1, 1,
-                                     a.o_lat + ((size_t)seg.n * a.num_heads + seg.g * kHG) * kDc, tid,
-                                     merge_scratch, [] { named_bar_sync(kMathBar, kMathWarps * 32); });
+        const bool last = atomicAdd(&arrive[t], 1) == c_last - c_first;
+        if (last) __threadfence();
+        flag[0] = last;
+      }
+      named_bar_sync(kMathBar, kMathWarps * 32);
+      if (flag[0] != 0) {
+        // online split-softmax merge over the parts in CTA order (the same
+        // order whichever CTA merges, so repeated launches agree bit for bit):
+        // running maximum M and weight sum d per row, O accumulated in o[]
+        float M0 = -INFINITY, M1 = -INFINITY, d0 = 0.f, d1 = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+        auto add_part = [&](const float4* v, float la, float lb) {
+          const float n0 = fmaxf(M0, la), n1 = fmaxf(M1, lb);
+          const float b0 = n0 == -INFINITY ? 0.f : n0, b1 = n1 == -INFINITY ? 0.f : n1;
+          const float so0 = fast_exp2(M0 - b0), so1 = fast_exp2(M1 - b1);
+          const float sn0 = fast_exp2(la - b0), sn1 = fast_exp2(lb - b1);
+#pragma unroll
+          for (int nt = 0; nt < 16; ++nt) {
+            o[nt][0] = fmaf(o[nt][0], so0, v[nt].x * sn0);
+            o[nt][1] = fmaf(o[nt][1], so0, v[nt].y * sn0);
+            o[nt][2] = fmaf(o[nt][2], so1, v[nt].z * sn1);
+            o[nt][3] = fmaf(o[nt][3], so1, v[nt].w * sn1);
+          }
+          d0 = fmaf(d0, so0, sn0);
+          d1 = fmaf(d1, so1, sn1);
+          M0 = n0;
+          M1 = n1;
+        };
+        const float4* op4 = reinterpret_cast<const float4*>(o_out) + tid;
+        for (int c = c_first; c <= c_last; c += 2) {
+          // two parts per round trip: data and log-sum-exps together
+          const bool two = c + 1 <= c_last;
+          const int64_t sa = (int64_t)c + t, sb = two ? sa + 1 : sa;
+          float4 va[16], vb[16];
+#pragma unroll
+          for (int nt = 0; nt < 16; ++nt) {
+            va[nt] = __ldcg(op4 + ((size_t)sa * 16 + nt) * 128);
+            vb[nt] = __ldcg(op4 + ((size_t)sb * 16 + nt) * 128);
+          }
+          const float la0 = __ldcg(lse_out + (size_t)sa * kHG + g);
+          const float la1 = __ldcg(lse_out + (size_t)sa * kHG + g + 8);
+          const float lb0 = __ldcg(lse_out + (size_t)sb * kHG + g);
+          const float lb1 = __ldcg(lse_out + (size_t)sb * kHG + g + 8);
+          add_part(va, la0, la1);
+          if (two) add_part(vb, lb0, lb1);
+        }
+        const float r0 = d0 > 0.f ? 1.f / d0 : 0.f, r1 = d1 > 0.f ? 1.f / d1 : 0.f;
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) {
+          o[nt][0] *= r0; o[nt][1] *= r0;
+          o[nt][2] *= r1; o[nt][3] *= r1;
+        }
+        store_rows(o_tile);
         if (tid == 0) arrive[t] = 0;  // every part has arrived: ready for the next launch
       }
       named_bar_sync(kMathBar, kMathWarps * 32);
@@ -400,12 +552,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t launch_decode_bf16(const DecodeArgs& a, const CUtensorMap& cache_map,
                                const CUtensorMap& q_map, cudaStream_t stream) {
   constexpr int NST = 2;
-  const int smem = Smem<NST>::alloc;
-  cudaError_t e = cudaFuncSetAttribute(decode_bf16_kernel<NST>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(decode_bf16_kernel<NST>, dim3(a.num_ctas), dim3(kThreads), smem, stream,
-                    cache_map, q_map, a);
+  // the maximum shared-memory carveout keeps an SM ready for a decode CTA
+  // while small kernels before and after it share the SM
+  auto launch = [&](auto kernel, int smem) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(kernel, dim3(a.num_ctas), dim3(kThreads), smem, stream, cache_map, q_map, a);
+  };
+  if (a.self_plan) return launch(decode_bf16_kernel<NST, true>, Smem<NST, true>::alloc);
+  return launch(decode_bf16_kernel<NST, false>, Smem<NST, false>::alloc);
 }
 
 }  // namespace mla

@@ -327,6 +327,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // The whole warp walks the stages; lane 0 issues the copies. Block ids
     // come from the block table 32 at a time (one per lane, handed out by
     // shuffles), so a stage never waits on a dependent global load.
+    const uint64_t policy = l2_evict_first_policy();  // the cache is read once per step
     int stage_i = 0;
     bool ok = true;
     while (ok && sw.next(seg)) {
@@ -380,8 +381,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               const int y = blk[i] * bs + (tok % bs);
 #pragma unroll 1
               for (int j = 0; j < nslab; ++j)
-                tma_load_2d(dst + j * kSlab + (i << bsr_shift) * 128, &cache_map,
-                            64 * (slab0 + j), y, &bars[kFull0 + slot]);
+                tma_load_2d_hint(dst + j * kSlab + (i << bsr_shift) * 128, &cache_map,
+                                 64 * (slab0 + j), y, &bars[kFull0 + slot], policy);
             }
           }
         }

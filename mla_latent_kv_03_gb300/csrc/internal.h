@@ -36,6 +36,14 @@ struct DecodeArgs {
   float scale_log2;  // softmax_scale * log2(e)
   void* workspace;
   float* o_lat;      // non-null: merge the splits in the decode kernel (fused combine)
+  // Self-planned launch (bf16 warp-mma kernel, num_q <= kSelfMaxRows): the
+  // kernel derives the split plan from these itself and writes it to the
+  // workspace; self_plan = 0 follows a plan already in the workspace.
+  const int32_t* seq_lens;
+  const int32_t* query_start_loc;
+  int32_t batch;
+  int32_t self_plan;  // 0: planned; 1: self-planned; 2: self-planned, cache reads
+                      // start before the preceding kernel has finished
 };
 
 cudaError_t launch_cache_write(const mla_config& cfg, const void* c_kv, const void* k_pe,

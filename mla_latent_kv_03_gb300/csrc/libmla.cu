@@ -234,7 +234,9 @@ size_t mla_decode_workspace_size(const mla_config* cfg, int64_t num_q, int32_t b
 mla_status mla_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
   if (!workspace || ws_bytes < sizeof(WsHeader) || !aligned(workspace, 256))
     return MLA_ERR_INVALID_ARGUMENT;
-  return from_cuda(cudaMemsetAsync(workspace, 0, sizeof(WsHeader), as_stream(stream)));
+  // the header and the fused merge's fixed counters
+  const size_t n = ws_bytes < kLayoutStart ? ws_bytes : kLayoutStart;
+  return from_cuda(cudaMemsetAsync(workspace, 0, n, as_stream(stream)));
 }
 
 mla_status mla_decode_plan(const mla_config* cfg, const int32_t* seq_lens,
@@ -263,10 +265,19 @@ mla_status mla_decode_plan(const mla_config* cfg, const int32_t* seq_lens,
 
 namespace {
 
+// The bf16 warp-mma kernel plans its own split for up to kSelfMaxRows rows.
+bool use_self_plan(const mla_config* cfg, int64_t num_q, int32_t batch) {
+  return cfg->dtype == MLA_BF16 && !use_tc(cfg, num_q, batch) && num_q <= kSelfMaxRows;
+}
+
+// self_plan: 0 = follow the plan in the workspace; 1 = plan in the kernel from
+// seq_lens / query_start_loc; 2 = the same, with cache reads starting before
+// the preceding kernel has finished.
 mla_status decode_impl(const mla_config* cfg, const void* q_abs, const void* cache,
                        int64_t num_blocks, const int32_t* block_table, int32_t max_blocks_per_seq,
                        int32_t batch, int64_t num_q, void* workspace, size_t ws_bytes, float* o_lat,
-                       void* stream) {
+                       void* stream, int self_plan = 0, const int32_t* seq_lens = nullptr,
+                       const int32_t* query_start_loc = nullptr) {
   mla_status s = check_cfg(cfg);
   if (s != MLA_OK) return s;
   if (num_q < 0 || batch < 0 || num_blocks < 0 || max_blocks_per_seq < 0)
@@ -286,7 +297,8 @@ mla_status decode_impl(const mla_config* cfg, const void* q_abs, const void* cac
   cudaStream_t st = as_stream(stream);
   const double log2e = 1.4426950408889634;
   DecodeArgs da{q_abs, cache, num_blocks, block_table, max_blocks_per_seq, cfg->block_size,
-                cfg->num_heads, G, C, num_q, (float)(cfg->softmax_scale * log2e), workspace, o_lat};
+                cfg->num_heads, G, C, num_q, (float)(cfg->softmax_scale * log2e), workspace, o_lat,
+                seq_lens, query_start_loc, batch, self_plan};
   if (cfg->dtype == MLA_F32) return from_cuda(launch_decode_f32(da, st));
   // With num_blocks == 0 every block id is rejected before any copy, so the
   // map below is never used to read; it still needs a non-empty extent.
@@ -361,11 +373,54 @@ mla_status mla_decode_paged(const mla_config* cfg, const void* q_abs, const void
     return MLA_ERR_INVALID_ARGUMENT;
   if (!aligned(q_abs, 16) || !aligned(cache, 16) || !aligned(block_table, 4))
     return MLA_ERR_INVALID_ARGUMENT;
+  if (use_self_plan(cfg, num_q, batch)) {
+    // one launch: the kernel plans and writes the plan to the workspace
+    if (!aligned(seq_lens, 4) || !aligned(query_start_loc, 4)) return MLA_ERR_INVALID_ARGUMENT;
+    return decode_impl(cfg, q_abs, cache, num_blocks, block_table, max_blocks_per_seq, batch, num_q,
+                       workspace, ws_bytes, nullptr, stream, 1, seq_lens, query_start_loc);
+  }
   s = mla_decode_plan(cfg, seq_lens, query_start_loc, batch, num_q, max_blocks_per_seq, workspace,
                       ws_bytes, stream);
   if (s != MLA_OK) return s;
   return mla_decode_planned(cfg, q_abs, cache, num_blocks, block_table, max_blocks_per_seq, batch,
                             num_q, workspace, ws_bytes, stream);
+}
+
+mla_status mla_decode_paged_combine(const mla_config* cfg, const void* q_abs, const void* cache,
+                                    int64_t num_blocks, const int32_t* block_table,
+                                    int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                    const int32_t* query_start_loc, int32_t batch, int64_t num_q,
+                                    void* workspace, size_t ws_bytes, float* o_lat, void* stream) {
+  mla_status s = check_cfg(cfg);
+  if (s != MLA_OK) return s;
+  if (num_q < 0 || batch < 0 || num_blocks < 0 || max_blocks_per_seq < 0)
+    return MLA_ERR_INVALID_ARGUMENT;
+  if (num_q > kMaxRows) return MLA_ERR_UNSUPPORTED;
+  if (num_blocks * cfg->block_size > ((int64_t)1 << 31)) return MLA_ERR_UNSUPPORTED;
+  if (!workspace || !aligned(workspace, 256)) return MLA_ERR_INVALID_ARGUMENT;
+  if (num_q == 0) return MLA_OK;
+  if (!q_abs || !cache || !block_table || !seq_lens || !query_start_loc || batch == 0 || !o_lat)
+    return MLA_ERR_INVALID_ARGUMENT;
+  if (!aligned(q_abs, 16) || !aligned(cache, 16) || !aligned(block_table, 4) ||
+      !aligned(seq_lens, 4) || !aligned(query_start_loc, 4) || !aligned(o_lat, 16))
+    return MLA_ERR_INVALID_ARGUMENT;
+  if (!use_self_plan(cfg, num_q, batch)) {
+    s = mla_decode_plan(cfg, seq_lens, query_start_loc, batch, num_q, max_blocks_per_seq, workspace,
+                        ws_bytes, stream);
+    if (s != MLA_OK) return s;
+    return mla_decode_combine(cfg, q_abs, cache, num_blocks, block_table, max_blocks_per_seq,
+                              batch, num_q, workspace, ws_bytes, o_lat, stream);
+  }
+  // as in mla_decode_combine: few (row, head group) tiles per CTA are merged
+  // faster by the merge kernel than by the decode CTAs
+  const int C = decode_ctas(cfg, false);
+  const bool split_heavy = num_q * (cfg->num_heads / kHG) * 4 < C;
+  s = decode_impl(cfg, q_abs, cache, num_blocks, block_table, max_blocks_per_seq, batch, num_q,
+                  workspace, ws_bytes, split_heavy ? nullptr : o_lat, stream, 2, seq_lens,
+                  query_start_loc);
+  if (s != MLA_OK || !split_heavy) return s;
+  return from_cuda(launch_combine(workspace, cfg->num_heads / kHG, C, num_q, batch, o_lat,
+                                  as_stream(stream)));
 }
 
 mla_status mla_combine(const mla_config* cfg, const void* workspace, size_t ws_bytes,

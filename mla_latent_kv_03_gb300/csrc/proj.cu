@@ -19,8 +19,8 @@ namespace mla {
 namespace {
 
 // ---------------------------------------------------------------------------
-// absorb_q, bf16. CTA = (16*MW query rows, 128 latent columns, head h); a
-// fifth column of CTAs (blockIdx.y == 4) does the RoPE part.
+// absorb_q, bf16. CTA = (16*MW query rows, 128 latent columns, head h);
+// MW more columns of CTAs (blockIdx.y >= 4) do the RoPE part, 16 rows each.
 // The CTA's weight slice W_uk[h][col0:col0+128][0:128] (32 KB) is copied to
 // shared memory with cp.async in one go (rows of 256 B, 16-byte chunks
 // XOR-swizzled by row so ldmatrix is conflict-free); the query fragments of
@@ -40,19 +40,20 @@ __global__ void __launch_bounds__(128) absorb_bf16_kernel(
   const int g = lane >> 2, q = lane & 3;
   const int h = blockIdx.z, row0 = blockIdx.x * ROWS, col0 = blockIdx.y * 128;
 
-  if (blockIdx.y == 4) {
-    // rotate-half RoPE of q_pe into q_abs[..., 512:576] for this CTA's rows;
-    // all loads of a thread are issued before any of them is used
+  if (blockIdx.y >= 4) {
+    // rotate-half RoPE of q_pe into q_abs[..., 512:576] for 16 of this row
+    // block's rows; all loads of a thread are issued before any of them is used
     pdl_wait();
     pdl_launch_dependents();
-    constexpr int kPer = ROWS * 32 / 128;
+    constexpr int kPer = 16 * 32 / 128;
+    const int rrow0 = row0 + 16 * (blockIdx.y - 4);
     const int p = tid & 31;
     const float fhi = freq.hi[p], flo = freq.lo[p];
     float x1[kPer], x2[kPer];
     int pos[kPer];
 #pragma unroll
     for (int it = 0; it < kPer; ++it) {
-      const int r = row0 + (tid >> 5) + 4 * it;
+      const int r = rrow0 + (tid >> 5) + 4 * it;
       const bool ok = r < num_q;
       const __nv_bfloat16* x = q_pe + ((size_t)r * H + h) * kDr;
       x1[it] = ok ? __bfloat162float(x[p]) : 0.f;
@@ -61,7 +62,7 @@ __global__ void __launch_bounds__(128) absorb_bf16_kernel(
     }
 #pragma unroll
     for (int it = 0; it < kPer; ++it) {
-      const int r = row0 + (tid >> 5) + 4 * it;
+      const int r = rrow0 + (tid >> 5) + 4 * it;
       if (r >= num_q) continue;
       float cs, sn;
       rope_cos_sin(pos[it], fhi, flo, &cs, &sn);
@@ -234,6 +235,103 @@ __global__ void __launch_bounds__(128) out_proj_bf16_kernel(const float* __restr
       if (ok_hi)
         *reinterpret_cast<uint32_t*>(out + ((size_t)r_hi * H + h) * kDv + col) =
             pack_bf16(acc[nt][2], acc[nt][3]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// out_proj, bf16, fewer than 256 rows. CTA = (32 query rows, 32 output
+// columns, head h): the weight slice W_uv[h][0:512][col0:col0+32] is 32 KB,
+// so the CTA fits on an SM beside a decode CTA. Launched as the decode's
+// dependent it stages its weights while the decode still runs and then waits
+// only for o_lat, which it loads in one round (all 16 k-steps of a warp's
+// fragments at once). Warp w owns rows 16 (w & 1) .. +16 and K half w >> 1;
+// the K halves are summed through shared memory. Slice rows are 64 bytes,
+// 16-byte chunk c of row k at chunk c ^ ((k >> 1) & 3) (conflict-free
+// ldmatrix.trans).
+// ---------------------------------------------------------------------------
+constexpr int kOpSmallSmem = 512 * 64 + 2 * 16 * 32 * 4;  // 36 KB
+
+__device__ __forceinline__ uint32_t sw64(int row, int chunk) {
+  return (uint32_t)(row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4));
+}
+
+__global__ void __launch_bounds__(128) out_proj_small_kernel(const float* __restrict__ o_lat,
+                                                             const __nv_bfloat16* __restrict__ W_uv,
+                                                             __nv_bfloat16* __restrict__ out,
+                                                             int num_q, int H) {
+  extern __shared__ __align__(128) uint8_t smem_os[];
+  uint8_t* sB = smem_os;                                           // 512 x 64 B
+  float* sRed = reinterpret_cast<float*>(smem_os + 512 * 64);     // [2][16][32]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, q = lane & 3;
+  const int h = blockIdx.z, col0 = blockIdx.y * 32;
+  const int rb = warp & 1, kh = warp >> 1;
+
+  const __nv_bfloat16* src = W_uv + (size_t)h * kDc * kDv + col0;
+  for (int i = tid; i < 512 * 4; i += 128) {
+    const int r = i >> 2, ch = i & 3;
+    cp_async16(sB + sw64(r, ch), src + (size_t)r * kDv + ch * 8);
+  }
+  cp_async_commit();
+  // the weights do not depend on earlier kernels; o_lat does
+  pdl_wait();
+  pdl_launch_dependents();
+
+  const int r_lo = blockIdx.x * 32 + 16 * rb + g, r_hi = r_lo + 8;
+  const bool ok_lo = r_lo < num_q, ok_hi = r_hi < num_q;
+  const int k0 = kh * 256;
+  const float* plo = o_lat + ((size_t)r_lo * H + h) * kDc + k0 + 2 * q;
+  const float* phi = o_lat + ((size_t)r_hi * H + h) * kDc + k0 + 2 * q;
+  float2 x[16][4];
+#pragma unroll
+  for (int ks = 0; ks < 16; ++ks) {
+    const float2 z = make_float2(0.f, 0.f);
+    x[ks][0] = ok_lo ? *reinterpret_cast<const float2*>(plo + ks * 16) : z;
+    x[ks][1] = ok_hi ? *reinterpret_cast<const float2*>(phi + ks * 16) : z;
+    x[ks][2] = ok_lo ? *reinterpret_cast<const float2*>(plo + ks * 16 + 8) : z;
+    x[ks][3] = ok_hi ? *reinterpret_cast<const float2*>(phi + ks * 16 + 8) : z;
+  }
+  cp_async_wait_all();
+  __syncthreads();
+
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+#pragma unroll
+  for (int ks = 0; ks < 16; ++ks) {
+    const uint32_t a0 = pack_bf16(x[ks][0].x, x[ks][0].y), a1 = pack_bf16(x[ks][1].x, x[ks][1].y);
+    const uint32_t a2 = pack_bf16(x[ks][2].x, x[ks][2].y), a3 = pack_bf16(x[ks][3].x, x[ks][3].y);
+    const int kr = k0 + ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+    for (int np = 0; np < 2; ++np) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(smem_u32(sB + sw64(kr, np * 2 + (lane >> 4))), b0, b1, b2, b3);
+      mma_16816(acc[2 * np], a0, a1, a2, a3, b0, b1);
+      mma_16816(acc[2 * np + 1], a0, a1, a2, a3, b2, b3);
+    }
+  }
+  float* red = sRed + rb * 16 * 32;
+  if (kh == 1) {
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      *reinterpret_cast<float2*>(red + g * 32 + nt * 8 + 2 * q) = make_float2(acc[nt][0], acc[nt][1]);
+      *reinterpret_cast<float2*>(red + (g + 8) * 32 + nt * 8 + 2 * q) = make_float2(acc[nt][2], acc[nt][3]);
+    }
+  }
+  __syncthreads();
+  if (kh == 0) {
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const int c = nt * 8 + 2 * q;
+      const float2 lo = *reinterpret_cast<const float2*>(red + g * 32 + c);
+      const float2 hi = *reinterpret_cast<const float2*>(red + (g + 8) * 32 + c);
+      if (ok_lo)
+        *reinterpret_cast<uint32_t*>(out + ((size_t)r_lo * H + h) * kDv + col0 + c) =
+            pack_bf16(acc[nt][0] + lo.x, acc[nt][1] + lo.y);
+      if (ok_hi)
+        *reinterpret_cast<uint32_t*>(out + ((size_t)r_hi * H + h) * kDv + col0 + c) =
+            pack_bf16(acc[nt][2] + hi.x, acc[nt][3] + hi.y);
     }
   }
 }
@@ -691,12 +789,23 @@ cudaError_t launch_absorb_q(const mla_config& cfg, const void* q_nope, const voi
         (int)num_q, H, freq);
     return cudaGetLastError();
   }
-  if (num_q >= 256) {
-    return launch_pdl(absorb_bf16_kernel<4>, dim3((unsigned)((num_q + 63) / 64), 5, H), dim3(128), 0,
+  // More than 16 rows: 64 rows per CTA, so that a batch of up to 64 rows
+  // takes one CTA per (head, column block) and each fits on an SM beside a
+  // decode CTA (32 KB of shared memory; the carveout stays at its maximum).
+  if (num_q > 16) {
+    cudaError_t e = cudaFuncSetAttribute(absorb_bf16_kernel<4>,
+                                         cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(absorb_bf16_kernel<4>, dim3((unsigned)((num_q + 63) / 64), 8, H), dim3(128), 0,
                       stream, (const __nv_bfloat16*)q_nope, (const __nv_bfloat16*)q_pe,
                       q_positions, (const __nv_bfloat16*)W_uk, (__nv_bfloat16*)q_abs, (int)num_q,
                       H, freq);
   } else {
+    cudaError_t e = cudaFuncSetAttribute(absorb_bf16_kernel<1>,
+                                         cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
     return launch_pdl(absorb_bf16_kernel<1>, dim3((unsigned)((num_q + 15) / 16), 5, H), dim3(128), 0,
                       stream, (const __nv_bfloat16*)q_nope, (const __nv_bfloat16*)q_pe,
                       q_positions, (const __nv_bfloat16*)W_uk, (__nv_bfloat16*)q_abs, (int)num_q,
@@ -715,6 +824,17 @@ cudaError_t launch_out_proj(const mla_config& cfg, const float* o_lat, const voi
     return cudaGetLastError();
   }
   const bool big = num_q >= 256;
+  if (!big) {
+    cudaError_t e = cudaFuncSetAttribute(out_proj_small_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kOpSmallSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(out_proj_small_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(out_proj_small_kernel, dim3((unsigned)((num_q + 31) / 32), kDv / 32, H),
+                      dim3(128), kOpSmallSmem, stream, o_lat, (const __nv_bfloat16*)W_uv,
+                      (__nv_bfloat16*)out, (int)num_q, H);
+  }
   const int smem = 512 * 128 + (big ? 0 : 4 * 16 * 64 * 4);
   cudaError_t e = big ? cudaFuncSetAttribute(out_proj_bf16_kernel<4>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem)

@@ -29,7 +29,8 @@ DEV_TIMEOUT, DEV_BAD_BLOCK, DEV_BAD_SEQ, DEV_BAD_SLOT = 1, 2, 4, 8
 EXPORTS = (
     "mla_default_config", "mla_cache_write", "mla_absorb_q", "mla_decode_workspace_size",
     "mla_workspace_init", "mla_decode_paged", "mla_decode_plan", "mla_decode_planned",
-    "mla_decode_combine", "mla_decode_paged_noalloc", "mla_combine_out_proj",
+    "mla_decode_combine", "mla_decode_paged_combine", "mla_decode_paged_noalloc",
+    "mla_combine_out_proj",
     "mla_combine", "mla_out_proj",
     "mla_get_device_status", "mla_selftest_wait_timeout", "mla_status_string", "mla_version",
 )
@@ -66,6 +67,8 @@ _SIGS = {
     "mla_decode_plan": (_i32, [_cfgp, _vp, _vp, _i32, _i64, _i32, _vp, _sz, _vp]),
     "mla_decode_planned": (_i32, [_cfgp, _vp, _vp, _i64, _vp, _i32, _i32, _i64, _vp, _sz, _vp]),
     "mla_decode_combine": (_i32, [_cfgp, _vp, _vp, _i64, _vp, _i32, _i32, _i64, _vp, _sz, _vp, _vp]),
+    "mla_decode_paged_combine": (_i32, [_cfgp, _vp, _vp, _i64, _vp, _i32, _vp, _vp, _i32, _i64,
+                                        _vp, _sz, _vp, _vp]),
     "mla_decode_paged_noalloc": (_i32, [_cfgp, _vp, _vp, _i64, _vp, _i32, _vp, _vp, _i32, _i64,
                                         _vp, _vp, _vp]),
     "mla_combine": (_i32, [_cfgp, _vp, _sz, _i32, _i64, _vp, _vp]),
@@ -191,6 +194,18 @@ def mla_decode_paged(cfg: MlaConfig, q_abs, cache, block_table, seq_lens, query_
         _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(query_start_loc, torch.int32, "query_start_loc"),
         seq_lens.shape[0], q_abs.shape[0], _ptr(workspace, None, "workspace"),
         workspace.numel() * workspace.element_size(), _stream(stream)), "mla_decode_paged")
+
+
+def mla_decode_paged_combine(cfg: MlaConfig, q_abs, cache, block_table, seq_lens,
+                             query_start_loc, workspace, o_lat, stream=None) -> None:
+    dt = _torch_dtype(cfg)
+    _check(load().mla_decode_paged_combine(
+        ctypes.byref(cfg), _ptr(q_abs, dt, "q_abs"), _ptr(cache, dt, "cache"), cache.shape[0],
+        _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+        _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(query_start_loc, torch.int32, "query_start_loc"),
+        seq_lens.shape[0], q_abs.shape[0], _ptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(), _ptr(o_lat, torch.float32, "o_lat"),
+        _stream(stream)), "mla_decode_paged_combine")
 
 
 def mla_decode_plan(cfg: MlaConfig, seq_lens, query_start_loc, num_q: int,

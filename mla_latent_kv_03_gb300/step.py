@@ -105,6 +105,11 @@ class MlaDecodeStep:
         L.mla_decode_combine(self.cfg, self.q_abs, self.cache, self.block_table, self.w.batch,
                              self.workspace, self.o_lat, stream=stream)
 
+    def decode_paged_combine(self, stream=None) -> None:
+        L.mla_decode_paged_combine(self.cfg, self.q_abs, self.cache, self.block_table,
+                                   self.seq_lens, self.query_start_loc, self.workspace, self.o_lat,
+                                   stream=stream)
+
     def combine(self, stream=None) -> None:
         L.mla_combine(self.cfg, self.workspace, self.w.batch, self.o_lat, stream=stream)
 

@@ -80,6 +80,7 @@ def test_cache_write_bad_slot_sets_status_and_writes_nothing():
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("dtype,nq,heads", [("f32", 3, 16), ("bf16", 1, 16), ("bf16", 37, 32),
+                                            ("bf16", 64, 16), ("bf16", 200, 16),
                                             ("bf16", 600, 16), ("bf16", 5, 128)])
 def test_absorb_q(dtype, nq, heads):
     w = W.make("aq", [40] * nq, [1] * nq, heads, 64, dtype, seed=23)
@@ -94,7 +95,7 @@ def test_absorb_q(dtype, nq, heads):
 
 
 @pytest.mark.parametrize("dtype,nq,heads", [("f32", 3, 16), ("bf16", 1, 16), ("bf16", 64, 16),
-                                            ("bf16", 600, 16), ("bf16", 9, 128)])
+                                            ("bf16", 37, 32), ("bf16", 600, 16), ("bf16", 9, 128)])
 def test_out_proj(dtype, nq, heads):
     w = W.make("op", [8] * nq, [1] * nq, heads, 64, dtype, seed=24)
     s = MlaDecodeStep(w, device=DEV)
@@ -236,6 +237,123 @@ def test_bounded_wait_times_out_and_context_survives():
     s.populate()
     max_abs, _ = errors(to_f64(s.step()), ref_out(w))
     assert max_abs <= 1e-4
+
+
+# ---------------------------------------------------------------------------
+# the self-planned decode: one launch plans, decodes (and merges)
+# ---------------------------------------------------------------------------
+
+SELF_CASES = ["bs16_bf16", "bs32_h32_bf16", "empty_seq_bf16", "ragged_tails_bf16"]
+
+
+def _plan_bytes(s):
+    """Header fields, row_info and cta_start of the decode workspace (the
+    16-row layout: fixed counters end at 2,304 bytes, then row_info[num_q],
+    then cta_start[num_ctas], each 256-byte aligned)."""
+    ws = s.workspace.cpu().numpy()
+    nq = s.w.num_q
+    hdr = ws[4:40].view(np.int32)
+    ctas = int(hdr[4])
+    ri0 = 2304
+    cs0 = ri0 + (nq * 16 + 255) // 256 * 256
+    return hdr.copy(), ws[ri0:ri0 + nq * 16].view(np.int32).copy(), ws[cs0:cs0 + ctas * 16].view(np.int32).copy()
+
+
+@pytest.mark.parametrize("name", SELF_CASES)
+@pytest.mark.parametrize("num_ctas", [0, 7, 500])
+def test_self_planned_decode_writes_the_plan_kernels_plan(name, num_ctas):
+    w = SMALL[name]()
+    a = MlaDecodeStep(w, device=DEV, num_ctas=num_ctas)
+    b = MlaDecodeStep(w, device=DEV, num_ctas=num_ctas)
+    a.populate()
+    a.absorb()
+    a.decode()                      # one launch: the kernel plans for itself
+    b.plan()                        # the plan kernel
+    torch.cuda.synchronize()
+    assert a.device_status()[0][0] == 0
+    for x, y, what in zip(_plan_bytes(a), _plan_bytes(b), ("header", "row_info", "cta_start")):
+        assert np.array_equal(x, y), f"{what} differs from the plan kernel's"
+    # and the partials it left are the planned decode's, bit for bit
+    a.combine()
+    o_self = a.o_lat.clone()
+    a.decode_planned()
+    a.combine()
+    torch.cuda.synchronize()
+    assert torch.equal(o_self, a.o_lat)
+
+
+@pytest.mark.parametrize("name", SELF_CASES)
+@pytest.mark.parametrize("num_ctas", [0, 7, 500])
+def test_decode_paged_combine_matches_oracle_and_repeats(name, num_ctas):
+    w = SMALL[name]()
+    s = MlaDecodeStep(w, device=DEV, num_ctas=num_ctas)
+    s.populate()
+    s.absorb()
+    outs = []
+    for _ in range(3):
+        s.o_lat.fill_(float("nan"))                  # rows nobody visits must become 0
+        s.decode_paged_combine()
+        outs.append(s.o_lat.clone())
+    torch.cuda.synchronize()
+    assert s.device_status()[0][0] == 0
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2]), "counters not reset"
+    fused = to_f64(outs[0])
+    ref = ref_o_lat_from(w, to_f64(s.cache), to_f64(s.q_abs))
+    empty = np.isnan(ref).all(axis=(1, 2))
+    assert np.all(fused[empty] == 0)
+    assert_close(fused, ref, w.dtype, f"decode_paged_combine o_lat {name}")
+    s.decode_planned()
+    s.combine()
+    np.testing.assert_allclose(fused, to_f64(s.o_lat), rtol=0, atol=1e-5)
+
+
+@pytest.mark.parametrize("num_ctas", [0, 40])
+def test_decode_paged_combine_serving_shape(num_ctas):
+    # 16 rows of 4,096 tokens: every row is cut into several parts (about 7
+    # with one CTA per SM, 2 with 40 CTAs), merged by the CTA that finishes last
+    w = W.make("srv16", [4096] * 16, [1] * 16, 16, 64, "bf16", seed=47)
+    s = MlaDecodeStep(w, device=DEV, num_ctas=num_ctas)
+    s.populate()
+    s.absorb()
+    s.decode_paged_combine()
+    s.out_proj()
+    torch.cuda.synchronize()
+    assert s.device_status()[0][0] == 0
+    ref = ref_o_lat_from(w, to_f64(s.cache), to_f64(s.q_abs))
+    assert_close(to_f64(s.o_lat), ref, "bf16", f"o_lat, num_ctas={num_ctas}")
+    assert_close(to_f64(s.out), ref_out(w), "bf16", f"out, num_ctas={num_ctas}")
+
+
+def test_decode_paged_combine_many_parts():
+    # the 3,000-token row (47 tiles, 2 per CTA) is cut into 24 parts: twelve
+    # rounds of two parts in the merging CTA
+    lens = [3000] + [1] * 9 + [333, 64]
+    w = W.make("many_self", lens, [1] * len(lens), 16, 64, "bf16", seed=48)
+    s = MlaDecodeStep(w, device=DEV, num_ctas=40)
+    s.populate()
+    s.absorb()
+    s.decode_paged_combine()
+    s.out_proj()
+    torch.cuda.synchronize()
+    assert s.device_status()[0][0] == 0
+    assert_close(to_f64(s.out), ref_out(w), "bf16", "self-planned, 24 parts")
+
+
+def test_decode_paged_combine_reports_a_bad_sequence():
+    w = W.make("badseq_self", [50, 60], [1, 1], 16, 64, "bf16", seed=49)
+    s = MlaDecodeStep(w, device=DEV)
+    s.populate()
+    s.absorb()
+    s.seq_lens[0] = 0                                 # one query row, zero tokens
+    s.o_lat.fill_(float("nan"))
+    s.decode_paged_combine()
+    (st, bits), _ = s.device_status()
+    assert st == 7 and bits & L.DEV_BAD_SEQ
+    got = to_f64(s.o_lat)
+    assert np.all(got[0] == 0)
+    ref = ref_o_lat_from(w, to_f64(s.cache), to_f64(s.q_abs))
+    assert_close(got[1:2], ref[1:2], "bf16", "other sequence")
+    L.mla_workspace_init(s.workspace)                 # re-init after a device error
 
 
 # ---------------------------------------------------------------------------
