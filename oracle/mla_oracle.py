@@ -240,6 +240,53 @@ def naive_attention(c_hat, k_rot, q_nope, q_rot, W_uk, W_uv, q_positions,
     return np.where((den > 0)[..., None], out, 0.0)
 
 
+def naive_kv_rows(c_hat, k_rot, W_uk, W_uv) -> np.ndarray:
+    """[MI17 "版本 1: MLAAttentionNaive"]: the rows the full key/value cache holds.
+
+    For token t and head h: [K_nope[t,h] (128) || k_rot[t] (64) || V[t,h] (128)]
+    with K_nope[t,h] = c_hat[t] @ W_uk[h] and V[t,h] = c_hat[t] @ W_uv[h]: the
+    page caches the whole key (nope || rope) and the value of every head, 16 x
+    (192 + 128) x 2 = 10,240 bytes/token/layer in bf16. "版本 2" re-expands the
+    latent cache into exactly these rows at every step.  -> [L, H, 320]
+    """
+    c_hat, k_rot = _f64(c_hat), _f64(k_rot)
+    W_uk, W_uv = _f64(W_uk), _f64(W_uv)
+    L, H = c_hat.shape[0], W_uk.shape[0]
+    k_nope = np.einsum("tc,hcd->thd", c_hat, W_uk)
+    v = np.einsum("tc,hcv->thv", c_hat, W_uv)
+    rope_part = np.broadcast_to(k_rot[:, None, :], (L, H, k_rot.shape[-1]))
+    return np.concatenate([k_nope, rope_part, v], axis=-1)
+
+
+def expanded_attention(kv_rows, q, q_positions, scale: float,
+                       nope_dim: int = QK_NOPE_HEAD_DIM,
+                       rope_dim: int = QK_ROPE_HEAD_DIM) -> np.ndarray:
+    """The naive form's attention step over expanded rows ([MI17 "版本 1"]).
+
+    kv_rows [L, H, nope+rope+v] = [K_nope || k_rot || V] per head (as
+    naive_kv_rows), q [n, H, nope+rope] = [q_nope || q_rot];
+    out[n,h] = softmax_t(scale * q[n,h] . K[t,h], causal) @ V[t,h] -> [n, H, v].
+    """
+    kv_rows, q = _f64(kv_rows), _f64(q)
+    kd = nope_dim + rope_dim
+    K, V = kv_rows[..., :kd], kv_rows[..., kd:]
+    n, H = q.shape[0], q.shape[1]
+    L = kv_rows.shape[0]
+    out = np.zeros((n, H, V.shape[-1]))
+    if L == 0 or n == 0:
+        return out
+    s = scale * np.einsum("nhe,the->nht", q, K)
+    vis = causal_visible(q_positions, L)[:, None, :]
+    s = np.where(vis, s, -np.inf)
+    any_vis = vis.any(axis=-1)
+    m = np.where(any_vis, s.max(axis=-1), 0.0)
+    p = np.where(vis, np.exp(s - m[..., None]), 0.0)
+    den = p.sum(axis=-1)
+    safe = np.where(den > 0, den, 1.0)
+    out = np.einsum("nht,thv->nhv", p / safe[..., None], V)
+    return np.where((den > 0)[..., None], out, 0.0)
+
+
 def mla_sequence_naive(c_kv_raw, k_pe_raw, kv_positions, q_nope, q_pe,
                        q_positions, W_uk, W_uv, rms_weight, eps: float,
                        base: float, scale: float) -> np.ndarray:

@@ -215,14 +215,33 @@ def _check_against_brute_force(case):
     bf_out, bf_lse = _brute_force(*args)
     naive = O.mla_sequence_naive(*args)
     absorbed, _, lse = O.mla_sequence_absorbed(*args)
-    return (float(np.max(np.abs(naive - bf_out))), float(np.max(np.abs(absorbed - bf_out))),
-            float(np.max(np.abs(lse - bf_lse))))
+    # the full key/value cache form: expanded rows, then plain attention
+    c_hat = O.rms_norm(case["c_kv_raw"], case["rms_weight"], case["eps"])
+    k_rot = O.rope(case["k_pe_raw"], case["kv_positions"], case["base"])
+    rows = O.naive_kv_rows(c_hat, k_rot, case["W_uk"], case["W_uv"])
+    q = np.concatenate([case["q_nope"], O.rope(case["q_pe"], case["q_positions"], case["base"])], -1)
+    expanded = O.expanded_attention(rows, q, case["q_positions"], case["scale"],
+                                    nope_dim=case["q_nope"].shape[-1],
+                                    rope_dim=case["q_pe"].shape[-1])
+    return (max(float(np.max(np.abs(naive - bf_out))), float(np.max(np.abs(expanded - bf_out)))),
+            float(np.max(np.abs(absorbed - bf_out))), float(np.max(np.abs(lse - bf_lse))))
 
 
 @pytest.mark.parametrize("seed", [7, 8])
 def test_oracle_matches_50_digit_brute_force(seed):
     e_naive, e_abs, e_lse = _check_against_brute_force(_tiny_case(seed))
     assert e_naive < 1e-13 and e_abs < 1e-13 and e_lse < 1e-13, (e_naive, e_abs, e_lse)
+
+
+def test_naive_rows_are_the_pages_10240_bytes():
+    """mini-infer-17, "版本 1": 16 x (192 + 128) x 2 = 10,240 bytes/token/layer."""
+    rng = np.random.default_rng(3)
+    rows = O.naive_kv_rows(rng.standard_normal((2, 512)), rng.standard_normal((2, 64)),
+                           rng.standard_normal((16, 512, 128)), rng.standard_normal((16, 512, 128)))
+    assert rows.shape == (2, 16, 320)
+    assert rows.shape[1] * rows.shape[2] * 2 == golden("naive_bytes_per_token_layer")
+    # every head carries the same shared rope key
+    assert np.array_equal(rows[:, 0, 128:192], rows[:, 15, 128:192])
 
 
 # ---------------------------------------------------------------------------
@@ -399,7 +418,15 @@ def _visible_off_by_one(q_positions, kv_len):
     return t[None, :] < np.asarray(q_positions)[:, None]
 
 
+def _naive_rows_value_from_uk(c_hat, k_rot, W_uk, W_uv):
+    c_hat, k_rot = np.asarray(c_hat, np.float64), np.asarray(k_rot, np.float64)
+    L, H = c_hat.shape[0], np.asarray(W_uk).shape[0]
+    k = np.einsum("tc,hcd->thd", c_hat, W_uk)
+    return np.concatenate([k, np.broadcast_to(k_rot[:, None, :], (L, H, k_rot.shape[-1])), k], -1)
+
+
 MUTANTS = {
+    "naive_rows_value_from_W_uk": ("naive_kv_rows", _naive_rows_value_from_uk),
     "rope_interleaved_pairs": ("rope", _rope_interleaved),
     "rope_wrong_direction": ("rope", _rope_sign_flipped),
     "rmsnorm_sum_not_mean": ("rms_norm", _rms_no_eps_sum),
