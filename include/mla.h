@@ -266,6 +266,65 @@ mla_status mla_out_proj(const mla_config* cfg, const float* o_lat, const void* W
                         void* out, int64_t num_q, void* stream);
 
 /*
+ * The pages' other two forms of the same attention, for their comparison of
+ * the three ([MI17] "版本 1: MLAAttentionNaive", "版本 2:
+ * MLAAttentionLatentCache", "实验结果"). bf16 only (MLA_ERR_UNSUPPORTED
+ * otherwise). Their cache holds, for every slot and head h, the row
+ *   [K_nope (128) || k_rot (64) || V (128)],
+ *   K_nope = c_hat W_uk[h], V = c_hat W_uv[h], k_rot the shared rope key,
+ * in kv_cache [num_blocks, block_size, H, 320] bf16 (10,240 bytes per token
+ * for 16 heads). The expansion runs on tcgen05 tensor cores (bf16 operands,
+ * fp32 accumulation, one rounding to bf16).
+ *
+ * mla_naive_workspace_size -- bytes of the workspace these calls need for up
+ * to num_q query rows, blocks of max_blocks_per_seq entries and num_tokens new
+ * tokens. Its first 4 bytes are the device status word (MLA_DEV_* bits, read
+ * with mla_get_device_status); zero it (mla_workspace_init) once.
+ */
+size_t mla_naive_workspace_size(const mla_config* cfg, int64_t num_q, int32_t max_blocks_per_seq,
+                                int64_t num_tokens);
+
+/*
+ * mla_naive_cache_write -- version 1's cache write: RMSNorm and RoPE as
+ * mla_cache_write, then the expansion of each new token into the rows of
+ * every head at slot_mapping[t] (< 0: skipped; >= num_blocks * block_size:
+ * MLA_DEV_BAD_SLOT). Same inputs as mla_cache_write plus W_uk, W_uv
+ * [H, 512, 128].
+ */
+mla_status mla_naive_cache_write(const mla_config* cfg, const void* c_kv, const void* k_pe,
+                                 const int32_t* positions, const int64_t* slot_mapping,
+                                 int64_t num_tokens, const void* rms_weight, const void* W_uk,
+                                 const void* W_uv, void* kv_cache, int64_t num_blocks,
+                                 void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * mla_latent_expand -- version 2's per-step re-expansion: every cached token
+ * of every sequence (the latent cache and block table of mla_decode_paged) is
+ * expanded into kv_cache at the same slot. Followed by mla_naive_decode on
+ * kv_cache, it is version 2's attention.
+ */
+mla_status mla_latent_expand(const mla_config* cfg, const void* cache, int64_t num_blocks,
+                             const int32_t* block_table, int32_t max_blocks_per_seq,
+                             const int32_t* seq_lens, int32_t batch, const void* W_uk,
+                             const void* W_uv, void* kv_cache, void* workspace, size_t ws_bytes,
+                             void* stream);
+
+/*
+ * mla_naive_decode -- attention over the expanded rows:
+ *   q[n,h]   = [q_nope[n,h] || RoPE(q_pe[n,h], q_positions[n])]
+ *   out[n,h] = sum_t softmax_t(softmax_scale * q[n,h] . K[t,h]) V[t,h]
+ * over the causal visible tokens of row n's sequence (the conventions of
+ * mla_decode_paged). q_nope [num_q, H, 128], q_pe [num_q, H, 64] bf16;
+ * out [num_q, H, 128] bf16 (zeros for a row that sees no token).
+ */
+mla_status mla_naive_decode(const mla_config* cfg, const void* q_nope, const void* q_pe,
+                            const int32_t* q_positions, const void* kv_cache, int64_t num_blocks,
+                            const int32_t* block_table, int32_t max_blocks_per_seq,
+                            const int32_t* seq_lens, const int32_t* query_start_loc,
+                            int32_t batch, int64_t num_q, void* workspace, size_t ws_bytes,
+                            void* out, void* stream);
+
+/*
  * mla_decode_paged_noalloc -- mla_decode_paged followed by mla_combine for
  * callers that cannot allocate device memory (a step callback with a fixed
  * memory budget, a real-time loop where cudaMalloc would stall or fail, a

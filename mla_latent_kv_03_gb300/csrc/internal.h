@@ -96,4 +96,12 @@ cudaError_t launch_combine_out_proj(const mla_config& cfg, const void* workspace
 cudaError_t launch_wait_timeout_selftest(uint32_t* status, int64_t timeout_ns,
                                          cudaStream_t stream);
 
+// Shared host helpers of libmla.cu: the configuration check of every call and
+// the TMA descriptors (bf16, 128-byte swizzle) of 576-value rows and of a
+// row-major [rows, cols] matrix.
+mla_status validate_config(const mla_config* cfg);
+bool encode_row_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows);
+bool encode_map_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                   uint32_t box_cols, uint32_t box_rows);
+
 }  // namespace mla

@@ -146,6 +146,17 @@ inline mla_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MLA_OK : 
 
 }  // namespace
 
+namespace mla {
+mla_status validate_config(const mla_config* cfg) { return check_cfg(cfg); }
+bool encode_row_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
+  return make_row_map(map, base, rows, box_rows);
+}
+bool encode_map_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                   uint32_t box_cols, uint32_t box_rows) {
+  return make_map_2d(map, base, cols, rows, box_cols, box_rows);
+}
+}  // namespace mla
+
 extern "C" {
 
 int32_t mla_version(void) { return 1; }

@@ -1,0 +1,713 @@
+// The pages' two other forms of the same attention, for their three-way
+// comparison ("mini-infer-17: MLA Attention", sections "版本 1:
+// MLAAttentionNaive", "版本 2: MLAAttentionLatentCache" and "实验结果"):
+//   version 1 caches the expanded key and value of every head:
+//     row (token t, head h) = [K_nope (128) || k_rot (64) || V (128)],
+//     K_nope = c_hat W_uk[h], V = c_hat W_uv[h]  (16 x 320 x 2 = 10,240 B/token)
+//   version 2 caches the latent (as the absorbed form does) and re-expands
+//     every cached token into those rows at every step, then attends.
+//
+// Kernels:
+//   wt_prep_kernel      W_uk, W_uv [H, 512, 128] -> Wt [H, 256, 512] (K-major
+//                       B operand of the expansion: rows 0-127 W_uk^T, 128-255 W_uv^T)
+//   expand_tc_kernel    tcgen05 GEMM: 128 latent rows x 512 -> 256 columns of
+//                       one head (K_nope || V) in TMEM, plus the shared k_rot,
+//                       written as the rows above
+//   naive_decode_kernel split-KV attention of one (query row, head) per warp
+//                       over the expanded rows (HBM-bound: 640 B per token
+//                       and head)
+//   naive_merge_kernel  the split-softmax merge into out [num_q, H, 128]
+#include "async_copy.cuh"
+#include "common.cuh"
+#include "internal.h"
+#include "tcgen05.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kNv = 320;  // one (token, head) row of the expanded cache
+
+// ---------------------------------------------------------------------------
+// Wt[h][j][c] = W_uk[h][c][j] (j < 128), W_uv[h][c][j - 128] (j >= 128).
+// 32 x 32 tiles through shared memory; grid (512 / 32, 256 / 32, H).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) wt_prep_kernel(const __nv_bfloat16* __restrict__ W_uk,
+                                                      const __nv_bfloat16* __restrict__ W_uv,
+                                                      __nv_bfloat16* __restrict__ Wt) {
+  __shared__ __nv_bfloat16 t[32][33];
+  const int c0 = blockIdx.x * 32, j0 = blockIdx.y * 32, h = blockIdx.z;
+  const __nv_bfloat16* W = j0 < kDn ? W_uk : W_uv;
+  const int jj0 = j0 < kDn ? j0 : j0 - kDn;
+  pdl_wait();  // Wt lives in a workspace an earlier kernel may still read
+  pdl_launch_dependents();
+  for (int r = threadIdx.y; r < 32; r += 8)
+    t[r][threadIdx.x] = W[((size_t)h * kDc + c0 + r) * kDn + jj0 + threadIdx.x];
+  __syncthreads();
+  for (int r = threadIdx.y; r < 32; r += 8)
+    Wt[((size_t)h * 256 + j0 + r) * kDc + c0 + threadIdx.x] = t[threadIdx.x][r];
+}
+
+__global__ void iota_kernel(int64_t* __restrict__ out, int64_t n) {
+  pdl_wait();
+  pdl_launch_dependents();
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    out[i] = i;
+}
+
+// ---------------------------------------------------------------------------
+// expand_tc_kernel. CTA = (128 source rows, head h). D[r, j] = sum_c X[r, c]
+// Wt[h][j][c] over the 512 latent columns in 8 chunks of 64: the X chunk (128
+// rows, by TMA boxes of box_rows rows: pages of the latent cache, or slices of
+// a dense buffer) and the Wt chunk (256 rows) stream through a 2-stage ring,
+// 4 tcgen05.mma (M 128, N 256, K 16) per chunk into a 256-column TMEM
+// accumulator. Epilogue: thread r (TMEM lane r) converts row r to bf16 and
+// writes [K_nope || k_rot || V] of (slot, h), k_rot copied from the source
+// row's rope columns. 97 KB of shared memory and 256 TMEM columns: two CTAs
+// per SM, one's epilogue under the other's MMAs.
+//   mode 0: rows [128 x, 128 x + 128) of a dense [num_rows, 576] buffer, row t
+//           written to slot dst_slots[t] (< 0: skipped).
+//   mode 1: tokens [128 k, 128 k + 128) of sequence b (x = b * tiles_per_seq
+//           + k), read from and written to the same slot of the block table.
+// ---------------------------------------------------------------------------
+struct ExArgs {
+  const int64_t* dst_slots;
+  int64_t num_rows;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  int32_t max_blocks_per_seq;
+  int32_t tiles_per_seq;
+  int64_t num_blocks;          // latent cache blocks (mode 1)
+  int32_t block_size;
+  int32_t box_rows;            // rows of one source TMA box
+  int32_t H;
+  int32_t mode;
+  const __nv_bfloat16* src;    // the rows the source map views ([rows, 576])
+  __nv_bfloat16* kv;           // [num_slots, H, 320]
+  int64_t num_slots;
+  uint32_t* status;
+};
+
+constexpr int kExRows = 128;
+constexpr int kExA = kExRows * 128;  // 16 KB: 128 rows x 64 columns
+constexpr int kExB = 256 * 128;      // 32 KB: 256 weight rows x 64 columns
+constexpr int kExThreads = 128;
+
+struct ExSmem {
+  static constexpr int a = 0;                    // [2]
+  static constexpr int b = a + 2 * kExA;         // [2]
+  static constexpr int dst = b + 2 * kExB;       // int[128]: destination slot (-1: none)
+  static constexpr int src = dst + kExRows * 4;  // int[128]: source row
+  static constexpr int box = src + kExRows * 4;  // int[8]: first source row of each box
+  static constexpr int bars = box + 32;          // full[2], empty[2], done
+  static constexpr int misc = bars + 5 * 8;      // tmem base, valid-row count
+  static constexpr int bytes = misc + 16;
+  static constexpr int alloc = bytes + 1024;
+};
+
+__global__ void __launch_bounds__(kExThreads, 2) expand_tc_kernel(
+    const __grid_constant__ CUtensorMap src_map, const __grid_constant__ CUtensorMap wt_map,
+    ExArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int h = blockIdx.y;
+  int* s_dst = reinterpret_cast<int*>(sm + ExSmem::dst);
+  int* s_src = reinterpret_cast<int*>(sm + ExSmem::src);
+  int* s_box = reinterpret_cast<int*>(sm + ExSmem::box);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + ExSmem::bars);
+  uint64_t* empty = full + 2;
+  uint64_t* done = full + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + ExSmem::misc);
+  int* s_nvalid = reinterpret_cast<int*>(sm + ExSmem::misc + 4);
+  const int nbox = kExRows / a.box_rows;
+
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(done, 1);
+    fence_mbar_init();
+    prefetch_tensormap(&src_map);
+    prefetch_tensormap(&wt_map);
+    *s_nvalid = 0;
+  }
+  // the source rows, Wt and the destination come from or go to earlier kernels
+  pdl_wait();
+  pdl_launch_dependents();
+  __syncthreads();
+
+  // ---- where each of the 128 rows comes from and goes to
+  {
+    const int r = tid;
+    int dst = -1, src = 0;
+    if (a.mode == 0) {
+      const int64_t t = (int64_t)blockIdx.x * kExRows + r;
+      if (t < a.num_rows) {
+        const int64_t slot = a.dst_slots[t];
+        if (slot >= a.num_slots) {
+          set_status(a.status, MLA_DEV_BAD_SLOT);
+        } else if (slot >= 0) {
+          dst = (int)slot;
+        }
+        src = (int)t;
+      }
+      if (r < nbox) s_box[r] = (int)((int64_t)blockIdx.x * kExRows + r * a.box_rows);
+    } else {
+      const int b = blockIdx.x / a.tiles_per_seq, k = blockIdx.x % a.tiles_per_seq;
+      const int len = a.seq_lens[b];
+      const int64_t max_len = (int64_t)a.max_blocks_per_seq * a.block_size;
+      const bool bad = len < 0 || (int64_t)len > max_len;
+      if (bad && k == 0 && h == 0 && r == 0) set_status(a.status, MLA_DEV_BAD_SEQ);
+      const int tok = k * kExRows + r;
+      const int32_t* bt = a.block_table + (size_t)b * a.max_blocks_per_seq;
+      if (!bad && tok < len) {
+        const int page = bt[tok / a.block_size];
+        if (page >= 0 && page < a.num_blocks) {
+          dst = src = page * a.block_size + tok % a.block_size;
+        } else if (tok % a.block_size == 0 && h == 0) {
+          set_status(a.status, MLA_DEV_BAD_BLOCK);
+        }
+      }
+      if (r < nbox) {
+        const int t0 = k * kExRows + r * a.box_rows;
+        int y = 0;  // boxes without a valid page read row 0; their rows are not written
+        if (!bad && t0 < len) {
+          const int page = bt[t0 / a.block_size];
+          if (page >= 0 && page < a.num_blocks) y = page * a.block_size;
+        }
+        s_box[r] = y;
+      }
+    }
+    s_dst[r] = dst;
+    s_src[r] = src;
+    if (dst >= 0) atomicAdd(s_nvalid, 1);
+  }
+  __syncthreads();
+  if (*s_nvalid == 0) return;  // nothing to write (before any copy or TMEM use)
+
+  if (warp == 0) tc::alloc(tmem_slot, 256);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  int fills[2] = {0, 0};
+  bool ok = true;
+  if (tid == 0) {
+    // ------------------------------------------------------------ producer
+#pragma unroll 1
+    for (int kc = 0; kc < 8; ++kc) {
+      const int st = kc & 1;
+      if (kc >= 2 && !mbar_wait(&empty[st], ((kc >> 1) - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      mbar_arrive_expect_tx(&full[st], kExA + kExB);
+      uint8_t* da = sm + ExSmem::a + st * kExA;
+      for (int i = 0; i < nbox; ++i)
+        tma_load_2d(da + i * a.box_rows * 128, &src_map, 64 * kc, s_box[i], &full[st]);
+      tma_load_2d(sm + ExSmem::b + st * kExB, &wt_map, 64 * kc, h * 256, &full[st]);
+      ++fills[st];
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issue
+    constexpr uint32_t kId = tc::idesc_bf16(kExRows, 256, false, false);
+    const bool leader = tc::elect_one();
+#pragma unroll 1
+    for (int kc = 0; kc < 8; ++kc) {
+      const int st = kc & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&full[st], (kc >> 1) & 1));
+      if (!ok) break;
+      if (leader) {
+        tc::fence_after_sync();
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t ad = tc::smem_desc(smem_u32(sm + ExSmem::a + st * kExA) + 32 * ks, 16,
+                                            1024, tc::kSwizzle128);
+          const uint64_t bd = tc::smem_desc(smem_u32(sm + ExSmem::b + st * kExB) + 32 * ks, 16,
+                                            1024, tc::kSwizzle128);
+          tc::mma_bf16(tmem, ad, bd, kId, kc > 0 || ks > 0);
+        }
+        tc::commit(&empty[st]);
+      }
+      __syncwarp();
+    }
+    if (ok && leader) tc::commit(done);
+    __syncwarp();
+  }
+  // every copy and MMA must land before TMEM is read or freed
+  const bool okd = __syncthreads_and(mbar_wait(done, 0) && ok) != 0;
+  if (!okd) {
+    if (tid == 0) {
+      set_status(a.status, MLA_DEV_TIMEOUT);
+      for (int i = 0; i < 2; ++i)
+        if (fills[i] > 0) mbar_wait(&full[i], (fills[i] - 1) & 1);
+    }
+  }
+  tc::fence_after_sync();
+  if (okd) {
+    // ------------------------------------------------------------ epilogue
+    const int r = tid;
+    const int dst = s_dst[r];
+    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+    __nv_bfloat16* out = a.kv + ((size_t)(dst < 0 ? 0 : dst) * a.H + h) * kNv;
+#pragma unroll 1
+    for (int cb = 0; cb < 8; ++cb) {
+      uint32_t v[32];
+      tc::ld32(trow + 32 * cb, v);  // every lane: the load is warp-collective
+      tc::wait_ld();
+      if (dst >= 0) {
+        uint4* o = reinterpret_cast<uint4*>(out + (cb < 4 ? 32 * cb : 192 + 32 * (cb - 4)));
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          o[q] = make_uint4(pack_bf16(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                            pack_bf16(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                            pack_bf16(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                            pack_bf16(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+      }
+    }
+    if (dst >= 0) {
+      // the shared rope key, as the source row holds it
+      const uint4* kr = reinterpret_cast<const uint4*>(a.src + (size_t)s_src[r] * kRow + kDc);
+      uint4* o = reinterpret_cast<uint4*>(out + kDn);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) o[q] = kr[q];
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 0) tc::dealloc(tmem, 256);
+}
+
+// ---------------------------------------------------------------------------
+// naive_decode_kernel. Warp = (query row n, head h, split s); CTA = 8 heads of
+// one (row, split). The query [q_nope || RoPE(q_pe)] sits in shared memory;
+// per 32 tokens, lane l scores token l against its 192-value key (24 16-byte
+// loads of one row), the warp updates the online softmax, then lanes own 4 of
+// the 128 value dimensions and accumulate the 32 weighted value rows (256
+// contiguous bytes per token across the warp). Output: the split's
+// normalised partial and base-2 log-sum-exp.
+// ---------------------------------------------------------------------------
+struct NdArgs {
+  const __nv_bfloat16* q_nope;  // [num_q, H, 128]
+  const __nv_bfloat16* q_pe;    // [num_q, H, 64]
+  const int32_t* q_positions;
+  const __nv_bfloat16* kv;      // [num_slots, H, 320]
+  int64_t num_blocks;
+  const int32_t* block_table;
+  int32_t max_blocks_per_seq;
+  int32_t block_size;
+  const int32_t* seq_lens;
+  const int32_t* query_start_loc;
+  int32_t batch;
+  int32_t num_q;
+  int32_t H;
+  int32_t splits;
+  int32_t split_len;  // a multiple of 32
+  float scale_log2;
+  RopeFreq freq;
+  float* part_o;      // [num_q, H, splits, 128]
+  float* part_lse;    // [num_q, H, splits]
+  uint32_t* status;
+};
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+__global__ void __launch_bounds__(256) naive_decode_kernel(NdArgs a) {
+  __shared__ float sq[8][kDn + kDr];
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  const int n = blockIdx.x, s = blockIdx.y, h = blockIdx.z * 8 + w;
+  pdl_wait();  // the cache and the query come from earlier kernels
+  pdl_launch_dependents();
+
+  // the sequence of row n: the last b with query_start_loc[b] <= n
+  const int32_t* qsl = a.query_start_loc;
+  int lo = 0, hi = a.batch;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (qsl[mid] <= n) lo = mid; else hi = mid;
+  }
+  const int b = lo, q0 = qsl[b], q1 = qsl[b + 1], len = a.seq_lens[b], ql = q1 - q0;
+  const bool covered = q0 <= n && n < q1;
+  const bool bad = !covered || ql > len || len < 0 ||
+                   (int64_t)len > (int64_t)a.max_blocks_per_seq * a.block_size;
+  if (bad && covered && s == 0 && tid == 0) set_status(a.status, MLA_DEV_BAD_SEQ);
+  const int visible = bad ? 0 : len - ql + (n - q0) + 1;
+  const int t0 = s * a.split_len, t1 = min(visible, t0 + a.split_len);
+
+  // query of (n, h): nope part as given, rope part rotated to position q_positions[n]
+  {
+    const __nv_bfloat16* qn = a.q_nope + ((size_t)n * a.H + h) * kDn;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sq[w][lane + 32 * i] = __bfloat162float(qn[lane + 32 * i]);
+    const __nv_bfloat16* qp = a.q_pe + ((size_t)n * a.H + h) * kDr;
+    const float x1 = __bfloat162float(qp[lane]), x2 = __bfloat162float(qp[lane + 32]);
+    float cs, sn;
+    rope_cos_sin(a.q_positions[n], a.freq.hi[lane], a.freq.lo[lane], &cs, &sn);
+    sq[w][kDn + lane] = x1 * cs - x2 * sn;
+    sq[w][kDn + 32 + lane] = x2 * cs + x1 * sn;
+  }
+  __syncwarp();
+
+  const int32_t* bt = a.block_table + (size_t)b * a.max_blocks_per_seq;
+  const int bs = a.block_size;
+  float m = -INFINITY, l = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+  for (int tb = t0; tb < t1; tb += 32) {
+    const int t = tb + lane;
+    int slot = -1;
+    if (t < t1) {
+      const int page = bt[t / bs];
+      if (page >= 0 && page < a.num_blocks) {
+        slot = page * bs + t % bs;
+      } else if (t % bs == 0 && w == 0) {
+        set_status(a.status, MLA_DEV_BAD_BLOCK);
+      }
+    }
+    float sc = -INFINITY;
+    if (slot >= 0) {
+      const uint4* kr = reinterpret_cast<const uint4*>(a.kv + ((size_t)slot * a.H + h) * kNv);
+      float dot = 0.f;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint4 kk[12];
+#pragma unroll
+        for (int i = 0; i < 12; ++i) kk[i] = __ldg(kr + 12 * half + i);
+#pragma unroll
+        for (int i = 0; i < 12; ++i) {
+          const float* qv = &sq[w][96 * half + 8 * i];
+          dot = fmaf(bf_lo(kk[i].x), qv[0], dot);
+          dot = fmaf(bf_hi(kk[i].x), qv[1], dot);
+          dot = fmaf(bf_lo(kk[i].y), qv[2], dot);
+          dot = fmaf(bf_hi(kk[i].y), qv[3], dot);
+          dot = fmaf(bf_lo(kk[i].z), qv[4], dot);
+          dot = fmaf(bf_hi(kk[i].z), qv[5], dot);
+          dot = fmaf(bf_lo(kk[i].w), qv[6], dot);
+          dot = fmaf(bf_hi(kk[i].w), qv[7], dot);
+        }
+      }
+      sc = dot * a.scale_log2;
+    }
+    const float mn = fmaxf(m, warp_max(sc));
+    if (mn == -INFINITY) continue;  // warp-uniform: no visible token so far
+    const float alpha = fast_exp2(m - mn);
+    const float p = slot >= 0 ? fast_exp2(sc - mn) : 0.f;
+    l = l * alpha + warp_sum(p);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] *= alpha;
+    m = mn;
+#pragma unroll 8
+    for (int j = 0; j < 32; ++j) {
+      const float pj = __shfl_sync(0xffffffffu, p, j);
+      const int sj = __shfl_sync(0xffffffffu, slot, j);
+      const uint2 v = sj >= 0 ? __ldg(reinterpret_cast<const uint2*>(
+                                    a.kv + ((size_t)sj * a.H + h) * kNv + kDn + kDr + 4 * lane))
+                              : make_uint2(0u, 0u);
+      acc[0] = fmaf(pj, bf_lo(v.x), acc[0]);
+      acc[1] = fmaf(pj, bf_hi(v.x), acc[1]);
+      acc[2] = fmaf(pj, bf_lo(v.y), acc[2]);
+      acc[3] = fmaf(pj, bf_hi(v.y), acc[3]);
+    }
+  }
+  const size_t pi = ((size_t)n * a.H + h) * a.splits + s;
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  *reinterpret_cast<float4*>(a.part_o + pi * kDv + 4 * lane) =
+      make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+  if (lane == 0) a.part_lse[pi] = l > 0.f ? m + log2f(l) : -INFINITY;
+}
+
+// Split-softmax merge: out[n, h] = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M),
+// zeros for a (row, head) that saw no token. Warp = (row, head), lanes own 4
+// dimensions; grid (num_q, H / 8).
+__global__ void __launch_bounds__(256) naive_merge_kernel(const float* __restrict__ part_o,
+                                                          const float* __restrict__ part_lse,
+                                                          int splits, int H,
+                                                          __nv_bfloat16* __restrict__ out) {
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = blockIdx.x, h = blockIdx.y * 8 + w;
+  pdl_wait();
+  pdl_launch_dependents();
+  const size_t base = ((size_t)n * H + h) * splits;
+  float M = -INFINITY;
+  for (int s = 0; s < splits; ++s) M = fmaxf(M, part_lse[base + s]);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float den = 0.f;
+  if (M != -INFINITY) {
+    for (int s = 0; s < splits; ++s) {
+      const float ls = part_lse[base + s];
+      if (ls == -INFINITY) continue;
+      const float wgt = fast_exp2(ls - M);
+      const float4 o = *reinterpret_cast<const float4*>(part_o + (base + s) * kDv + 4 * lane);
+      den += wgt;
+      acc.x = fmaf(wgt, o.x, acc.x);
+      acc.y = fmaf(wgt, o.y, acc.y);
+      acc.z = fmaf(wgt, o.z, acc.z);
+      acc.w = fmaf(wgt, o.w, acc.w);
+    }
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  uint2 r;
+  r.x = pack_bf16(acc.x * inv, acc.y * inv);
+  r.y = pack_bf16(acc.z * inv, acc.w * inv);
+  *reinterpret_cast<uint2*>(out + ((size_t)n * H + h) * kDv + 4 * lane) = r;
+}
+
+}  // namespace
+
+namespace {
+
+// Splits of the naive decode: about 4,096 warps over the whole batch, each
+// split a multiple of 32 tokens (the same on every call with these sizes, so
+// the workspace size follows from them).
+struct NaiveSplit {
+  int splits, split_len;
+};
+
+NaiveSplit naive_split(int64_t num_q, int H, int64_t max_len) {
+  const int64_t pairs = num_q * H > 0 ? num_q * H : 1;
+  const int64_t smax = max_len > 32 ? (max_len + 31) / 32 : 1;
+  int64_t s = (4096 + pairs - 1) / pairs;
+  if (s > smax) s = smax;
+  if (s < 1) s = 1;
+  int64_t len = (max_len + s - 1) / s;
+  len = len < 32 ? 32 : (len + 31) / 32 * 32;
+  s = max_len > 0 ? (max_len + len - 1) / len : 1;
+  return {(int)s, (int)len};
+}
+
+// Workspace: [0, 256) status word and padding; Wt [H, 256, 512] bf16; then
+// either (cache write) the normed rows [T, 576] bf16 and their indices [T]
+// int64, or (decode) the partials [num_q, H, S, 128] f32 and log-sum-exps
+// [num_q, H, S] f32.
+struct NaiveWs {
+  size_t wt, rows, slots, part_o, part_lse, write_end, decode_end;
+};
+
+NaiveWs naive_ws(int H, int64_t num_tokens, int64_t num_q, int splits) {
+  NaiveWs L;
+  L.wt = 256;
+  const size_t u = align_up(L.wt + (size_t)H * 256 * kDc * 2, 256);
+  L.rows = u;
+  L.slots = align_up(L.rows + (size_t)num_tokens * kRow * 2, 256);
+  L.write_end = align_up(L.slots + (size_t)num_tokens * 8, 256);
+  L.part_o = u;
+  L.part_lse = align_up(L.part_o + (size_t)num_q * H * splits * kDv * 4, 256);
+  L.decode_end = align_up(L.part_lse + (size_t)num_q * H * splits * 4, 256);
+  return L;
+}
+
+inline mla_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
+inline bool is_aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+mla_status naive_common_checks(const mla_config* cfg) {
+  mla_status s = validate_config(cfg);
+  if (s != MLA_OK) return s;
+  if (cfg->dtype != MLA_BF16) return MLA_ERR_UNSUPPORTED;  // the comparison forms are bf16
+  return MLA_OK;
+}
+
+// Wt, then the expansion of the rows `src_map` views.
+cudaError_t expand(const mla_config& cfg, const void* W_uk, const void* W_uv, uint8_t* ws,
+                   const CUtensorMap& src_map, const ExArgs& ea, unsigned grid_x, cudaStream_t st) {
+  const int H = cfg.num_heads;
+  __nv_bfloat16* Wt = reinterpret_cast<__nv_bfloat16*>(ws + 256);
+  cudaError_t e = launch_pdl(wt_prep_kernel, dim3(kDc / 32, 256 / 32, H), dim3(32, 8), 0, st,
+                             (const __nv_bfloat16*)W_uk, (const __nv_bfloat16*)W_uv, Wt);
+  if (e != cudaSuccess) return e;
+  CUtensorMap wt_map;
+  if (!encode_map_2d(&wt_map, Wt, kDc, (uint64_t)H * 256, 64, 256)) return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(expand_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           ExSmem::alloc);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(expand_tc_kernel, dim3(grid_x, H), dim3(kExThreads), ExSmem::alloc, st,
+                    src_map, wt_map, ea);
+}
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+size_t mla_naive_workspace_size(const mla_config* cfg, int64_t num_q, int32_t max_blocks_per_seq,
+                                int64_t num_tokens) {
+  if (naive_common_checks(cfg) != MLA_OK || num_q < 0 || max_blocks_per_seq < 0 || num_tokens < 0)
+    return 0;
+  const NaiveSplit sp = naive_split(num_q, cfg->num_heads, (int64_t)max_blocks_per_seq * cfg->block_size);
+  const NaiveWs L = naive_ws(cfg->num_heads, num_tokens, num_q, sp.splits);
+  return L.write_end > L.decode_end ? L.write_end : L.decode_end;
+}
+
+mla_status mla_naive_cache_write(const mla_config* cfg, const void* c_kv, const void* k_pe,
+                                 const int32_t* positions, const int64_t* slot_mapping,
+                                 int64_t num_tokens, const void* rms_weight, const void* W_uk,
+                                 const void* W_uv, void* kv_cache, int64_t num_blocks,
+                                 void* workspace, size_t ws_bytes, void* stream) {
+  mla_status s = naive_common_checks(cfg);
+  if (s != MLA_OK) return s;
+  if (num_tokens < 0 || num_blocks < 0 || num_tokens > ((int64_t)1 << 24))
+    return MLA_ERR_INVALID_ARGUMENT;
+  if (num_blocks * cfg->block_size > ((int64_t)1 << 31) / cfg->num_heads)
+    return MLA_ERR_UNSUPPORTED;
+  if (!workspace || !is_aligned(workspace, 256)) return MLA_ERR_INVALID_ARGUMENT;
+  if (num_tokens == 0) return MLA_OK;
+  if (!c_kv || !k_pe || !positions || !slot_mapping || !rms_weight || !W_uk || !W_uv || !kv_cache)
+    return MLA_ERR_INVALID_ARGUMENT;
+  if (!is_aligned(c_kv, 16) || !is_aligned(k_pe, 16) || !is_aligned(rms_weight, 16) ||
+      !is_aligned(W_uk, 16) || !is_aligned(W_uv, 16) || !is_aligned(kv_cache, 16) ||
+      !is_aligned(positions, 4) || !is_aligned(slot_mapping, 8))
+    return MLA_ERR_INVALID_ARGUMENT;
+  const NaiveWs L = naive_ws(cfg->num_heads, num_tokens, 0, 1);
+  if (ws_bytes < L.write_end) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+  int64_t* rows_idx = reinterpret_cast<int64_t*>(ws + L.slots);
+  void* rows = ws + L.rows;
+  // 1. the normed latent and rotated key of each new token, as dense rows
+  const int bs = cfg->block_size;
+  cudaError_t e = launch_pdl(iota_kernel, dim3((unsigned)((num_tokens + 255) / 256 < 1024
+                                                               ? (num_tokens + 255) / 256 : 1024)),
+                             dim3(256), 0, st, rows_idx, num_tokens);
+  if (e == cudaSuccess)
+    e = launch_cache_write(*cfg, c_kv, k_pe, positions, rows_idx, num_tokens, rms_weight, rows,
+                           (num_tokens + bs - 1) / bs, status, st);
+  if (e != cudaSuccess) return MLA_ERR_CUDA;
+  // 2. expand them into the rows of every head, at slot_mapping
+  CUtensorMap src_map;
+  if (!encode_row_map(&src_map, rows, (uint64_t)num_tokens, 64)) return MLA_ERR_CUDA;
+  ExArgs ea{};
+  ea.dst_slots = slot_mapping;
+  ea.num_rows = num_tokens;
+  ea.block_size = bs;
+  ea.box_rows = 64;
+  ea.H = cfg->num_heads;
+  ea.mode = 0;
+  ea.src = reinterpret_cast<const __nv_bfloat16*>(rows);
+  ea.kv = reinterpret_cast<__nv_bfloat16*>(kv_cache);
+  ea.num_slots = num_blocks * bs;
+  ea.status = status;
+  return cuda_status(expand(*cfg, W_uk, W_uv, ws, src_map, ea,
+                            (unsigned)((num_tokens + kExRows - 1) / kExRows), st));
+}
+
+mla_status mla_latent_expand(const mla_config* cfg, const void* cache, int64_t num_blocks,
+                             const int32_t* block_table, int32_t max_blocks_per_seq,
+                             const int32_t* seq_lens, int32_t batch, const void* W_uk,
+                             const void* W_uv, void* kv_cache, void* workspace, size_t ws_bytes,
+                             void* stream) {
+  mla_status s = naive_common_checks(cfg);
+  if (s != MLA_OK) return s;
+  if (num_blocks < 0 || max_blocks_per_seq < 0 || batch < 0) return MLA_ERR_INVALID_ARGUMENT;
+  if (num_blocks * cfg->block_size > ((int64_t)1 << 31) / cfg->num_heads)
+    return MLA_ERR_UNSUPPORTED;
+  if (!workspace || !is_aligned(workspace, 256)) return MLA_ERR_INVALID_ARGUMENT;
+  if (batch == 0 || max_blocks_per_seq == 0 || num_blocks == 0) return MLA_OK;
+  if (!cache || !block_table || !seq_lens || !W_uk || !W_uv || !kv_cache)
+    return MLA_ERR_INVALID_ARGUMENT;
+  if (!is_aligned(cache, 16) || !is_aligned(W_uk, 16) || !is_aligned(W_uv, 16) ||
+      !is_aligned(kv_cache, 16) || !is_aligned(block_table, 4) || !is_aligned(seq_lens, 4))
+    return MLA_ERR_INVALID_ARGUMENT;
+  const NaiveWs L = naive_ws(cfg->num_heads, 0, 0, 1);
+  if (ws_bytes < L.write_end) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  const int bs = cfg->block_size;
+  const int64_t max_len = (int64_t)max_blocks_per_seq * bs;
+  const int64_t tiles = (max_len + kExRows - 1) / kExRows;
+  if ((int64_t)batch * tiles > 0x7fffffff) return MLA_ERR_UNSUPPORTED;
+  CUtensorMap src_map;
+  if (!encode_row_map(&src_map, cache, (uint64_t)num_blocks * bs, (uint32_t)bs)) return MLA_ERR_CUDA;
+  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+  ExArgs ea{};
+  ea.block_table = block_table;
+  ea.seq_lens = seq_lens;
+  ea.max_blocks_per_seq = max_blocks_per_seq;
+  ea.tiles_per_seq = (int32_t)tiles;
+  ea.num_blocks = num_blocks;
+  ea.block_size = bs;
+  ea.box_rows = bs;
+  ea.H = cfg->num_heads;
+  ea.mode = 1;
+  ea.src = reinterpret_cast<const __nv_bfloat16*>(cache);
+  ea.kv = reinterpret_cast<__nv_bfloat16*>(kv_cache);
+  ea.num_slots = num_blocks * bs;
+  ea.status = reinterpret_cast<uint32_t*>(ws);
+  return cuda_status(expand(*cfg, W_uk, W_uv, ws, src_map, ea, (unsigned)(batch * tiles),
+                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mla_status mla_naive_decode(const mla_config* cfg, const void* q_nope, const void* q_pe,
+                            const int32_t* q_positions, const void* kv_cache, int64_t num_blocks,
+                            const int32_t* block_table, int32_t max_blocks_per_seq,
+                            const int32_t* seq_lens, const int32_t* query_start_loc,
+                            int32_t batch, int64_t num_q, void* workspace, size_t ws_bytes,
+                            void* out, void* stream) {
+  mla_status s = naive_common_checks(cfg);
+  if (s != MLA_OK) return s;
+  if (num_q < 0 || batch < 0 || num_blocks < 0 || max_blocks_per_seq < 0)
+    return MLA_ERR_INVALID_ARGUMENT;
+  if (num_q > 0x7fffffff || num_blocks * cfg->block_size > ((int64_t)1 << 31) / cfg->num_heads)
+    return MLA_ERR_UNSUPPORTED;
+  if (!workspace || !is_aligned(workspace, 256)) return MLA_ERR_INVALID_ARGUMENT;
+  if (num_q == 0) return MLA_OK;
+  if (!q_nope || !q_pe || !q_positions || !kv_cache || !block_table || !seq_lens ||
+      !query_start_loc || !out || batch == 0)
+    return MLA_ERR_INVALID_ARGUMENT;
+  if (!is_aligned(q_nope, 16) || !is_aligned(q_pe, 16) || !is_aligned(kv_cache, 16) ||
+      !is_aligned(out, 16) || !is_aligned(q_positions, 4) || !is_aligned(block_table, 4) ||
+      !is_aligned(seq_lens, 4) || !is_aligned(query_start_loc, 4))
+    return MLA_ERR_INVALID_ARGUMENT;
+  const int H = cfg->num_heads;
+  const NaiveSplit sp = naive_split(num_q, H, (int64_t)max_blocks_per_seq * cfg->block_size);
+  if (sp.splits > 65535) return MLA_ERR_UNSUPPORTED;  // grid.y
+  const NaiveWs L = naive_ws(H, 0, num_q, sp.splits);
+  if (ws_bytes < L.decode_end) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  NdArgs na{};
+  na.q_nope = reinterpret_cast<const __nv_bfloat16*>(q_nope);
+  na.q_pe = reinterpret_cast<const __nv_bfloat16*>(q_pe);
+  na.q_positions = q_positions;
+  na.kv = reinterpret_cast<const __nv_bfloat16*>(kv_cache);
+  na.num_blocks = num_blocks;
+  na.block_table = block_table;
+  na.max_blocks_per_seq = max_blocks_per_seq;
+  na.block_size = cfg->block_size;
+  na.seq_lens = seq_lens;
+  na.query_start_loc = query_start_loc;
+  na.batch = batch;
+  na.num_q = (int32_t)num_q;
+  na.H = H;
+  na.splits = sp.splits;
+  na.split_len = sp.split_len;
+  na.scale_log2 = (float)(cfg->softmax_scale * 1.4426950408889634);
+  na.freq = make_rope_freq((double)cfg->rope_base);
+  na.part_o = reinterpret_cast<float*>(ws + L.part_o);
+  na.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
+  na.status = reinterpret_cast<uint32_t*>(ws);
+  cudaError_t e = launch_pdl(naive_decode_kernel, dim3((unsigned)num_q, sp.splits, H / 8),
+                             dim3(256), 0, st, na);
+  if (e != cudaSuccess) return MLA_ERR_CUDA;
+  return cuda_status(launch_pdl(naive_merge_kernel, dim3((unsigned)num_q, H / 8), dim3(256), 0,
+                                st, (const float*)na.part_o, (const float*)na.part_lse,
+                                sp.splits, H, reinterpret_cast<__nv_bfloat16*>(out)));
+}
+
+}  // extern "C"

@@ -30,7 +30,8 @@ EXPORTS = (
     "mla_default_config", "mla_cache_write", "mla_absorb_q", "mla_decode_workspace_size",
     "mla_workspace_init", "mla_decode_paged", "mla_decode_plan", "mla_decode_planned",
     "mla_decode_combine", "mla_decode_paged_combine", "mla_decode_paged_noalloc",
-    "mla_combine_out_proj",
+    "mla_combine_out_proj", "mla_naive_workspace_size", "mla_naive_cache_write",
+    "mla_latent_expand", "mla_naive_decode",
     "mla_combine", "mla_out_proj",
     "mla_get_device_status", "mla_selftest_wait_timeout", "mla_status_string", "mla_version",
 )
@@ -71,6 +72,13 @@ _SIGS = {
                                         _vp, _sz, _vp, _vp]),
     "mla_decode_paged_noalloc": (_i32, [_cfgp, _vp, _vp, _i64, _vp, _i32, _vp, _vp, _i32, _i64,
                                         _vp, _vp, _vp]),
+    "mla_naive_workspace_size": (_sz, [_cfgp, _i64, _i32, _i64]),
+    "mla_naive_cache_write": (_i32, [_cfgp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _i64,
+                                     _vp, _sz, _vp]),
+    "mla_latent_expand": (_i32, [_cfgp, _vp, _i64, _vp, _i32, _vp, _i32, _vp, _vp, _vp, _vp, _sz,
+                                 _vp]),
+    "mla_naive_decode": (_i32, [_cfgp, _vp, _vp, _vp, _vp, _i64, _vp, _i32, _vp, _vp, _i32, _i64,
+                                _vp, _sz, _vp, _vp]),
     "mla_combine": (_i32, [_cfgp, _vp, _sz, _i32, _i64, _vp, _vp]),
     "mla_combine_out_proj": (_i32, [_cfgp, _vp, _sz, _i32, _i64, _vp, _vp, _vp]),
     "mla_out_proj": (_i32, [_cfgp, _vp, _vp, _vp, _i64, _vp]),
@@ -247,6 +255,52 @@ def mla_decode_paged_noalloc(cfg: MlaConfig, q_abs, cache, block_table, seq_lens
         _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(query_start_loc, torch.int32, "query_start_loc"),
         seq_lens.shape[0], q_abs.shape[0], _ptr(o_lat, torch.float32, "o_lat"),
         _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)), "mla_decode_paged_noalloc")
+
+
+def mla_naive_workspace_size(cfg: MlaConfig, num_q: int, max_blocks_per_seq: int,
+                             num_tokens: int) -> int:
+    return int(load().mla_naive_workspace_size(ctypes.byref(cfg), num_q, max_blocks_per_seq,
+                                               num_tokens))
+
+
+def _nbytes(t) -> int:
+    return t.numel() * t.element_size()
+
+
+def mla_naive_cache_write(cfg: MlaConfig, c_kv, k_pe, positions, slot_mapping, rms_weight, W_uk,
+                          W_uv, kv_cache, workspace, stream=None) -> None:
+    dt = _torch_dtype(cfg)
+    _check(load().mla_naive_cache_write(
+        ctypes.byref(cfg), _ptr(c_kv, dt, "c_kv"), _ptr(k_pe, dt, "k_pe"),
+        _ptr(positions, torch.int32, "positions"), _ptr(slot_mapping, torch.int64, "slot_mapping"),
+        c_kv.shape[0], _ptr(rms_weight, dt, "rms_weight"), _ptr(W_uk, dt, "W_uk"),
+        _ptr(W_uv, dt, "W_uv"), _ptr(kv_cache, dt, "kv_cache"), kv_cache.shape[0],
+        _ptr(workspace, None, "workspace"), _nbytes(workspace), _stream(stream)),
+        "mla_naive_cache_write")
+
+
+def mla_latent_expand(cfg: MlaConfig, cache, block_table, seq_lens, W_uk, W_uv, kv_cache,
+                      workspace, stream=None) -> None:
+    dt = _torch_dtype(cfg)
+    _check(load().mla_latent_expand(
+        ctypes.byref(cfg), _ptr(cache, dt, "cache"), cache.shape[0],
+        _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+        _ptr(seq_lens, torch.int32, "seq_lens"), seq_lens.shape[0], _ptr(W_uk, dt, "W_uk"),
+        _ptr(W_uv, dt, "W_uv"), _ptr(kv_cache, dt, "kv_cache"),
+        _ptr(workspace, None, "workspace"), _nbytes(workspace), _stream(stream)),
+        "mla_latent_expand")
+
+
+def mla_naive_decode(cfg: MlaConfig, q_nope, q_pe, q_positions, kv_cache, block_table, seq_lens,
+                     query_start_loc, workspace, out, stream=None) -> None:
+    dt = _torch_dtype(cfg)
+    _check(load().mla_naive_decode(
+        ctypes.byref(cfg), _ptr(q_nope, dt, "q_nope"), _ptr(q_pe, dt, "q_pe"),
+        _ptr(q_positions, torch.int32, "q_positions"), _ptr(kv_cache, dt, "kv_cache"),
+        kv_cache.shape[0], _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+        _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(query_start_loc, torch.int32, "query_start_loc"),
+        seq_lens.shape[0], q_nope.shape[0], _ptr(workspace, None, "workspace"), _nbytes(workspace),
+        _ptr(out, dt, "out"), _stream(stream)), "mla_naive_decode")
 
 
 def mla_combine(cfg: MlaConfig, workspace, batch: int, o_lat, stream=None) -> None:

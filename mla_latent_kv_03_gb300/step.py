@@ -129,6 +129,37 @@ class MlaDecodeStep:
         self.out_proj(stream)
         return self.out
 
+    # -- the pages' other two forms (full K/V cache; latent re-expanded) ----
+    def naive_setup(self) -> None:
+        """Buffers of the expanded cache ([num_blocks, block_size, H, 320]) and
+        the workspace of its calls."""
+        w = self.w
+        self.kv_naive = torch.empty((w.num_blocks, w.block_size, w.num_heads, 320),
+                                    dtype=self.dt, device=self.device)
+        n = L.mla_naive_workspace_size(self.cfg, w.num_q, self.block_table.shape[1],
+                                       max(int(self.c_kv.shape[0]), 1))
+        if n == 0:
+            raise L.MlaError(L.MLA_OK + 2, "mla_naive_workspace_size")
+        self.naive_ws = torch.empty(n, dtype=torch.uint8, device=self.device)
+        L.mla_workspace_init(self.naive_ws)
+        self.out_naive = torch.empty((w.num_q, w.num_heads, 128), dtype=self.dt, device=self.device)
+
+    def naive_populate(self) -> None:
+        """Version 1's cache: every token expanded into the rows of every head."""
+        L.mla_naive_cache_write(self.cfg, self.c_kv, self.k_pe, self.kv_positions,
+                                self.slot_mapping, self.rms_weight, self.W_uk, self.W_uv,
+                                self.kv_naive, self.naive_ws)
+
+    def latent_expand(self, stream=None) -> None:
+        """Version 2: re-expand the whole latent cache into kv_naive."""
+        L.mla_latent_expand(self.cfg, self.cache, self.block_table, self.seq_lens, self.W_uk,
+                            self.W_uv, self.kv_naive, self.naive_ws, stream=stream)
+
+    def naive_decode(self, stream=None) -> None:
+        L.mla_naive_decode(self.cfg, self.q_nope, self.q_pe, self.q_positions, self.kv_naive,
+                           self.block_table, self.seq_lens, self.query_start_loc, self.naive_ws,
+                           self.out_naive, stream=stream)
+
     def device_status(self):
         """(status, bits) of the decode workspace and of the cache-write word."""
         s1 = L.mla_get_device_status(self.workspace)

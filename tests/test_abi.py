@@ -98,3 +98,19 @@ def test_decode_rejects_small_workspace_on_host(lib):
     assert s == 3
     s = lib.mla_decode_paged(ctypes.byref(cfg), p, p, 16, p, 4, p, p, 4, 70000, p, 1 << 40, None)
     assert s == 2  # more query rows than one plan holds
+
+
+def test_naive_forms_are_bf16_only_and_check_their_workspace(lib):
+    f32 = L.make_config(16, 64, "f32")
+    bf16 = L.make_config(16, 64, "bf16")
+    assert lib.mla_naive_workspace_size(ctypes.byref(f32), 4, 4, 4) == 0
+    p = ctypes.c_void_p(1 << 20)
+    # rejected on the host before any device work
+    assert lib.mla_naive_decode(ctypes.byref(f32), p, p, p, p, 16, p, 4, p, p, 4, 4, p,
+                                1 << 30, p, None) == 2
+    need = lib.mla_naive_workspace_size(ctypes.byref(bf16), 4, 4, 0)
+    # the 256-byte header plus the transposed weights [16, 256, 512] bf16, at least
+    assert need >= 256 + 16 * 256 * 512 * 2
+    assert lib.mla_naive_decode(ctypes.byref(bf16), p, p, p, p, 16, p, 4, p, p, 4, 4, p,
+                                256, p, None) == 3
+    assert lib.mla_latent_expand(ctypes.byref(bf16), p, 16, p, 4, p, 4, p, p, p, p, 256, None) == 3
