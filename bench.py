@@ -71,6 +71,10 @@ def parse_args(argv=None):
     p.add_argument("--kernel-launches", type=int, default=1000)
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--form", choices=["absorbed", "full_kv", "latent"], default="absorbed",
+                   help="absorbed: the latent decode (default); full_kv: the page's version 1 "
+                        "(expanded K/V cache, decode only); latent: version 2 (the latent cache "
+                        "re-expanded every step, then the same decode)")
     return p.parse_args(argv)
 
 
@@ -360,8 +364,15 @@ def run_ours(args, world, rank, local):
     L.load()
     w = make_workload(args.workload, rank)
     mixed = bool(w.is_new.sum() > w.batch)   # a step that writes more than one token per sequence
+    form = args.form
+    if form != "absorbed" and (mixed or w.dtype != "bf16"):
+        raise SystemExit("--form full_kv / latent: bf16 decode workloads only")
     s = MlaDecodeStep(w, device=dev)
     s.populate(include_new=not mixed)
+    if form != "absorbed":
+        s.naive_setup()
+        if form == "full_kv":
+            s.naive_populate()        # version 1's cache (untimed, as the latent cache is)
     torch.cuda.synchronize()
     latent = step_latent_bytes(w)
     stream = torch.cuda.Stream(device=dev)
@@ -370,6 +381,13 @@ def run_ours(args, world, rank, local):
     self_planned, decode_launches = decode_call_launches(w, torch.cuda.get_device_properties(dev))
 
     def one_step():
+        if form == "full_kv":
+            s.naive_decode()
+            return
+        if form == "latent":
+            s.latent_expand()
+            s.naive_decode()
+            return
         if self_planned:
             # one kernel plans, decodes and merges; it starts its cache stream
             # while the absorption finishes
@@ -393,6 +411,9 @@ def run_ours(args, world, rank, local):
         s.out_proj()
 
     launches_per_step = 2 + decode_launches + (1 if mixed else 0)
+    if form != "absorbed":
+        # decode + merge; version 2 adds the weight transpose and the expansion
+        launches_per_step = 2 if form == "full_kv" else 4
     # eager warm-up (also builds the lazy state), then capture one step
     with torch.cuda.stream(stream):
         for _ in range(3):
@@ -443,8 +464,14 @@ def run_ours(args, world, rank, local):
     per_graph = 20
     kgraph = torch.cuda.CUDAGraph()
     # the decode kernel of the step: the self-planned one on the warp-mma
-    # path, else the planned decode (the plan is in the workspace by now)
-    decode_alone = s.decode_paged_combine if self_planned else s.decode_combine
+    # path, else the planned decode (the plan is in the workspace by now);
+    # for the other forms their dominant call
+    if form == "full_kv":
+        decode_alone = s.naive_decode
+    elif form == "latent":
+        decode_alone = s.latent_expand
+    else:
+        decode_alone = s.decode_paged_combine if self_planned else s.decode_combine
     with torch.cuda.graph(kgraph, stream=stream):
         for _ in range(per_graph):
             decode_alone()
@@ -467,28 +494,55 @@ def run_ours(args, world, rank, local):
     mode = s.decode_mode()
     # (row, head) x visible token pairs, each a 576-wide score and a 512-wide
     # accumulation: the tensor-core work the attention needs at the least
-    attn_flops = int(w.num_heads) * int(sum(int(p) + 1 for p in w.q_positions)) * (576 + 512) * 2
+    pairs = int(sum(int(p) + 1 for p in w.q_positions))
+    attn_flops = int(w.num_heads) * pairs * (576 + 512) * 2
     tpeak, _ = tensor_peak()
-    kernel = ("decode_f32_kernel" if w.dtype != "bf16" else
-              "decode_tc_kernel" if mode == 1 else "decode_bf16_kernel")
-    traffic = profiled_traffic(kernel, args.workload)
-    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": traffic,
-                "kernel": kernel,
-                "attention_tflops": round(attn_flops / (kernel_ms * 1e-3) / 1e12, 1),
-                "attention_tensor_frac": round(attn_flops / (kernel_ms * 1e-3) / 1e12 / tpeak, 4),
-                "attention_flops": attn_flops,
-                "kernel_us": round(kernel_ms * 1e3, 2), "algorithmic_bytes": decode_bytes,
-                "peak_kind": f"{peak_kind} HBM copy bandwidth (burst)",
-                "frac_of_nominal_8TBs": round(achieved / NOMINAL_HBM_GBS, 4)}
+    if form == "full_kv":
+        kernel = "naive_decode_kernel"
+        nbytes = pairs * int(w.num_heads) * 640 + int(w.block_table.size) * 4
+        achieved = nbytes / (kernel_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                    "frac": round(achieved / peak, 4), "traffic": profiled_traffic(kernel, args.workload),
+                    "kernel": kernel, "kernel_us": round(kernel_ms * 1e3, 2),
+                    "algorithmic_bytes": nbytes,
+                    "peak_kind": f"{peak_kind} HBM copy bandwidth (burst)"}
+    elif form == "latent":
+        kernel = "expand_tc_kernel"
+        cached = int(sum(int(x) for x in w.seq_lens))
+        flops = cached * int(w.num_heads) * 256 * 512 * 2
+        tflops = flops / (kernel_ms * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "achieved": round(tflops, 1), "peak": tpeak,
+                    "unit": "TFLOP/s", "frac": round(tflops / tpeak, 4),
+                    "traffic": profiled_traffic(kernel, args.workload), "kernel": kernel,
+                    "kernel_us": round(kernel_ms * 1e3, 2), "algorithmic_flops": flops,
+                    "written_bytes": cached * int(w.num_heads) * 640,
+                    "peak_kind": "measured bf16 dense (cuBLAS, burst)"}
+    else:
+        kernel = ("decode_f32_kernel" if w.dtype != "bf16" else
+                  "decode_tc_kernel" if mode == 1 else "decode_bf16_kernel")
+        traffic = profiled_traffic(kernel, args.workload)
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                    "frac": round(achieved / peak, 4), "traffic": traffic,
+                    "kernel": kernel,
+                    "attention_tflops": round(attn_flops / (kernel_ms * 1e-3) / 1e12, 1),
+                    "attention_tensor_frac": round(attn_flops / (kernel_ms * 1e-3) / 1e12 / tpeak, 4),
+                    "attention_flops": attn_flops,
+                    "kernel_us": round(kernel_ms * 1e3, 2), "algorithmic_bytes": decode_bytes,
+                    "peak_kind": f"{peak_kind} HBM copy bandwidth (burst)",
+                    "frac_of_nominal_8TBs": round(achieved / NOMINAL_HBM_GBS, 4)}
 
     # ---- end to end through the same calls, host buffers, eager launches
-    e2e = run_e2e(args, s, w, stream, latent, world, mixed, one_step)
+    e2e = run_e2e(args, s, w, stream, latent, world, mixed, one_step,
+                  s.out if form == "absorbed" else s.out_naive)
 
     # ---- status: the timed work must not have flagged anything
     (st1, bits1), (st2, bits2) = s.device_status()
     if st1 != 0 or st2 != 0:
         raise SystemExit(f"device status after bench: decode {bits1:#x}, cache write {bits2:#x}")
+    if form != "absorbed":
+        st3, bits3 = L.mla_get_device_status(s.naive_ws)
+        if st3 != 0:
+            raise SystemExit(f"device status after bench: {form} {bits3:#x}")
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -500,7 +554,7 @@ def run_ours(args, world, rank, local):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype, "data": "synthetic (seeded; shapes of DeepSeek-V2-Lite attention)",
-            "config": {"workload": w.name, "batch": w.batch, "num_heads": w.num_heads,
+            "config": {"workload": w.name, "form": form, "batch": w.batch, "num_heads": w.num_heads,
                        "seq_lens": "all 4096" if args.workload == "serving" else "see workload",
                        "block_size": w.block_size, "latent_bytes_per_step": latent,
                        "l2": "inputs larger than L2: the latent cache read each step exceeds 129 MB",
@@ -517,7 +571,7 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
-def run_e2e(args, s, w, stream, latent, world, mixed, one_step):
+def run_e2e(args, s, w, stream, latent, world, mixed, one_step, out):
     """Same step through the public calls, eager launches, with this step's
     inputs copied from pinned host memory and the output copied back."""
     import torch
@@ -525,7 +579,7 @@ def run_e2e(args, s, w, stream, latent, world, mixed, one_step):
     if mixed:
         ins += [s.c_kv_new, s.k_pe_new, s.pos_new, s.slot_new]
     host_in = [t.detach().cpu().pin_memory() for t in ins]
-    host_out = torch.empty(s.out.shape, dtype=s.out.dtype, pin_memory=True)
+    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = host_out.numel() * host_out.element_size()
 
@@ -533,7 +587,7 @@ def run_e2e(args, s, w, stream, latent, world, mixed, one_step):
         for d, h in zip(ins, host_in):
             d.copy_(h, non_blocking=True)
         one_step()
-        host_out.copy_(s.out, non_blocking=True)
+        host_out.copy_(out, non_blocking=True)
 
     n = max(1, args.e2e_steps)
     with torch.cuda.stream(stream):
