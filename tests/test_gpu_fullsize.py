@@ -61,3 +61,92 @@ def test_mixed_prefill_decode_sampled():
     (st1, _), (st2, _) = s.device_status()
     assert st1 == 0 and st2 == 0
     _check(w, s, [0, 3, 4, 63], [0, 5, 15], "mixed prefill + decode")
+
+
+# ---------------------------------------------------------------------------
+# the step exactly as the bench times it: captured in a CUDA graph (every
+# kernel with programmatic dependent launch), replayed, then checked
+# ---------------------------------------------------------------------------
+
+def _bench_step(s, w, side, ev_fork, ev_join):
+    mixed = bool(w.is_new.sum() > w.batch)
+    tc = w.num_heads >= 64 or w.num_q >= 4 * w.batch
+    if not tc and w.num_q <= 256:
+        s.absorb()
+        s.decode_paged_combine()      # plan + decode + split merge, one kernel
+        s.out_proj()
+        return
+    cur = torch.cuda.current_stream()
+    ev_fork.record(cur)
+    side.wait_event(ev_fork)
+    with torch.cuda.stream(side):
+        s.plan()
+        ev_join.record(side)
+    if mixed:
+        s.write_new()
+    s.absorb()
+    cur.wait_event(ev_join)
+    s.decode_combine()
+    s.out_proj()
+
+
+def _run_graphed(w, s, steps=3, replays=2):
+    stream, side = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_fork, ev_join = torch.cuda.Event(), torch.cuda.Event()
+    with torch.cuda.stream(stream):
+        _bench_step(s, w, side, ev_fork, ev_join)   # eager once (lazy state)
+    stream.synchronize()
+    s.out.fill_(float("nan"))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(steps):
+            _bench_step(s, w, side, ev_fork, ev_join)
+    with torch.cuda.stream(stream):
+        for _ in range(replays):
+            g.replay()
+    stream.synchronize()
+
+
+def test_serving_bench_step_graphed_and_the_other_forms():
+    w = W.serving()
+    s = MlaDecodeStep(w, device=DEV)
+    s.populate()
+    s.naive_setup()
+    _run_graphed(w, s)
+    assert s.device_status()[0][0] == 0
+    seqs, heads = [0, 17, 40, 63], list(range(16))
+    ref = ref_out(w, seqs=seqs, heads=heads)
+    rows = np.concatenate([np.arange(w.q_range(b).start, w.q_range(b).stop) for b in seqs])
+    assert_close(to_f64(s.out)[rows], ref[rows], "bf16", "serving, graphed bench step")
+    # the pages' other two forms at the same size
+    s.naive_populate()
+    s.naive_decode()
+    torch.cuda.synchronize()
+    assert_close(to_f64(s.out_naive)[rows], ref[rows], "bf16", "serving, full K/V cache")
+    s.kv_naive.view(torch.int16).fill_(0x7FC1)
+    s.latent_expand()
+    s.naive_decode()
+    torch.cuda.synchronize()
+    assert L.mla_get_device_status(s.naive_ws)[0] == 0
+    assert_close(to_f64(s.out_naive)[rows], ref[rows], "bf16", "serving, latent re-expanded")
+
+
+def test_ragged_H128_bench_step_graphed():
+    w = W.ragged_h128()
+    s = MlaDecodeStep(w, device=DEV)
+    s.populate()
+    _run_graphed(w, s)
+    assert s.device_status()[0][0] == 0
+    lens = w.seq_lens
+    seqs = sorted({int(np.argmin(lens)), int(np.argmax(lens)), 7})
+    _check(w, s, seqs, [0, 64, 127], "ragged H=128, graphed bench step")
+
+
+def test_mixed_bench_step_graphed():
+    w = W.mixed()
+    s = MlaDecodeStep(w, device=DEV)
+    s.populate(include_new=False)
+    _run_graphed(w, s)
+    (st1, _), (st2, _) = s.device_status()
+    assert st1 == 0 and st2 == 0
+    _check(w, s, [1, 4, 50], [3, 12], "mixed, graphed bench step")
