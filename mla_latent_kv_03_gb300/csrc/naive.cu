@@ -56,7 +56,8 @@ __global__ void iota_kernel(int64_t* __restrict__ out, int64_t n) {
 }
 
 // ---------------------------------------------------------------------------
-// expand_tc_kernel. CTA = (128 source rows, head h). D[r, j] = sum_c X[r, c]
+// expand_tc_kernel. CTA = (128 source rows, head h), blockIdx.x = tile * H + h.
+// D[r, j] = sum_c X[r, c]
 // Wt[h][j][c] over the 512 latent columns in 8 chunks of 64: the X chunk (128
 // rows, by TMA boxes of box_rows rows: pages of the latent cache, or slices of
 // a dense buffer) and the Wt chunk (256 rows) stream through a 2-stage ring,
@@ -67,8 +68,9 @@ __global__ void iota_kernel(int64_t* __restrict__ out, int64_t n) {
 // per SM, one's epilogue under the other's MMAs.
 //   mode 0: rows [128 x, 128 x + 128) of a dense [num_rows, 576] buffer, row t
 //           written to slot dst_slots[t] (< 0: skipped).
-//   mode 1: tokens [128 k, 128 k + 128) of sequence b (x = b * tiles_per_seq
-//           + k), read from and written to the same slot of the block table.
+//   mode 1: tokens [128 k, 128 k + 128) of sequence b (tile = b *
+//           tiles_per_seq + k), read from and written to the same slot of the
+//           block table.
 // ---------------------------------------------------------------------------
 struct ExArgs {
   const int64_t* dst_slots;
@@ -112,7 +114,10 @@ __global__ void __launch_bounds__(kExThreads, 2) expand_tc_kernel(
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int h = blockIdx.y;
+  // heads vary fastest: the H CTAs of one tile run together, so its rows are
+  // read from DRAM once and from L2 by the other heads
+  const int h = blockIdx.x % a.H;
+  const int tile = blockIdx.x / a.H;
   int* s_dst = reinterpret_cast<int*>(sm + ExSmem::dst);
   int* s_src = reinterpret_cast<int*>(sm + ExSmem::src);
   int* s_box = reinterpret_cast<int*>(sm + ExSmem::box);
@@ -144,7 +149,7 @@ __global__ void __launch_bounds__(kExThreads, 2) expand_tc_kernel(
     const int r = tid;
     int dst = -1, src = 0;
     if (a.mode == 0) {
-      const int64_t t = (int64_t)blockIdx.x * kExRows + r;
+      const int64_t t = (int64_t)tile * kExRows + r;
       if (t < a.num_rows) {
         const int64_t slot = a.dst_slots[t];
         if (slot >= a.num_slots) {
@@ -154,9 +159,9 @@ __global__ void __launch_bounds__(kExThreads, 2) expand_tc_kernel(
         }
         src = (int)t;
       }
-      if (r < nbox) s_box[r] = (int)((int64_t)blockIdx.x * kExRows + r * a.box_rows);
+      if (r < nbox) s_box[r] = (int)((int64_t)tile * kExRows + r * a.box_rows);
     } else {
-      const int b = blockIdx.x / a.tiles_per_seq, k = blockIdx.x % a.tiles_per_seq;
+      const int b = tile / a.tiles_per_seq, k = tile % a.tiles_per_seq;
       const int len = a.seq_lens[b];
       const int64_t max_len = (int64_t)a.max_blocks_per_seq * a.block_size;
       const bool bad = len < 0 || (int64_t)len > max_len;
@@ -286,10 +291,10 @@ __global__ void __launch_bounds__(kExThreads, 2) expand_tc_kernel(
 // ---------------------------------------------------------------------------
 // naive_decode_kernel. Warp = (query row n, head h, split s); CTA = 8 heads of
 // one (row, split). The query [q_nope || RoPE(q_pe)] sits in shared memory;
-// per 32 tokens, lane l scores token l against its 192-value key (24 16-byte
-// loads of one row), the warp updates the online softmax, then lanes own 4 of
-// the 128 value dimensions and accumulate the 32 weighted value rows (256
-// contiguous bytes per token across the warp). Output: the split's
+// per 32 tokens, groups of 8 lanes score 4 tokens at a time (each lane 48
+// contiguous bytes of a key, partial dots summed by shuffles), the warp
+// updates the online softmax, then lanes own 4 of the 128 value dimensions and
+// accumulate the 32 weighted value rows (256 contiguous bytes per token). Output: the split's
 // normalised partial and base-2 log-sum-exp.
 // ---------------------------------------------------------------------------
 struct NdArgs {
@@ -381,30 +386,47 @@ __global__ void __launch_bounds__(256) naive_decode_kernel(NdArgs a) {
         set_status(a.status, MLA_DEV_BAD_BLOCK);
       }
     }
-    float sc = -INFINITY;
-    if (slot >= 0) {
-      const uint4* kr = reinterpret_cast<const uint4*>(a.kv + ((size_t)slot * a.H + h) * kNv);
-      float dot = 0.f;
+    // scores: 8 lanes share a token's 384-byte key (48 bytes each, so one
+    // warp load covers 4 whole rows); partial dots summed over the 8 lanes,
+    // then lane t takes token t's score
+    const int g = lane >> 3, sub = lane & 7;
+    float dots[8];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint4 kk[12];
+    for (int i = 0; i < 8; ++i) {
+      const int st = __shfl_sync(0xffffffffu, slot, 4 * i + g);
+      float d = 0.f;
+      if (st >= 0) {
+        const uint4* kr =
+            reinterpret_cast<const uint4*>(a.kv + ((size_t)st * a.H + h) * kNv) + 3 * sub;
+        const float* qv = &sq[w][24 * sub];
 #pragma unroll
-        for (int i = 0; i < 12; ++i) kk[i] = __ldg(kr + 12 * half + i);
-#pragma unroll
-        for (int i = 0; i < 12; ++i) {
-          const float* qv = &sq[w][96 * half + 8 * i];
-          dot = fmaf(bf_lo(kk[i].x), qv[0], dot);
-          dot = fmaf(bf_hi(kk[i].x), qv[1], dot);
-          dot = fmaf(bf_lo(kk[i].y), qv[2], dot);
-          dot = fmaf(bf_hi(kk[i].y), qv[3], dot);
-          dot = fmaf(bf_lo(kk[i].z), qv[4], dot);
-          dot = fmaf(bf_hi(kk[i].z), qv[5], dot);
-          dot = fmaf(bf_lo(kk[i].w), qv[6], dot);
-          dot = fmaf(bf_hi(kk[i].w), qv[7], dot);
+        for (int c = 0; c < 3; ++c) {
+          const uint4 kk = __ldg(kr + c);
+          d = fmaf(bf_lo(kk.x), qv[8 * c + 0], d);
+          d = fmaf(bf_hi(kk.x), qv[8 * c + 1], d);
+          d = fmaf(bf_lo(kk.y), qv[8 * c + 2], d);
+          d = fmaf(bf_hi(kk.y), qv[8 * c + 3], d);
+          d = fmaf(bf_lo(kk.z), qv[8 * c + 4], d);
+          d = fmaf(bf_hi(kk.z), qv[8 * c + 5], d);
+          d = fmaf(bf_lo(kk.w), qv[8 * c + 6], d);
+          d = fmaf(bf_hi(kk.w), qv[8 * c + 7], d);
         }
       }
-      sc = dot * a.scale_log2;
+      dots[i] = d;
     }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      dots[i] += __shfl_xor_sync(0xffffffffu, dots[i], 4);
+      dots[i] += __shfl_xor_sync(0xffffffffu, dots[i], 2);
+      dots[i] += __shfl_xor_sync(0xffffffffu, dots[i], 1);
+    }
+    float dot = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float v = __shfl_sync(0xffffffffu, dots[i], 8 * (lane & 3));
+      if ((lane >> 2) == i) dot = v;
+    }
+    const float sc = slot >= 0 ? dot * a.scale_log2 : -INFINITY;
     const float mn = fmaxf(m, warp_max(sc));
     if (mn == -INFINITY) continue;  // warp-uniform: no visible token so far
     const float alpha = fast_exp2(m - mn);
@@ -525,7 +547,7 @@ mla_status naive_common_checks(const mla_config* cfg) {
 
 // Wt, then the expansion of the rows `src_map` views.
 cudaError_t expand(const mla_config& cfg, const void* W_uk, const void* W_uv, uint8_t* ws,
-                   const CUtensorMap& src_map, const ExArgs& ea, unsigned grid_x, cudaStream_t st) {
+                   const CUtensorMap& src_map, const ExArgs& ea, unsigned tiles, cudaStream_t st) {
   const int H = cfg.num_heads;
   __nv_bfloat16* Wt = reinterpret_cast<__nv_bfloat16*>(ws + 256);
   cudaError_t e = launch_pdl(wt_prep_kernel, dim3(kDc / 32, 256 / 32, H), dim3(32, 8), 0, st,
@@ -536,8 +558,8 @@ cudaError_t expand(const mla_config& cfg, const void* W_uk, const void* W_uv, ui
   e = cudaFuncSetAttribute(expand_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            ExSmem::alloc);
   if (e != cudaSuccess) return e;
-  return launch_pdl(expand_tc_kernel, dim3(grid_x, H), dim3(kExThreads), ExSmem::alloc, st,
-                    src_map, wt_map, ea);
+  return launch_pdl(expand_tc_kernel, dim3(tiles * (unsigned)H), dim3(kExThreads), ExSmem::alloc,
+                    st, src_map, wt_map, ea);
 }
 
 }  // namespace
@@ -631,7 +653,7 @@ mla_status mla_latent_expand(const mla_config* cfg, const void* cache, int64_t n
   const int bs = cfg->block_size;
   const int64_t max_len = (int64_t)max_blocks_per_seq * bs;
   const int64_t tiles = (max_len + kExRows - 1) / kExRows;
-  if ((int64_t)batch * tiles > 0x7fffffff) return MLA_ERR_UNSUPPORTED;
+  if ((int64_t)batch * tiles * cfg->num_heads > 0x7fffffff) return MLA_ERR_UNSUPPORTED;
   CUtensorMap src_map;
   if (!encode_row_map(&src_map, cache, (uint64_t)num_blocks * bs, (uint32_t)bs)) return MLA_ERR_CUDA;
   uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
