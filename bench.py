@@ -57,6 +57,10 @@ PROFILES = {
     ("decode_tc_kernel", "ragged_h128"): (
         "decode_tc_ragged_B32_H128.md",
         ["decode_tc.cu", "common.cuh", "cluster.cuh", "tcgen05.cuh", "merge.cuh", "async_copy.cuh"]),
+    ("expand_tc_kernel", "serving"): (
+        "expand_tc_serving_B64_L4096.md", ["naive.cu", "common.cuh", "tcgen05.cuh", "async_copy.cuh"]),
+    ("naive_decode_kernel", "serving"): (
+        "naive_decode_serving_B64_L4096.md", ["naive.cu", "common.cuh", "tcgen05.cuh", "async_copy.cuh"]),
 }
 
 

@@ -56,21 +56,29 @@ __global__ void iota_kernel(int64_t* __restrict__ out, int64_t n) {
 }
 
 // ---------------------------------------------------------------------------
-// expand_tc_kernel. CTA = (128 source rows, head h), blockIdx.x = tile * H + h.
-// D[r, j] = sum_c X[r, c]
-// Wt[h][j][c] over the 512 latent columns in 8 chunks of 64: the X chunk (128
-// rows, by TMA boxes of box_rows rows: pages of the latent cache, or slices of
-// a dense buffer) and the Wt chunk (256 rows) stream through a 2-stage ring,
-// 4 tcgen05.mma (M 128, N 256, K 16) per chunk into a 256-column TMEM
-// accumulator. Epilogue: thread r (TMEM lane r) converts row r to bf16 and
-// writes [K_nope || k_rot || V] of (slot, h), k_rot copied from the source
-// row's rope columns. 97 KB of shared memory and 256 TMEM columns: two CTAs
-// per SM, one's epilogue under the other's MMAs.
-//   mode 0: rows [128 x, 128 x + 128) of a dense [num_rows, 576] buffer, row t
-//           written to slot dst_slots[t] (< 0: skipped).
+// expand_tc_kernel: a persistent tcgen05 GEMM, one CTA per SM. A unit is (128
+// source rows, head h), numbered tile * H + h so that the H units of a tile
+// run on neighbouring CTAs at the same time and its rows are read from DRAM
+// once. D[r, j] = sum_c X[r, c] Wt[h][j][c] over the 512 latent columns in 8
+// chunks of 64 columns.
+//   warp 0   producer: the X chunk (128 rows, TMA boxes of box_rows rows: pages
+//            of the latent cache, or slices of a dense buffer) and the Wt chunk
+//            (256 rows) into a 4-stage ring; a unit's box rows are looked up
+//            one unit ahead
+//   warp 1   MMA: 4 tcgen05.mma (M 128, N 256, K 16) per chunk into one of two
+//            256-column TMEM accumulators, alternating by unit
+//   warps 2-5 epilogue (TMEM lanes 32 (w % 4) ...): thread r converts row r of
+//            the finished accumulator to bf16, a 64-column block at a time,
+//            into the warp's staging rows in shared memory, and the warp writes
+//            [K_nope || k_rot || V] of (slot, h) as whole 128-byte lines (k_rot
+//            copied from the source row), while the MMAs of the next unit fill
+//            the other accumulator
+// Every unit goes through the pipeline; rows past a sequence's end (or with
+// slot < 0) are computed from row 0 and not written.
+//   mode 0: rows [128 tile, 128 tile + 128) of a dense [num_rows, 576] buffer,
+//           row t written to slot dst_slots[t] (< 0: skipped).
 //   mode 1: tokens [128 k, 128 k + 128) of sequence b (tile = b *
-//           tiles_per_seq + k), read from and written to the same slot of the
-//           block table.
+//           tiles_per_seq + k), read from and written to the same slot.
 // ---------------------------------------------------------------------------
 struct ExArgs {
   const int64_t* dst_slots;
@@ -84,6 +92,7 @@ struct ExArgs {
   int32_t box_rows;            // rows of one source TMA box
   int32_t H;
   int32_t mode;
+  int32_t total_units;         // tiles * H
   const __nv_bfloat16* src;    // the rows the source map views ([rows, 576])
   __nv_bfloat16* kv;           // [num_slots, H, 320]
   int64_t num_slots;
@@ -93,199 +102,266 @@ struct ExArgs {
 constexpr int kExRows = 128;
 constexpr int kExA = kExRows * 128;  // 16 KB: 128 rows x 64 columns
 constexpr int kExB = 256 * 128;      // 32 KB: 256 weight rows x 64 columns
-constexpr int kExThreads = 128;
+constexpr int kExStages = 4;
+constexpr int kExThreads = 192;   // producer, MMA, 4 epilogue warps
 
 struct ExSmem {
-  static constexpr int a = 0;                    // [2]
-  static constexpr int b = a + 2 * kExA;         // [2]
-  static constexpr int dst = b + 2 * kExB;       // int[128]: destination slot (-1: none)
-  static constexpr int src = dst + kExRows * 4;  // int[128]: source row
-  static constexpr int box = src + kExRows * 4;  // int[8]: first source row of each box
-  static constexpr int bars = box + 32;          // full[2], empty[2], done
-  static constexpr int misc = bars + 5 * 8;      // tmem base, valid-row count
+  static constexpr int a = 0;                              // [stages]
+  static constexpr int b = a + kExStages * kExA;           // [stages]
+  static constexpr int stg = b + kExStages * kExB;         // [4 warps] 32 rows x 128 B
+  static constexpr int bars = stg + 4 * 32 * 128;         // full, empty, tfull[2], tempty[2], mdone
+  static constexpr int misc = bars + (2 * kExStages + 5) * 8;  // tmem base
   static constexpr int bytes = misc + 16;
   static constexpr int alloc = bytes + 1024;
 };
 
-__global__ void __launch_bounds__(kExThreads, 2) expand_tc_kernel(
+// First source row of box `i` of unit tile (mode 1: the page's first row, or
+// row 0 past the sequence's end or for a rejected block id).
+__device__ __forceinline__ int ex_box_row(const ExArgs& a, int tile, int i) {
+  if (a.mode == 0) return tile * kExRows + i * a.box_rows;
+  const int b = tile / a.tiles_per_seq, k = tile % a.tiles_per_seq;
+  const int len = a.seq_lens[b];
+  if (len < 0 || (int64_t)len > (int64_t)a.max_blocks_per_seq * a.block_size) return 0;
+  const int t0 = k * kExRows + i * a.box_rows;
+  if (t0 >= len) return 0;
+  const int page = a.block_table[(size_t)b * a.max_blocks_per_seq + t0 / a.block_size];
+  return page >= 0 && page < a.num_blocks ? page * a.block_size : 0;
+}
+
+// Destination slot (-1: not written) and source row of row r of unit (tile, h);
+// reports bad sequences, blocks and slots once.
+__device__ __forceinline__ void ex_row(const ExArgs& a, int tile, int h, int r, int* dst,
+                                       int* src) {
+  *dst = -1;
+  *src = 0;
+  if (a.mode == 0) {
+    const int64_t t = (int64_t)tile * kExRows + r;
+    if (t >= a.num_rows) return;
+    const int64_t slot = a.dst_slots[t];
+    if (slot >= a.num_slots) {
+      if (h == 0) set_status(a.status, MLA_DEV_BAD_SLOT);
+    } else if (slot >= 0) {
+      *dst = (int)slot;
+    }
+    *src = (int)t;
+    return;
+  }
+  const int b = tile / a.tiles_per_seq, k = tile % a.tiles_per_seq;
+  const int len = a.seq_lens[b];
+  if (len < 0 || (int64_t)len > (int64_t)a.max_blocks_per_seq * a.block_size) {
+    if (k == 0 && h == 0 && r == 0) set_status(a.status, MLA_DEV_BAD_SEQ);
+    return;
+  }
+  const int tok = k * kExRows + r;
+  if (tok >= len) return;
+  const int page = a.block_table[(size_t)b * a.max_blocks_per_seq + tok / a.block_size];
+  if (page >= 0 && page < a.num_blocks) {
+    *dst = *src = page * a.block_size + tok % a.block_size;
+  } else if (tok % a.block_size == 0 && h == 0) {
+    set_status(a.status, MLA_DEV_BAD_BLOCK);
+  }
+}
+
+__global__ void __launch_bounds__(kExThreads, 1) expand_tc_kernel(
     const __grid_constant__ CUtensorMap src_map, const __grid_constant__ CUtensorMap wt_map,
     ExArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
-  const int tid = threadIdx.x, warp = tid >> 5;
-  // heads vary fastest: the H CTAs of one tile run together, so its rows are
-  // read from DRAM once and from L2 by the other heads
-  const int h = blockIdx.x % a.H;
-  const int tile = blockIdx.x / a.H;
-  int* s_dst = reinterpret_cast<int*>(sm + ExSmem::dst);
-  int* s_src = reinterpret_cast<int*>(sm + ExSmem::src);
-  int* s_box = reinterpret_cast<int*>(sm + ExSmem::box);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + ExSmem::bars);
-  uint64_t* empty = full + 2;
-  uint64_t* done = full + 4;
+  uint64_t* empty = full + kExStages;
+  uint64_t* tfull = empty + kExStages;   // [2] accumulator j % 2 complete
+  uint64_t* tempty = tfull + 2;          // [2] accumulator j % 2 read out (4 warp arrivals)
+  uint64_t* mdone = tempty + 2;          // every MMA issued so far has completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + ExSmem::misc);
-  int* s_nvalid = reinterpret_cast<int*>(sm + ExSmem::misc + 4);
   const int nbox = kExRows / a.box_rows;
+  const int H = a.H;
 
   if (tid == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kExStages; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
-    mbar_init(done, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 4);
+    }
+    mbar_init(mdone, 1);
     fence_mbar_init();
     prefetch_tensormap(&src_map);
     prefetch_tensormap(&wt_map);
-    *s_nvalid = 0;
   }
   // the source rows, Wt and the destination come from or go to earlier kernels
   pdl_wait();
   pdl_launch_dependents();
-  __syncthreads();
-
-  // ---- where each of the 128 rows comes from and goes to
-  {
-    const int r = tid;
-    int dst = -1, src = 0;
-    if (a.mode == 0) {
-      const int64_t t = (int64_t)tile * kExRows + r;
-      if (t < a.num_rows) {
-        const int64_t slot = a.dst_slots[t];
-        if (slot >= a.num_slots) {
-          set_status(a.status, MLA_DEV_BAD_SLOT);
-        } else if (slot >= 0) {
-          dst = (int)slot;
-        }
-        src = (int)t;
-      }
-      if (r < nbox) s_box[r] = (int)((int64_t)tile * kExRows + r * a.box_rows);
-    } else {
-      const int b = tile / a.tiles_per_seq, k = tile % a.tiles_per_seq;
-      const int len = a.seq_lens[b];
-      const int64_t max_len = (int64_t)a.max_blocks_per_seq * a.block_size;
-      const bool bad = len < 0 || (int64_t)len > max_len;
-      if (bad && k == 0 && h == 0 && r == 0) set_status(a.status, MLA_DEV_BAD_SEQ);
-      const int tok = k * kExRows + r;
-      const int32_t* bt = a.block_table + (size_t)b * a.max_blocks_per_seq;
-      if (!bad && tok < len) {
-        const int page = bt[tok / a.block_size];
-        if (page >= 0 && page < a.num_blocks) {
-          dst = src = page * a.block_size + tok % a.block_size;
-        } else if (tok % a.block_size == 0 && h == 0) {
-          set_status(a.status, MLA_DEV_BAD_BLOCK);
-        }
-      }
-      if (r < nbox) {
-        const int t0 = k * kExRows + r * a.box_rows;
-        int y = 0;  // boxes without a valid page read row 0; their rows are not written
-        if (!bad && t0 < len) {
-          const int page = bt[t0 / a.block_size];
-          if (page >= 0 && page < a.num_blocks) y = page * a.block_size;
-        }
-        s_box[r] = y;
-      }
-    }
-    s_dst[r] = dst;
-    s_src[r] = src;
-    if (dst >= 0) atomicAdd(s_nvalid, 1);
-  }
-  __syncthreads();
-  if (*s_nvalid == 0) return;  // nothing to write (before any copy or TMEM use)
-
-  if (warp == 0) tc::alloc(tmem_slot, 256);
+  if (warp == 0) tc::alloc(tmem_slot, 512);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  int fills[2] = {0, 0};
-  bool ok = true;
-  if (tid == 0) {
+  if (warp == 0) {
     // ------------------------------------------------------------ producer
+    int c = 0;
+    int last_fill[kExStages];
+#pragma unroll
+    for (int i = 0; i < kExStages; ++i) last_fill[i] = -1;
+    bool ok = true;
+    int u = blockIdx.x;
+    int ycur = (u < a.total_units && lane < nbox) ? ex_box_row(a, u / H, lane) : 0;
+    for (; ok && u < a.total_units; u += gridDim.x) {
+      const int un = u + gridDim.x;  // look the next unit's boxes up now
+      const int ynext = (un < a.total_units && lane < nbox) ? ex_box_row(a, un / H, lane) : 0;
+      int ys[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ys[i] = __shfl_sync(0xffffffffu, ycur, i);
+      const int h = u % H;
 #pragma unroll 1
-    for (int kc = 0; kc < 8; ++kc) {
-      const int st = kc & 1;
-      if (kc >= 2 && !mbar_wait(&empty[st], ((kc >> 1) - 1) & 1)) {
-        ok = false;
-        break;
+      for (int kc = 0; kc < 8; ++kc, ++c) {
+        const int st = c % kExStages;
+        if (c >= kExStages &&
+            !__all_sync(0xffffffffu, mbar_wait(&empty[st], ((c / kExStages) - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[st], kExA + kExB);
+          uint8_t* da = sm + ExSmem::a + st * kExA;
+          for (int i = 0; i < nbox; ++i)
+            tma_load_2d(da + i * a.box_rows * 128, &src_map, 64 * kc, ys[i], &full[st]);
+          tma_load_2d(sm + ExSmem::b + st * kExB, &wt_map, 64 * kc, h * 256, &full[st]);
+        }
+        last_fill[st] = c;
+        __syncwarp();
       }
-      mbar_arrive_expect_tx(&full[st], kExA + kExB);
-      uint8_t* da = sm + ExSmem::a + st * kExA;
-      for (int i = 0; i < nbox; ++i)
-        tma_load_2d(da + i * a.box_rows * 128, &src_map, 64 * kc, s_box[i], &full[st]);
-      tma_load_2d(sm + ExSmem::b + st * kExB, &wt_map, 64 * kc, h * 256, &full[st]);
-      ++fills[st];
+      ycur = ynext;
     }
+    if (!ok && lane == 0) set_status(a.status, MLA_DEV_TIMEOUT);
+    // no copy may still be in flight when the CTA ends
+    if (lane == 0)
+      for (int i = 0; i < kExStages; ++i)
+        if (last_fill[i] >= 0) mbar_wait(&full[i], (last_fill[i] / kExStages) & 1);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
     constexpr uint32_t kId = tc::idesc_bf16(kExRows, 256, false, false);
     const bool leader = tc::elect_one();
-#pragma unroll 1
-    for (int kc = 0; kc < 8; ++kc) {
-      const int st = kc & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&full[st], (kc >> 1) & 1));
-      if (!ok) break;
-      if (leader) {
-        tc::fence_after_sync();
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t ad = tc::smem_desc(smem_u32(sm + ExSmem::a + st * kExA) + 32 * ks, 16,
-                                            1024, tc::kSwizzle128);
-          const uint64_t bd = tc::smem_desc(smem_u32(sm + ExSmem::b + st * kExB) + 32 * ks, 16,
-                                            1024, tc::kSwizzle128);
-          tc::mma_bf16(tmem, ad, bd, kId, kc > 0 || ks > 0);
-        }
-        tc::commit(&empty[st]);
+    int c = 0, j = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < a.total_units; u += gridDim.x, ++j) {
+      const int buf = j & 1;
+      if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(&tempty[buf], ((j >> 1) - 1) & 1))) {
+        ok = false;
+        break;
       }
+      tc::fence_after_sync();
+      const uint32_t d = tmem + (uint32_t)buf * 256;
+#pragma unroll 1
+      for (int kc = 0; kc < 8; ++kc, ++c) {
+        const int st = c % kExStages;
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[st], (c / kExStages) & 1))) {
+          ok = false;
+          break;
+        }
+        if (leader) {
+          tc::fence_after_sync();
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t ad = tc::smem_desc(smem_u32(sm + ExSmem::a + st * kExA) + 32 * ks, 16,
+                                              1024, tc::kSwizzle128);
+            const uint64_t bd = tc::smem_desc(smem_u32(sm + ExSmem::b + st * kExB) + 32 * ks, 16,
+                                              1024, tc::kSwizzle128);
+            tc::mma_bf16(d, ad, bd, kId, kc > 0 || ks > 0);
+          }
+          tc::commit(&empty[st]);
+        }
+        __syncwarp();
+      }
+      if (ok && leader) tc::commit(&tfull[buf]);
       __syncwarp();
     }
-    if (ok && leader) tc::commit(done);
+    if (!ok && leader) set_status(a.status, MLA_DEV_TIMEOUT);
+    // every MMA must have completed before TMEM is freed
+    if (leader) tc::commit(mdone);
     __syncwarp();
-  }
-  // every copy and MMA must land before TMEM is read or freed
-  const bool okd = __syncthreads_and(mbar_wait(done, 0) && ok) != 0;
-  if (!okd) {
-    if (tid == 0) {
-      set_status(a.status, MLA_DEV_TIMEOUT);
-      for (int i = 0; i < 2; ++i)
-        if (fills[i] > 0) mbar_wait(&full[i], (fills[i] - 1) & 1);
-    }
-  }
-  tc::fence_after_sync();
-  if (okd) {
+    mbar_wait(mdone, 0);
+  } else {
     // ------------------------------------------------------------ epilogue
-    const int r = tid;
-    const int dst = s_dst[r];
-    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-    __nv_bfloat16* out = a.kv + ((size_t)(dst < 0 ? 0 : dst) * a.H + h) * kNv;
-#pragma unroll 1
-    for (int cb = 0; cb < 8; ++cb) {
-      uint32_t v[32];
-      tc::ld32(trow + 32 * cb, v);  // every lane: the load is warp-collective
-      tc::wait_ld();
-      if (dst >= 0) {
-        uint4* o = reinterpret_cast<uint4*>(out + (cb < 4 ? 32 * cb : 192 + 32 * (cb - 4)));
+    const int q = warp & 3;          // TMEM lane quadrant of this warp
+    const int r = q * 32 + lane;     // row of the tile
+    int j = 0;
+    for (int u = blockIdx.x; u < a.total_units; u += gridDim.x, ++j) {
+      const int buf = j & 1, tile = u / H, h = u % H;
+      int dst, src;
+      ex_row(a, tile, h, r, &dst, &src);   // while the MMAs run
+      // the shared rope key of the row, as the source row holds it (loaded now:
+      // its latency hides under the MMAs)
+      uint4 kr[8];
+      {
+        const uint4* p = reinterpret_cast<const uint4*>(a.src + (size_t)src * kRow + kDc);
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          o[q] = make_uint4(pack_bf16(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
-                            pack_bf16(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
-                            pack_bf16(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
-                            pack_bf16(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+        for (int k = 0; k < 8; ++k) kr[k] = dst >= 0 ? p[k] : make_uint4(0u, 0u, 0u, 0u);
       }
-    }
-    if (dst >= 0) {
-      // the shared rope key, as the source row holds it
-      const uint4* kr = reinterpret_cast<const uint4*>(a.src + (size_t)s_src[r] * kRow + kDc);
-      uint4* o = reinterpret_cast<uint4*>(out + kDn);
+      if (!__all_sync(0xffffffffu, mbar_wait(&tfull[buf], (j >> 1) & 1))) {
+        if (lane == 0) set_status(a.status, MLA_DEV_TIMEOUT);
+        break;
+      }
+      tc::fence_after_sync();
+      const uint32_t trow = tmem + (uint32_t)buf * 256 + ((uint32_t)(q * 32) << 16);
+      // Five 64-column blocks of the output row (K_nope 0-63, 64-127, k_rot,
+      // V 0-63, 64-127): each thread puts its row's 128 bytes in the warp's
+      // staging rows (16-byte chunks XOR-swizzled by row), then the warp
+      // stores 4 rows per instruction as whole 128-byte lines.
+      uint8_t* stg = sm + ExSmem::stg + q * 32 * 128;
+#pragma unroll 1
+      for (int blk = 0; blk < 5; ++blk) {
+        uint4 ch[8];
+        if (blk == 2) {
 #pragma unroll
-      for (int q = 0; q < 8; ++q) o[q] = kr[q];
+          for (int k = 0; k < 8; ++k) ch[k] = kr[k];
+        } else {
+          const uint32_t col = blk < 2 ? 64u * blk : 128u + 64u * (blk - 3);
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t v[32];
+            tc::ld32(trow + col + 32 * half, v);   // every lane: warp-collective
+            tc::wait_ld();
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              ch[4 * half + k] =
+                  make_uint4(pack_bf16(__uint_as_float(v[8 * k]), __uint_as_float(v[8 * k + 1])),
+                             pack_bf16(__uint_as_float(v[8 * k + 2]), __uint_as_float(v[8 * k + 3])),
+                             pack_bf16(__uint_as_float(v[8 * k + 4]), __uint_as_float(v[8 * k + 5])),
+                             pack_bf16(__uint_as_float(v[8 * k + 6]), __uint_as_float(v[8 * k + 7])));
+          }
+          if (blk == 4) {
+            // the last TMEM read of this unit: the accumulator may take unit j + 2
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[buf]);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          *reinterpret_cast<uint4*>(stg + lane * 128 + ((k ^ (lane & 7)) << 4)) = ch[k];
+        __syncwarp();
+        const int ocol = blk * 64;  // output columns of this block
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int row = 4 * i + (lane >> 3), c = lane & 7;
+          const int d = __shfl_sync(0xffffffffu, dst, row);
+          if (d >= 0)
+            *reinterpret_cast<uint4*>(a.kv + ((size_t)d * H + h) * kNv + ocol + 8 * c) =
+                *reinterpret_cast<const uint4*>(stg + row * 128 + ((c ^ (row & 7)) << 4));
+        }
+        __syncwarp();
+      }
     }
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (warp == 0) tc::dealloc(tmem, 256);
+  if (warp == 0) tc::dealloc(tmem, 512);
 }
 
 // ---------------------------------------------------------------------------
@@ -558,8 +634,16 @@ cudaError_t expand(const mla_config& cfg, const void* W_uk, const void* W_uv, ui
   e = cudaFuncSetAttribute(expand_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            ExSmem::alloc);
   if (e != cudaSuccess) return e;
-  return launch_pdl(expand_tc_kernel, dim3(tiles * (unsigned)H), dim3(kExThreads), ExSmem::alloc,
-                    st, src_map, wt_map, ea);
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  ExArgs args = ea;
+  args.total_units = (int32_t)(tiles * (unsigned)H);
+  const unsigned grid = (unsigned)args.total_units < (unsigned)sms ? (unsigned)args.total_units
+                                                                    : (unsigned)sms;
+  return launch_pdl(expand_tc_kernel, dim3(grid), dim3(kExThreads), ExSmem::alloc, st, src_map,
+                    wt_map, args);
 }
 
 }  // namespace
