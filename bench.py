@@ -75,6 +75,8 @@ def parse_args(argv=None):
     p.add_argument("--kernel-launches", type=int, default=1000)
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--ref-seconds", type=float, default=120.0,
+                   help="host time the reference arm's timed steps aim at in total")
     p.add_argument("--form", choices=["absorbed", "full_kv", "latent"], default="absorbed",
                    help="absorbed: the latent decode (default); full_kv: the page's version 1 "
                         "(expanded K/V cache, decode only); latent: version 2 (the latent cache "
@@ -651,14 +653,16 @@ def run_reference(args, world, rank):
     w = make_workload(args.workload, 0)
     cores = len(os.sched_getaffinity(0))
     gen = sample_pairs(w, seed=1)
-    # size each step's sample so the whole run stays within about two minutes
+    # size each step's sample so the whole run stays within --ref-seconds (two
+    # minutes by default)
     probe = [next(gen)]
     t_pair = oracle_pair_seconds(w, probe)
     n_steps = args.steps + args.warmup
-    per_step = max(1, int(120.0 / max(t_pair * n_steps, 1e-9)))
+    budget = args.ref_seconds
+    per_step = max(1, int(budget / max(t_pair * n_steps, 1e-9)))
     prefix = None
-    if t_pair * n_steps > 150.0:   # even one pair per step is too long: use a token prefix
-        prefix = max(64, int(int(w.seq_lens.max()) * 150.0 / (t_pair * n_steps)))
+    if t_pair * n_steps > 1.25 * budget:   # even one pair per step is too long: use a token prefix
+        prefix = max(64, int(int(w.seq_lens.max()) * 1.25 * budget / (t_pair * n_steps)))
     for _ in range(args.warmup):
         oracle_pair_seconds(w, [next(gen) for _ in range(per_step)], prefix)
     spent, pairs = 0.0, []
