@@ -228,13 +228,14 @@ mla_status mla_decode_combine(const mla_config* cfg, const void* q_abs, const vo
  * (row, 16-head group) last merges its parts); with fewer than num_ctas / 4
  * (row, head group) tiles it is that kernel without the merge followed by the
  * merge kernel. Elsewhere it is mla_decode_plan + mla_decode_combine.
- * Ordering: the kernel may start reading the cache and block_table before
- * the kernel launched just before it on the stream has finished (programmatic
- * dependent launch, as every libmla kernel uses); q_abs, seq_lens and
- * query_start_loc are read, and the workspace and o_lat written, only after
- * it has finished. So the kernel immediately before this call must not write
- * the cache or the block table: in a layer step it is mla_absorb_q, with
- * mla_cache_write before it. Rows that see no token get zeros. The result
+ * Ordering: on the one-launch path the kernel may start reading seq_lens,
+ * query_start_loc, the block table and the cache before the kernel launched
+ * just before it on the stream has finished (programmatic dependent launch,
+ * as every libmla kernel uses); q_abs is read, and the workspace and o_lat
+ * written, only after it has finished. So the kernel immediately before this
+ * call must write none of those four inputs: in a layer step it is
+ * mla_absorb_q, with mla_cache_write before it. (A kernel that does not use
+ * programmatic launch, or a copy, finishes before this call starts.) Rows that see no token get zeros. The result
  * equals mla_decode_paged followed by mla_combine up to fp32 rounding of the
  * merge order. The arrival counters are left at zero after a successful call.
  */
