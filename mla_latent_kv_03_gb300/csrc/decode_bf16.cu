@@ -24,10 +24,11 @@
 //
 // Self-planned launches (SELF): every CTA computes the split plan from
 // seq_lens / query_start_loc itself (no plan kernel) and the math warps write
-// it to the workspace for a later merge kernel. With early streaming the
-// producer issues its first cache tiles before the preceding kernel in the
-// stream has finished (programmatic dependent launch); only the query copy
-// and every global write wait for it.
+// it to the workspace for a later merge kernel. With early streaming the plan
+// (seq_lens, query_start_loc) and the producer's first cache tiles (block
+// table, cache) are read before the preceding kernel in the stream has
+// finished (programmatic dependent launch); only the query copy and every
+// global write wait for it.
 //
 // Fused merge: a (row, head group) cut into parts is merged by the CTA that
 // finishes its part last. Parts are published in the math threads' fragment
