@@ -240,6 +240,68 @@ def naive_attention(c_hat, k_rot, q_nope, q_rot, W_uk, W_uv, q_positions,
     return np.where((den > 0)[..., None], out, 0.0)
 
 
+# ---------------------------------------------------------------------------
+# FP8 latent cache. The pages name "FP8 KV" handling of MLA only as a later
+# chapter ([MI17] "下一章": 量化对 MLA / MoE 的特殊处理); the reading taken here
+# (stated as such): each row holds c_hat / kv_scale as OCP e4m3 codes (1 sign,
+# 4 exponent bits with bias 7, 3 mantissa bits, no infinities, 448 the largest
+# finite value), rounded to nearest with ties to even and saturated at +-448,
+# followed by k_rot in bf16; kv_scale is one positive number per cache.
+# ---------------------------------------------------------------------------
+E4M3_MAX = 448.0
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Value of each e4m3 code (NaN for S.1111.111)."""
+    c = np.asarray(codes, np.int64)
+    sign = np.where((c >> 7) & 1, -1.0, 1.0)
+    e = (c >> 3) & 15
+    m = (c & 7).astype(np.float64)
+    val = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    val = np.where((e == 15) & ((c & 7) == 7), np.nan, val)
+    return sign * val
+
+
+def e4m3_round(x) -> np.ndarray:
+    """x rounded to the e4m3 grid: nearest value, ties to the even mantissa,
+    saturated at +-448. In the binade [2^e, 2^(e+1)) (and the subnormals,
+    which share the spacing of e = -6) the grid is k * 2^(e-3), k integer, and
+    k is even exactly when the mantissa is."""
+    x = np.asarray(x, np.float64)
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    e = np.clip(np.floor(np.log2(np.where(a > 0, a, 1.0))), -6, 8)
+    step = np.exp2(e - 3)
+    q = a / step
+    k = np.floor(q)
+    frac = q - k
+    k = np.where(frac > 0.5, k + 1, np.where(frac < 0.5, k, k + (k % 2)))
+    v = np.minimum(k * step, E4M3_MAX)
+    return np.copysign(np.where(a > 0, v, 0.0), x)
+
+
+def e4m3_encode(v) -> np.ndarray:
+    """Code of each value already on the e4m3 grid (|v| <= 448)."""
+    v = np.asarray(v, np.float64)
+    sign = (np.signbit(v)).astype(np.int64) << 7
+    a = np.abs(v)
+    sub = a < 2.0 ** -6
+    e = np.floor(np.log2(np.where(sub, 1.0, a)))
+    m_norm = np.round((a / np.exp2(e) - 1.0) * 8.0).astype(np.int64)
+    m_sub = np.round(a / 2.0 ** -9).astype(np.int64)
+    code = np.where(sub, m_sub, ((e.astype(np.int64) + 7) << 3) | m_norm)
+    return (sign | code).astype(np.uint8)
+
+
+def fp8_latent_rows(c_kv_raw, k_pe_raw, positions, rms_weight, eps: float, base: float,
+                    kv_scale: float):
+    """The FP8 cache row of each token (reading above): the e4m3 codes of
+    c_hat / kv_scale [T, 512] uint8, and k_rot [T, 64] (stored in bf16).
+    Dequantised latent = e4m3_decode(codes) * kv_scale."""
+    c_hat = rms_norm(c_kv_raw, rms_weight, eps)
+    codes = e4m3_encode(e4m3_round(c_hat / float(kv_scale)))
+    return codes, rope(k_pe_raw, positions, base)
+
+
 def naive_kv_rows(c_hat, k_rot, W_uk, W_uv) -> np.ndarray:
     """[MI17 "版本 1: MLAAttentionNaive"]: the rows the full key/value cache holds.
 

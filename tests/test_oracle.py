@@ -451,3 +451,49 @@ def test_mutants_are_caught(mutant, monkeypatch):
         pos = np.array([0, 3, 50, 1000])
         caught.append(not np.allclose(O.rope(x, pos, 1e4), _rope_complex(x, pos, 1e4)))
     assert any(caught), f"planted mistake {mutant} passed every pin"
+
+
+# ---------------------------------------------------------------------------
+# FP8 (e4m3) cache rows
+# ---------------------------------------------------------------------------
+
+def test_e4m3_every_code_round_trips():
+    codes = np.arange(256, dtype=np.uint8)
+    vals = O.e4m3_decode(codes)
+    finite = ~np.isnan(vals)
+    assert int((~finite).sum()) == 2                      # S.1111.111
+    assert np.nanmax(vals) == O.E4M3_MAX and np.nanmin(vals) == -O.E4M3_MAX
+    assert np.array_equal(O.e4m3_encode(vals[finite]), codes[finite])
+    assert np.array_equal(O.e4m3_round(vals[finite]), vals[finite])
+
+
+def test_e4m3_round_matches_torch_float8_cast():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(11)
+    x = np.concatenate([rng.standard_normal(20000) * s for s in (0.01, 0.3, 3.0, 60.0)])
+    x = np.clip(x, -O.E4M3_MAX, O.E4M3_MAX).astype(np.float32).astype(np.float64)
+    ref = torch.from_numpy(x).to(torch.float32).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(O.e4m3_round(x), ref)
+
+
+def test_e4m3_ties_go_to_even_and_large_values_saturate():
+    # 1.0625 lies halfway between 1.0 (mantissa 0) and 1.125 (mantissa 1)
+    assert O.e4m3_round(1.0625) == 1.0 and O.e4m3_round(1.1875) == 1.25
+    assert O.e4m3_round(-2.0 ** -10) == 0.0                # half the smallest subnormal
+    assert O.e4m3_round(3 * 2.0 ** -10) == 2.0 ** -8       # 1.5 subnormal steps -> 2
+    assert O.e4m3_round(1e6) == O.E4M3_MAX and O.e4m3_round(-500.0) == -O.E4M3_MAX
+
+
+def test_fp8_rows_dequantise_within_half_a_step():
+    rng = np.random.default_rng(12)
+    c = rng.standard_normal((40, 512))
+    k_pe = rng.standard_normal((40, 64))
+    codes, k_rot = O.fp8_latent_rows(c, k_pe, np.arange(40), np.ones(512), 1e-6, 1e4, 0.05)
+    c_hat = O.rms_norm(c, np.ones(512), 1e-6)
+    deq = O.e4m3_decode(codes) * 0.05
+    # half a step of a 3-bit mantissa (relative 2^-4), or half the subnormal step
+    bound = np.maximum(np.abs(c_hat) * 2.0 ** -4, 0.05 * 2.0 ** -10) + 1e-15
+    assert np.all(np.abs(deq - c_hat) <= bound)
+    # and a plain rounding would not be enough: the error is that of e4m3, not bf16
+    assert np.max(np.abs(deq - c_hat)) > 2.0 ** -9
+    assert np.array_equal(k_rot, O.rope(k_pe, np.arange(40), 1e4))
