@@ -77,10 +77,11 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--ref-seconds", type=float, default=120.0,
                    help="host time the reference arm's timed steps aim at in total")
-    p.add_argument("--form", choices=["absorbed", "full_kv", "latent"], default="absorbed",
+    p.add_argument("--form", choices=["absorbed", "full_kv", "latent", "fp8"], default="absorbed",
                    help="absorbed: the latent decode (default); full_kv: the page's version 1 "
                         "(expanded K/V cache, decode only); latent: version 2 (the latent cache "
-                        "re-expanded every step, then the same decode)")
+                        "re-expanded every step, then the same decode); fp8: the absorbed step "
+                        "over an e4m3 latent cache (640 bytes per token, kv_scale 0.02)")
     return p.parse_args(argv)
 
 
@@ -372,21 +373,31 @@ def run_ours(args, world, rank, local):
     mixed = bool(w.is_new.sum() > w.batch)   # a step that writes more than one token per sequence
     form = args.form
     if form != "absorbed" and (mixed or w.dtype != "bf16"):
-        raise SystemExit("--form full_kv / latent: bf16 decode workloads only")
+        raise SystemExit("--form full_kv / latent / fp8: bf16 decode workloads only")
     s = MlaDecodeStep(w, device=dev)
     s.populate(include_new=not mixed)
-    if form != "absorbed":
+    if form in ("full_kv", "latent"):
         s.naive_setup()
         if form == "full_kv":
             s.naive_populate()        # version 1's cache (untimed, as the latent cache is)
+    if form == "fp8":
+        s.fp8_setup(0.02)             # about max |c_hat| / 448 for these inputs
+        s.fp8_populate()
     torch.cuda.synchronize()
     latent = step_latent_bytes(w)
+    if form == "fp8":
+        latent = latent * 640 // 1152   # the FP8 rows the step reads
     stream = torch.cuda.Stream(device=dev)
     side = torch.cuda.Stream(device=dev)
     ev_fork, ev_join = torch.cuda.Event(), torch.cuda.Event()
     self_planned, decode_launches = decode_call_launches(w, torch.cuda.get_device_properties(dev))
 
     def one_step():
+        if form == "fp8":
+            s.absorb()
+            s.decode_paged_combine_fp8()
+            s.out_proj()
+            return
         if form == "full_kv":
             s.naive_decode()
             return
@@ -417,7 +428,7 @@ def run_ours(args, world, rank, local):
         s.out_proj()
 
     launches_per_step = 2 + decode_launches + (1 if mixed else 0)
-    if form != "absorbed":
+    if form in ("full_kv", "latent"):
         # decode + merge; version 2 adds the weight transpose and the expansion
         launches_per_step = 2 if form == "full_kv" else 4
     # eager warm-up (also builds the lazy state), then capture one step
@@ -474,6 +485,8 @@ def run_ours(args, world, rank, local):
     # for the other forms their dominant call
     if form == "full_kv":
         decode_alone = s.naive_decode
+    elif form == "fp8":
+        decode_alone = s.decode_paged_combine_fp8
     elif form == "latent":
         decode_alone = s.latent_expand
     else:
@@ -525,7 +538,8 @@ def run_ours(args, world, rank, local):
                     "peak_kind": "measured bf16 dense (cuBLAS, burst)"}
     else:
         kernel = ("decode_f32_kernel" if w.dtype != "bf16" else
-                  "decode_tc_kernel" if mode == 1 else "decode_bf16_kernel")
+                  "decode_tc_kernel" if mode == 1 else
+                  "decode_bf16_kernel_fp8" if form == "fp8" else "decode_bf16_kernel")
         traffic = profiled_traffic(kernel, args.workload)
         roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                     "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -539,13 +553,13 @@ def run_ours(args, world, rank, local):
 
     # ---- end to end through the same calls, host buffers, eager launches
     e2e = run_e2e(args, s, w, stream, latent, world, mixed, one_step,
-                  s.out if form == "absorbed" else s.out_naive)
+                  s.out if form in ("absorbed", "fp8") else s.out_naive)
 
     # ---- status: the timed work must not have flagged anything
     (st1, bits1), (st2, bits2) = s.device_status()
     if st1 != 0 or st2 != 0:
         raise SystemExit(f"device status after bench: decode {bits1:#x}, cache write {bits2:#x}")
-    if form != "absorbed":
+    if form in ("full_kv", "latent"):
         st3, bits3 = L.mla_get_device_status(s.naive_ws)
         if st3 != 0:
             raise SystemExit(f"device status after bench: {form} {bits3:#x}")

@@ -246,6 +246,50 @@ mla_status mla_decode_paged_combine(const mla_config* cfg, const void* q_abs, co
                                     void* workspace, size_t ws_bytes, float* o_lat, void* stream);
 
 /*
+ * FP8 latent cache. The pages name "FP8 KV" handling of MLA only as a later
+ * chapter ([MI17] "下一章"); the format is this library's reading: each row of
+ * cache8 [num_blocks, block_size, 640] bytes holds the 512 OCP e4m3 codes of
+ * c_hat / kv_scale (round to nearest, ties to even, saturating at +-448)
+ * followed by k_rot as 64 bf16 values, i.e. 640 instead of 1,152 bytes per
+ * token. kv_scale > 0 is one number for the whole cache.
+ *
+ * mla_cache_write_fp8 -- mla_cache_write into that layout (bf16 inputs only).
+ */
+mla_status mla_cache_write_fp8(const mla_config* cfg, const void* c_kv, const void* k_pe,
+                               const int32_t* positions, const int64_t* slot_mapping,
+                               int64_t num_tokens, const void* rms_weight, float kv_scale,
+                               void* cache8, int64_t num_blocks, uint32_t* dev_status,
+                               void* stream);
+
+/*
+ * mla_decode_fp8_workspace_size -- bytes of workspace mla_decode_paged_combine_fp8
+ * needs for these sizes on the current device (0 for an invalid cfg).
+ */
+size_t mla_decode_fp8_workspace_size(const mla_config* cfg, int64_t num_q, int32_t batch);
+
+/*
+ * mla_decode_paged_combine_fp8 -- mla_decode_paged_combine over the FP8 cache:
+ * the latent columns of a row are its codes times kv_scale, the rope columns
+ * its bf16 values. Same inputs and ordering rules as mla_decode_paged_combine
+ * plus kv_scale. Supported on the 16-head warp-mma path with num_q <= 256
+ * (bf16 q_abs, 16 or 32 heads, not a prefill chunk); MLA_ERR_UNSUPPORTED
+ * otherwise. The codes convert to f16 exactly and the query's latent part
+ * goes to f16 scaled per head by a power of two (exact for every element down
+ * to 2^-28 of the head's largest), so the result equals attention over the
+ * dequantised cache up to fp32 rounding order and the f16 rounding of the
+ * probabilities. The workspace must hold mla_decode_fp8_workspace_size()
+ * bytes (at cfg->num_ctas = 0 this launch runs two CTAs per SM) and be
+ * initialised like any decode workspace.
+ */
+mla_status mla_decode_paged_combine_fp8(const mla_config* cfg, const void* q_abs,
+                                        const void* cache8, int64_t num_blocks,
+                                        const int32_t* block_table, int32_t max_blocks_per_seq,
+                                        const int32_t* seq_lens, const int32_t* query_start_loc,
+                                        int32_t batch, int64_t num_q, float kv_scale,
+                                        void* workspace, size_t ws_bytes, float* o_lat,
+                                        void* stream);
+
+/*
  * mla_combine -- merge the split partials of mla_decode_paged.
  * For each (n, h): M = max_s lse_s, o_lat = sum_s 2^(lse_s - M) o_s /
  * sum_s 2^(lse_s - M) (the split-softmax identity; lse is kept in base 2

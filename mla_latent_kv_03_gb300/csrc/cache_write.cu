@@ -9,6 +9,8 @@
 // One warp per token. Lane l holds latent values [16l, 16l+16) (16-byte
 // vector loads and stores) and the RoPE pair (l, l+32). HBM-bound: reads and
 // writes 1,152 bytes per token (bf16); 8 warps per CTA, grid-stride.
+#include <cuda_fp8.h>
+
 #include "async_copy.cuh"
 #include "common.cuh"
 #include "internal.h"
@@ -95,7 +97,75 @@ __global__ void __launch_bounds__(256) cache_write_kernel(
   }
 }
 
+// The FP8 cache row (640 bytes): e4m3 codes of c_hat / kv_scale (round to
+// nearest even, saturating at +-448), then k_rot in bf16. Inputs bf16.
+__global__ void __launch_bounds__(256) cache_write_fp8_kernel(
+    const __nv_bfloat16* __restrict__ c_kv, const __nv_bfloat16* __restrict__ k_pe,
+    const int32_t* __restrict__ positions, const int64_t* __restrict__ slot_mapping,
+    int64_t num_tokens, const __nv_bfloat16* __restrict__ w, uint8_t* __restrict__ cache8,
+    int64_t num_slots, float eps, float inv_scale, RopeFreq freq, uint32_t* status) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  Vec16<__nv_bfloat16> wv;
+  wv.load(w + lane * 16);
+  const float fhi = freq.hi[lane], flo = freq.lo[lane];
+  for (int64_t t = warp0; t < num_tokens; t += nwarps) {
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;  // padding token
+    if (slot >= num_slots) {
+      if (lane == 0) set_status(status, MLA_DEV_BAD_SLOT);
+      continue;
+    }
+    Vec16<__nv_bfloat16> x;
+    x.load(c_kv + t * kDc + lane * 16);
+    const __nv_bfloat16* kp = k_pe + t * kDr;
+    const float x1 = __bfloat162float(kp[lane]), x2 = __bfloat162float(kp[lane + 32]);
+    const int pos = positions[t];
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) ss = fmaf(x.get(i), x.get(i), ss);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float r = 1.0f / sqrtf(ss * (1.0f / kDc) + eps);
+    uint32_t q[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 a = make_float2(x.get(4 * i) * r * wv.get(4 * i) * inv_scale,
+                                   x.get(4 * i + 1) * r * wv.get(4 * i + 1) * inv_scale);
+      const float2 b = make_float2(x.get(4 * i + 2) * r * wv.get(4 * i + 2) * inv_scale,
+                                   x.get(4 * i + 3) * r * wv.get(4 * i + 3) * inv_scale);
+      q[i] = (uint32_t)__nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E4M3) |
+             ((uint32_t)__nv_cvt_float2_to_fp8x2(b, __NV_SATFINITE, __NV_E4M3) << 16);
+    }
+    uint8_t* dst = cache8 + slot * kRow8;
+    *reinterpret_cast<uint4*>(dst + lane * 16) = make_uint4(q[0], q[1], q[2], q[3]);
+    float cs, sn;
+    rope_cos_sin(pos, fhi, flo, &cs, &sn);
+    __nv_bfloat16* kr = reinterpret_cast<__nv_bfloat16*>(dst + kDc);
+    kr[lane] = __float2bfloat16_rn(x1 * cs - x2 * sn);
+    kr[lane + 32] = __float2bfloat16_rn(x2 * cs + x1 * sn);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_cache_write_fp8(const mla_config& cfg, const void* c_kv, const void* k_pe,
+                                   const int32_t* positions, const int64_t* slot_mapping,
+                                   int64_t num_tokens, const void* rms_weight, float kv_scale,
+                                   void* cache8, int64_t num_blocks, uint32_t* dev_status,
+                                   cudaStream_t stream) {
+  if (num_tokens == 0) return cudaSuccess;
+  int64_t blocks = (num_tokens + 7) / 8;
+  if (blocks > 4096) blocks = 4096;
+  return launch_pdl(cache_write_fp8_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
+                    (const __nv_bfloat16*)c_kv, (const __nv_bfloat16*)k_pe, positions,
+                    slot_mapping, num_tokens, (const __nv_bfloat16*)rms_weight, (uint8_t*)cache8,
+                    num_blocks * cfg.block_size, cfg.rms_eps, 1.0f / kv_scale,
+                    make_rope_freq((double)cfg.rope_base), dev_status);
+}
 
 cudaError_t launch_cache_write(const mla_config& cfg, const void* c_kv, const void* k_pe,
                                const int32_t* positions, const int64_t* slot_mapping,

@@ -19,6 +19,7 @@ constexpr int kDr = 64;           // qk_rope_head_dim
 constexpr int kDn = 128;          // qk_nope_head_dim
 constexpr int kDv = 128;          // v_head_dim
 constexpr int kRow = kDc + kDr;   // 576 values per cache row
+constexpr int kRow8 = kDc + 2 * kDr;  // 640 bytes per FP8 cache row: 512 e4m3 codes, 64 bf16
 constexpr int kTile = 64;         // kv tokens per work unit
 constexpr int kHG = 16;           // heads per query tile (one m16 row block)
 constexpr uint32_t kMagic = 0x4d4c4131u;  // "MLA1"

@@ -44,12 +44,20 @@ struct DecodeArgs {
   int32_t batch;
   int32_t self_plan;  // 0: planned; 1: self-planned; 2: self-planned, cache reads
                       // start before the preceding kernel has finished
+  float kv_scale;     // FP8 cache: the latent is the codes times kv_scale
 };
 
 cudaError_t launch_cache_write(const mla_config& cfg, const void* c_kv, const void* k_pe,
                                const int32_t* positions, const int64_t* slot_mapping,
                                int64_t num_tokens, const void* rms_weight, void* cache,
                                int64_t num_blocks, uint32_t* dev_status, cudaStream_t stream);
+
+// The FP8 cache row: 512 e4m3 codes of c_hat / kv_scale, then k_rot in bf16.
+cudaError_t launch_cache_write_fp8(const mla_config& cfg, const void* c_kv, const void* k_pe,
+                                   const int32_t* positions, const int64_t* slot_mapping,
+                                   int64_t num_tokens, const void* rms_weight, float kv_scale,
+                                   void* cache8, int64_t num_blocks, uint32_t* dev_status,
+                                   cudaStream_t stream);
 
 cudaError_t launch_absorb_q(const mla_config& cfg, const void* q_nope, const void* q_pe,
                             const int32_t* q_positions, const void* W_uk, void* q_abs,
@@ -58,8 +66,11 @@ cudaError_t launch_absorb_q(const mla_config& cfg, const void* q_nope, const voi
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream);
 cudaError_t launch_plan_tc(const PlanArgs& a, cudaStream_t stream);
 
+// rope_map non-null: the FP8 cache (cache_map views its rows as 640 bytes,
+// rope_map as 320 bf16), self-planned launches only.
 cudaError_t launch_decode_bf16(const DecodeArgs& a, const CUtensorMap& cache_map,
-                               const CUtensorMap& q_map, cudaStream_t stream);
+                               const CUtensorMap& q_map, const CUtensorMap* rope_map,
+                               cudaStream_t stream);
 
 cudaError_t launch_decode_f32(const DecodeArgs& a, cudaStream_t stream);
 

@@ -69,6 +69,12 @@ int decode_ctas(const mla_config* cfg, bool tc) {
   return C >= 2 ? (C & ~1) : 2;
 }
 
+// The FP8 cache's decode runs two CTAs to an SM by default.
+int decode_ctas_fp8(const mla_config* cfg) {
+  const int C = resolve_num_ctas(cfg);
+  return (cfg->num_ctas > 0 || C <= 0) ? C : 2 * C;
+}
+
 size_t ws_bytes_needed(const mla_config* cfg, int64_t num_q, int32_t batch, bool tc, int C) {
   const int G = cfg->num_heads / kHG;
   return tc ? ws_layout_tc(num_q, G, C / 2, batch).total : ws_layout(num_q, G, C).total;
@@ -118,6 +124,30 @@ bool make_map_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t row
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// The two views of the FP8 cache's 640-byte rows: the e4m3 codes as bytes
+// (boxes of 128 codes x box_rows rows, 128-byte swizzle) and the row as 320 bf16
+// values for the rope columns (elements 256-319; boxes of 64 x box_rows,
+// 128-byte swizzle).
+bool make_fp8_maps(CUtensorMap* codes, CUtensorMap* rope, const void* base, uint64_t rows,
+                   uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t stride[1] = {(cuuint64_t)kRow8};
+  const cuuint32_t estr[2] = {1, 1};
+  const cuuint64_t cdims[2] = {(cuuint64_t)kRow8, (cuuint64_t)rows};
+  const cuuint32_t cbox[2] = {128, box_rows};
+  CUresult r = fn(codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), cdims, stride,
+                  cbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  const cuuint64_t rdims[2] = {(cuuint64_t)kRow8 / 2, (cuuint64_t)rows};
+  const cuuint32_t rbox[2] = {64, box_rows};
+  r = fn(rope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), rdims, stride, rbox,
+         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -242,6 +272,13 @@ size_t mla_decode_workspace_size(const mla_config* cfg, int64_t num_q, int32_t b
   return ws_bytes_needed(cfg, num_q, batch, tc, C);
 }
 
+size_t mla_decode_fp8_workspace_size(const mla_config* cfg, int64_t num_q, int32_t batch) {
+  if (check_cfg(cfg) != MLA_OK || num_q < 0 || batch < 0) return 0;
+  const int C = decode_ctas_fp8(cfg);
+  if (C <= 0) return 0;
+  return ws_bytes_needed(cfg, num_q, batch, false, C);
+}
+
 mla_status mla_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
   if (!workspace || ws_bytes < sizeof(WsHeader) || !aligned(workspace, 256))
     return MLA_ERR_INVALID_ARGUMENT;
@@ -325,7 +362,7 @@ mla_status decode_impl(const mla_config* cfg, const void* q_abs, const void* cac
   if (!make_row_map(&cache_map, cache, map_rows, (uint32_t)cfg->block_size) ||
       !make_row_map(&q_map, q_abs, (uint64_t)num_q * cfg->num_heads, kHG))
     return MLA_ERR_CUDA;
-  return from_cuda(launch_decode_bf16(da, cache_map, q_map, st));
+  return from_cuda(launch_decode_bf16(da, cache_map, q_map, nullptr, st));
 }
 
 }  // namespace
@@ -432,6 +469,71 @@ mla_status mla_decode_paged_combine(const mla_config* cfg, const void* q_abs, co
   if (s != MLA_OK || !split_heavy) return s;
   return from_cuda(launch_combine(workspace, cfg->num_heads / kHG, C, num_q, batch, o_lat,
                                   as_stream(stream)));
+}
+
+mla_status mla_cache_write_fp8(const mla_config* cfg, const void* c_kv, const void* k_pe,
+                               const int32_t* positions, const int64_t* slot_mapping,
+                               int64_t num_tokens, const void* rms_weight, float kv_scale,
+                               void* cache8, int64_t num_blocks, uint32_t* dev_status,
+                               void* stream) {
+  mla_status s = check_cfg(cfg);
+  if (s != MLA_OK) return s;
+  if (cfg->dtype != MLA_BF16) return MLA_ERR_UNSUPPORTED;
+  if (num_tokens < 0 || num_blocks < 0 || !(kv_scale > 0.f) || !std::isfinite(kv_scale))
+    return MLA_ERR_INVALID_ARGUMENT;
+  if (num_tokens == 0) return MLA_OK;
+  if (!c_kv || !k_pe || !positions || !slot_mapping || !rms_weight || !cache8)
+    return MLA_ERR_INVALID_ARGUMENT;
+  if (!aligned(c_kv, 16) || !aligned(k_pe, 16) || !aligned(rms_weight, 16) ||
+      !aligned(cache8, 16) || !aligned(positions, 4) || !aligned(slot_mapping, 8) ||
+      !aligned(dev_status, 4))
+    return MLA_ERR_INVALID_ARGUMENT;
+  return from_cuda(launch_cache_write_fp8(*cfg, c_kv, k_pe, positions, slot_mapping, num_tokens,
+                                          rms_weight, kv_scale, cache8, num_blocks, dev_status,
+                                          as_stream(stream)));
+}
+
+mla_status mla_decode_paged_combine_fp8(const mla_config* cfg, const void* q_abs,
+                                        const void* cache8, int64_t num_blocks,
+                                        const int32_t* block_table, int32_t max_blocks_per_seq,
+                                        const int32_t* seq_lens, const int32_t* query_start_loc,
+                                        int32_t batch, int64_t num_q, float kv_scale,
+                                        void* workspace, size_t ws_bytes, float* o_lat,
+                                        void* stream) {
+  mla_status s = check_cfg(cfg);
+  if (s != MLA_OK) return s;
+  if (num_q < 0 || batch < 0 || num_blocks < 0 || max_blocks_per_seq < 0 ||
+      !(kv_scale > 0.f) || !std::isfinite(kv_scale))
+    return MLA_ERR_INVALID_ARGUMENT;
+  // the 16-head warp-mma path that plans for itself
+  if (!use_self_plan(cfg, num_q, batch)) return MLA_ERR_UNSUPPORTED;
+  if (num_blocks * cfg->block_size > ((int64_t)1 << 31)) return MLA_ERR_UNSUPPORTED;
+  if (!workspace || !aligned(workspace, 256)) return MLA_ERR_INVALID_ARGUMENT;
+  if (num_q == 0) return MLA_OK;
+  if (!q_abs || !cache8 || !block_table || !seq_lens || !query_start_loc || batch == 0 || !o_lat)
+    return MLA_ERR_INVALID_ARGUMENT;
+  if (!aligned(q_abs, 16) || !aligned(cache8, 16) || !aligned(block_table, 4) ||
+      !aligned(seq_lens, 4) || !aligned(query_start_loc, 4) || !aligned(o_lat, 16))
+    return MLA_ERR_INVALID_ARGUMENT;
+  const int C = decode_ctas_fp8(cfg);
+  if (C <= 0) return MLA_ERR_CUDA;
+  const int G = cfg->num_heads / kHG;
+  if (ws_bytes < ws_bytes_needed(cfg, num_q, batch, false, C)) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  const bool split_heavy = num_q * G * 4 < C;
+  const double log2e = 1.4426950408889634;
+  DecodeArgs da{q_abs, cache8, num_blocks, block_table, max_blocks_per_seq, cfg->block_size,
+                cfg->num_heads, G, C, num_q, (float)(cfg->softmax_scale * log2e), workspace,
+                split_heavy ? nullptr : o_lat, seq_lens, query_start_loc, batch, 2, kv_scale};
+  const uint64_t map_rows = num_blocks > 0 ? (uint64_t)num_blocks * cfg->block_size
+                                           : (uint64_t)cfg->block_size;
+  CUtensorMap codes_map, rope_map, q_map;
+  if (!make_fp8_maps(&codes_map, &rope_map, cache8, map_rows, (uint32_t)cfg->block_size) ||
+      !make_row_map(&q_map, q_abs, (uint64_t)num_q * cfg->num_heads, kHG))
+    return MLA_ERR_CUDA;
+  cudaStream_t st = as_stream(stream);
+  s = from_cuda(launch_decode_bf16(da, codes_map, q_map, &rope_map, st));
+  if (s != MLA_OK || !split_heavy) return s;
+  return from_cuda(launch_combine(workspace, G, C, num_q, batch, o_lat, st));
 }
 
 mla_status mla_combine(const mla_config* cfg, const void* workspace, size_t ws_bytes,

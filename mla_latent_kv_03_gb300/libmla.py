@@ -30,7 +30,9 @@ EXPORTS = (
     "mla_default_config", "mla_cache_write", "mla_absorb_q", "mla_decode_workspace_size",
     "mla_workspace_init", "mla_decode_paged", "mla_decode_plan", "mla_decode_planned",
     "mla_decode_combine", "mla_decode_paged_combine", "mla_decode_paged_noalloc",
-    "mla_combine_out_proj", "mla_naive_workspace_size", "mla_naive_cache_write",
+    "mla_combine_out_proj", "mla_cache_write_fp8", "mla_decode_fp8_workspace_size",
+    "mla_decode_paged_combine_fp8",
+    "mla_naive_workspace_size", "mla_naive_cache_write",
     "mla_latent_expand", "mla_naive_decode",
     "mla_combine", "mla_out_proj",
     "mla_get_device_status", "mla_selftest_wait_timeout", "mla_status_string", "mla_version",
@@ -63,6 +65,7 @@ _SIGS = {
     "mla_cache_write": (_i32, [_cfgp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _i64, _vp, _vp]),
     "mla_absorb_q": (_i32, [_cfgp, _vp, _vp, _vp, _vp, _vp, _i64, _vp]),
     "mla_decode_workspace_size": (_sz, [_cfgp, _i64, _i32]),
+    "mla_decode_fp8_workspace_size": (_sz, [_cfgp, _i64, _i32]),
     "mla_workspace_init": (_i32, [_vp, _sz, _vp]),
     "mla_decode_paged": (_i32, [_cfgp, _vp, _vp, _i64, _vp, _i32, _vp, _vp, _i32, _i64, _vp, _sz, _vp]),
     "mla_decode_plan": (_i32, [_cfgp, _vp, _vp, _i32, _i64, _i32, _vp, _sz, _vp]),
@@ -72,6 +75,10 @@ _SIGS = {
                                         _vp, _sz, _vp, _vp]),
     "mla_decode_paged_noalloc": (_i32, [_cfgp, _vp, _vp, _i64, _vp, _i32, _vp, _vp, _i32, _i64,
                                         _vp, _vp, _vp]),
+    "mla_cache_write_fp8": (_i32, [_cfgp, _vp, _vp, _vp, _vp, _i64, _vp, ctypes.c_float, _vp,
+                                   _i64, _vp, _vp]),
+    "mla_decode_paged_combine_fp8": (_i32, [_cfgp, _vp, _vp, _i64, _vp, _i32, _vp, _vp, _i32,
+                                            _i64, ctypes.c_float, _vp, _sz, _vp, _vp]),
     "mla_naive_workspace_size": (_sz, [_cfgp, _i64, _i32, _i64]),
     "mla_naive_cache_write": (_i32, [_cfgp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _i64,
                                      _vp, _sz, _vp]),
@@ -187,6 +194,10 @@ def mla_decode_workspace_size(cfg: MlaConfig, num_q: int, batch: int) -> int:
     return int(load().mla_decode_workspace_size(ctypes.byref(cfg), num_q, batch))
 
 
+def mla_decode_fp8_workspace_size(cfg: MlaConfig, num_q: int, batch: int) -> int:
+    return int(load().mla_decode_fp8_workspace_size(ctypes.byref(cfg), num_q, batch))
+
+
 def mla_workspace_init(workspace, stream=None) -> None:
     _check(load().mla_workspace_init(_ptr(workspace, None, "workspace"), workspace.numel() *
                                      workspace.element_size(), _stream(stream)),
@@ -255,6 +266,30 @@ def mla_decode_paged_noalloc(cfg: MlaConfig, q_abs, cache, block_table, seq_lens
         _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(query_start_loc, torch.int32, "query_start_loc"),
         seq_lens.shape[0], q_abs.shape[0], _ptr(o_lat, torch.float32, "o_lat"),
         _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)), "mla_decode_paged_noalloc")
+
+
+def mla_cache_write_fp8(cfg: MlaConfig, c_kv, k_pe, positions, slot_mapping, rms_weight,
+                        kv_scale: float, cache8, status, stream=None) -> None:
+    dt = _torch_dtype(cfg)
+    _check(load().mla_cache_write_fp8(
+        ctypes.byref(cfg), _ptr(c_kv, dt, "c_kv"), _ptr(k_pe, dt, "k_pe"),
+        _ptr(positions, torch.int32, "positions"), _ptr(slot_mapping, torch.int64, "slot_mapping"),
+        c_kv.shape[0], _ptr(rms_weight, dt, "rms_weight"), float(kv_scale),
+        _ptr(cache8, torch.uint8, "cache8"), cache8.shape[0], _ptr(status, None, "status"),
+        _stream(stream)), "mla_cache_write_fp8")
+
+
+def mla_decode_paged_combine_fp8(cfg: MlaConfig, q_abs, cache8, block_table, seq_lens,
+                                 query_start_loc, kv_scale: float, workspace, o_lat,
+                                 stream=None) -> None:
+    dt = _torch_dtype(cfg)
+    _check(load().mla_decode_paged_combine_fp8(
+        ctypes.byref(cfg), _ptr(q_abs, dt, "q_abs"), _ptr(cache8, torch.uint8, "cache8"),
+        cache8.shape[0], _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+        _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(query_start_loc, torch.int32, "query_start_loc"),
+        seq_lens.shape[0], q_abs.shape[0], float(kv_scale), _ptr(workspace, None, "workspace"),
+        _nbytes(workspace), _ptr(o_lat, torch.float32, "o_lat"), _stream(stream)),
+        "mla_decode_paged_combine_fp8")
 
 
 def mla_naive_workspace_size(cfg: MlaConfig, num_q: int, max_blocks_per_seq: int,

@@ -129,6 +129,30 @@ class MlaDecodeStep:
         self.out_proj(stream)
         return self.out
 
+    # -- the FP8 latent cache -----------------------------------------------
+    def fp8_setup(self, kv_scale: float) -> None:
+        """The FP8 cache ([num_blocks, block_size, 640] bytes) and its scale."""
+        w = self.w
+        self.kv_scale = float(kv_scale)
+        self.cache8 = torch.empty((w.num_blocks, w.block_size, 640), dtype=torch.uint8,
+                                  device=self.device)
+        need = L.mla_decode_fp8_workspace_size(self.cfg, int(w.num_q), w.batch)
+        if need == 0:
+            raise L.MlaError(L.MLA_OK + 2, "mla_decode_fp8_workspace_size")
+        if need > self.workspace.numel():
+            self.workspace = torch.empty(need, dtype=torch.uint8, device=self.device)
+            L.mla_workspace_init(self.workspace)
+
+    def fp8_populate(self) -> None:
+        L.mla_cache_write_fp8(self.cfg, self.c_kv, self.k_pe, self.kv_positions,
+                              self.slot_mapping, self.rms_weight, self.kv_scale, self.cache8,
+                              self.status)
+
+    def decode_paged_combine_fp8(self, stream=None) -> None:
+        L.mla_decode_paged_combine_fp8(self.cfg, self.q_abs, self.cache8, self.block_table,
+                                       self.seq_lens, self.query_start_loc, self.kv_scale,
+                                       self.workspace, self.o_lat, stream=stream)
+
     # -- the pages' other two forms (full K/V cache; latent re-expanded) ----
     def naive_setup(self) -> None:
         """Buffers of the expanded cache ([num_blocks, block_size, H, 320]) and
