@@ -54,6 +54,9 @@ PROFILES = {
     ("decode_bf16_kernel", "serving"): (
         "decode_bf16_serving_B64_L4096.md",
         ["decode_bf16.cu", "common.cuh", "sched.cuh", "merge.cuh", "async_copy.cuh"]),
+    ("decode_bf16_kernel_fp8", "serving"): (
+        "decode_bf16_fp8_serving_B64_L4096.md",
+        ["decode_bf16.cu", "common.cuh", "sched.cuh", "merge.cuh", "async_copy.cuh"]),
     ("decode_tc_kernel", "ragged_h128"): (
         "decode_tc_ragged_B32_H128.md",
         ["decode_tc.cu", "common.cuh", "cluster.cuh", "tcgen05.cuh", "merge.cuh", "async_copy.cuh"]),
