@@ -80,11 +80,15 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--ref-seconds", type=float, default=120.0,
                    help="host time the reference arm's timed steps aim at in total")
-    p.add_argument("--form", choices=["absorbed", "full_kv", "latent", "fp8"], default="absorbed",
+    p.add_argument("--form", choices=["absorbed", "full_kv", "latent", "fp8", "layer"],
+                   default="absorbed",
                    help="absorbed: the latent decode (default); full_kv: the page's version 1 "
                         "(expanded K/V cache, decode only); latent: version 2 (the latent cache "
                         "re-expanded every step, then the same decode); fp8: the absorbed step "
-                        "over an e4m3 latent cache (640 bytes per token, kv_scale 0.02)")
+                        "over an e4m3 latent cache (640 bytes per token, kv_scale 0.02); "
+                        "layer: the whole attention layer from the hidden states (q_proj, "
+                        "kv_a_proj and the cache write of the new tokens, the absorbed step, "
+                        "o_proj; hidden size 2048)")
     return p.parse_args(argv)
 
 
@@ -345,6 +349,21 @@ def cpu_baseline(w, seconds: float):
 # our arm
 # ---------------------------------------------------------------------------
 
+HIDDEN_SIZE = 2048   # DeepSeek-V2-Lite's hidden size, for --form layer
+
+
+def proj_launches(M, N, K, sms):
+    """Kernels of one projection call: the tile kernel, plus the sum of the
+    K splits when the library splits K (fewer than two tiles per SM; the
+    split doubles while that holds, it divides the 64-wide K steps and it is
+    below 8)."""
+    tiles = ((M + 63) // 64) * (N // 64)
+    s = 1
+    while tiles * s < 2 * sms and (K // 64) % (2 * s) == 0 and s < 8:
+        s *= 2
+    return 2 if s > 1 else 1
+
+
 def decode_call_launches(w, props):
     """(self-planned, kernel launches) of one mla_decode_paged_combine call,
     following the library's choice: the 16-head warp-mma path plans inside
@@ -376,7 +395,7 @@ def run_ours(args, world, rank, local):
     mixed = bool(w.is_new.sum() > w.batch)   # a step that writes more than one token per sequence
     form = args.form
     if form != "absorbed" and (mixed or w.dtype != "bf16"):
-        raise SystemExit("--form full_kv / latent / fp8: bf16 decode workloads only")
+        raise SystemExit("--form full_kv / latent / fp8 / layer: bf16 decode workloads only")
     s = MlaDecodeStep(w, device=dev)
     s.populate(include_new=not mixed)
     if form in ("full_kv", "latent"):
@@ -386,6 +405,9 @@ def run_ours(args, world, rank, local):
     if form == "fp8":
         s.fp8_setup(0.02)             # about max |c_hat| / 448 for these inputs
         s.fp8_populate()
+    if form == "layer":
+        s.layer_setup(HIDDEN_SIZE)
+        s.layer_populate()            # the old tokens' rows from their projected latents
     torch.cuda.synchronize()
     latent = step_latent_bytes(w)
     if form == "fp8":
@@ -396,6 +418,9 @@ def run_ours(args, world, rank, local):
     self_planned, decode_launches = decode_call_launches(w, torch.cuda.get_device_properties(dev))
 
     def one_step():
+        if form == "layer":
+            s.layer_step()
+            return
         if form == "fp8":
             s.absorb()
             s.decode_paged_combine_fp8()
@@ -434,6 +459,14 @@ def run_ours(args, world, rank, local):
     if form in ("full_kv", "latent"):
         # decode + merge; version 2 adds the weight transpose and the expansion
         launches_per_step = 2 if form == "full_kv" else 4
+    if form == "layer":
+        # the absorbed step, the new tokens' cache write, and the three
+        # projections (each one kernel, plus its split-K sum when it splits)
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        H, T = w.num_heads, w.num_q
+        launches_per_step = 2 + decode_launches + 1 + sum(
+            proj_launches(T, n, k, sms) for n, k in
+            ((H * 192, HIDDEN_SIZE), (576, HIDDEN_SIZE), (HIDDEN_SIZE, H * 128)))
     # eager warm-up (also builds the lazy state), then capture one step
     with torch.cuda.stream(stream):
         for _ in range(3):
@@ -556,6 +589,7 @@ def run_ours(args, world, rank, local):
 
     # ---- end to end through the same calls, host buffers, eager launches
     e2e = run_e2e(args, s, w, stream, latent, world, mixed, one_step,
+                  s.y if form == "layer" else
                   s.out if form in ("absorbed", "fp8") else s.out_naive)
 
     # ---- status: the timed work must not have flagged anything
@@ -566,6 +600,10 @@ def run_ours(args, world, rank, local):
         st3, bits3 = L.mla_get_device_status(s.naive_ws)
         if st3 != 0:
             raise SystemExit(f"device status after bench: {form} {bits3:#x}")
+    if form == "layer":
+        st3, bits3 = L.mla_get_device_status(s.proj_ws)
+        if st3 != 0:
+            raise SystemExit(f"device status after bench: projections {bits3:#x}")
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -603,6 +641,10 @@ def run_e2e(args, s, w, stream, latent, world, mixed, one_step, out):
     steps like the device-resident timing."""
     import torch
     names = ["q_nope", "q_pe", "q_positions", "seq_lens", "query_start_loc", "block_table"]
+    if hasattr(s, "hidden_new") and out is getattr(s, "y", None):
+        # the layer step: the new tokens' hidden states replace q and the latents
+        names = ["hidden_new", "q_positions", "seq_lens", "query_start_loc", "block_table",
+                 "pos_new", "slot_new"]
     if mixed:
         names += ["c_kv_new", "k_pe_new", "pos_new", "slot_new"]
     ins = [getattr(s, n) for n in names]

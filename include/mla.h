@@ -414,6 +414,44 @@ mla_status mla_combine_out_proj(const mla_config* cfg, const void* workspace, si
                                 void* stream);
 
 /*
+ * Projections on either side of the attention ([MI17] "版本 1:
+ * MLAAttentionNaive": q_proj, kv_a_proj_with_mqa, o_proj; [VLB07] 2.2). bf16
+ * only (MLA_ERR_UNSUPPORTED otherwise); hidden_size a positive multiple of 64,
+ * num_tokens <= 2^30. Each computes Y = X W^T in fp32 with one rounding to
+ * bf16, W in a linear layer's [out, in] layout, all tensors row-major and
+ * 16-byte aligned:
+ *
+ * mla_q_proj:    hidden [T, hidden_size], W_q [H * 192, hidden_size] (rows
+ *                h * 192 + 0..127 give q_nope[:, h], h * 192 + 128..191 give
+ *                q_pe[:, h]); q_nope [T, H, 128], q_pe [T, H, 64] (outputs).
+ * mla_kv_a_proj: hidden [T, hidden_size], W_kv_a [576, hidden_size] (rows
+ *                0..511 give c_kv, 512..575 give k_pe); c_kv [T, 512],
+ *                k_pe [T, 64] (outputs) -- the raw inputs of mla_cache_write,
+ *                which applies the kv_a_layernorm and RoPE.
+ * mla_o_proj:    attn_out [T, H * 128] (the [T, H, 128] out of mla_out_proj),
+ *                W_o [hidden_size, H * 128]; y [T, hidden_size] (output).
+ *
+ * workspace: mla_proj_workspace_size(cfg, num_tokens, hidden_size) bytes,
+ * 256-byte aligned; its first 4 bytes are a device status word (zero it with
+ * mla_workspace_init once; a wait that ran out sets MLA_DEV_TIMEOUT, read it
+ * with mla_get_device_status); the rest holds fp32 partial sums when K is
+ * split across CTAs (few tokens). Results do not depend on the split beyond
+ * fp32 rounding order, and repeated calls agree bit for bit. The weight may be
+ * read before the kernel launched just before the call on the same stream has
+ * finished, so that kernel must not write it.
+ */
+size_t mla_proj_workspace_size(const mla_config* cfg, int64_t num_tokens, int32_t hidden_size);
+mla_status mla_q_proj(const mla_config* cfg, const void* hidden, const void* W_q, void* q_nope,
+                      void* q_pe, int64_t num_tokens, int32_t hidden_size, void* workspace,
+                      size_t ws_bytes, void* stream);
+mla_status mla_kv_a_proj(const mla_config* cfg, const void* hidden, const void* W_kv_a,
+                         void* c_kv, void* k_pe, int64_t num_tokens, int32_t hidden_size,
+                         void* workspace, size_t ws_bytes, void* stream);
+mla_status mla_o_proj(const mla_config* cfg, const void* attn_out, const void* W_o, void* y,
+                      int64_t num_tokens, int32_t hidden_size, void* workspace, size_t ws_bytes,
+                      void* stream);
+
+/*
  * mla_get_device_status -- synchronise `stream`, read the device status word
  * at `status_word` (a workspace's first word, or the dev_status buffer given
  * to mla_cache_write), optionally clear it, and map it to a status: the

@@ -32,6 +32,7 @@ EXPORTS = (
     "mla_decode_combine", "mla_decode_paged_combine", "mla_decode_paged_noalloc",
     "mla_combine_out_proj", "mla_cache_write_fp8", "mla_decode_fp8_workspace_size",
     "mla_decode_paged_combine_fp8",
+    "mla_proj_workspace_size", "mla_q_proj", "mla_kv_a_proj", "mla_o_proj",
     "mla_naive_workspace_size", "mla_naive_cache_write",
     "mla_latent_expand", "mla_naive_decode",
     "mla_combine", "mla_out_proj",
@@ -66,6 +67,10 @@ _SIGS = {
     "mla_absorb_q": (_i32, [_cfgp, _vp, _vp, _vp, _vp, _vp, _i64, _vp]),
     "mla_decode_workspace_size": (_sz, [_cfgp, _i64, _i32]),
     "mla_decode_fp8_workspace_size": (_sz, [_cfgp, _i64, _i32]),
+    "mla_proj_workspace_size": (_sz, [_cfgp, _i64, _i32]),
+    "mla_q_proj": (_i32, [_cfgp, _vp, _vp, _vp, _vp, _i64, _i32, _vp, _sz, _vp]),
+    "mla_kv_a_proj": (_i32, [_cfgp, _vp, _vp, _vp, _vp, _i64, _i32, _vp, _sz, _vp]),
+    "mla_o_proj": (_i32, [_cfgp, _vp, _vp, _vp, _i64, _i32, _vp, _sz, _vp]),
     "mla_workspace_init": (_i32, [_vp, _sz, _vp]),
     "mla_decode_paged": (_i32, [_cfgp, _vp, _vp, _i64, _vp, _i32, _vp, _vp, _i32, _i64, _vp, _sz, _vp]),
     "mla_decode_plan": (_i32, [_cfgp, _vp, _vp, _i32, _i64, _i32, _vp, _sz, _vp]),
@@ -359,6 +364,37 @@ def mla_out_proj(cfg: MlaConfig, o_lat, W_uv, out, stream=None) -> None:
     _check(load().mla_out_proj(
         ctypes.byref(cfg), _ptr(o_lat, torch.float32, "o_lat"), _ptr(W_uv, dt, "W_uv"),
         _ptr(out, dt, "out"), o_lat.shape[0], _stream(stream)), "mla_out_proj")
+
+
+def mla_proj_workspace_size(cfg: MlaConfig, num_tokens: int, hidden_size: int) -> int:
+    return int(load().mla_proj_workspace_size(ctypes.byref(cfg), num_tokens, hidden_size))
+
+
+def mla_q_proj(cfg: MlaConfig, hidden, W_q, q_nope, q_pe, workspace, stream=None) -> None:
+    dt = _torch_dtype(cfg)
+    _check(load().mla_q_proj(
+        ctypes.byref(cfg), _ptr(hidden, dt, "hidden"), _ptr(W_q, dt, "W_q"),
+        _ptr(q_nope, dt, "q_nope"), _ptr(q_pe, dt, "q_pe"), hidden.shape[0], hidden.shape[1],
+        _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream)), "mla_q_proj")
+
+
+def mla_kv_a_proj(cfg: MlaConfig, hidden, W_kv_a, c_kv, k_pe, workspace, stream=None) -> None:
+    dt = _torch_dtype(cfg)
+    _check(load().mla_kv_a_proj(
+        ctypes.byref(cfg), _ptr(hidden, dt, "hidden"), _ptr(W_kv_a, dt, "W_kv_a"),
+        _ptr(c_kv, dt, "c_kv"), _ptr(k_pe, dt, "k_pe"), hidden.shape[0], hidden.shape[1],
+        _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream)), "mla_kv_a_proj")
+
+
+def mla_o_proj(cfg: MlaConfig, attn_out, W_o, y, workspace, stream=None) -> None:
+    dt = _torch_dtype(cfg)
+    _check(load().mla_o_proj(
+        ctypes.byref(cfg), _ptr(attn_out, dt, "attn_out"), _ptr(W_o, dt, "W_o"),
+        _ptr(y, dt, "y"), attn_out.shape[0], y.shape[1],
+        _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream)), "mla_o_proj")
 
 
 def mla_get_device_status(status_word, clear: bool = True, stream=None):

@@ -14,6 +14,7 @@ import numpy as np
 import torch
 
 from . import libmla as L
+from . import workloads as W
 from .workloads import Workload
 
 
@@ -152,6 +153,54 @@ class MlaDecodeStep:
         L.mla_decode_paged_combine_fp8(self.cfg, self.q_abs, self.cache8, self.block_table,
                                        self.seq_lens, self.query_start_loc, self.kv_scale,
                                        self.workspace, self.o_lat, stream=stream)
+
+    # -- the projections either side (the whole attention layer) -----------
+    def layer_setup(self, hidden_size: int = 2048, seed: int = 7) -> None:
+        """Hidden states of every token and the q_proj / kv_a_proj / o_proj
+        weights (bf16), plus the buffers the layer step writes."""
+        w, dev = self.w, self.device
+        li = W.layer_inputs(w, hidden_size, seed)
+        self.layer = li
+        self.hidden_size = hidden_size
+        dt = torch.bfloat16
+        self.hidden = _dev(li.hidden, dt, dev)
+        self.W_q = _dev(li.W_q, dt, dev)
+        self.W_kv_a = _dev(li.W_kv_a, dt, dev)
+        self.W_o = _dev(li.W_o, dt, dev)
+        new = torch.from_numpy(np.nonzero(w.is_new)[0]).to(dev)
+        self.hidden_new = self.hidden[new].contiguous()
+        self.y = torch.empty((w.num_q, hidden_size), dtype=dt, device=dev)
+        # the split (and so the partials' size) depends on the token count
+        need = min(L.mla_proj_workspace_size(self.cfg, max(n, 1), hidden_size)
+                   for n in (w.num_tokens, w.num_q))
+        need = max(L.mla_proj_workspace_size(self.cfg, max(n, 1), hidden_size)
+                   for n in (w.num_tokens, w.num_q)) if need else 0
+        if need == 0:
+            raise L.MlaError(L.MLA_OK + 2, "mla_proj_workspace_size")
+        self.proj_ws = torch.empty(need, dtype=torch.uint8, device=dev)
+        L.mla_workspace_init(self.proj_ws)
+
+    def layer_populate(self) -> None:
+        """kv_a_proj of every token, then the cache write of the old ones."""
+        L.mla_kv_a_proj(self.cfg, self.hidden, self.W_kv_a, self.c_kv, self.k_pe, self.proj_ws)
+        new = torch.from_numpy(np.nonzero(self.w.is_new)[0]).to(self.device)
+        self.c_kv_new = self.c_kv[new].contiguous()
+        self.k_pe_new = self.k_pe[new].contiguous()
+        self.populate(include_new=False)
+
+    def layer_step(self, stream=None) -> torch.Tensor:
+        """One decode step of the whole layer: q_proj and kv_a_proj of the new
+        tokens, their cache write, absorb, decode + merge, out_proj, o_proj."""
+        L.mla_q_proj(self.cfg, self.hidden_new, self.W_q, self.q_nope, self.q_pe, self.proj_ws,
+                     stream=stream)
+        L.mla_kv_a_proj(self.cfg, self.hidden_new, self.W_kv_a, self.c_kv_new, self.k_pe_new,
+                        self.proj_ws, stream=stream)
+        self.write_new(stream=stream)
+        self.absorb(stream=stream)
+        self.decode_paged_combine(stream=stream)
+        self.out_proj(stream=stream)
+        L.mla_o_proj(self.cfg, self.out, self.W_o, self.y, self.proj_ws, stream=stream)
+        return self.y
 
     # -- the pages' other two forms (full K/V cache; latent re-expanded) ----
     def naive_setup(self) -> None:

@@ -167,6 +167,31 @@ def make(name: str, seq_lens, q_lens, num_heads: int, block_size: int, dtype: st
         rms_weight=np.ones(KV_LORA_RANK, dtype=np.float32))
 
 
+@dataclasses.dataclass
+class LayerInputs:
+    """Inputs of the projections either side of the attention for one
+    workload: every token's hidden state (in the workload's token order) and
+    the three weights in a linear layer's [out, in] layout."""
+    hidden: np.ndarray   # f32 [T, D] (bf16 values)
+    W_q: np.ndarray      # f32 [H * 192, D]
+    W_kv_a: np.ndarray   # f32 [576, D]
+    W_o: np.ndarray      # f32 [D, H * 128]
+
+
+def layer_inputs(w: Workload, hidden_size: int = 2048, seed: int = 7) -> LayerInputs:
+    """hidden ~ N(0, 1); W_q, W_kv_a ~ N(0, 1/D); W_o ~ N(0, 1/(H * 128));
+    all rounded to bf16. D = 2048 is DeepSeek-V2-Lite's hidden size."""
+    rng = np.random.default_rng(seed)
+    H, D, T = w.num_heads, hidden_size, w.num_tokens
+    s_in = np.float32(1.0 / math.sqrt(D))
+    hidden = rng.standard_normal((T, D), dtype=np.float32)
+    W_q = rng.standard_normal((H * (NOPE_DIM + ROPE_DIM), D), dtype=np.float32) * s_in
+    W_kv_a = rng.standard_normal((KV_LORA_RANK + ROPE_DIM, D), dtype=np.float32) * s_in
+    W_o = rng.standard_normal((D, H * V_DIM), dtype=np.float32) * np.float32(1.0 / math.sqrt(H * V_DIM))
+    r = lambda a: round_to_dtype(a, "bf16")  # noqa: E731
+    return LayerInputs(hidden=r(hidden), W_q=r(W_q), W_kv_a=r(W_kv_a), W_o=r(W_o))
+
+
 # The workloads the pages' statement of the problem names, plus small cases of
 # the same shapes that the oracle finishes in seconds.
 def tiny(seed: int = 1) -> Workload:

@@ -377,6 +377,49 @@ def mla_sequence_absorbed(c_kv_raw, k_pe_raw, kv_positions, q_nope, q_pe,
     return out_proj(o_lat, W_uv), o_lat, lse
 
 
+# ---------------------------------------------------------------------------
+# Projections either side of the attention ([MI17] "版本 1: MLAAttentionNaive":
+# q_proj, kv_a_proj_with_mqa, o_proj; [VLB07] 2.2). Weights are in a linear
+# layer's [out, in] layout: y = x W^T.
+# ---------------------------------------------------------------------------
+
+def q_proj(hidden, W_q, num_heads: int):
+    """q = hidden W_q^T viewed per head as [qk_nope | qk_rope] and split:
+    returns (q_nope [T, H, 128], q_pe [T, H, 64])."""
+    q = _f64(hidden) @ _f64(W_q).T
+    q = q.reshape(q.shape[0], num_heads, QK_NOPE_HEAD_DIM + QK_ROPE_HEAD_DIM)
+    return q[..., :QK_NOPE_HEAD_DIM], q[..., QK_NOPE_HEAD_DIM:]
+
+
+def kv_a_proj(hidden, W_kv_a):
+    """kv_a_proj_with_mqa: hidden W_kv_a^T split into the latent and the
+    shared rope key: returns (c_kv [T, 512], k_pe [T, 64]), both raw (the
+    kv_a_layernorm and RoPE come after, in the cache write)."""
+    kv = _f64(hidden) @ _f64(W_kv_a).T
+    return kv[:, :KV_LORA_RANK], kv[:, KV_LORA_RANK:]
+
+
+def o_proj(attn_out, W_o):
+    """o_proj over the heads' concatenated values: attn_out [T, H, 128]
+    flattened to [T, H * 128], times W_o^T -> [T, hidden]."""
+    a = _f64(attn_out)
+    return a.reshape(a.shape[0], -1) @ _f64(W_o).T
+
+
+def mla_layer_naive(hidden, kv_positions, W_q, W_kv_a, W_uk, W_uv, W_o, rms_weight,
+                    eps: float, base: float, scale: float, num_new: int) -> np.ndarray:
+    """One sequence through the whole attention layer in the naive form: the
+    sequence's hidden states (all of its tokens, the last num_new of them
+    being the step's queries) projected to queries and to latents, the naive
+    attention, o_proj. Returns [num_new, hidden]. [MI17] "版本 1"."""
+    q_nope, q_pe = q_proj(hidden[-num_new:], W_q, _f64(W_uk).shape[0])
+    c_kv, k_pe = kv_a_proj(hidden, W_kv_a)
+    q_positions = np.asarray(kv_positions)[-num_new:]
+    out = mla_sequence_naive(c_kv, k_pe, kv_positions, q_nope, q_pe, q_positions, W_uk, W_uv,
+                             rms_weight, eps, base, scale)
+    return o_proj(out, W_o)
+
+
 def gather_paged(cache, block_table_row, seq_len: int, block_size: int):
     """Read one sequence's rows back out of a paged cache, in logical order.
 

@@ -497,3 +497,95 @@ def test_fp8_rows_dequantise_within_half_a_step():
     # and a plain rounding would not be enough: the error is that of e4m3, not bf16
     assert np.max(np.abs(deq - c_hat)) > 2.0 ** -9
     assert np.array_equal(k_rot, O.rope(k_pe, np.arange(40), 1e4))
+
+
+# ---------------------------------------------------------------------------
+# Projections either side of the attention. With one-hot weights a projection
+# only moves inputs, so the layout the page states (q_proj viewed per head as
+# [qk_nope | qk_rope] then split; the kv_a output split at kv_lora_rank; o_proj
+# over the heads' values laid head after head) is checked entry by entry.
+# ---------------------------------------------------------------------------
+
+def _one_hot(rows, cols, rng):
+    src = rng.permutation(cols)[:rows]
+    Wt = np.zeros((rows, cols))
+    Wt[np.arange(rows), src] = 1.0
+    return Wt, src
+
+
+def test_q_proj_one_hot_weights_pick_head_major_nope_then_rope():
+    rng = np.random.default_rng(21)
+    H, D = 3, 640
+    W_q, src = _one_hot(H * 192, D, rng)
+    x = rng.standard_normal((4, D))
+    q_nope, q_pe = O.q_proj(x, W_q, H)
+    assert q_nope.shape == (4, H, 128) and q_pe.shape == (4, H, 64)
+    for t in range(4):
+        for h in range(H):
+            for d in range(128):
+                assert q_nope[t, h, d] == x[t, src[h * 192 + d]]
+            for d in range(64):
+                assert q_pe[t, h, d] == x[t, src[h * 192 + 128 + d]]
+
+
+def test_kv_a_proj_one_hot_weights_split_latent_then_rope_key():
+    rng = np.random.default_rng(22)
+    D = 704
+    W, src = _one_hot(576, D, rng)
+    x = rng.standard_normal((3, D))
+    c_kv, k_pe = O.kv_a_proj(x, W)
+    assert c_kv.shape == (3, 512) and k_pe.shape == (3, 64)
+    for t in range(3):
+        assert all(c_kv[t, c] == x[t, src[c]] for c in range(512))
+        assert all(k_pe[t, d] == x[t, src[512 + d]] for d in range(64))
+
+
+def test_o_proj_one_hot_weights_read_heads_in_order():
+    rng = np.random.default_rng(23)
+    H, D = 2, 192
+    W_o, src = _one_hot(D, H * 128, rng)
+    a = rng.standard_normal((5, H, 128))
+    y = O.o_proj(a, W_o)
+    for t in range(5):
+        for j in range(D):
+            h, v = divmod(int(src[j]), 128)
+            assert y[t, j] == a[t, h, v]
+
+
+def test_projections_are_linear_in_the_weight_rows():
+    # a weight row that is the sum of two one-hot rows adds the two inputs
+    rng = np.random.default_rng(24)
+    D = 256
+    x = rng.standard_normal((2, D))
+    W = np.zeros((576, D))
+    W[7, 3] = 1.0
+    W[7, 11] = 2.0
+    W[600 - 30, 5] = -1.0
+    c_kv, k_pe = O.kv_a_proj(x, W)
+    assert np.allclose(c_kv[:, 7], x[:, 3] + 2 * x[:, 11], rtol=0, atol=1e-15)
+    assert np.allclose(k_pe[:, 570 - 512], -x[:, 5], rtol=0, atol=1e-15)
+
+
+def test_layer_naive_equals_absorbed_and_is_causal():
+    rng = np.random.default_rng(25)
+    H, D, T, new = 2, 256, 9, 3
+    hid = rng.standard_normal((T, D))
+    s = 1 / math.sqrt(D)
+    W_q = rng.standard_normal((H * 192, D)) * s
+    W_kv_a = rng.standard_normal((576, D)) * s
+    W_uk = rng.standard_normal((H, 512, 128)) / math.sqrt(512)
+    W_uv = rng.standard_normal((H, 512, 128)) / math.sqrt(512)
+    W_o = rng.standard_normal((D, H * 128)) / math.sqrt(H * 128)
+    pos = np.arange(T)
+    args = (W_q, W_kv_a, W_uk, W_uv, W_o, np.ones(512), 1e-6, 1e4, 1 / math.sqrt(192))
+    y = O.mla_layer_naive(hid, pos, *args, num_new=new)
+    # the same layer through the absorbed form
+    q_nope, q_pe = O.q_proj(hid[-new:], W_q, H)
+    c_kv, k_pe = O.kv_a_proj(hid, W_kv_a)
+    out, _, _ = O.mla_sequence_absorbed(c_kv, k_pe, pos, q_nope, q_pe, pos[-new:], W_uk, W_uv,
+                                        np.ones(512), 1e-6, 1e4, 1 / math.sqrt(192))
+    assert np.allclose(y, O.o_proj(out, W_o), rtol=1e-12, atol=1e-12)
+    # query row j sees tokens up to its own position: dropping later tokens
+    # leaves it unchanged
+    y_short = O.mla_layer_naive(hid[:T - 1], pos[:T - 1], *args, num_new=new - 1)
+    assert np.allclose(y[:new - 1], y_short, rtol=1e-12, atol=1e-12)
