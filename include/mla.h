@@ -90,6 +90,9 @@ typedef struct {
   float rope_base;       /* RoPE base (10000 for DeepSeek-V2-Lite)            */
   int32_t dtype;         /* mla_dtype                                         */
   int32_t num_ctas;      /* 0 = one per SM                                    */
+  int32_t rope_interleaved; /* RoPE pairs: 0 = (i, i + 32) (rotate-half, the
+                               default), 1 = (2i, 2i + 1); the same pairing
+                               for k_pe and q_pe, inv_freq_i = base^(-2i/64) */
 } mla_config;
 
 void mla_default_config(mla_config* cfg, int32_t num_heads, int32_t block_size,

@@ -15,6 +15,7 @@
 // Every wait is bounded; a CTA that times out writes NaN rows.
 #include "async_copy.cuh"
 #include "common.cuh"
+#include "rope_pairs.cuh"
 #include "internal.h"
 #include "tcgen05.cuh"
 
@@ -40,7 +41,7 @@ struct AbSmem {
 __global__ void __launch_bounds__(kAbThreads) absorb_tc_kernel(
     const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap w_map,
     const __nv_bfloat16* __restrict__ q_pe, const int32_t* __restrict__ q_pos,
-    __nv_bfloat16* __restrict__ q_abs, int num_q, int H, RopeFreq freq) {
+    __nv_bfloat16* __restrict__ q_abs, int num_q, int H, RopeFreq freq, int interleaved) {
   extern __shared__ uint8_t smem_raw[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.z, row0 = blockIdx.x * kAbRows;
@@ -131,7 +132,7 @@ __global__ void __launch_bounds__(kAbThreads) absorb_tc_kernel(
   if (blockIdx.y == 0) {
     // rotate-half RoPE of q_pe into q_abs[..., 512:576] for this CTA's rows
     // (warp w: rows w + 4 i; lane: pair p), eight rows' loads in flight at a time
-    const int p = lane;
+    const int p = lane, i1 = rope_i1(interleaved, p), i2 = rope_i2(interleaved, p);
     const float fhi = freq.hi[p], flo = freq.lo[p];
 #pragma unroll 1
     for (int rb = warp; rb < kAbRows; rb += 32) {
@@ -142,8 +143,8 @@ __global__ void __launch_bounds__(kAbThreads) absorb_tc_kernel(
         const int n = row0 + rb + 4 * u;
         const bool ok = n < num_q;
         const __nv_bfloat16* x = q_pe + ((size_t)(ok ? n : 0) * H + h) * kDr;
-        x1[u] = ok ? __bfloat162float(x[p]) : 0.f;
-        x2[u] = ok ? __bfloat162float(x[p + 32]) : 0.f;
+        x1[u] = ok ? __bfloat162float(x[i1]) : 0.f;
+        x2[u] = ok ? __bfloat162float(x[i2]) : 0.f;
         pos[u] = ok ? q_pos[n] : 0;
       }
 #pragma unroll
@@ -153,8 +154,8 @@ __global__ void __launch_bounds__(kAbThreads) absorb_tc_kernel(
         float cs, sn;
         rope_cos_sin(pos[u], fhi, flo, &cs, &sn);
         __nv_bfloat16* o = q_abs + ((size_t)n * H + h) * kRow + kDc;
-        o[p] = __float2bfloat16_rn(x1[u] * cs - x2[u] * sn);
-        o[p + 32] = __float2bfloat16_rn(x2[u] * cs + x1[u] * sn);
+        o[i1] = __float2bfloat16_rn(x1[u] * cs - x2[u] * sn);
+        o[i2] = __float2bfloat16_rn(x2[u] * cs + x1[u] * sn);
       }
     }
   }
@@ -175,7 +176,8 @@ cudaError_t launch_absorb_tc(const CUtensorMap& q_map, const CUtensorMap& w_map,
   return launch_pdl(absorb_tc_kernel,
                     dim3((unsigned)((num_q + kAbRows - 1) / kAbRows), 2, cfg.num_heads),
                     dim3(kAbThreads), smem, stream, q_map, w_map, (const __nv_bfloat16*)q_pe,
-                    q_positions, (__nv_bfloat16*)q_abs, (int)num_q, cfg.num_heads, freq);
+                    q_positions, (__nv_bfloat16*)q_abs, (int)num_q, cfg.num_heads, freq,
+                    cfg.rope_interleaved);
 }
 
 }  // namespace mla

@@ -13,6 +13,7 @@
 
 #include "async_copy.cuh"
 #include "common.cuh"
+#include "rope_pairs.cuh"
 #include "internal.h"
 
 namespace mla {
@@ -58,7 +59,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) cache_write_kernel(
     const T* __restrict__ c_kv, const T* __restrict__ k_pe, const int32_t* __restrict__ positions,
     const int64_t* __restrict__ slot_mapping, int64_t num_tokens, const T* __restrict__ w,
-    T* __restrict__ cache, int64_t num_slots, float eps, RopeFreq freq, uint32_t* status) {
+    T* __restrict__ cache, int64_t num_slots, float eps, RopeFreq freq, int interleaved,
+    uint32_t* status) {
   pdl_wait();
   pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
@@ -77,7 +79,8 @@ __global__ void __launch_bounds__(256) cache_write_kernel(
     Vec16<T> x;
     x.load(c_kv + t * kDc + lane * 16);
     const T* kp = k_pe + t * kDr;
-    const float x1 = to_f32(kp[lane]), x2 = to_f32(kp[lane + 32]);
+    const int i1 = rope_i1(interleaved, lane), i2 = rope_i2(interleaved, lane);
+    const float x1 = to_f32(kp[i1]), x2 = to_f32(kp[i2]);
     const int pos = positions[t];
     float ss = 0.f;
 #pragma unroll
@@ -92,8 +95,8 @@ __global__ void __launch_bounds__(256) cache_write_kernel(
     y.store(dst + lane * 16);
     float cs, sn;
     rope_cos_sin(pos, fhi, flo, &cs, &sn);
-    dst[kDc + lane] = from_f32<T>(x1 * cs - x2 * sn);
-    dst[kDc + lane + 32] = from_f32<T>(x2 * cs + x1 * sn);
+    dst[kDc + i1] = from_f32<T>(x1 * cs - x2 * sn);
+    dst[kDc + i2] = from_f32<T>(x2 * cs + x1 * sn);
   }
 }
 
@@ -103,7 +106,8 @@ __global__ void __launch_bounds__(256) cache_write_fp8_kernel(
     const __nv_bfloat16* __restrict__ c_kv, const __nv_bfloat16* __restrict__ k_pe,
     const int32_t* __restrict__ positions, const int64_t* __restrict__ slot_mapping,
     int64_t num_tokens, const __nv_bfloat16* __restrict__ w, uint8_t* __restrict__ cache8,
-    int64_t num_slots, float eps, float inv_scale, RopeFreq freq, uint32_t* status) {
+    int64_t num_slots, float eps, float inv_scale, RopeFreq freq, int interleaved,
+    uint32_t* status) {
   pdl_wait();
   pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
@@ -122,7 +126,8 @@ __global__ void __launch_bounds__(256) cache_write_fp8_kernel(
     Vec16<__nv_bfloat16> x;
     x.load(c_kv + t * kDc + lane * 16);
     const __nv_bfloat16* kp = k_pe + t * kDr;
-    const float x1 = __bfloat162float(kp[lane]), x2 = __bfloat162float(kp[lane + 32]);
+    const int i1 = rope_i1(interleaved, lane), i2 = rope_i2(interleaved, lane);
+    const float x1 = __bfloat162float(kp[i1]), x2 = __bfloat162float(kp[i2]);
     const int pos = positions[t];
     float ss = 0.f;
 #pragma unroll
@@ -145,8 +150,8 @@ __global__ void __launch_bounds__(256) cache_write_fp8_kernel(
     float cs, sn;
     rope_cos_sin(pos, fhi, flo, &cs, &sn);
     __nv_bfloat16* kr = reinterpret_cast<__nv_bfloat16*>(dst + kDc);
-    kr[lane] = __float2bfloat16_rn(x1 * cs - x2 * sn);
-    kr[lane + 32] = __float2bfloat16_rn(x2 * cs + x1 * sn);
+    kr[i1] = __float2bfloat16_rn(x1 * cs - x2 * sn);
+    kr[i2] = __float2bfloat16_rn(x2 * cs + x1 * sn);
   }
 }
 
@@ -164,7 +169,7 @@ cudaError_t launch_cache_write_fp8(const mla_config& cfg, const void* c_kv, cons
                     (const __nv_bfloat16*)c_kv, (const __nv_bfloat16*)k_pe, positions,
                     slot_mapping, num_tokens, (const __nv_bfloat16*)rms_weight, (uint8_t*)cache8,
                     num_blocks * cfg.block_size, cfg.rms_eps, 1.0f / kv_scale,
-                    make_rope_freq((double)cfg.rope_base), dev_status);
+                    make_rope_freq((double)cfg.rope_base), cfg.rope_interleaved, dev_status);
 }
 
 cudaError_t launch_cache_write(const mla_config& cfg, const void* c_kv, const void* k_pe,
@@ -181,12 +186,13 @@ cudaError_t launch_cache_write(const mla_config& cfg, const void* c_kv, const vo
     return launch_pdl(cache_write_kernel<__nv_bfloat16>, dim3((unsigned)blocks), dim3(threads), 0,
                       stream, (const __nv_bfloat16*)c_kv, (const __nv_bfloat16*)k_pe, positions,
                       slot_mapping, num_tokens, (const __nv_bfloat16*)rms_weight,
-                      (__nv_bfloat16*)cache, num_slots, cfg.rms_eps, freq, dev_status);
+                      (__nv_bfloat16*)cache, num_slots, cfg.rms_eps, freq, cfg.rope_interleaved,
+                      dev_status);
   } else {
     return launch_pdl(cache_write_kernel<float>, dim3((unsigned)blocks), dim3(threads), 0, stream,
                       (const float*)c_kv, (const float*)k_pe, positions, slot_mapping, num_tokens,
                       (const float*)rms_weight, (float*)cache, num_slots, cfg.rms_eps, freq,
-                      dev_status);
+                      cfg.rope_interleaved, dev_status);
   }
   return cudaGetLastError();
 }

@@ -31,6 +31,7 @@ mla_status check_cfg(const mla_config* cfg) {
   if (bs != 16 && bs != 32 && bs != 64) return MLA_ERR_UNSUPPORTED;
   if (cfg->dtype != MLA_F32 && cfg->dtype != MLA_BF16) return MLA_ERR_UNSUPPORTED;
   if (cfg->num_ctas < 0 || cfg->num_ctas > 65535) return MLA_ERR_INVALID_ARGUMENT;
+  if (cfg->rope_interleaved != 0 && cfg->rope_interleaved != 1) return MLA_ERR_INVALID_ARGUMENT;
   if (!std::isfinite(cfg->softmax_scale) || !(cfg->rms_eps >= 0.f) ||
       !std::isfinite(cfg->rms_eps) || !(cfg->rope_base > 0.f) || !std::isfinite(cfg->rope_base))
     return MLA_ERR_INVALID_ARGUMENT;
@@ -220,6 +221,7 @@ void mla_default_config(mla_config* cfg, int32_t num_heads, int32_t block_size, 
   cfg->rope_base = 10000.0f;
   cfg->dtype = dtype;
   cfg->num_ctas = 0;
+  cfg->rope_interleaved = 0;
 }
 
 mla_status mla_cache_write(const mla_config* cfg, const void* c_kv, const void* k_pe,

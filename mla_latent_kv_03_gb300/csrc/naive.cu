@@ -19,6 +19,7 @@
 //   naive_merge_kernel  the split-softmax merge into out [num_q, H, 128]
 #include "async_copy.cuh"
 #include "common.cuh"
+#include "rope_pairs.cuh"
 #include "internal.h"
 #include "tcgen05.cuh"
 
@@ -391,6 +392,7 @@ struct NdArgs {
   int32_t split_len;  // a multiple of 32
   float scale_log2;
   RopeFreq freq;
+  int32_t rope_interleaved;
   float* part_o;      // [num_q, H, splits, 128]
   float* part_lse;    // [num_q, H, splits]
   uint32_t* status;
@@ -439,11 +441,12 @@ __global__ void __launch_bounds__(256) naive_decode_kernel(NdArgs a) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) sq[w][lane + 32 * i] = __bfloat162float(qn[lane + 32 * i]);
     const __nv_bfloat16* qp = a.q_pe + ((size_t)n * a.H + h) * kDr;
-    const float x1 = __bfloat162float(qp[lane]), x2 = __bfloat162float(qp[lane + 32]);
+    const int i1 = rope_i1(a.rope_interleaved, lane), i2 = rope_i2(a.rope_interleaved, lane);
+    const float x1 = __bfloat162float(qp[i1]), x2 = __bfloat162float(qp[i2]);
     float cs, sn;
     rope_cos_sin(a.q_positions[n], a.freq.hi[lane], a.freq.lo[lane], &cs, &sn);
-    sq[w][kDn + lane] = x1 * cs - x2 * sn;
-    sq[w][kDn + 32 + lane] = x2 * cs + x1 * sn;
+    sq[w][kDn + i1] = x1 * cs - x2 * sn;
+    sq[w][kDn + i2] = x2 * cs + x1 * sn;
   }
   __syncwarp();
 
@@ -805,6 +808,7 @@ mla_status mla_naive_decode(const mla_config* cfg, const void* q_nope, const voi
   na.split_len = sp.split_len;
   na.scale_log2 = (float)(cfg->softmax_scale * 1.4426950408889634);
   na.freq = make_rope_freq((double)cfg->rope_base);
+  na.rope_interleaved = cfg->rope_interleaved;
   na.part_o = reinterpret_cast<float*>(ws + L.part_o);
   na.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
   na.status = reinterpret_cast<uint32_t*>(ws);

@@ -13,6 +13,7 @@
 // 1e-4 absolute).
 #include "async_copy.cuh"
 #include "common.cuh"
+#include "rope_pairs.cuh"
 #include "internal.h"
 
 namespace mla {
@@ -32,7 +33,7 @@ template <int MW>
 __global__ void __launch_bounds__(128) absorb_bf16_kernel(
     const __nv_bfloat16* __restrict__ q_nope, const __nv_bfloat16* __restrict__ q_pe,
     const int32_t* __restrict__ q_pos, const __nv_bfloat16* __restrict__ W_uk,
-    __nv_bfloat16* __restrict__ q_abs, int num_q, int H, RopeFreq freq) {
+    __nv_bfloat16* __restrict__ q_abs, int num_q, int H, RopeFreq freq, int interleaved) {
   constexpr int NT = MW == 1 ? 4 : 16;   // 8-column n-tiles per warp
   constexpr int ROWS = 16 * MW;
   __shared__ __align__(1024) uint8_t sB[128 * 256];
@@ -47,7 +48,7 @@ __global__ void __launch_bounds__(128) absorb_bf16_kernel(
     pdl_launch_dependents();
     constexpr int kPer = 16 * 32 / 128;
     const int rrow0 = row0 + 16 * (blockIdx.y - 4);
-    const int p = tid & 31;
+    const int p = tid & 31, i1 = rope_i1(interleaved, p), i2 = rope_i2(interleaved, p);
     const float fhi = freq.hi[p], flo = freq.lo[p];
     float x1[kPer], x2[kPer];
     int pos[kPer];
@@ -56,8 +57,8 @@ __global__ void __launch_bounds__(128) absorb_bf16_kernel(
       const int r = rrow0 + (tid >> 5) + 4 * it;
       const bool ok = r < num_q;
       const __nv_bfloat16* x = q_pe + ((size_t)r * H + h) * kDr;
-      x1[it] = ok ? __bfloat162float(x[p]) : 0.f;
-      x2[it] = ok ? __bfloat162float(x[p + 32]) : 0.f;
+      x1[it] = ok ? __bfloat162float(x[i1]) : 0.f;
+      x2[it] = ok ? __bfloat162float(x[i2]) : 0.f;
       pos[it] = ok ? q_pos[r] : 0;
     }
 #pragma unroll
@@ -67,8 +68,8 @@ __global__ void __launch_bounds__(128) absorb_bf16_kernel(
       float cs, sn;
       rope_cos_sin(pos[it], fhi, flo, &cs, &sn);
       __nv_bfloat16* o = q_abs + ((size_t)r * H + h) * kRow + kDc;
-      o[p] = __float2bfloat16_rn(x1[it] * cs - x2[it] * sn);
-      o[p + 32] = __float2bfloat16_rn(x2[it] * cs + x1[it] * sn);
+      o[i1] = __float2bfloat16_rn(x1[it] * cs - x2[it] * sn);
+      o[i2] = __float2bfloat16_rn(x2[it] * cs + x1[it] * sn);
     }
     return;
   }
@@ -697,7 +698,7 @@ constexpr int kAbsorbF32Rows = 64;
 __global__ void __launch_bounds__(256) absorb_f32_kernel(
     const float* __restrict__ q_nope, const float* __restrict__ q_pe,
     const int32_t* __restrict__ q_pos, const float* __restrict__ W_uk, float* __restrict__ q_abs,
-    int num_q, int H, RopeFreq freq) {
+    int num_q, int H, RopeFreq freq, int interleaved) {
   const int h = blockIdx.x, chunk = blockIdx.y, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   if (chunk == kDc / kAbsorbF32Rows) {
@@ -708,8 +709,9 @@ __global__ void __launch_bounds__(256) absorb_f32_kernel(
       float cs, sn;
       rope_cos_sin(q_pos[n], freq.hi[p], freq.lo[p], &cs, &sn);
       float* out = q_abs + ((size_t)n * H + h) * kRow + kDc;
-      out[p] = x[p] * cs - x[p + 32] * sn;
-      out[p + 32] = x[p + 32] * cs + x[p] * sn;
+      const int i1 = rope_i1(interleaved, p), i2 = rope_i2(interleaved, p);
+      out[i1] = x[i1] * cs - x[i2] * sn;
+      out[i2] = x[i2] * cs + x[i1] * sn;
     }
     return;
   }
@@ -783,10 +785,11 @@ cudaError_t launch_absorb_q(const mla_config& cfg, const void* q_nope, const voi
   if (num_q == 0) return cudaSuccess;
   const int H = cfg.num_heads;
   const RopeFreq freq = make_rope_freq((double)cfg.rope_base);
+  const int inter = cfg.rope_interleaved;
   if (cfg.dtype == MLA_F32) {
     absorb_f32_kernel<<<dim3(H, kDc / kAbsorbF32Rows + 1), 256, 0, stream>>>(
         (const float*)q_nope, (const float*)q_pe, q_positions, (const float*)W_uk, (float*)q_abs,
-        (int)num_q, H, freq);
+        (int)num_q, H, freq, inter);
     return cudaGetLastError();
   }
   // More than 16 rows: 64 rows per CTA, so that a batch of up to 64 rows
@@ -800,7 +803,7 @@ cudaError_t launch_absorb_q(const mla_config& cfg, const void* q_nope, const voi
     return launch_pdl(absorb_bf16_kernel<4>, dim3((unsigned)((num_q + 63) / 64), 8, H), dim3(128), 0,
                       stream, (const __nv_bfloat16*)q_nope, (const __nv_bfloat16*)q_pe,
                       q_positions, (const __nv_bfloat16*)W_uk, (__nv_bfloat16*)q_abs, (int)num_q,
-                      H, freq);
+                      H, freq, inter);
   } else {
     cudaError_t e = cudaFuncSetAttribute(absorb_bf16_kernel<1>,
                                          cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -809,7 +812,7 @@ cudaError_t launch_absorb_q(const mla_config& cfg, const void* q_nope, const voi
     return launch_pdl(absorb_bf16_kernel<1>, dim3((unsigned)((num_q + 15) / 16), 5, H), dim3(128), 0,
                       stream, (const __nv_bfloat16*)q_nope, (const __nv_bfloat16*)q_pe,
                       q_positions, (const __nv_bfloat16*)W_uk, (__nv_bfloat16*)q_abs, (int)num_q,
-                      H, freq);
+                      H, freq, inter);
   }
   return cudaGetLastError();
 }

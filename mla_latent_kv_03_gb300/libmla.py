@@ -54,6 +54,7 @@ class MlaConfig(ctypes.Structure):
         ("v_head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
         ("softmax_scale", ctypes.c_float), ("rms_eps", ctypes.c_float),
         ("rope_base", ctypes.c_float), ("dtype", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
+        ("rope_interleaved", ctypes.c_int32),
     ]
 
 
@@ -138,7 +139,7 @@ def _check(status: int, where: str) -> None:
 
 def make_config(num_heads: int, block_size: int, dtype: str, num_ctas: int = 0,
                 softmax_scale: Optional[float] = None, rms_eps: Optional[float] = None,
-                rope_base: Optional[float] = None) -> MlaConfig:
+                rope_base: Optional[float] = None, rope_interleaved: bool = False) -> MlaConfig:
     cfg = MlaConfig()
     load().mla_default_config(ctypes.byref(cfg), num_heads, block_size,
                               MLA_BF16 if dtype == "bf16" else MLA_F32)
@@ -149,6 +150,7 @@ def make_config(num_heads: int, block_size: int, dtype: str, num_ctas: int = 0,
         cfg.rms_eps = rms_eps
     if rope_base is not None:
         cfg.rope_base = rope_base
+    cfg.rope_interleaved = int(bool(rope_interleaved))
     return cfg
 
 

@@ -24,12 +24,12 @@ def _dev(a: np.ndarray, dtype, device) -> torch.Tensor:
 
 class MlaDecodeStep:
     def __init__(self, w: Workload, device: str = "cuda", num_ctas: int = 0,
-                 cache_fill: Optional[float] = None):
+                 cache_fill: Optional[float] = None, rope_interleaved: bool = False):
         self.w = w
         self.device = device
         self.cfg = L.make_config(w.num_heads, w.block_size, w.dtype, num_ctas=num_ctas,
                                  softmax_scale=w.softmax_scale, rms_eps=w.rms_eps,
-                                 rope_base=w.rope_base)
+                                 rope_base=w.rope_base, rope_interleaved=rope_interleaved)
         dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
         self.dt = dt
         H = w.num_heads

@@ -75,11 +75,13 @@ def rope_inv_freq(rope_dim: int, base: float) -> np.ndarray:
     return np.float64(base) ** (-2.0 * i / rope_dim)
 
 
-def rope(x, positions, base: float) -> np.ndarray:
-    """Rotate-half RoPE on the last axis of ``x``.
+def rope(x, positions, base: float, interleaved: bool = False) -> np.ndarray:
+    """RoPE on the last axis of ``x``.
 
-    ``x`` is [T, ..., d]; ``positions`` is [T]. Pair (x_i, x_{i+d/2}) is
-    rotated by angle positions[t] * inv_freq_i.
+    ``x`` is [T, ..., d]; ``positions`` is [T]. Pair i is rotated by angle
+    positions[t] * inv_freq_i: the pair (x_i, x_{i+d/2}) (rotate-half, the
+    reading taken for the pages) or, with ``interleaved``, (x_{2i}, x_{2i+1})
+    (the other pairing in use, left open by the pages).
     [VLB07 2.4; MI17 "MLA 的数学结构" (k_pe shared by all heads, MQA style)]
     """
     x = _f64(x)
@@ -88,12 +90,18 @@ def rope(x, positions, base: float) -> np.ndarray:
     pos = _f64(positions).reshape((-1,) + (1,) * (x.ndim - 1))
     ang = pos * rope_inv_freq(d, base)           # [T, 1.., half]
     cos, sin = np.cos(ang), np.sin(ang)
+    if interleaved:
+        x1, x2 = x[..., 0::2], x[..., 1::2]
+        out = np.empty_like(x)
+        out[..., 0::2] = x1 * cos - x2 * sin
+        out[..., 1::2] = x2 * cos + x1 * sin
+        return out
     x1, x2 = x[..., :half], x[..., half:]
     return np.concatenate([x1 * cos - x2 * sin, x2 * cos + x1 * sin], axis=-1)
 
 
 def latent_cache_rows(c_kv_raw, k_pe_raw, positions, rms_weight, eps: float,
-                      base: float) -> np.ndarray:
+                      base: float, interleaved: bool = False) -> np.ndarray:
     """The row that the paged cache must hold for each token: [c_hat || k_hat].
 
     c_hat = RMSNorm(c_kv_raw) * w (512), k_hat = RoPE(k_pe_raw, pos) (64).
@@ -102,7 +110,7 @@ def latent_cache_rows(c_kv_raw, k_pe_raw, positions, rms_weight, eps: float,
      MI17 "版本 2": the cache holds only compressed_kv + k_pe]
     """
     return np.concatenate(
-        [rms_norm(c_kv_raw, rms_weight, eps), rope(k_pe_raw, positions, base)],
+        [rms_norm(c_kv_raw, rms_weight, eps), rope(k_pe_raw, positions, base, interleaved)],
         axis=-1)
 
 
@@ -110,7 +118,8 @@ def latent_cache_rows(c_kv_raw, k_pe_raw, positions, rms_weight, eps: float,
 # Absorbed form: the per-step decode path
 # ---------------------------------------------------------------------------
 
-def absorb_q(q_nope, q_pe, q_positions, W_uk, base: float) -> np.ndarray:
+def absorb_q(q_nope, q_pe, q_positions, W_uk, base: float,
+             interleaved: bool = False) -> np.ndarray:
     """q_abs[n,h] = [W_uk[h] @ q_nope[n,h] || RoPE(q_pe[n,h], pos_n)].
 
     W_uk is [H, kv_lora_rank, qk_nope] (the absorbed key weight of
@@ -118,7 +127,7 @@ def absorb_q(q_nope, q_pe, q_positions, W_uk, base: float) -> np.ndarray:
     rows, transposed). q_lat[n,h,c] = sum_d W_uk[h,c,d] * q_nope[n,h,d].
     """
     q_lat = np.einsum("hcd,nhd->nhc", _f64(W_uk), _f64(q_nope))
-    return np.concatenate([q_lat, rope(q_pe, q_positions, base)], axis=-1)
+    return np.concatenate([q_lat, rope(q_pe, q_positions, base, interleaved)], axis=-1)
 
 
 def causal_visible(q_positions, kv_len: int) -> np.ndarray:
@@ -293,13 +302,13 @@ def e4m3_encode(v) -> np.ndarray:
 
 
 def fp8_latent_rows(c_kv_raw, k_pe_raw, positions, rms_weight, eps: float, base: float,
-                    kv_scale: float):
+                    kv_scale: float, interleaved: bool = False):
     """The FP8 cache row of each token (reading above): the e4m3 codes of
     c_hat / kv_scale [T, 512] uint8, and k_rot [T, 64] (stored in bf16).
     Dequantised latent = e4m3_decode(codes) * kv_scale."""
     c_hat = rms_norm(c_kv_raw, rms_weight, eps)
     codes = e4m3_encode(e4m3_round(c_hat / float(kv_scale)))
-    return codes, rope(k_pe_raw, positions, base)
+    return codes, rope(k_pe_raw, positions, base, interleaved)
 
 
 def naive_kv_rows(c_hat, k_rot, W_uk, W_uv) -> np.ndarray:
@@ -351,15 +360,15 @@ def expanded_attention(kv_rows, q, q_positions, scale: float,
 
 def mla_sequence_naive(c_kv_raw, k_pe_raw, kv_positions, q_nope, q_pe,
                        q_positions, W_uk, W_uv, rms_weight, eps: float,
-                       base: float, scale: float) -> np.ndarray:
+                       base: float, scale: float, interleaved: bool = False) -> np.ndarray:
     """End-to-end attention output for one sequence from raw inputs.
 
     kv_a_layernorm on the latent, RoPE on k_pe and q_pe, then the naive form.
     [MI17 "版本 1" and pitfall 3; VLB07 2.2 forward steps 1-4]
     """
     c_hat = rms_norm(c_kv_raw, rms_weight, eps)
-    k_rot = rope(k_pe_raw, kv_positions, base)
-    q_rot = rope(q_pe, q_positions, base)
+    k_rot = rope(k_pe_raw, kv_positions, base, interleaved)
+    q_rot = rope(q_pe, q_positions, base, interleaved)
     return naive_attention(c_hat, k_rot, q_nope, q_rot, W_uk, W_uv,
                            q_positions, scale)
 

@@ -589,3 +589,41 @@ def test_layer_naive_equals_absorbed_and_is_causal():
     # leaves it unchanged
     y_short = O.mla_layer_naive(hid[:T - 1], pos[:T - 1], *args, num_new=new - 1)
     assert np.allclose(y[:new - 1], y_short, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# Interleaved RoPE pairing (the option the pages leave open)
+# ---------------------------------------------------------------------------
+
+def test_interleaved_rope_is_complex_rotation_of_adjacent_pairs():
+    rng = np.random.default_rng(31)
+    x = rng.standard_normal((5, 3, 64))
+    pos = np.array([0, 1, 7, 100, 4095])
+    got = O.rope(x, pos, 1e4, interleaved=True)
+    inv = 1e4 ** (-np.arange(32) * 2 / 64)
+    for t in range(5):
+        z = (x[t, :, 0::2] + 1j * x[t, :, 1::2]) * np.exp(1j * pos[t] * inv)
+        assert np.allclose(got[t, :, 0::2], z.real, rtol=0, atol=1e-12)
+        assert np.allclose(got[t, :, 1::2], z.imag, rtol=0, atol=1e-12)
+    assert np.array_equal(O.rope(x, np.zeros(5, int), 1e4, interleaved=True), x)
+
+
+def test_interleaved_rope_is_rotate_half_on_permuted_coordinates():
+    # moving element 2i to i and 2i+1 to 32 + i turns one pairing into the other
+    rng = np.random.default_rng(32)
+    x = rng.standard_normal((6, 64))
+    pos = rng.integers(0, 5000, 6)
+    perm = np.concatenate([np.arange(0, 64, 2), np.arange(1, 64, 2)])
+    inter = O.rope(x, pos, 1e4, interleaved=True)
+    half = O.rope(x[:, perm], pos, 1e4)
+    assert np.allclose(inter[:, perm], half, rtol=0, atol=1e-12)
+    # and the two pairings differ as functions (the option is not a no-op)
+    assert not np.allclose(inter, O.rope(x, pos, 1e4), atol=1e-3)
+
+
+def test_interleaved_attention_scores_depend_only_on_relative_position():
+    rng = np.random.default_rng(33)
+    q, k = rng.standard_normal(64), rng.standard_normal(64)
+    s = [O.rope(q[None], [m], 1e4, True)[0] @ O.rope(k[None], [n], 1e4, True)[0]
+         for m, n in ((10, 3), (110, 103), (1010, 1003))]
+    assert np.allclose(s, s[0], rtol=0, atol=1e-9)
