@@ -114,3 +114,52 @@ def test_naive_forms_are_bf16_only_and_check_their_workspace(lib):
     assert lib.mla_naive_decode(ctypes.byref(bf16), p, p, p, p, 16, p, 4, p, p, 4, 4, p,
                                 256, p, None) == 3
     assert lib.mla_latent_expand(ctypes.byref(bf16), p, 16, p, 4, p, 4, p, p, p, p, 256, None) == 3
+
+
+def test_rope_pairing_field_defaults_to_rotate_half_and_is_checked(lib):
+    cfg = L.make_config(16, 64, "bf16")
+    assert cfg.rope_interleaved == 0
+    assert L.make_config(16, 64, "bf16", rope_interleaved=True).rope_interleaved == 1
+    cfg.rope_interleaved = 2
+    p = ctypes.c_void_p(256)
+    assert lib.mla_absorb_q(ctypes.byref(cfg), p, p, p, p, p, 1, None) == 1
+
+
+def test_fp8_calls_check_their_arguments_on_the_host(lib):
+    bf16 = L.make_config(16, 64, "bf16")
+    f32 = L.make_config(16, 64, "f32")
+    h128 = L.make_config(128, 64, "bf16")
+    p = ctypes.c_void_p(1 << 20)
+    f = ctypes.c_float
+    assert lib.mla_cache_write_fp8(ctypes.byref(f32), p, p, p, p, 4, p, f(1.0), p, 4, None, None) == 2
+    for bad in (0.0, -1.0, float("nan"), float("inf")):
+        assert lib.mla_cache_write_fp8(ctypes.byref(bf16), p, p, p, p, 4, p, f(bad), p, 4, None,
+                                       None) == 1
+    assert lib.mla_cache_write_fp8(ctypes.byref(bf16), None, None, None, None, 0, None, f(1.0),
+                                   None, 0, None, None) == 0
+    dec = lib.mla_decode_paged_combine_fp8
+    assert dec(ctypes.byref(bf16), p, p, 16, p, 4, p, p, 4, 4, f(0.0), p, 1 << 30, p, None) == 1
+    # 128 heads take the tensor-core path, which has no FP8 form
+    assert dec(ctypes.byref(h128), p, p, 16, p, 4, p, p, 4, 4, f(1.0), p, 1 << 30, p, None) == 2
+    assert lib.mla_decode_fp8_workspace_size(None, 4, 4) == 0
+
+
+def test_projections_check_their_arguments_on_the_host(lib):
+    bf16 = L.make_config(16, 64, "bf16")
+    f32 = L.make_config(16, 64, "f32")
+    p = ctypes.c_void_p(1 << 20)
+    ws = ctypes.c_void_p(1 << 21)
+    assert lib.mla_proj_workspace_size(ctypes.byref(f32), 64, 2048) == 0
+    assert lib.mla_proj_workspace_size(ctypes.byref(bf16), 64, 100) == 0
+    assert lib.mla_proj_workspace_size(ctypes.byref(bf16), -1, 2048) == 0
+    for fn in (lib.mla_q_proj, lib.mla_kv_a_proj):
+        assert fn(ctypes.byref(f32), p, p, p, p, 4, 2048, ws, 1 << 20, None) == 2      # bf16 only
+        assert fn(ctypes.byref(bf16), p, p, p, p, 4, 2000, ws, 1 << 20, None) == 2     # K % 64
+        assert fn(ctypes.byref(bf16), p, p, p, p, 4, 2048, None, 1 << 20, None) == 1   # workspace
+        assert fn(ctypes.byref(bf16), p, p, p, p, 4, 2048, ctypes.c_void_p((1 << 21) + 16),
+                  1 << 20, None) == 1                                                  # 256-aligned
+        assert fn(ctypes.byref(bf16), ctypes.c_void_p((1 << 20) + 2), p, p, p, 4, 2048, ws,
+                  1 << 20, None) == 1                                                  # 16-aligned
+        assert fn(ctypes.byref(bf16), None, None, None, None, 0, 2048, ws, 256, None) == 0
+    assert lib.mla_o_proj(ctypes.byref(bf16), p, p, None, 4, 2048, ws, 1 << 20, None) == 1
+    assert lib.mla_o_proj(ctypes.byref(bf16), p, p, p, -1, 2048, ws, 1 << 20, None) == 1
