@@ -35,6 +35,15 @@
 // order (thread i's 16 float4 at [slot][nt][i]), so each thread of the
 // merging CTA reads exactly the values it adds, coalesced, two parts per round
 // trip with their log-sum-exps in the same round trip, in CTA order.
+//
+// FP8 cache (FP8, self-planned only): rows of 512 e4m3 codes (times kv_scale)
+// and 64 bf16 rope values. The producer loads the codes as 4 boxes of 128
+// codes and the rope columns as one bf16 box (40 KB stages); the math warps
+// read both MMAs' latent operands straight from the codes, converting code
+// pairs to f16 in registers (exact), against a query whose latent part was
+// converted once per segment to f16, scaled per head by a power of two; the
+// rope part stays bf16. One query buffer keeps the CTA at 106 KB, so two CTAs
+// share an SM and cover each other's latencies.
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 

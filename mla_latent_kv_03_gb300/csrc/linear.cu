@@ -17,9 +17,8 @@
 // give too few tiles for the GPU, so K is split across a grid z dimension:
 // every split writes fp32 partials and a second kernel adds them in split
 // order (repeated calls agree bit for bit). Column n of Y goes to one of two
-// outputs: with h = n / P and
-// d = n % P, d < Q goes to y0[m][h][d] (row length (N / P) Q) and the rest to
-// y1[m][h][d - Q] (row length (N / P) (P - Q)).
+// outputs: with h = n / P and d = n % P, d < Q goes to y0[m][h][d] (row length
+// (N / P) Q) and the rest to y1[m][h][d - Q] (row length (N / P) (P - Q)).
 #include <cuda_bf16.h>
 
 #include "async_copy.cuh"
