@@ -11,6 +11,7 @@ from _helpers import assert_close, ref_out, to_f64
 from mla_latent_kv_03_gb300 import libmla as L
 from mla_latent_kv_03_gb300 import workloads as W
 from mla_latent_kv_03_gb300.step import MlaDecodeStep
+from oracle import mla_oracle as O
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -150,3 +151,64 @@ def test_mixed_bench_step_graphed():
     (st1, _), (st2, _) = s.device_status()
     assert st1 == 0 and st2 == 0
     _check(w, s, [1, 4, 50], [3, 12], "mixed, graphed bench step")
+
+
+def _graph_replay(step_fn, steps=3, replays=2):
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        step_fn()                      # eager once (lazy state)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(steps):
+            step_fn()
+    with torch.cuda.stream(stream):
+        for _ in range(replays):
+            g.replay()
+    stream.synchronize()
+
+
+def test_serving_fp8_bench_step_graphed():
+    # bench.py --form fp8: two CTAs per SM, kv_scale 0.02
+    w = W.serving()
+    s = MlaDecodeStep(w, device=DEV)
+    s.fp8_setup(0.02)
+    s.fp8_populate()
+
+    def step():
+        s.absorb()
+        s.decode_paged_combine_fp8()
+        s.out_proj()
+
+    s.out.fill_(float("nan"))
+    _graph_replay(step)
+    assert s.device_status()[0][0] == 0
+    seqs = [0, 23, 63]
+    q_abs = O.absorb_q(w.q_nope, w.q_pe, w.q_positions, w.W_uk, w.rope_base)
+    for b in seqs:
+        tr, qr = w.token_range(b), w.q_range(b)
+        codes, k_rot = O.fp8_latent_rows(w.c_kv_raw[tr], w.k_pe_raw[tr], w.kv_positions[tr],
+                                         w.rms_weight, w.rms_eps, w.rope_base, 0.02)
+        rows = np.concatenate([O.e4m3_decode(codes) * 0.02, k_rot], -1)
+        o, _ = O.latent_attention(q_abs[qr], rows, w.q_positions[qr], w.softmax_scale)
+        assert_close(to_f64(s.out)[qr], O.out_proj(o, w.W_uv), "bf16", f"fp8 serving seq {b}")
+
+
+def test_serving_layer_bench_step_graphed():
+    # bench.py --form layer: hidden states -> q_proj, kv_a_proj + cache write,
+    # absorb, decode + merge, out_proj, o_proj (hidden 2048)
+    w = W.serving()
+    s = MlaDecodeStep(w, device=DEV)
+    s.layer_setup(2048)
+    s.layer_populate()
+    s.y.fill_(float("nan"))
+    _graph_replay(s.layer_step)
+    assert s.device_status()[0][0] == 0
+    assert L.mla_get_device_status(s.proj_ws)[0] == 0
+    li = s.layer
+    for b in (5, 62):
+        tr, qr = w.token_range(b), w.q_range(b)
+        ref = O.mla_layer_naive(li.hidden[tr], w.kv_positions[tr], li.W_q, li.W_kv_a, w.W_uk,
+                                w.W_uv, li.W_o, w.rms_weight, w.rms_eps, w.rope_base,
+                                w.softmax_scale, num_new=1)
+        assert_close(to_f64(s.y)[qr], ref, "bf16", f"layer serving seq {b}")
