@@ -373,6 +373,23 @@ mla_status mla_naive_decode(const mla_config* cfg, const void* q_nope, const voi
                             void* out, void* stream);
 
 /*
+ * mla_naive_prefill -- mla_naive_decode's result (same arguments, same
+ * conventions, zeros for a row that sees no token) on tensor cores, for
+ * prefill chunks: a CTA takes 64 query rows of one sequence and one head and
+ * reads each key tile of the expanded rows once for all of them (m16n8k16
+ * warp mma, bf16 in, fp32 accumulation, the probabilities rounded to bf16).
+ * Decode rows (one row per sequence) are better served by mla_naive_decode,
+ * which splits the keys. Only the status word of the workspace is used
+ * (ws_bytes >= 256).
+ */
+mla_status mla_naive_prefill(const mla_config* cfg, const void* q_nope, const void* q_pe,
+                             const int32_t* q_positions, const void* kv_cache, int64_t num_blocks,
+                             const int32_t* block_table, int32_t max_blocks_per_seq,
+                             const int32_t* seq_lens, const int32_t* query_start_loc,
+                             int32_t batch, int64_t num_q, void* workspace, size_t ws_bytes,
+                             void* out, void* stream);
+
+/*
  * mla_decode_paged_noalloc -- mla_decode_paged followed by mla_combine for
  * callers that cannot allocate device memory (a step callback with a fixed
  * memory budget, a real-time loop where cudaMalloc would stall or fail, a

@@ -114,5 +114,9 @@ mla_status validate_config(const mla_config* cfg);
 bool encode_row_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows);
 bool encode_map_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
                    uint32_t box_cols, uint32_t box_rows);
+// 3-D map over (d, head, row) of a [rows, heads, dims] bf16 tensor: box =
+// (box_d, 1, box_rows), 128-byte swizzle.
+bool encode_map_heads(CUtensorMap* map, const void* base, uint64_t dims, uint64_t heads,
+                      uint64_t rows, uint32_t box_d, uint32_t box_rows);
 
 }  // namespace mla

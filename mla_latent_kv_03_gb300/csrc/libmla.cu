@@ -186,6 +186,10 @@ bool encode_map_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t r
                    uint32_t box_cols, uint32_t box_rows) {
   return make_map_2d(map, base, cols, rows, box_cols, box_rows);
 }
+bool encode_map_heads(CUtensorMap* map, const void* base, uint64_t dims, uint64_t heads,
+                      uint64_t rows, uint32_t box_d, uint32_t box_rows) {
+  return make_map_heads(map, base, dims, heads, rows, box_d, box_rows);
+}
 }  // namespace mla
 
 extern "C" {

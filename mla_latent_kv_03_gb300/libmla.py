@@ -34,7 +34,7 @@ EXPORTS = (
     "mla_decode_paged_combine_fp8",
     "mla_proj_workspace_size", "mla_q_proj", "mla_kv_a_proj", "mla_o_proj",
     "mla_naive_workspace_size", "mla_naive_cache_write",
-    "mla_latent_expand", "mla_naive_decode",
+    "mla_latent_expand", "mla_naive_decode", "mla_naive_prefill",
     "mla_combine", "mla_out_proj",
     "mla_get_device_status", "mla_selftest_wait_timeout", "mla_status_string", "mla_version",
 )
@@ -92,6 +92,8 @@ _SIGS = {
                                  _vp]),
     "mla_naive_decode": (_i32, [_cfgp, _vp, _vp, _vp, _vp, _i64, _vp, _i32, _vp, _vp, _i32, _i64,
                                 _vp, _sz, _vp, _vp]),
+    "mla_naive_prefill": (_i32, [_cfgp, _vp, _vp, _vp, _vp, _i64, _vp, _i32, _vp, _vp, _i32, _i64,
+                                 _vp, _sz, _vp, _vp]),
     "mla_combine": (_i32, [_cfgp, _vp, _sz, _i32, _i64, _vp, _vp]),
     "mla_combine_out_proj": (_i32, [_cfgp, _vp, _sz, _i32, _i64, _vp, _vp, _vp]),
     "mla_out_proj": (_i32, [_cfgp, _vp, _vp, _vp, _i64, _vp]),
@@ -343,6 +345,18 @@ def mla_naive_decode(cfg: MlaConfig, q_nope, q_pe, q_positions, kv_cache, block_
         _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(query_start_loc, torch.int32, "query_start_loc"),
         seq_lens.shape[0], q_nope.shape[0], _ptr(workspace, None, "workspace"), _nbytes(workspace),
         _ptr(out, dt, "out"), _stream(stream)), "mla_naive_decode")
+
+
+def mla_naive_prefill(cfg: MlaConfig, q_nope, q_pe, q_positions, kv_cache, block_table, seq_lens,
+                      query_start_loc, workspace, out, stream=None) -> None:
+    dt = _torch_dtype(cfg)
+    _check(load().mla_naive_prefill(
+        ctypes.byref(cfg), _ptr(q_nope, dt, "q_nope"), _ptr(q_pe, dt, "q_pe"),
+        _ptr(q_positions, torch.int32, "q_positions"), _ptr(kv_cache, dt, "kv_cache"),
+        kv_cache.shape[0], _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+        _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(query_start_loc, torch.int32, "query_start_loc"),
+        seq_lens.shape[0], q_nope.shape[0], _ptr(workspace, None, "workspace"), _nbytes(workspace),
+        _ptr(out, dt, "out"), _stream(stream)), "mla_naive_prefill")
 
 
 def mla_combine(cfg: MlaConfig, workspace, batch: int, o_lat, stream=None) -> None:

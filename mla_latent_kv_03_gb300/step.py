@@ -233,6 +233,11 @@ class MlaDecodeStep:
                            self.block_table, self.seq_lens, self.query_start_loc, self.naive_ws,
                            self.out_naive, stream=stream)
 
+    def naive_prefill(self, stream=None) -> None:
+        L.mla_naive_prefill(self.cfg, self.q_nope, self.q_pe, self.q_positions, self.kv_naive,
+                            self.block_table, self.seq_lens, self.query_start_loc, self.naive_ws,
+                            self.out_naive, stream=stream)
+
     def device_status(self):
         """(status, bits) of the decode workspace and of the cache-write word."""
         s1 = L.mla_get_device_status(self.workspace)

@@ -159,3 +159,79 @@ def test_bad_block_is_reported_and_skipped():
     got = to_f64(s.out_naive)
     assert np.all(np.isfinite(got))
     assert_close(got[1:2], ref_out(w, seqs=[1])[1:2], "bf16", "other sequence")
+
+
+# ---------------------------------------------------------------------------
+# mla_naive_prefill: the same attention in 64-row tensor-core tiles
+# ---------------------------------------------------------------------------
+
+PREFILL_CASES = dict(CASES)
+PREFILL_CASES.update({
+    "multi_tile_bs16": lambda: W.make("pf_mt16", [300, 70, 129], [200, 64, 129], 16, 16, "bf16",
+                                      seed=57),
+    "multi_tile_h32": lambda: W.make("pf_mt32", [600, 5], [260, 5], 32, 64, "bf16", seed=58),
+})
+
+
+def _expanded_ref(w, s):
+    kv = to_f64(s.kv_naive).reshape(-1, w.num_heads, 320)
+    q = np.concatenate([w.q_nope.astype(np.float64),
+                        O.rope(w.q_pe, w.q_positions, w.rope_base)], -1)
+    ref = np.zeros((w.num_q, w.num_heads, 128))
+    for b in range(w.batch):
+        qr = w.q_range(b)
+        if qr.stop == qr.start:
+            continue
+        ref[qr] = O.expanded_attention(kv[_slots_of(w, b)], q[qr], w.q_positions[qr],
+                                       w.softmax_scale)
+    return ref
+
+
+@pytest.mark.parametrize("name", sorted(PREFILL_CASES))
+def test_naive_prefill_vs_expanded_oracle_and_decode(name):
+    w = PREFILL_CASES[name]()
+    s = MlaDecodeStep(w, device=DEV)
+    s.naive_setup()
+    s.naive_populate()
+    s.out_naive.fill_(float("nan"))
+    s.naive_prefill()
+    torch.cuda.synchronize()
+    assert L.mla_get_device_status(s.naive_ws)[0] == 0
+    first = s.out_naive.clone()
+    got = to_f64(first)
+    assert_close(got, _expanded_ref(w, s), "bf16", f"naive prefill {name}")
+    # the same rows through the split CUDA-core path
+    s.naive_decode()
+    torch.cuda.synchronize()
+    assert_close(got, to_f64(s.out_naive), "bf16", f"prefill vs decode {name}")
+    # and a repeated launch agrees bit for bit
+    s.naive_prefill()
+    torch.cuda.synchronize()
+    assert torch.equal(s.out_naive, first)
+
+
+def test_naive_prefill_interleaved_rope_and_bad_sequence():
+    w = W.make("pf_ri", [150, 64, 20], [40, 1, 20], 16, 64, "bf16", seed=59)
+    s = MlaDecodeStep(w, device=DEV, rope_interleaved=True)
+    s.naive_setup()
+    s.naive_populate()
+    s.naive_prefill()
+    torch.cuda.synchronize()
+    kv = to_f64(s.kv_naive).reshape(-1, w.num_heads, 320)
+    q = np.concatenate([w.q_nope.astype(np.float64),
+                        O.rope(w.q_pe, w.q_positions, w.rope_base, interleaved=True)], -1)
+    ref = np.zeros((w.num_q, w.num_heads, 128))
+    for b in range(w.batch):
+        qr = w.q_range(b)
+        ref[qr] = O.expanded_attention(kv[_slots_of(w, b)], q[qr], w.q_positions[qr],
+                                       w.softmax_scale)
+    assert_close(to_f64(s.out_naive), ref, "bf16", "naive prefill, interleaved RoPE")
+    # a query chunk longer than its sequence: status set, its rows zero
+    s.seq_lens[1] = 0
+    s.out_naive.fill_(float("nan"))
+    s.naive_prefill()
+    st, bits = L.mla_get_device_status(s.naive_ws)
+    assert st == 7 and bits & L.DEV_BAD_SEQ
+    got = to_f64(s.out_naive)
+    assert np.all(got[w.q_range(1)] == 0)
+    assert_close(got[w.q_range(0)], ref[w.q_range(0)], "bf16", "other sequence")
