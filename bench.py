@@ -62,6 +62,9 @@ PROFILES = {
         ["decode_tc.cu", "common.cuh", "cluster.cuh", "tcgen05.cuh", "merge.cuh", "async_copy.cuh"]),
     ("expand_tc_kernel", "serving"): (
         "expand_tc_serving_B64_L4096.md", ["naive.cu", "common.cuh", "tcgen05.cuh", "async_copy.cuh"]),
+    ("naive_prefill_kernel", "mixed"): (
+        "naive_prefill_mixed_P4_D60.md",
+        ["prefill.cu", "common.cuh", "async_copy.cuh", "rope_pairs.cuh"]),
     ("naive_decode_kernel", "serving"): (
         "naive_decode_serving_B64_L4096.md", ["naive.cu", "common.cuh", "tcgen05.cuh", "async_copy.cuh"]),
 }
@@ -394,8 +397,9 @@ def run_ours(args, world, rank, local):
     w = make_workload(args.workload, rank)
     mixed = bool(w.is_new.sum() > w.batch)   # a step that writes more than one token per sequence
     form = args.form
-    if form != "absorbed" and (mixed or w.dtype != "bf16"):
-        raise SystemExit("--form full_kv / latent / fp8 / layer: bf16 decode workloads only")
+    if form != "absorbed" and (w.dtype != "bf16" or (mixed and form != "full_kv")):
+        raise SystemExit("--form full_kv / latent / fp8 / layer: bf16 decode workloads only "
+                         "(full_kv also takes prefill chunks)")
     s = MlaDecodeStep(w, device=dev)
     s.populate(include_new=not mixed)
     if form in ("full_kv", "latent"):
@@ -427,7 +431,13 @@ def run_ours(args, world, rank, local):
             s.out_proj()
             return
         if form == "full_kv":
-            s.naive_decode()
+            if mixed:
+                # version 1 on prefill chunks: the new tokens' rows, then the
+                # tensor-core attention in 64-row tiles
+                s.naive_write_new()
+                s.naive_prefill()
+            else:
+                s.naive_decode()
             return
         if form == "latent":
             s.latent_expand()
@@ -457,8 +467,10 @@ def run_ours(args, world, rank, local):
 
     launches_per_step = 2 + decode_launches + (1 if mixed else 0)
     if form in ("full_kv", "latent"):
-        # decode + merge; version 2 adds the weight transpose and the expansion
-        launches_per_step = 2 if form == "full_kv" else 4
+        # decode + merge; version 2 adds the weight transpose and the expansion;
+        # version 1 on prefill chunks: the new tokens' cache write (index list,
+        # latent rows, weight transpose, expansion) and the attention
+        launches_per_step = (5 if mixed else 2) if form == "full_kv" else 4
     if form == "layer":
         # the absorbed step, the new tokens' cache write, and the three
         # projections (each one kernel, plus its split-K sum when it splits)
@@ -520,7 +532,7 @@ def run_ours(args, world, rank, local):
     # path, else the planned decode (the plan is in the workspace by now);
     # for the other forms their dominant call
     if form == "full_kv":
-        decode_alone = s.naive_decode
+        decode_alone = s.naive_prefill if mixed else s.naive_decode
     elif form == "fp8":
         decode_alone = s.decode_paged_combine_fp8
     elif form == "latent":
@@ -552,7 +564,19 @@ def run_ours(args, world, rank, local):
     pairs = int(sum(int(p) + 1 for p in w.q_positions))
     attn_flops = int(w.num_heads) * pairs * (576 + 512) * 2
     tpeak, _ = tensor_peak()
-    if form == "full_kv":
+    if form == "full_kv" and mixed:
+        kernel = "naive_prefill_kernel"
+        # (row, head) x visible token pairs, a 192-wide score and a 128-wide
+        # accumulation each
+        flops = int(w.num_heads) * pairs * (192 + 128) * 2
+        tflops = flops / (kernel_ms * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "achieved": round(tflops, 1), "peak": tpeak,
+                    "unit": "TFLOP/s", "frac": round(tflops / tpeak, 4),
+                    "traffic": profiled_traffic(kernel, args.workload), "kernel": kernel,
+                    "kernel_us": round(kernel_ms * 1e3, 2), "algorithmic_flops": flops,
+                    "absorbed_attention_flops": attn_flops,
+                    "peak_kind": "measured bf16 dense (cuBLAS, burst)"}
+    elif form == "full_kv":
         kernel = "naive_decode_kernel"
         nbytes = pairs * int(w.num_heads) * 640 + int(w.block_table.size) * 4
         achieved = nbytes / (kernel_ms * 1e-3) / 1e9

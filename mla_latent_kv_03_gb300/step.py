@@ -223,6 +223,12 @@ class MlaDecodeStep:
                                 self.slot_mapping, self.rms_weight, self.W_uk, self.W_uv,
                                 self.kv_naive, self.naive_ws)
 
+    def naive_write_new(self, stream=None) -> None:
+        """Version 1's cache write of the step's new tokens."""
+        L.mla_naive_cache_write(self.cfg, self.c_kv_new, self.k_pe_new, self.pos_new,
+                                self.slot_new, self.rms_weight, self.W_uk, self.W_uv,
+                                self.kv_naive, self.naive_ws, stream=stream)
+
     def latent_expand(self, stream=None) -> None:
         """Version 2: re-expand the whole latent cache into kv_naive."""
         L.mla_latent_expand(self.cfg, self.cache, self.block_table, self.seq_lens, self.W_uk,
