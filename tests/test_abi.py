@@ -163,3 +163,23 @@ def test_projections_check_their_arguments_on_the_host(lib):
         assert fn(ctypes.byref(bf16), None, None, None, None, 0, 2048, ws, 256, None) == 0
     assert lib.mla_o_proj(ctypes.byref(bf16), p, p, None, 4, 2048, ws, 1 << 20, None) == 1
     assert lib.mla_o_proj(ctypes.byref(bf16), p, p, p, -1, 2048, ws, 1 << 20, None) == 1
+
+
+def test_naive_prefill_checks_its_arguments_on_the_host(lib):
+    f32 = L.make_config(16, 64, "f32")
+    bf16 = L.make_config(16, 64, "bf16")
+    p = ctypes.c_void_p(1 << 20)
+    ws = ctypes.c_void_p(1 << 21)
+    fn = lib.mla_naive_prefill
+    assert fn(ctypes.byref(f32), p, p, p, p, 16, p, 4, p, p, 4, 4, ws, 256, p, None) == 2
+    assert fn(ctypes.byref(bf16), p, p, p, p, 16, p, 4, p, p, 4, 4, None, 256, p, None) == 1
+    assert fn(ctypes.byref(bf16), p, p, p, p, 16, p, 4, p, p, 4, 4, ws, 128, p, None) == 1
+    assert fn(ctypes.byref(bf16), ctypes.c_void_p((1 << 20) + 8), p, p, p, 16, p, 4, p, p, 4, 4,
+              ws, 256, p, None) == 1
+    assert fn(ctypes.byref(bf16), p, p, p, p, 16, p, 4, p, p, 4, -1, ws, 256, p, None) == 1
+    # no rows: nothing to do, nothing touched
+    assert fn(ctypes.byref(bf16), None, None, None, None, 16, None, 4, None, None, 4, 0, ws, 256,
+              None, None) == 0
+    # more query tiles than one launch holds
+    assert fn(ctypes.byref(bf16), p, p, p, p, 16, p, 4, p, p, 4, 64 * 70000, ws, 256, p,
+              None) == 2
