@@ -83,7 +83,7 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--ref-seconds", type=float, default=120.0,
                    help="host time the reference arm's timed steps aim at in total")
-    p.add_argument("--form", choices=["absorbed", "full_kv", "latent", "fp8", "layer"],
+    p.add_argument("--form", choices=["absorbed", "full_kv", "latent", "fp8", "layer", "hybrid"],
                    default="absorbed",
                    help="absorbed: the latent decode (default); full_kv: the page's version 1 "
                         "(expanded K/V cache, decode only); latent: version 2 (the latent cache "
@@ -91,7 +91,9 @@ def parse_args(argv=None):
                         "over an e4m3 latent cache (640 bytes per token, kv_scale 0.02); "
                         "layer: the whole attention layer from the hidden states (q_proj, "
                         "kv_a_proj and the cache write of the new tokens, the absorbed step, "
-                        "o_proj; hidden size 2048)")
+                        "o_proj; hidden size 2048); hybrid (prefill + decode batches): prefill "
+                        "sequences re-expanded and attended on tensor cores in the expanded form, "
+                        "decode rows absorbed, concurrently")
     return p.parse_args(argv)
 
 
@@ -367,6 +369,17 @@ def proj_launches(M, N, K, sms):
     return 2 if s > 1 else 1
 
 
+def w_decode_part(w):
+    """The decode sequences of a prefill + decode batch, as the hybrid step's
+    absorbed call sees them (their rows, their sequence count)."""
+    import types
+    import numpy as np
+    ql = np.diff(w.query_start_loc)
+    d = ql <= 1
+    return types.SimpleNamespace(dtype=w.dtype, num_heads=w.num_heads, num_q=int(ql[d].sum()),
+                                 batch=int(d.sum()))
+
+
 def decode_call_launches(w, props):
     """(self-planned, kernel launches) of one mla_decode_paged_combine call,
     following the library's choice: the 16-head warp-mma path plans inside
@@ -397,7 +410,9 @@ def run_ours(args, world, rank, local):
     w = make_workload(args.workload, rank)
     mixed = bool(w.is_new.sum() > w.batch)   # a step that writes more than one token per sequence
     form = args.form
-    if form != "absorbed" and (w.dtype != "bf16" or (mixed and form != "full_kv")):
+    if form == "hybrid" and not mixed:
+        raise SystemExit("--form hybrid: prefill + decode workloads only")
+    if form not in ("absorbed", "hybrid") and (w.dtype != "bf16" or (mixed and form != "full_kv")):
         raise SystemExit("--form full_kv / latent / fp8 / layer: bf16 decode workloads only "
                          "(full_kv also takes prefill chunks)")
     s = MlaDecodeStep(w, device=dev)
@@ -409,6 +424,8 @@ def run_ours(args, world, rank, local):
     if form == "fp8":
         s.fp8_setup(0.02)             # about max |c_hat| / 448 for these inputs
         s.fp8_populate()
+    if form == "hybrid":
+        s.hybrid_setup()
     if form == "layer":
         s.layer_setup(HIDDEN_SIZE)
         s.layer_populate()            # the old tokens' rows from their projected latents
@@ -422,6 +439,9 @@ def run_ours(args, world, rank, local):
     self_planned, decode_launches = decode_call_launches(w, torch.cuda.get_device_properties(dev))
 
     def one_step():
+        if form == "hybrid":
+            s.hybrid_step(side)
+            return
         if form == "layer":
             s.layer_step()
             return
@@ -471,6 +491,11 @@ def run_ours(args, world, rank, local):
         # version 1 on prefill chunks: the new tokens' cache write (index list,
         # latent rows, weight transpose, expansion) and the attention
         launches_per_step = (5 if mixed else 2) if form == "full_kv" else 4
+    if form == "hybrid":
+        # cache write; absorb, decode (+ merge if split-heavy), out_proj of the
+        # decode rows; weight transpose, expansion and attention of the prefill rows
+        _, dl = decode_call_launches(w_decode_part(w), torch.cuda.get_device_properties(dev))
+        launches_per_step = 1 + 2 + dl + 3
     if form == "layer":
         # the absorbed step, the new tokens' cache write, and the three
         # projections (each one kernel, plus its split-K sum when it splits)
@@ -531,7 +556,9 @@ def run_ours(args, world, rank, local):
     # the decode kernel of the step: the self-planned one on the warp-mma
     # path, else the planned decode (the plan is in the workspace by now);
     # for the other forms their dominant call
-    if form == "full_kv":
+    if form == "hybrid":
+        decode_alone = s.hybrid_prefill_attention
+    elif form == "full_kv":
         decode_alone = s.naive_prefill if mixed else s.naive_decode
     elif form == "fp8":
         decode_alone = s.decode_paged_combine_fp8
@@ -564,11 +591,13 @@ def run_ours(args, world, rank, local):
     pairs = int(sum(int(p) + 1 for p in w.q_positions))
     attn_flops = int(w.num_heads) * pairs * (576 + 512) * 2
     tpeak, _ = tensor_peak()
-    if form == "full_kv" and mixed:
+    if (form == "full_kv" and mixed) or form == "hybrid":
         kernel = "naive_prefill_kernel"
         # (row, head) x visible token pairs, a 192-wide score and a 128-wide
-        # accumulation each
-        flops = int(w.num_heads) * pairs * (192 + 128) * 2
+        # accumulation each (hybrid: the prefill rows only)
+        kpairs = pairs if form == "full_kv" else int(
+            sum(int(p) + 1 for p in w.q_positions[:s.hy_rows]))
+        flops = int(w.num_heads) * kpairs * (192 + 128) * 2
         tflops = flops / (kernel_ms * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": round(tflops, 1), "peak": tpeak,
                     "unit": "TFLOP/s", "frac": round(tflops / tpeak, 4),
@@ -620,7 +649,7 @@ def run_ours(args, world, rank, local):
     (st1, bits1), (st2, bits2) = s.device_status()
     if st1 != 0 or st2 != 0:
         raise SystemExit(f"device status after bench: decode {bits1:#x}, cache write {bits2:#x}")
-    if form in ("full_kv", "latent"):
+    if form in ("full_kv", "latent", "hybrid"):
         st3, bits3 = L.mla_get_device_status(s.naive_ws)
         if st3 != 0:
             raise SystemExit(f"device status after bench: {form} {bits3:#x}")
@@ -673,6 +702,8 @@ def run_e2e(args, s, w, stream, latent, world, mixed, one_step, out):
                  "pos_new", "slot_new"]
     if mixed:
         names += ["c_kv_new", "k_pe_new", "pos_new", "slot_new"]
+    if hasattr(s, "qsl_decode"):
+        names += ["qsl_decode"]
     out_name = next(n for n in ("y", "out", "out_naive") if getattr(s, n, None) is out)
     ins = [getattr(s, n) for n in names]
     offs, total = [], 0

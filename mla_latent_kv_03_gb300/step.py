@@ -244,6 +244,64 @@ class MlaDecodeStep:
                             self.block_table, self.seq_lens, self.query_start_loc, self.naive_ws,
                             self.out_naive, stream=stream)
 
+    # -- a prefill + decode batch split by form ----------------------------
+    def hybrid_setup(self) -> None:
+        """Prefill sequences (more than one new row) take the expanded form,
+        decode sequences the absorbed one; the batch holds the prefill
+        sequences first. Buffers of the expanded rows, the decode rows'
+        query_start_loc from 0, and the fork/join events."""
+        w = self.w
+        ql = np.diff(w.query_start_loc)
+        npf = int((ql > 1).sum())
+        if not (np.all(ql[:npf] > 1) and np.all(ql[npf:] <= 1)):
+            raise ValueError("hybrid step: prefill sequences must come first")
+        self.hy_seqs = npf
+        self.hy_rows = int(w.query_start_loc[npf])
+        self.qsl_decode = _dev((w.query_start_loc[npf:] - w.query_start_loc[npf]).astype(np.int32),
+                               torch.int32, self.device)
+        self.naive_setup()
+        self.hy_fork, self.hy_join = torch.cuda.Event(), torch.cuda.Event()
+
+    def hybrid_prefill(self, stream=None) -> None:
+        """The prefill sequences: their latent rows re-expanded per head, then
+        the tensor-core attention of their rows."""
+        P, R = self.hy_seqs, self.hy_rows
+        L.mla_latent_expand(self.cfg, self.cache, self.block_table[:P], self.seq_lens[:P],
+                            self.W_uk, self.W_uv, self.kv_naive, self.naive_ws, stream=stream)
+        self.hybrid_prefill_attention(stream=stream)
+
+    def hybrid_prefill_attention(self, stream=None) -> None:
+        P, R = self.hy_seqs, self.hy_rows
+        L.mla_naive_prefill(self.cfg, self.q_nope[:R], self.q_pe[:R], self.q_positions[:R],
+                            self.kv_naive, self.block_table[:P], self.seq_lens[:P],
+                            self.query_start_loc[:P + 1], self.naive_ws, self.out_naive[:R],
+                            stream=stream)
+
+    def hybrid_decode(self, stream=None) -> None:
+        """The decode sequences through the absorbed step; their output rows go
+        to out_naive as well."""
+        P, R = self.hy_seqs, self.hy_rows
+        L.mla_absorb_q(self.cfg, self.q_nope[R:], self.q_pe[R:], self.q_positions[R:], self.W_uk,
+                       self.q_abs[R:], stream=stream)
+        L.mla_decode_paged_combine(self.cfg, self.q_abs[R:], self.cache, self.block_table[P:],
+                                   self.seq_lens[P:], self.qsl_decode, self.workspace,
+                                   self.o_lat[R:], stream=stream)
+        L.mla_out_proj(self.cfg, self.o_lat[R:], self.W_uv, self.out_naive[R:], stream=stream)
+
+    def hybrid_step(self, side: torch.cuda.Stream) -> torch.Tensor:
+        """The new tokens' latent rows, then the decode part on `side` and the
+        prefill part on the current stream, concurrently."""
+        self.write_new()
+        cur = torch.cuda.current_stream()
+        self.hy_fork.record(cur)
+        side.wait_event(self.hy_fork)
+        with torch.cuda.stream(side):
+            self.hybrid_decode()
+            self.hy_join.record(side)
+        self.hybrid_prefill()
+        cur.wait_event(self.hy_join)
+        return self.out_naive
+
     def device_status(self):
         """(status, bits) of the decode workspace and of the cache-write word."""
         s1 = L.mla_get_device_status(self.workspace)

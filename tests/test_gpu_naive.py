@@ -235,3 +235,25 @@ def test_naive_prefill_interleaved_rope_and_bad_sequence():
     got = to_f64(s.out_naive)
     assert np.all(got[w.q_range(1)] == 0)
     assert_close(got[w.q_range(0)], ref[w.q_range(0)], "bf16", "other sequence")
+
+
+def test_hybrid_step_on_the_mixed_batch_sampled():
+    # prefill sequences in the expanded form on tensor cores, decode rows
+    # absorbed, concurrently; checked on sampled sequences and heads
+    from _helpers import ref_out
+    w = W.mixed()
+    s = MlaDecodeStep(w, device=DEV)
+    s.populate(include_new=False)
+    s.hybrid_setup()
+    s.out_naive.fill_(float("nan"))
+    side = torch.cuda.Stream()
+    out = to_f64(s.hybrid_step(side))
+    torch.cuda.synchronize()
+    (st1, _), (st2, _) = s.device_status()
+    assert st1 == 0 and st2 == 0
+    assert L.mla_get_device_status(s.naive_ws)[0] == 0
+    assert not np.isnan(out).any()
+    seqs, heads = [1, 3, 4, 63], [0, 9, 15]
+    ref = ref_out(w, seqs=seqs, heads=heads)
+    rows = np.concatenate([np.arange(w.q_range(b).start, w.q_range(b).stop) for b in seqs])
+    assert_close(out[:, heads][rows], ref[rows], "bf16", "hybrid mixed step")
