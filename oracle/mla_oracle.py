@@ -22,7 +22,7 @@ Sources (web pages; section headings as printed on them)
 [HYB]   bxzpzcl.cn article on KV/state-cache management for hybrid (GDN/KDA)
         models in vLLM/SGLang: sections 2.2 and 2.3 (cache-size formulas).
 
-Readings where the sources are silent (each one also listed in the design doc):
+Readings where the sources are silent:
   * RoPE uses rotate-half pairing (x_i, x_{i+d/2}), inv_freq_i = base^(-2i/d).
   * A token's RoPE position is its 0-based index within its sequence.
   * The latent cache stores the RMSNorm'd c_kv (the pages' engine stores the
