@@ -16,7 +16,7 @@
 // warps), then O += P V with P taken from the score registers and V through
 // ldmatrix.trans. Rows of a key tile that are not live tokens have their V
 // zeroed in shared memory first, so P = 0 never meets garbage. Every wait is
-// bounded. 168 registers and 106 KB of shared memory let two
+// bounded. 168 registers and 105 KB of shared memory let two
 // CTAs share an SM: each scheduler's register partition (16,384) then holds
 // its three warps of them.
 #include <cuda_bf16.h>
