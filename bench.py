@@ -81,6 +81,14 @@ def parse_args(argv=None):
     p.add_argument("--kernel-launches", type=int, default=1000)
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--repeats", type=int, default=15,
+                   help="timed windows of exactly K steps each; the line reports the median "
+                        "window (fewer when K steps take long, at least 3)")
+    p.add_argument("--flushed-steps", type=int, default=50,
+                   help="single steps timed with L2 flushed before each")
+    p.add_argument("--code-hash", default=None, metavar="KERNEL:WORKLOAD",
+                   help="print the code hash a profile summary of KERNEL on WORKLOAD records, "
+                        "and exit")
     p.add_argument("--ref-seconds", type=float, default=120.0,
                    help="host time the reference arm's timed steps aim at in total")
     p.add_argument("--form", choices=["absorbed", "full_kv", "latent", "fp8", "layer", "hybrid"],
@@ -225,32 +233,55 @@ class ClockSampler:
                 "samples": len(use), "samples_in_window": len(sel)}
 
 
-def source_hash(names) -> str:
+def strip_comments(text: str) -> str:
+    """C++/CUDA source without its comments and with whitespace runs
+    collapsed: two sources that differ only in comments or layout compile to
+    the same kernel and give the same string. String literals in the kernels
+    hold no comment markers."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
+def code_hash(names) -> str:
+    """Hash of the code (comments and layout excluded) of the kernel sources a
+    profile summary covers. A summary records this value when it is captured
+    (`python bench.py --code-hash KERNEL:WORKLOAD` on the box, right after the
+    ncu run); any later change to the code voids its DRAM figure until the
+    kernel is captured again."""
     h = hashlib.sha256()
     for name in names:
-        with open(os.path.join(ROOT, "mla_latent_kv_03_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "mla_latent_kv_03_gb300", "csrc", name)) as f:
+            h.update(strip_comments(f.read()).encode())
+        h.update(b"\0")
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel: str, workload: str):
-    """DRAM bytes per decode launch from the committed ncu summary of this
-    kernel on this workload, or None if there is none or the kernel's sources
-    changed since it was taken."""
-    entry = PROFILES.get((kernel, workload))
-    if entry is None:
-        return None
-    fname, sources = entry
+def profile_fields(fname: str) -> dict:
+    """The `- key: `value`` lines of a committed profile summary."""
     try:
         text = open(os.path.join(ROOT, "profiles", fname)).read()
     except OSError:
-        return None
+        return {}
     vals = {}
     for line in text.splitlines():
         if ":" in line and line.strip().startswith("- "):
             k, v = line.strip()[2:].split(":", 1)
             vals[k.strip()] = v.strip().strip("`")
-    if vals.get("source_sha256") != source_hash(sources):
+    return vals
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary of this
+    kernel on this workload, or None if there is none or the kernel's code
+    changed since it was captured."""
+    entry = PROFILES.get((kernel, workload))
+    if entry is None:
+        return None
+    fname, sources = entry
+    vals = profile_fields(fname)
+    if vals.get("code_sha256") != code_hash(sources):
         return None
     try:
         return float(vals["dram_bytes_per_launch_full_size"].replace(",", ""))
@@ -528,27 +559,53 @@ def run_ours(args, world, rank, local):
         run_steps(args.warmup)
     stream.synchronize()
 
-    # ---- timed region: K steps, inputs resident in HBM
-    sampler = ClockSampler(local)
-    sampler.start()
-    barrier(world)
-    torch.cuda.synchronize()
+    # ---- timed region: windows of exactly K steps, inputs resident in HBM;
+    # each window bracketed by a barrier and a synchronize, its time the max
+    # over ranks; the line reports the median window
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_wall0 = time.time()
     with torch.cuda.stream(stream):
         e0.record(stream)
-        run_steps(args.steps)
+        run_steps(min(args.steps, 20))
         e1.record(stream)
     e1.synchronize()
+    est_ms = e0.elapsed_time(e1) / min(args.steps, 20)
+    repeats = max(3, min(args.repeats, int(30e3 / max(est_ms * args.steps, 1e-3))))
+    sampler = ClockSampler(local)
+    sampler.start()
+    windows = []
+    t_wall0 = time.time()
+    for _ in range(repeats):
+        barrier(world)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            run_steps(args.steps)
+            e1.record(stream)
+        e1.synchronize()
+        torch.cuda.synchronize()
+        barrier(world)
+        windows.append(max_over_ranks(e0.elapsed_time(e1), world))
     t_wall1 = time.time()
-    torch.cuda.synchronize()
-    barrier(world)
     clocks = ClockSampler.summarise(sampler.stop(), t_wall0, t_wall1)
-    ms = e0.elapsed_time(e1)
-    ms_max = max_over_ranks(ms, world)
+    ms_max = statistics.median(windows)
     total_bytes = sum_over_ranks(float(latent) * args.steps, world)
     value = total_bytes / (ms_max * 1e-3) / 1e9
     ms_per_step = ms_max / args.steps
+
+    # ---- single steps with L2 flushed before each (a 512 MB write between
+    # steps, outside the timed pair of events)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    f0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.flushed_steps)]
+    f1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.flushed_steps)]
+    with torch.cuda.stream(stream):
+        for i in range(args.flushed_steps):
+            flush.zero_()
+            f0[i].record(stream)
+            graph1.replay()
+            f1[i].record(stream)
+    stream.synchronize()
+    flushed_ms = statistics.median(a.elapsed_time(b) for a, b in zip(f0, f1))
+    del flush
 
     # ---- decode kernel alone: back-to-back launches, CUDA events on its stream
     per_graph = 20
@@ -640,6 +697,19 @@ def run_ours(args, world, rank, local):
                     "peak_kind": f"{peak_kind} HBM copy bandwidth (burst)",
                     "frac_of_nominal_8TBs": round(achieved / NOMINAL_HBM_GBS, 4)}
 
+    # the step's algorithmic bytes: every visible latent row once, both
+    # weights, the query inputs, the output and the block table
+    elem = 2 if w.dtype == "bf16" else 4
+    step_bytes = (latent + 2 * int(w.num_heads) * 512 * 128 * elem
+                  + int(w.num_q) * int(w.num_heads) * (192 + 128) * elem
+                  + int(w.block_table.size) * 4)
+    if form in ("absorbed", "fp8"):
+        roofline["step_bytes"] = step_bytes
+        roofline["step_frac"] = round(step_bytes / (ms_per_step * 1e-3) / 1e9 / peak, 4)
+        roofline["step_frac_of_nominal_8TBs"] = round(
+            step_bytes / (ms_per_step * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4)
+        roofline["step_frac_l2_flushed"] = round(step_bytes / (flushed_ms * 1e-3) / 1e9 / peak, 4)
+
     # ---- end to end through the same calls, host buffers, eager launches
     e2e = run_e2e(args, s, w, stream, latent, world, mixed, one_step,
                   s.y if form == "layer" else
@@ -671,11 +741,19 @@ def run_ours(args, world, rank, local):
             "config": {"workload": w.name, "form": form, "batch": w.batch, "num_heads": w.num_heads,
                        "seq_lens": "all 4096" if args.workload == "serving" else "see workload",
                        "block_size": w.block_size, "latent_bytes_per_step": latent,
-                       "l2": "inputs larger than L2: the latent cache read each step exceeds 129 MB",
-                       "graph": "steps captured in CUDA graphs of 10; exactly K steps replayed"
+                       "l2": "inputs larger than L2: the latent cache read each step exceeds "
+                             "129 MB; us_per_step_l2_flushed times single steps after a 512 MB "
+                             "write",
+                       "graph": "steps captured in CUDA graphs of 10; windows of exactly K "
+                                "steps replayed, median window reported"
                                 + ("" if self_planned else " (plan forked onto a side stream)"),
                        "parallelism": f"replicas x{world} (independent batches per GPU)"},
             "us_per_step": round(ms_per_step * 1e3, 2),
+            "us_per_step_l2_flushed": round(flushed_ms * 1e3, 2),
+            "timed_windows": {"repeats": repeats, "steps_each": args.steps,
+                              "us_per_step_min": round(min(windows) / args.steps * 1e3, 2),
+                              "us_per_step_median": round(ms_per_step * 1e3, 2),
+                              "us_per_step_max": round(max(windows) / args.steps * 1e3, 2)},
             "tokens_per_s": round(w.num_q * world / (ms_per_step * 1e-3), 1),
             "pct_of_nominal_8TBs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
             "pct_of_measured_hbm": round(100 * value / world / peak, 2),
@@ -838,6 +916,10 @@ def run_reference(args, world, rank):
 
 def main(argv=None):
     args = parse_args(argv)
+    if args.code_hash:
+        kernel, workload = args.code_hash.split(":")
+        print(code_hash(PROFILES[(kernel, workload)][1]))
+        return
     world, rank, local = dist_setup()
     if world != args.gpus and world > 1:
         raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE {world}")

@@ -403,10 +403,13 @@ mla_status mla_naive_prefill(const mla_config* cfg, const void* q_nope, const vo
  * the call uses the largest CTA count c below the SM count for which
  * mla_decode_workspace_size with num_ctas = c fits. A launch that does not
  * fit even so, or with the caller's fixed num_ctas, returns
- * MLA_ERR_WORKSPACE_TOO_SMALL and enqueues nothing.
+ * MLA_ERR_WORKSPACE_TOO_SMALL. Every refusal (that one, and the argument
+ * checks of mla_decode_paged, which run first and return the same codes)
+ * enqueues nothing and leaves the array as it was.
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
- * capture. Every call on a device shares the array and leaves its contents
+ * capture. The address is kept for the life of the process: after a
+ * cudaDeviceReset of a device, do not call this again on that device. Every call on a device shares the array and leaves its contents
  * for the next one: each call clears the status word and plan header itself,
  * and calls whose GPU work overlaps (other streams or host threads) race on
  * the array and must not be issued. dev_status (device word, may be NULL)

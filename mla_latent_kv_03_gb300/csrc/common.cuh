@@ -181,6 +181,27 @@ __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bits) {
   if (status) atomicOr(status, bits);
 }
 
+// Counting a finished split part on its q-tile's arrival counter (the fused
+// split merges). Protocol, in PTX memory-model terms:
+//   1. every thread that stored part of the partial (or its log-sum-exp)
+//      issues fence.acq_rel.gpu (__threadfence) after its stores;
+//   2. a CTA barrier orders those fences before the counting thread's atomic;
+//   3. the counting thread adds with atom.acq_rel.gpu: its release half
+//      publishes the CTA's stores, its acquire half -- on the CTA that counts
+//      last -- makes every other part's release visible to it;
+//   4. a second CTA barrier hands that to the merging threads, which read the
+//      parts through L2 (ld.global.cg), never through the non-coherent path.
+// The counter is reset to zero by the merging CTA after its merge; the next
+// launch's atomics come after this grid has completed.
+__device__ __forceinline__ int count_arrival(int* counter) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+               : "=r"(old)
+               : "l"(counter)
+               : "memory");
+  return old;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

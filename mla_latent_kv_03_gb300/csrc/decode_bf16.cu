@@ -712,17 +712,15 @@ __global__ void __maxnreg__(168)
         lse_out[(size_t)slot * kHG + g] = lse0;
         lse_out[(size_t)slot * kHG + g + 8] = lse1;
       }
-      // every thread's part is written (barrier), one thread publishes them
-      // (fence, count) and, if it counted last, orders the reads that follow
+      // every writing thread fences its stores, the barrier orders the
+      // fences before the count, and one thread counts the part with an
+      // acquire-release atomic (count_arrival); if it counted last, the
+      // second barrier orders the merge's reads after every part's release
       int* arrive = reinterpret_cast<int*>(ws + L.arrive);
+      __threadfence();
       named_bar_sync(kMathBar, kMathWarps * 32);
       int* flag = reinterpret_cast<int*>(smax);  // smax is free until the next tile
-      if (tid == 0) {
-        __threadfence();
-        const bool last = atomicAdd(&arrive[t], 1) == c_last - c_first;
-        if (last) __threadfence();
-        flag[0] = last;
-      }
+      if (tid == 0) flag[0] = count_arrival(&arrive[t]) == c_last - c_first;
       named_bar_sync(kMathBar, kMathWarps * 32);
       if (flag[0] != 0) {
         // online split-softmax merge over the parts in CTA order (the same

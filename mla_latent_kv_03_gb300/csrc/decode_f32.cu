@@ -155,12 +155,11 @@ __global__ void __launch_bounds__(256) decode_f32_kernel(DecodeArgs a) {
     }
     if (a.o_lat != nullptr && !direct) {
       int* arrive = reinterpret_cast<int*>(ws + L.arrive);
-      __threadfence();
+      __threadfence();   // publish protocol: see count_arrival
       __syncthreads();
-      if (tid == 0) sFlag[0] = atomicAdd(&arrive[t], 1) == c_last - c_first;
+      if (tid == 0) sFlag[0] = count_arrival(&arrive[t]) == c_last - c_first;
       __syncthreads();
       if (sFlag[0]) {
-        __threadfence();
         merge_qtile<256>(lse_out, o_out, (int64_t)c_first + t, c_last - c_first + 1, 1,
                          a.o_lat + ((size_t)seg.n * a.num_heads + seg.g * kHG) * kDc, tid, sMerge,
                          [] { __syncthreads(); });

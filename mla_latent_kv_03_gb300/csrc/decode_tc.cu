@@ -772,21 +772,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc::fence_before_sync();
       mbar_arrive(&bars[kOFree]);
       if (a.o_lat != nullptr && !direct) {
-        // count this part; the last part of this half merges the q-block
+        // count this part (fence per writing thread, barrier, acquire-release
+        // count: count_arrival); the last part of this half merges the
+        // q-block, reading the parts through L2 after the second barrier
         __threadfence();
         named_bar_sync(kSoftBar, 128);
-        if (r == 0) *merge_flag = atomicAdd(&arrive[seg.qb * 2 + h], 1) == c_last - c_first;
+        if (r == 0) *merge_flag = count_arrival(&arrive[seg.qb * 2 + h]) == c_last - c_first;
         named_bar_sync(kSoftBar, 128);
         if (*merge_flag) {
-          __threadfence();
           const int ns = c_last - c_first + 1;
           const int64_t s0 = (int64_t)c_first + seg.qb;
           // row r's max lse and 1 / weight sum over its parts
           float M = -INFINITY;
-          for (int s = 0; s < ns; ++s) M = fmaxf(M, lse_out[(s0 + s) * kQBlockRows + r]);
+          for (int s = 0; s < ns; ++s) M = fmaxf(M, __ldcg(lse_out + (s0 + s) * kQBlockRows + r));
           float den = 0.f;
           if (M != -INFINITY)
-            for (int s = 0; s < ns; ++s) den += fast_exp2(lse_out[(s0 + s) * kQBlockRows + r] - M);
+            for (int s = 0; s < ns; ++s) den += fast_exp2(__ldcg(lse_out + (s0 + s) * kQBlockRows + r) - M);
           const float dinv = den > 0.f ? 1.f / den : 0.f;
           const int rows_valid = min(kQBlockRows, (seg.t_end - seg.t_first) * kHG);
           const float4* op4 = reinterpret_cast<const float4*>(o_out) + 64 * h;
@@ -796,7 +797,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // float4 column tid % 64 of the half: coalesced, 16 rows per pass
             for (int s = 0; s < ns; ++s)
               wsm[s * kQBlockRows + r] =
-                  M == -INFINITY ? 0.f : fast_exp2(lse_out[(s0 + s) * kQBlockRows + r] - M) * dinv;
+                  M == -INFINITY ? 0.f : fast_exp2(__ldcg(lse_out + (s0 + s) * kQBlockRows + r) - M) * dinv;
             named_bar_sync(kSoftBar, 128);
             const int c4 = r & 63, rsub = r >> 6;
 #pragma unroll 1
@@ -809,7 +810,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const float4* src = op4 + (size_t)(s0 + s) * kQBlockRows * (kDc / 4) + c4;
                 float4 vv[16];
 #pragma unroll
-                for (int u = 0; u < 16; ++u) vv[u] = src[(size_t)(rsub + 2 * (k0 + u)) * (kDc / 4)];
+                for (int u = 0; u < 16; ++u) vv[u] = __ldcg(src + (size_t)(rsub + 2 * (k0 + u)) * (kDc / 4));
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
                   const float wgt = wsm[s * kQBlockRows + rsub + 2 * (k0 + u)];
@@ -832,8 +833,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int c = 0; c < 64; ++c) {
               float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
               for (int s = 0; s < ns; ++s) {
-                const float wgt = M == -INFINITY ? 0.f : fast_exp2(lse_out[(s0 + s) * kQBlockRows + r] - M) * dinv;
-                const float4 xv = op4[((size_t)(s0 + s) * kQBlockRows + r) * (kDc / 4) + c];
+                const float wgt = M == -INFINITY ? 0.f : fast_exp2(__ldcg(lse_out + (s0 + s) * kQBlockRows + r) - M) * dinv;
+                const float4 xv = __ldcg(op4 + ((size_t)(s0 + s) * kQBlockRows + r) * (kDc / 4) + c);
                 acc.x = fmaf(wgt, xv.x, acc.x);
                 acc.y = fmaf(wgt, xv.y, acc.y);
                 acc.z = fmaf(wgt, xv.z, acc.z);

@@ -111,6 +111,13 @@ cudaError_t launch_wait_timeout_selftest(uint32_t* status, int64_t timeout_ns,
 // the TMA descriptors (bf16, 128-byte swizzle) of 576-value rows and of a
 // row-major [rows, cols] matrix.
 mla_status validate_config(const mla_config* cfg);
+// Every host-side check mla_decode_paged makes on its arguments other than
+// the workspace (configuration, sizes, row limit, null and misaligned
+// pointers); MLA_OK for num_q == 0 once the sizes are valid.
+mla_status decode_paged_checks(const mla_config* cfg, const void* q_abs, const void* cache,
+                               int64_t num_blocks, const int32_t* block_table,
+                               int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                               const int32_t* query_start_loc, int32_t batch, int64_t num_q);
 bool encode_row_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows);
 bool encode_map_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
                    uint32_t box_cols, uint32_t box_rows);

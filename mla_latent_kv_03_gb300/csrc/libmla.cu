@@ -179,6 +179,25 @@ inline mla_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MLA_OK : 
 
 namespace mla {
 mla_status validate_config(const mla_config* cfg) { return check_cfg(cfg); }
+
+mla_status decode_paged_checks(const mla_config* cfg, const void* q_abs, const void* cache,
+                               int64_t num_blocks, const int32_t* block_table,
+                               int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                               const int32_t* query_start_loc, int32_t batch, int64_t num_q) {
+  mla_status s = check_cfg(cfg);
+  if (s != MLA_OK) return s;
+  if (num_q < 0 || batch < 0 || num_blocks < 0 || max_blocks_per_seq < 0)
+    return MLA_ERR_INVALID_ARGUMENT;
+  if (num_q > kMaxRows) return MLA_ERR_UNSUPPORTED;
+  if (num_blocks * cfg->block_size > ((int64_t)1 << 31)) return MLA_ERR_UNSUPPORTED;
+  if (num_q == 0) return MLA_OK;
+  if (!q_abs || !cache || !block_table || !seq_lens || !query_start_loc || batch == 0)
+    return MLA_ERR_INVALID_ARGUMENT;
+  if (!aligned(q_abs, 16) || !aligned(cache, 16) || !aligned(block_table, 4) ||
+      !aligned(seq_lens, 4) || !aligned(query_start_loc, 4))
+    return MLA_ERR_INVALID_ARGUMENT;
+  return MLA_OK;
+}
 bool encode_row_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
   return make_row_map(map, base, rows, box_rows);
 }
@@ -415,21 +434,14 @@ mla_status mla_decode_paged(const mla_config* cfg, const void* q_abs, const void
                             int32_t max_blocks_per_seq, const int32_t* seq_lens,
                             const int32_t* query_start_loc, int32_t batch, int64_t num_q,
                             void* workspace, size_t ws_bytes, void* stream) {
-  mla_status s = check_cfg(cfg);
+  mla_status s = mla::decode_paged_checks(cfg, q_abs, cache, num_blocks, block_table,
+                                          max_blocks_per_seq, seq_lens, query_start_loc, batch,
+                                          num_q);
   if (s != MLA_OK) return s;
-  if (num_q < 0 || batch < 0 || num_blocks < 0 || max_blocks_per_seq < 0)
-    return MLA_ERR_INVALID_ARGUMENT;
-  if (num_q > kMaxRows) return MLA_ERR_UNSUPPORTED;
-  if (num_blocks * cfg->block_size > ((int64_t)1 << 31)) return MLA_ERR_UNSUPPORTED;
   if (!workspace || !aligned(workspace, 256)) return MLA_ERR_INVALID_ARGUMENT;
   if (num_q == 0) return MLA_OK;
-  if (!q_abs || !cache || !block_table || !seq_lens || !query_start_loc || batch == 0)
-    return MLA_ERR_INVALID_ARGUMENT;
-  if (!aligned(q_abs, 16) || !aligned(cache, 16) || !aligned(block_table, 4))
-    return MLA_ERR_INVALID_ARGUMENT;
   if (use_self_plan(cfg, num_q, batch)) {
     // one launch: the kernel plans and writes the plan to the workspace
-    if (!aligned(seq_lens, 4) || !aligned(query_start_loc, 4)) return MLA_ERR_INVALID_ARGUMENT;
     return decode_impl(cfg, q_abs, cache, num_blocks, block_table, max_blocks_per_seq, batch, num_q,
                        workspace, ws_bytes, nullptr, stream, 1, seq_lens, query_start_loc);
   }

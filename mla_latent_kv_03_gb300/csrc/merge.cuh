@@ -2,9 +2,9 @@
 //
 // Each CTA that finishes its part of a q-tile (query row n, 16-head group g)
 // publishes its normalised partial and log-sum-exp, then counts itself in
-// arrive[t] (release: __threadfence before the atomic). The CTA that brings
-// the count to the number of parts merges all of them (acquire:
-// __threadfence after the atomic) with the split-softmax identity
+// arrive[t] (count_arrival: per-thread fences, a CTA barrier, an
+// acquire-release atomic). The CTA that brings the count to the number of
+// parts merges all of them with the split-softmax identity
 //   o = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M),  M = max_s lse_s,
 // while they are still in L2. A q-tile that lies inside one CTA's share is
 // written to o_lat directly and never touches the partial buffers.
@@ -17,14 +17,16 @@ namespace mla {
 constexpr int kMergeChunk = 16;  // slots whose weights are staged at a time
 
 // The parts are 16-row groups slot0, slot0 + stride, ... of the partial buffer.
-// Scratch: 32 + kMergeChunk * 16 floats of shared memory.
+// Scratch: 32 + kMergeChunk * 16 floats of shared memory. In a fused merge
+// other CTAs of the same launch wrote the parts, so they are read through L2
+// (ld.global.cg) and the pointers are not declared __restrict__ (which would
+// let the compiler use the non-coherent read-only path).
 // `sync` synchronises the `nthreads` participating threads (tid in [0, nthreads)).
 // All (slot, row) log-sum-exps of a chunk are fetched in one parallel round
 // trip; the partial rows of two slots are in flight at a time.
 template <int NTHREADS, typename Sync>
-__device__ __forceinline__ void merge_qtile(const float* __restrict__ lse,
-                                            const float* __restrict__ opart, int64_t slot0,
-                                            int nslots, int stride, float* __restrict__ out,
+__device__ __forceinline__ void merge_qtile(const float* lse, const float* opart, int64_t slot0,
+                                            int nslots, int stride, float* out,
                                             int tid, float* scratch, Sync sync) {
   constexpr int kItems = kHG * kDc / 4 / NTHREADS;  // float4 items per thread
   float* sM = scratch;
@@ -36,7 +38,7 @@ __device__ __forceinline__ void merge_qtile(const float* __restrict__ lse,
     const int ns = min(kMergeChunk, nslots - s0);
     sync();
     for (int i = tid; i < ns * kHG; i += NTHREADS)
-      sW[i] = lse[(slot0 + (int64_t)(s0 + i / kHG) * stride) * kHG + i % kHG];
+      sW[i] = __ldcg(lse + (slot0 + (int64_t)(s0 + i / kHG) * stride) * kHG + i % kHG);
     sync();
     if (tid < kHG) {
       const float Mold = sM[tid];
@@ -66,7 +68,7 @@ __device__ __forceinline__ void merge_qtile(const float* __restrict__ lse,
       const float M = sM[r];
       sW[i] = M == -INFINITY
                   ? 0.f
-                  : fast_exp2(lse[(slot0 + (int64_t)(s0 + i / kHG) * stride) * kHG + r] - M) * sInv[r];
+                  : fast_exp2(__ldcg(lse + (slot0 + (int64_t)(s0 + i / kHG) * stride) * kHG + r) - M) * sInv[r];
     }
     sync();
     for (int s = 0; s < ns; s += 2) {
@@ -76,8 +78,8 @@ __device__ __forceinline__ void merge_qtile(const float* __restrict__ lse,
       float4 v0[kItems], v1[kItems];
 #pragma unroll
       for (int j = 0; j < kItems; ++j) {
-        v0[j] = src0[tid + j * NTHREADS];
-        v1[j] = src1[tid + j * NTHREADS];
+        v0[j] = __ldcg(src0 + tid + j * NTHREADS);
+        v1[j] = __ldcg(src1 + tid + j * NTHREADS);
       }
 #pragma unroll
       for (int j = 0; j < kItems; ++j) {

@@ -28,7 +28,10 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) uint8_t g_scratch[kScratchBytes];
 
 // The host-side name g_scratch is only a stand-in for the device array; the
-// kernels get its device address, resolved once per device.
+// kernels get its device address, resolved once per device. The address is
+// kept for the life of the process: after cudaDeviceReset the module may be
+// loaded again elsewhere, so the library must not be called on that device
+// again in this process.
 void* g_scratch_ptr[kMaxDevices] = {};
 std::mutex g_scratch_mu;
 
@@ -57,14 +60,20 @@ mla_status mla_decode_paged_noalloc(const mla_config* cfg, const void* q_abs, co
                                     int32_t max_blocks_per_seq, const int32_t* seq_lens,
                                     const int32_t* query_start_loc, int32_t batch, int64_t num_q,
                                     float* o_lat, uint32_t* dev_status, void* stream) {
-  if (num_q < 0) return MLA_ERR_INVALID_ARGUMENT;
+  // every argument check of mla_decode_paged first, so that a refused call
+  // has touched nothing, the scratch included
+  mla_status s = mla::decode_paged_checks(cfg, q_abs, cache, num_blocks, block_table,
+                                          max_blocks_per_seq, seq_lens, query_start_loc, batch,
+                                          num_q);
+  if (s != MLA_OK) return s;
   if (num_q == 0) return MLA_OK;
   if (!o_lat || (reinterpret_cast<uintptr_t>(o_lat) & 15) != 0) return MLA_ERR_INVALID_ARGUMENT;
   if (dev_status && (reinterpret_cast<uintptr_t>(dev_status) & 3) != 0)
     return MLA_ERR_INVALID_ARGUMENT;
-  // the scratch must hold this launch's workspace
+  // the scratch must hold this launch's workspace; with the arguments valid,
+  // a zero size means the device query failed
   const size_t need = mla_decode_workspace_size(cfg, num_q, batch);
-  if (need == 0) return cfg ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARGUMENT;
+  if (need == 0) return MLA_ERR_CUDA;
   mla_config fit = *cfg;
   if (need > kScratchBytes) {
     if (cfg->num_ctas > 0) return MLA_ERR_WORKSPACE_TOO_SMALL;
@@ -88,9 +97,8 @@ mla_status mla_decode_paged_noalloc(const mla_config* cfg, const void* q_abs, co
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // status word and plan header start at zero on every call
   if (cudaMemsetAsync(ws, 0, sizeof(mla::WsHeader), st) != cudaSuccess) return MLA_ERR_CUDA;
-  mla_status s = mla_decode_paged(&fit, q_abs, cache, num_blocks, block_table, max_blocks_per_seq,
-                                  seq_lens, query_start_loc, batch, num_q, ws, kScratchBytes,
-                                  stream);
+  s = mla_decode_paged(&fit, q_abs, cache, num_blocks, block_table, max_blocks_per_seq, seq_lens,
+                       query_start_loc, batch, num_q, ws, kScratchBytes, stream);
   if (s != MLA_OK) return s;
   s = mla_combine(&fit, ws, kScratchBytes, batch, num_q, o_lat, stream);
   if (s != MLA_OK) return s;

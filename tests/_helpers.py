@@ -76,3 +76,25 @@ def bf16_ulp(x):
     """Spacing of bf16 numbers at |x| (8 significant bits)."""
     ax = np.maximum(np.abs(x), np.finfo(np.float32).tiny)
     return np.exp2(np.floor(np.log2(ax)) - 7)
+
+
+def ref_out_absorbed(w, seqs, rows_of=None):
+    """Output [num_q, H, 128] through the oracle's absorbed form (cache rows,
+    q_abs, latent attention, W_uv), which the oracle's tests hold equal to the
+    naive form to 1e-12; cheap enough for every head of long sequences.
+    rows_of(b) may pick a subset of sequence b's query rows (indices into
+    w.q_range(b)); other rows stay NaN."""
+    out = np.full((w.num_q, w.num_heads, 128), np.nan)
+    for b in seqs:
+        tr, qr = w.token_range(b), w.q_range(b)
+        if qr.stop == qr.start:
+            continue
+        idx = np.arange(qr.start, qr.stop)
+        if rows_of is not None:
+            idx = idx[np.asarray(rows_of(b), dtype=np.int64)]
+        rows = O.latent_cache_rows(w.c_kv_raw[tr], w.k_pe_raw[tr], w.kv_positions[tr],
+                                   w.rms_weight, w.rms_eps, w.rope_base)
+        q_abs = O.absorb_q(w.q_nope[idx], w.q_pe[idx], w.q_positions[idx], w.W_uk, w.rope_base)
+        o_lat, _ = O.latent_attention(q_abs, rows, w.q_positions[idx], w.softmax_scale)
+        out[idx] = O.out_proj(o_lat, w.W_uv)
+    return out

@@ -183,3 +183,49 @@ def test_naive_prefill_checks_its_arguments_on_the_host(lib):
     # more query tiles than one launch holds
     assert fn(ctypes.byref(bf16), p, p, p, p, 16, p, 4, p, p, 4, 64 * 70000, ws, 256, p,
               None) == 2
+
+
+def _decode_args(p, num_q=1, batch=1, num_blocks=4, mbps=4):
+    # q_abs, cache, num_blocks, block_table, max_blocks_per_seq, seq_lens,
+    # query_start_loc, batch, num_q
+    return [p, p, num_blocks, p, mbps, p, p, batch, num_q]
+
+
+@pytest.mark.parametrize("case", ["cfg", "num_ctas", "batch", "num_q", "blocks", "null_q", "mis_cache",
+                                  "mis_seq", "rows"])
+def test_noalloc_refuses_like_decode_paged(lib, case):
+    """The no-alloc decode runs mla_decode_paged's argument checks before it
+    touches its scratch, and returns the same codes."""
+    cfg = L.make_config(16, 64, "bf16")
+    p = ctypes.c_void_p(256)
+    args = _decode_args(p)
+    cfgp = ctypes.byref(cfg)
+    if case == "cfg":
+        cfg.num_heads = 24
+    elif case == "num_ctas":
+        cfg.num_ctas = -2
+    elif case == "batch":
+        args[7] = -1
+    elif case == "num_q":
+        args[8] = -1
+    elif case == "blocks":
+        args[2] = -1
+    elif case == "null_q":
+        args[0] = None
+    elif case == "mis_cache":
+        args[1] = ctypes.c_void_p(264)
+    elif case == "mis_seq":
+        args[5] = ctypes.c_void_p(258)
+    elif case == "rows":
+        args[8] = 48 * 1024 + 1
+    ws = ctypes.c_void_p(4096)
+    want = lib.mla_decode_paged(cfgp, *args, ws, 1 << 30, None)
+    assert want != 0
+    got = lib.mla_decode_paged_noalloc(cfgp, *args, p, None, None)
+    assert got == want, (case, got, want)
+
+
+def test_noalloc_with_no_rows_is_a_noop(lib):
+    cfg = L.make_config(16, 64, "bf16")
+    assert lib.mla_decode_paged_noalloc(ctypes.byref(cfg), None, None, 0, None, 0, None, None, 0, 0,
+                                        None, None, None) == 0

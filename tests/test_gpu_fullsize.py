@@ -1,13 +1,14 @@
 """Full-size workloads, in the launch configuration the bench times (one CTA
-per SM), checked against the naive fp64 oracle on sampled sequences and
-heads (the oracle expands K and V per head, so every row of every head would
-take minutes)."""
+per SM), checked against the fp64 oracle: the naive form (K and V expanded per
+head) on sampled sequences and heads, and the absorbed form (held equal to the
+naive one to 1e-12 by the oracle's own tests) on every head of at least 8
+sequences per workload, always including the shortest and the longest."""
 
 import numpy as np
 import pytest
 import torch
 
-from _helpers import assert_close, ref_out, to_f64
+from _helpers import assert_close, ref_out, ref_out_absorbed, to_f64
 from mla_latent_kv_03_gb300 import libmla as L
 from mla_latent_kv_03_gb300 import workloads as W
 from mla_latent_kv_03_gb300.step import MlaDecodeStep
@@ -212,3 +213,67 @@ def test_serving_layer_bench_step_graphed():
                                 w.W_uv, li.W_o, w.rms_weight, w.rms_eps, w.rope_base,
                                 w.softmax_scale, num_new=1)
         assert_close(to_f64(s.y)[qr], ref, "bf16", f"layer serving seq {b}")
+
+
+# ---------------------------------------------------------------------------
+# every head of many sequences, through the oracle's absorbed form, on the
+# step as the bench times it (graphed, fused merges)
+# ---------------------------------------------------------------------------
+
+def _check_all_heads(w, s, seqs, what, rows_of=None):
+    ref = ref_out_absorbed(w, seqs, rows_of)
+    m = ~np.isnan(ref[:, 0, 0])
+    assert m.sum() > 0
+    return assert_close(to_f64(s.out)[m], ref[m], w.dtype, what)
+
+
+def test_serving_16_sequences_every_head():
+    w = W.serving()
+    s = MlaDecodeStep(w, device=DEV)
+    s.populate()
+    _run_graphed(w, s)
+    assert s.device_status()[0][0] == 0
+    seqs = sorted({int(x) for x in np.linspace(0, w.batch - 1, 16)})
+    assert len(seqs) == 16
+    _check_all_heads(w, s, seqs, "serving, 16 sequences x 16 heads")
+
+
+def test_ragged_H128_8_sequences_every_head():
+    w = W.ragged_h128()
+    s = MlaDecodeStep(w, device=DEV)
+    s.populate()
+    _run_graphed(w, s)
+    assert s.device_status()[0][0] == 0
+    lens = np.asarray(w.seq_lens)
+    order = np.argsort(lens)
+    pick = {int(order[0]), int(order[-1])}
+    pick |= {int(order[k]) for k in np.linspace(1, len(order) - 2, 6).astype(int)}
+    seqs = sorted(pick)
+    assert len(seqs) >= 8
+    _check_all_heads(w, s, seqs, "ragged H=128, 8 sequences x 128 heads")
+
+
+def test_mixed_every_prefill_sequence_and_8_decode_sequences_every_head():
+    w = W.mixed()
+    s = MlaDecodeStep(w, device=DEV)
+    s.populate(include_new=False)
+    _run_graphed(w, s)
+    (st1, _), (st2, _) = s.device_status()
+    assert st1 == 0 and st2 == 0
+    ql = np.diff(np.asarray(w.query_start_loc))
+    prefill = [b for b in range(w.batch) if ql[b] > 1]
+    decode = [b for b in range(w.batch) if ql[b] == 1]
+    assert len(prefill) == 4
+    dec = [decode[int(k)] for k in np.linspace(0, len(decode) - 1, 8).astype(int)]
+    # 64 of each prefill chunk's 512 query rows (the first and the last among
+    # them), every decode row
+    rng = np.random.default_rng(9)
+
+    def rows_of(b):
+        n = int(ql[b])
+        if n == 1:
+            return [0]
+        return sorted({0, n - 1} | set(rng.choice(n, 62, replace=False).tolist()))
+
+    _check_all_heads(w, s, prefill + dec, "mixed: 4 prefill + 8 decode sequences x 16 heads",
+                     rows_of)

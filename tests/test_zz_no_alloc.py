@@ -92,3 +92,47 @@ def test_noalloc_refuses_a_workspace_beyond_the_scratch():
     assert _noalloc(lib, s, o, status) == 3     # MLA_ERR_WORKSPACE_TOO_SMALL, nothing enqueued
     torch.cuda.synchronize()
     assert torch.count_nonzero(o) == 0
+
+
+def test_noalloc_refuses_a_fixed_cta_count_that_does_not_fit():
+    """With the caller's own CTA count the call does not shrink it: a count
+    whose workspace exceeds the scratch is refused and o_lat is untouched."""
+    lib = L.load()
+    w = W.make("na_fixed", [300, 65, 1], [1, 1, 1], 16, 64, "bf16", seed=54)
+    s = MlaDecodeStep(w, device=DEV)
+    s.populate()
+    s.absorb()
+    s.cfg.num_ctas = 1000          # 1,000 split slots of 32 KB: beyond 16 MiB
+    assert L.mla_decode_workspace_size(s.cfg, w.num_q, w.batch) > SCRATCH
+    o = torch.full_like(s.o_lat, 7.0)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    assert _noalloc(lib, s, o, status) == 3
+    torch.cuda.synchronize()
+    assert bool(torch.all(o == 7.0))
+    assert int(status.item()) == 0
+
+
+def test_noalloc_reports_a_bad_block_through_dev_status():
+    """A block-table entry beyond the pool is skipped and its bit
+    (MLA_DEV_BAD_BLOCK) reaches the caller's status word; the rows of the other
+    sequences still match the workspace path."""
+    lib = L.load()
+    w = W.make("na_badblk", [130, 200], [1, 1], 16, 64, "bf16", seed=55)
+    s = MlaDecodeStep(w, device=DEV)
+    s.populate()
+    s.absorb()
+    s.decode()
+    s.combine()
+    torch.cuda.synchronize()
+    ref = s.o_lat.clone()
+    bt = s.block_table.clone()
+    s.block_table[0, 1] = s.cache.shape[0] + 5      # sequence 0's second page: out of range
+    o = torch.full_like(s.o_lat, float("nan"))
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    assert _noalloc(lib, s, o, status) == 0
+    torch.cuda.synchronize()
+    s.block_table.copy_(bt)
+    assert int(status.item()) & 2 == 2                # MLA_DEV_BAD_BLOCK
+    q1 = slice(int(w.query_start_loc[1]), int(w.query_start_loc[2]))
+    np.testing.assert_allclose(o[q1].cpu().numpy(), ref[q1].cpu().numpy(), rtol=0, atol=1e-5)
+    assert bool(torch.isfinite(o).all())
