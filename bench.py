@@ -62,9 +62,9 @@ PROFILES = {
         ["decode_tc.cu", "common.cuh", "cluster.cuh", "tcgen05.cuh", "merge.cuh", "async_copy.cuh"]),
     ("expand_tc_kernel", "serving"): (
         "expand_tc_serving_B64_L4096.md", ["naive.cu", "common.cuh", "tcgen05.cuh", "async_copy.cuh"]),
-    ("naive_prefill_kernel", "mixed"): (
-        "naive_prefill_mixed_P4_D60.md",
-        ["prefill.cu", "common.cuh", "async_copy.cuh", "rope_pairs.cuh"]),
+    ("naive_prefill_tc_kernel", "mixed"): (
+        "naive_prefill_tc_mixed_P4_D60.md",
+        ["prefill.cu", "common.cuh", "async_copy.cuh", "rope_pairs.cuh", "tcgen05.cuh"]),
     ("naive_decode_kernel", "serving"): (
         "naive_decode_serving_B64_L4096.md", ["naive.cu", "common.cuh", "tcgen05.cuh", "async_copy.cuh"]),
 }
@@ -649,7 +649,7 @@ def run_ours(args, world, rank, local):
     attn_flops = int(w.num_heads) * pairs * (576 + 512) * 2
     tpeak, _ = tensor_peak()
     if (form == "full_kv" and mixed) or form == "hybrid":
-        kernel = "naive_prefill_kernel"
+        kernel = "naive_prefill_tc_kernel"
         # (row, head) x visible token pairs, a 192-wide score and a 128-wide
         # accumulation each (hybrid: the prefill rows only)
         kpairs = pairs if form == "full_kv" else int(

@@ -132,7 +132,8 @@ template <int NST, bool SELF, bool FP8>
 __global__ void __maxnreg__(168)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap cache_map,
                        const __grid_constant__ CUtensorMap q_map,
-                       const __grid_constant__ CUtensorMap rope_map, DecodeArgs a) {
+                       const __grid_constant__ CUtensorMap rope_map,
+                       const __grid_constant__ CUtensorMap slab_map, DecodeArgs a) {
   using S = Smem<NST, SELF, FP8>;
   constexpr int QB = S::qbufs;
   extern __shared__ uint8_t smem_raw[];
@@ -166,6 +167,7 @@ __global__ void __maxnreg__(168)
     prefetch_tensormap(&cache_map);
     prefetch_tensormap(&q_map);
     if (FP8) prefetch_tensormap(&rope_map);
+    if (!FP8 && a.block_size == kTile) prefetch_tensormap(&slab_map);
   }
   __syncthreads();
   // early: only the cache stream may start before the preceding kernel ends
@@ -335,6 +337,9 @@ __global__ void __maxnreg__(168)
                                    blk[i] << bs_shift, &full[st], policy);
                 tma_load_2d_hint(dst + kCodesBytes + (i << bs_shift) * 128, &rope_map, 256,
                                  blk[i] << bs_shift, &full[st], policy);
+              } else if (ppt == 1) {
+                // a 64-token page: its nine 64-column slabs in one copy (3-D view)
+                tma_load_3d_hint(dst, &slab_map, 0, blk[i] << bs_shift, 0, &full[st], policy);
               } else {
 #pragma unroll 1
                 for (int j = 0; j < 9; ++j)
@@ -783,7 +788,7 @@ __global__ void __maxnreg__(168)
 
 cudaError_t launch_decode_bf16(const DecodeArgs& a, const CUtensorMap& cache_map,
                                const CUtensorMap& q_map, const CUtensorMap* rope_map,
-                               cudaStream_t stream) {
+                               const CUtensorMap* slab_map, cudaStream_t stream) {
   constexpr int NST = 2;
   // the maximum shared-memory carveout keeps an SM ready for a decode CTA
   // while small kernels before and after it share the SM
@@ -794,7 +799,7 @@ cudaError_t launch_decode_bf16(const DecodeArgs& a, const CUtensorMap& cache_map
                                cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     return launch_pdl(kernel, dim3(a.num_ctas), dim3(kThreads), smem, stream, cache_map, q_map,
-                      rope_map ? *rope_map : cache_map, a);
+                      rope_map ? *rope_map : cache_map, slab_map ? *slab_map : cache_map, a);
   };
   if (rope_map) {
     // the FP8 cache: self-planned launches only; 40 KB stages and one query

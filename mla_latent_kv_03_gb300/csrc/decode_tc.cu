@@ -270,7 +270,9 @@ __device__ __forceinline__ void load_q_cta(int h, const uint16_t* q_abs, int64_t
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    decode_tc_kernel(const __grid_constant__ CUtensorMap cache_map, DecodeArgs a, int batch) {
+    decode_tc_kernel(const __grid_constant__ CUtensorMap cache_map,
+                     const __grid_constant__ CUtensorMap slab4,
+                     const __grid_constant__ CUtensorMap slab5, DecodeArgs a, int batch) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -305,7 +307,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 1) tc::alloc(tmem_slot, kTmemCols);
-  if (warp == 0 && lane == 0) prefetch_tensormap(&cache_map);
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&cache_map);
+    prefetch_tensormap(h ? &slab5 : &slab4);
+  }
   tc::fence_before_sync();
   cl::sync();  // both CTAs' barriers exist before either copies into the other
   tc::fence_after_sync();
@@ -374,15 +379,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           info[slot] = make_int2(v, okmask);
           mbar_arrive_expect_tx(&bars[kFull0 + slot], (uint32_t)(nload * nslab * bsr * 128));
           uint8_t* dst = sStage + slot * kStage;
+          if (ppst == 1) {
+            // one copy: this CTA's column slabs of the 32-row box (3-D view)
+            if (okmask & 1)
+              tma_load_3d_hint(dst, h ? &slab5 : &slab4, 0, blk[0] * bs + (tstart % bs), slab0,
+                               &bars[kFull0 + slot], policy);
+          } else {
 #pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            if (okmask & (1 << i)) {
-              const int tok = tstart + (i << bsr_shift);
-              const int y = blk[i] * bs + (tok % bs);
+            for (int i = 0; i < 2; ++i) {
+              if (okmask & (1 << i)) {
+                const int tok = tstart + (i << bsr_shift);
+                const int y = blk[i] * bs + (tok % bs);
 #pragma unroll 1
-              for (int j = 0; j < nslab; ++j)
-                tma_load_2d_hint(dst + j * kSlab + (i << bsr_shift) * 128, &cache_map,
-                                 64 * (slab0 + j), y, &bars[kFull0 + slot], policy);
+                for (int j = 0; j < nslab; ++j)
+                  tma_load_2d_hint(dst + j * kSlab + (i << bsr_shift) * 128, &cache_map,
+                                   64 * (slab0 + j), y, &bars[kFull0 + slot], policy);
+              }
             }
           }
         }
@@ -885,13 +897,14 @@ int decode_tc_max_clusters() {
 }
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, int32_t batch, const CUtensorMap& cache_map,
+                             const CUtensorMap& slab4, const CUtensorMap& slab5,
                              cudaStream_t stream) {
   const int smem = Smem::alloc;
   cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(decode_tc_kernel, dim3(a.num_ctas), dim3(kThreads), smem, stream, cache_map, a,
-                    (int)batch);
+  return launch_pdl(decode_tc_kernel, dim3(a.num_ctas), dim3(kThreads), smem, stream, cache_map,
+                    slab4, slab5, a, (int)batch);
 }
 
 }  // namespace mla

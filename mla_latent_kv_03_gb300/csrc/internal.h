@@ -67,15 +67,21 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream);
 cudaError_t launch_plan_tc(const PlanArgs& a, cudaStream_t stream);
 
 // rope_map non-null: the FP8 cache (cache_map views its rows as 640 bytes,
-// rope_map as 320 bf16), self-planned launches only.
+// rope_map as 320 bf16), self-planned launches only. slab_map (bf16 cache
+// with 64-token pages): the 3-D view of make_slab_map with boxes of
+// (64, 64 rows, 9 slabs), one copy per page; it must be given for that case.
 cudaError_t launch_decode_bf16(const DecodeArgs& a, const CUtensorMap& cache_map,
                                const CUtensorMap& q_map, const CUtensorMap* rope_map,
-                               cudaStream_t stream);
+                               const CUtensorMap* slab_map, cudaStream_t stream);
 
 cudaError_t launch_decode_f32(const DecodeArgs& a, cudaStream_t stream);
 
-// Tensor-core decode (CTA pairs as clusters); num_ctas must be even.
+// Tensor-core decode (CTA pairs as clusters); num_ctas must be even. With
+// 32-row boxes, slab4 / slab5 are 3-D views of the cache (make_slab_map in
+// libmla.cu) whose boxes hold 4 / 5 column slabs of 32 rows: one copy per
+// stage and CTA.
 cudaError_t launch_decode_tc(const DecodeArgs& a, int32_t batch, const CUtensorMap& cache_map,
+                             const CUtensorMap& slab4, const CUtensorMap& slab5,
                              cudaStream_t stream);
 
 // CTA pairs of the tensor-core decode that fit on the current device at once
@@ -125,5 +131,9 @@ bool encode_map_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t r
 // (box_d, 1, box_rows), 128-byte swizzle.
 bool encode_map_heads(CUtensorMap* map, const void* base, uint64_t dims, uint64_t heads,
                       uint64_t rows, uint32_t box_d, uint32_t box_rows);
+// 4-D view of the same tensor whose box (64, box_rows, dims / 64, 1) holds
+// all dims / 64 column slabs of box_rows rows of one head, block-major.
+bool encode_map_heads_slabs(CUtensorMap* map, const void* base, uint64_t dims, uint64_t heads,
+                            uint64_t rows, uint32_t box_rows);
 
 }  // namespace mla

@@ -111,6 +111,26 @@ bool make_row_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t bo
   return r == CUDA_SUCCESS;
 }
 
+// 3-D bf16 view of rows of 576 values as (64 values, row, 64-value column
+// block): the row stride (1,152 bytes) is the middle dimension and the column
+// block (128 bytes) the outer one, so a box of (64, box_rows, nslab) lands in
+// shared memory block-major -- nslab slabs of box_rows x 128 bytes, each laid
+// out as one 2-D box of make_row_map would be -- in a single copy.
+bool make_slab_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows,
+                   uint32_t nslab) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(kRow / 64)};
+  const cuuint64_t strides[2] = {(cuuint64_t)kRow * 2, 128};
+  const cuuint32_t box[3] = {64, box_rows, nslab};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 2-D bf16 map over a row-major [rows, cols] matrix: box = box_cols x
 // box_rows, 128-byte swizzle.
 bool make_map_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
@@ -169,6 +189,25 @@ bool make_map_heads(CUtensorMap* map, const void* base, uint64_t dims, uint64_t 
   return r == CUDA_SUCCESS;
 }
 
+// 4-D bf16 view of a [rows, heads, dims] tensor (dims a multiple of 64) as
+// (64 values, row, 64-value column block, head): a box of (64, box_rows,
+// dims / 64, 1) lands block-major -- dims / 64 slabs of box_rows x 128 bytes of
+// one head -- in a single copy. 128-byte swizzle.
+bool make_map_heads_slabs(CUtensorMap* map, const void* base, uint64_t dims, uint64_t heads,
+                          uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t gdim[4] = {64, (cuuint64_t)rows, (cuuint64_t)(dims / 64), (cuuint64_t)heads};
+  const cuuint64_t strides[3] = {(cuuint64_t)dims * heads * 2, 128, (cuuint64_t)dims * 2};
+  const cuuint32_t box[4] = {64, box_rows, (cuuint32_t)(dims / 64), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), gdim,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Rows from which the projections run on tcgen05 (below, the latency-bound
 // warp-mma kernels are faster).
 constexpr int64_t kTcProjRows = 256;
@@ -208,6 +247,10 @@ bool encode_map_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t r
 bool encode_map_heads(CUtensorMap* map, const void* base, uint64_t dims, uint64_t heads,
                       uint64_t rows, uint32_t box_d, uint32_t box_rows) {
   return make_map_heads(map, base, dims, heads, rows, box_d, box_rows);
+}
+bool encode_map_heads_slabs(CUtensorMap* map, const void* base, uint64_t dims, uint64_t heads,
+                            uint64_t rows, uint32_t box_rows) {
+  return make_map_heads_slabs(map, base, dims, heads, rows, box_rows);
 }
 }  // namespace mla
 
@@ -382,12 +425,20 @@ mla_status decode_impl(const mla_config* cfg, const void* q_abs, const void* cac
     // boxes: 32-token half pages (or whole pages below 32 tokens)
     const uint32_t box_rows = cfg->block_size < 32 ? (uint32_t)cfg->block_size : 32u;
     if (!make_row_map(&cache_map, cache, map_rows, box_rows)) return MLA_ERR_CUDA;
-    return from_cuda(launch_decode_tc(da, batch, cache_map, st));
+    // with 32-token boxes, one copy per stage moves a CTA's 4 or 5 column slabs
+    CUtensorMap slab4 = cache_map, slab5 = cache_map;
+    if (box_rows == 32 && (!make_slab_map(&slab4, cache, map_rows, 32, 4) ||
+                           !make_slab_map(&slab5, cache, map_rows, 32, 5)))
+      return MLA_ERR_CUDA;
+    return from_cuda(launch_decode_tc(da, batch, cache_map, slab4, slab5, st));
   }
   if (!make_row_map(&cache_map, cache, map_rows, (uint32_t)cfg->block_size) ||
       !make_row_map(&q_map, q_abs, (uint64_t)num_q * cfg->num_heads, kHG))
     return MLA_ERR_CUDA;
-  return from_cuda(launch_decode_bf16(da, cache_map, q_map, nullptr, st));
+  CUtensorMap slab9 = cache_map;
+  if (cfg->block_size == kTile && !make_slab_map(&slab9, cache, map_rows, kTile, kRow / 64))
+    return MLA_ERR_CUDA;
+  return from_cuda(launch_decode_bf16(da, cache_map, q_map, nullptr, &slab9, st));
 }
 
 }  // namespace
@@ -549,7 +600,7 @@ mla_status mla_decode_paged_combine_fp8(const mla_config* cfg, const void* q_abs
       !make_row_map(&q_map, q_abs, (uint64_t)num_q * cfg->num_heads, kHG))
     return MLA_ERR_CUDA;
   cudaStream_t st = as_stream(stream);
-  s = from_cuda(launch_decode_bf16(da, codes_map, q_map, &rope_map, st));
+  s = from_cuda(launch_decode_bf16(da, codes_map, q_map, &rope_map, nullptr, st));
   if (s != MLA_OK || !split_heavy) return s;
   return from_cuda(launch_combine(workspace, G, C, num_q, batch, o_lat, st));
 }

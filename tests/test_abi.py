@@ -180,8 +180,8 @@ def test_naive_prefill_checks_its_arguments_on_the_host(lib):
     # no rows: nothing to do, nothing touched
     assert fn(ctypes.byref(bf16), None, None, None, None, 16, None, 4, None, None, 4, 0, ws, 256,
               None, None) == 0
-    # more query tiles than one launch holds
-    assert fn(ctypes.byref(bf16), p, p, p, p, 16, p, 4, p, p, 4, 64 * 70000, ws, 256, p,
+    # more query rows than the kernel indexes
+    assert fn(ctypes.byref(bf16), p, p, p, p, 16, p, 4, p, p, 4, 1 << 31, ws, 256, p,
               None) == 2
 
 
