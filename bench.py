@@ -389,10 +389,12 @@ HIDDEN_SIZE = 2048   # DeepSeek-V2-Lite's hidden size, for --form layer
 
 
 def proj_launches(M, N, K, sms):
-    """Kernels of one projection call: the tile kernel, plus the sum of the
-    K splits when the library splits K (fewer than two tiles per SM; the
-    split doubles while that holds, it divides the 64-wide K steps and it is
-    below 8)."""
+    """Kernels of one projection call: from 256 rows one tensor-core kernel;
+    below, the tile kernel plus the sum of the K splits when the library
+    splits K (fewer than two tiles per SM; the split doubles while that
+    holds, it divides the 64-wide K steps and it is below 8)."""
+    if M >= 256 and N % 64 == 0:
+        return 1
     tiles = ((M + 63) // 64) * (N // 64)
     s = 1
     while tiles * s < 2 * sms and (K // 64) % (2 * s) == 0 and s < 8:
@@ -443,9 +445,10 @@ def run_ours(args, world, rank, local):
     form = args.form
     if form == "hybrid" and not mixed:
         raise SystemExit("--form hybrid: prefill + decode workloads only")
-    if form not in ("absorbed", "hybrid") and (w.dtype != "bf16" or (mixed and form != "full_kv")):
+    if form not in ("absorbed", "hybrid") and (
+            w.dtype != "bf16" or (mixed and form not in ("full_kv", "layer"))):
         raise SystemExit("--form full_kv / latent / fp8 / layer: bf16 decode workloads only "
-                         "(full_kv also takes prefill chunks)")
+                         "(full_kv and layer also take prefill chunks)")
     s = MlaDecodeStep(w, device=dev)
     s.populate(include_new=not mixed)
     if form in ("full_kv", "latent"):
@@ -714,6 +717,34 @@ def run_ours(args, world, rank, local):
     e2e = run_e2e(args, s, w, stream, latent, world, mixed, one_step,
                   s.y if form == "layer" else
                   s.out if form in ("absorbed", "fp8") else s.out_naive)
+
+    # ---- the layer's three projections alone (graph of 20 steps' worth)
+    if form == "layer":
+        def projs():
+            L.mla_q_proj(s.cfg, s.hidden_new, s.W_q, s.q_nope, s.q_pe, s.proj_ws)
+            L.mla_kv_a_proj(s.cfg, s.hidden_new, s.W_kv_a, s.c_kv_new, s.k_pe_new, s.proj_ws)
+            L.mla_o_proj(s.cfg, s.out, s.W_o, s.y, s.proj_ws)
+        pg = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            projs()
+        stream.synchronize()
+        with torch.cuda.graph(pg, stream=stream):
+            for _ in range(20):
+                projs()
+        with torch.cuda.stream(stream):
+            pg.replay()
+            k0.record(stream)
+            for _ in range(10):
+                pg.replay()
+            k1.record(stream)
+        k1.synchronize()
+        proj_ms = k0.elapsed_time(k1) / 200
+        T, H = int(w.num_q), int(w.num_heads)
+        pflops = 2 * T * HIDDEN_SIZE * (H * 192 + 576 + H * 128)
+        roofline["projections"] = {
+            "us": round(proj_ms * 1e3, 2), "tflops": round(pflops / (proj_ms * 1e-3) / 1e12, 1),
+            "frac": round(pflops / (proj_ms * 1e-3) / 1e12 / tpeak, 4), "flops": pflops,
+            "what": "q_proj + kv_a_proj + o_proj of the step's tokens, back to back"}
 
     # ---- status: the timed work must not have flagged anything
     (st1, bits1), (st2, bits2) = s.device_status()

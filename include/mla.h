@@ -457,9 +457,12 @@ mla_status mla_combine_out_proj(const mla_config* cfg, const void* workspace, si
  * workspace: mla_proj_workspace_size(cfg, num_tokens, hidden_size) bytes,
  * 256-byte aligned; its first 4 bytes are a device status word (zero it with
  * mla_workspace_init once; a wait that ran out sets MLA_DEV_TIMEOUT, read it
- * with mla_get_device_status); the rest holds fp32 partial sums when K is
- * split across CTAs (few tokens). Results do not depend on the split beyond
- * fp32 rounding order, and repeated calls agree bit for bit. The weight may be
+ * with mla_get_device_status). Below 256 tokens K is split across CTAs and the
+ * rest of the workspace holds their fp32 partial sums, which a second kernel
+ * adds in split order; from 256 tokens one tcgen05 kernel computes each tile
+ * without splitting. Results do not depend on the split beyond fp32 rounding
+ * order, and repeated calls agree bit for bit. Calls that share a workspace
+ * must not overlap on the GPU. The weight may be
  * read before the kernel launched just before the call on the same stream has
  * finished, so that kernel must not write it.
  */

@@ -15,14 +15,15 @@
 //                                           peer's shared memory ahead of use)
 //   O_h += P . V[:, 256h : 256h + 256]    (each CTA half of the output)
 // so each CTA streams only its own columns of every cache row, and both CTAs
-// run the same softmax on the same sums (S_0 + S_1 == S_1 + S_0 in fp32),
+// run the same softmax on the same sums (each partial is rounded to f16 with
+// saturation before the exchange, and S_0 + S_1 == S_1 + S_0 in fp32),
 // giving identical probabilities and log-sum-exps.
 //
 // TMEM (512 columns): O half [0, 256), two score buffers [256, 320), two
 // probability buffers [320, 352) (bf16 pairs), this CTA's query columns
 // [352, 512) (bf16 pairs, the A operand of the score MMAs). Shared memory: a
-// ring of five 32-token cache stages of this CTA's columns (SWIZZLE_128B slabs
-// of 64 columns), four buffers of the peer's partial scores, three of this
+// ring of seven 32-token cache stages of this CTA's columns (SWIZZLE_128B slabs
+// of 64 columns), four buffers of the peer's partial scores, four of this
 // CTA's own (the source of the bulk copies to the peer), and merge weights.
 // Per CTA (384 threads):
 //   warp 0 (TMA producer): cache stages under full / empty mbarriers; every
@@ -71,7 +72,7 @@ constexpr int kSendWarp0 = 8;                  // warps 8-11: partial-score send
 constexpr int kSoftBar = 2;                    // named barrier of the softmax warps
 constexpr uint32_t kOCol = 0, kSCol = 256, kPCol = 320, kQCol = 352, kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.f;            // lazy rescale threshold (2^8)
-constexpr int kXRow = kTok * 2;                // one row of a stage's partial scores (bf16)
+constexpr int kXRow = kTok * 2;                // one row of a stage's partial scores (f16)
 constexpr int kXBytes = kQBlockRows * kXRow;   // one stage of partial scores
 constexpr int kXWarpBytes = kXBytes / 4;       // the 32 rows of one sender warp
 constexpr int kMergeSlots = 16;                // parts merged by the one-pass merge
@@ -158,6 +159,24 @@ struct TcWalker {
     return true;
   }
 };
+
+// Two scores (low, high) rounded to f16, saturating at +-65,504 (never inf).
+__device__ __forceinline__ uint32_t pack_f16_sat(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// The fp32 sums of the low and of the high halves of two f16 pairs (each sum
+// exact up to one fp32 rounding, and the same whichever pair comes first).
+__device__ __forceinline__ void add_f16x2_f32(uint32_t a, uint32_t c, float& lo, float& hi) {
+  asm("{\n\t.reg .b16 al, ah, cl, ch;\n\t.reg .f32 t0, t1;\n\t"
+      "mov.b32 {al, ah}, %2;\n\tmov.b32 {cl, ch}, %3;\n\t"
+      "cvt.f32.f16 t0, cl;\n\tcvt.f32.f16 t1, ch;\n\t"
+      "add.rn.f32.f16 %0, al, t0;\n\tadd.rn.f32.f16 %1, ah, t1;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(a), "r"(c));
+}
 
 // bounded wait that also gives up when another role has aborted
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
@@ -507,7 +526,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (has_work && warp >= kSendWarp0) {
     // ------------------------------------------------------------ senders
-    // Partial scores of every stage, in order: TMEM -> bf16 -> own staging
+    // Partial scores of every stage, in order: TMEM -> f16 -> own staging
     // buffer j % kXSend, which this CTA's softmax reads, and from which each
     // warp's bulk copy moves its 32 rows into the peer's buffer j % kXRecv,
     // counted on the peer's barrier. The score buffer is free as soon as the
@@ -539,7 +558,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_arrive(&bars[kSFree0 + b]);   // S[j % 2] may take stage j + 2's scores
         uint32_t pk[16];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) pk[k] = pack_bf16(__uint_as_float(sv[2 * k]), __uint_as_float(sv[2 * k + 1]));
+        for (int k = 0; k < 16; ++k) pk[k] = pack_f16_sat(__uint_as_float(sv[2 * k]), __uint_as_float(sv[2 * k + 1]));
         // staging buffer xs: this CTA's softmax has read stage j - kXSend from
         // it, and this warp's copy of that stage has read its rows
         const bool okf = j < kXSend ||
@@ -637,8 +656,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // live tokens: a prefix (sequence end, causal position) minus rejected blocks
         const int lim = min(v, pos - tstart + 1);
         // S = own partial + the peer's partial, both as the senders rounded
-        // them to bf16 (so both CTAs add the same two values), read from the
-        // staging and receive buffers (16-byte chunks swizzled by the row)
+        // them to f16 (so both CTAs add the same two values, in fp32), read
+        // from the staging and receive buffers (16-byte chunks swizzled by
+        // the row)
         float x[32];
         {
           const int sw4 = (r >> 1) & 3;
@@ -650,10 +670,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             pv[k] = *reinterpret_cast<const uint4*>(xp + ((k ^ sw4) << 4));
             ov[k] = *reinterpret_cast<const uint4*>(op + ((k ^ sw4) << 4));
           }
-          auto add2 = [&](int j, uint32_t a, uint32_t c) {
-            x[j] = __uint_as_float(a << 16) + __uint_as_float(c << 16);
-            x[j + 1] = __uint_as_float(a & 0xffff0000u) + __uint_as_float(c & 0xffff0000u);
-          };
+          auto add2 = [&](int j, uint32_t a, uint32_t c) { add_f16x2_f32(a, c, x[j], x[j + 1]); };
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             add2(8 * k, ov[k].x, pv[k].x);

@@ -24,6 +24,7 @@
 #include "async_copy.cuh"
 #include "common.cuh"
 #include "internal.h"
+#include "tcgen05.cuh"
 
 namespace mla {
 namespace {
@@ -202,12 +203,184 @@ __global__ void __launch_bounds__(256) linear_reduce_kernel(LinArgs a, int split
   }
 }
 
+// ---------------------------------------------------------------------------
+// Many rows (prefill chunks): the same Y = X W^T on tcgen05. A CTA owns a
+// 128 x NT tile of Y (NT = 256, or 192 / 128 / 64 when that does not divide
+// N) and the whole of K. Thread 0 streams 64-wide K steps of X (128 rows) and
+// W (NT rows) by TMA (SWIZZLE_128B) through a 4-stage ring, the weight tiles
+// of the first stages before the preceding kernel has finished; one elected
+// thread of warp 1 issues 4 tcgen05.mma (M 128, N NT, K 16) per step into a
+// TMEM accumulator; then thread r of the four warps reads row r of the tile
+// out of TMEM, rounds it to bf16 and writes it through the column map.
+// ---------------------------------------------------------------------------
+constexpr int kTcRows = 128;
+constexpr int kTcStages = 4;
+constexpr int kTcA = kTcRows * 128;            // 128 rows x 64 bf16: 16 KB
+constexpr int kTcB = 256 * 128;                // up to 256 rows x 64 bf16: 32 KB
+constexpr int kTcThreads = 128;
+
+struct LinTcSmem {
+  static constexpr int a = 0;
+  static constexpr int b = a + kTcStages * kTcA;
+  static constexpr int bars = b + kTcStages * kTcB;   // full[4], empty[4], done
+  static constexpr int misc = bars + (2 * kTcStages + 1) * 8;
+  static constexpr int bytes = misc + 16;
+  static constexpr int alloc = bytes + 1024;
+};
+static_assert(LinTcSmem::alloc <= 227 * 1024, "shared memory budget");
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    linear_tc_kernel(const __grid_constant__ CUtensorMap x_map,
+                     const __grid_constant__ CUtensorMap w_map, LinArgs a, int nt) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + LinTcSmem::bars);
+  uint64_t* empty = full + kTcStages;
+  uint64_t* done = empty + kTcStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + LinTcSmem::misc);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n0 = blockIdx.x * nt;
+  const int64_t m0 = (int64_t)blockIdx.y * kTcRows;
+  const int nk = a.K / kLB;
+  const uint32_t stage_tx = (uint32_t)(kTcA + nt * 128);
+
+  if (tid == 0) {
+    for (int i = 0; i < kTcStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(done, 1);
+    fence_mbar_init();
+    prefetch_tensormap(&x_map);
+    prefetch_tensormap(&w_map);
+  }
+  if (warp == 1) tc::alloc(tmem_slot, 256);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  bool ok = true;
+  int issued = 0;
+  if (tid == 0) {
+    // the weight needs no earlier kernel: its first tiles go out at once
+    const int pre = nk < kTcStages ? nk : kTcStages;
+    for (int kt = 0; kt < pre; ++kt) {
+      mbar_arrive_expect_tx(&full[kt], stage_tx);
+      tma_load_2d(sm + LinTcSmem::b + kt * kTcB, &w_map, kt * kLB, n0, &full[kt]);
+    }
+    pdl_wait();
+    for (int kt = 0; kt < pre; ++kt)
+      tma_load_2d(sm + LinTcSmem::a + kt * kTcA, &x_map, kt * kLB, (int)m0, &full[kt]);
+    issued = pre;
+  } else {
+    pdl_wait();
+  }
+  pdl_launch_dependents();
+  if (warp == 0) {
+    // ---- producer: the rest of the K steps, one stage behind the MMAs
+    if (lane == 0) {
+      for (int kt = issued; kt < nk; ++kt) {
+        const int s = kt % kTcStages;
+        if (!mbar_wait(&empty[s], ((kt / kTcStages) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], stage_tx);
+        tma_load_2d(sm + LinTcSmem::b + s * kTcB, &w_map, kt * kLB, n0, &full[s]);
+        tma_load_2d(sm + LinTcSmem::a + s * kTcA, &x_map, kt * kLB, (int)m0, &full[s]);
+        issued = kt + 1;
+      }
+      if (!ok) set_status(a.status, MLA_DEV_TIMEOUT);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---- MMA issuer
+    const uint32_t idesc = tc::idesc_bf16(kTcRows, nt, false, false);
+    const bool leader = tc::elect_one();
+    for (int kt = 0; kt < nk; ++kt) {
+      const int s = kt % kTcStages;
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (kt / kTcStages) & 1))) {
+        ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+      if (leader) {
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t ad = tc::smem_desc(smem_u32(sm + LinTcSmem::a + s * kTcA) + 32 * ks, 16,
+                                            1024, tc::kSwizzle128);
+          const uint64_t bd = tc::smem_desc(smem_u32(sm + LinTcSmem::b + s * kTcB) + 32 * ks, 16,
+                                            1024, tc::kSwizzle128);
+          tc::mma_bf16(tmem, ad, bd, idesc, kt > 0 || ks > 0);
+        }
+        tc::commit(&empty[s]);
+      }
+      __syncwarp();
+    }
+    if (leader) {
+      if (!ok) set_status(a.status, MLA_DEV_TIMEOUT);
+      tc::commit(done);   // every MMA issued (or none) has finished when this lands
+    }
+    __syncwarp();
+  }
+  // ---- epilogue: row r of the tile from TMEM lane r, bf16, through the column map
+  const bool okd = __syncthreads_and(mbar_wait(done, 0) && ok) != 0;
+  if (tid == 0 && issued > 0) {
+    // never leave with copies in flight
+    for (int kt = issued - kTcStages < 0 ? 0 : issued - kTcStages; kt < issued; ++kt)
+      if (!mbar_wait(&full[kt % kTcStages], (kt / kTcStages) & 1)) set_status(a.status, MLA_DEV_TIMEOUT);
+  }
+  tc::fence_after_sync();
+  const int64_t m = m0 + tid;
+  // okd is the same in every thread; the TMEM loads are warp-collective
+  // (.sync.aligned), so every lane takes them and only the stores depend on
+  // the row being one of the M rows
+  if (okd) {
+    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+    const int H = a.N / a.P;
+#pragma unroll 1
+    for (int c = 0; c < nt / 32; ++c) {
+      uint32_t v[32];
+      tc::ld32(trow + 32 * c, v);
+      tc::wait_ld();
+      if (m >= a.M) continue;
+      const int n = n0 + 32 * c, h = n / a.P, d = n - h * a.P;
+      __nv_bfloat16* dst = d < a.Q ? a.y0 + (m * H + h) * a.Q + d
+                                   : a.y1 + (m * H + h) * (a.P - a.Q) + (d - a.Q);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        reinterpret_cast<uint4*>(dst)[q] = make_uint4(
+            pack_bf16(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+            pack_bf16(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+            pack_bf16(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+            pack_bf16(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 1) tc::dealloc(tmem, 256);
+}
+
+// N tile of the tensor-core path: the largest of 256, 192, 128, 64 dividing N.
+int linear_tc_tile(int N) {
+  for (int t : {256, 192, 128, 64})
+    if (N % t == 0) return t;
+  return 0;
+}
+
 int sm_count() {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
   return sms;
 }
+
+// Rows from which the projections run on tcgen05 (below, the split-K warp-mma
+// kernel fills the GPU better).
+constexpr int64_t kLinTcRows = 256;
 
 // Workspace: the status word (bytes 0-3), then the partials.
 constexpr size_t kLPartialOff = 256;
@@ -223,6 +396,7 @@ int linear_splits(int64_t M, int N, int K, int sms) {
 }
 
 size_t linear_ws_bytes(int64_t M, int N, int K, int sms) {
+  if (M >= kLinTcRows && (N % 64) == 0) return kLPartialOff;   // the tensor-core path (no splits)
   const int s = linear_splits(M, N, K, sms);
   return kLPartialOff + (s > 1 ? (size_t)s * (size_t)M * (size_t)N * 4 : 0);
 }
@@ -231,6 +405,34 @@ mla_status run_linear(const void* x, const void* w, int64_t M, int N, int K, int
                       void* y0, void* y1, void* workspace, size_t ws_bytes, void* stream) {
   const int sms = sm_count();
   if (sms <= 0) return MLA_ERR_CUDA;
+  const int nt = linear_tc_tile(N);
+  if (M >= kLinTcRows && nt > 0) {
+    if (ws_bytes < 256) return MLA_ERR_WORKSPACE_TOO_SMALL;
+    CUtensorMap x_map, w_map;
+    if (!encode_map_2d(&x_map, x, (uint64_t)K, (uint64_t)M, kLB, kTcRows) ||
+        !encode_map_2d(&w_map, w, (uint64_t)K, (uint64_t)N, kLB, (uint32_t)nt))
+      return MLA_ERR_CUDA;
+    LinArgs a{};
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.k_split = K;
+    a.P = P;
+    a.Q = Q;
+    a.y0 = reinterpret_cast<__nv_bfloat16*>(y0);
+    a.y1 = reinterpret_cast<__nv_bfloat16*>(y1);
+    a.partial = nullptr;
+    a.status = reinterpret_cast<uint32_t*>(workspace);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaFuncSetAttribute(linear_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         LinTcSmem::alloc);
+    if (e == cudaSuccess)
+      e = launch_pdl(linear_tc_kernel, dim3((unsigned)(N / nt), (unsigned)((M + kTcRows - 1) / kTcRows)),
+                     dim3(kTcThreads), LinTcSmem::alloc, st, x_map, w_map, a, nt);
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+  }
+
   const int splits = linear_splits(M, N, K, sms);
   if (ws_bytes < linear_ws_bytes(M, N, K, sms)) return MLA_ERR_WORKSPACE_TOO_SMALL;
   CUtensorMap x_map, w_map;

@@ -60,7 +60,8 @@ def test_projection_launch_counts_follow_the_split_rule():
     # 64 tokens: too few tiles for 152 SMs, so K splits and a sum kernel follows
     assert bench.proj_launches(64, 16 * 192, 2048, 152) == 2
     assert bench.proj_launches(64, 576, 2048, 152) == 2
-    # thousands of tokens: enough tiles, one kernel
+    # from 256 tokens: one tensor-core kernel, no split
+    assert bench.proj_launches(256, 576, 2048, 152) == 1
     assert bench.proj_launches(4096, 16 * 192, 2048, 152) == 1
 
 

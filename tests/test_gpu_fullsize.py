@@ -277,3 +277,35 @@ def test_mixed_every_prefill_sequence_and_8_decode_sequences_every_head():
 
     _check_all_heads(w, s, prefill + dec, "mixed: 4 prefill + 8 decode sequences x 16 heads",
                      rows_of)
+
+
+def test_mixed_layer_bench_step_graphed():
+    # bench.py --workload mixed --form layer: the projections of the 2,108 new
+    # tokens run on the tensor-core projection kernel (from 256 rows)
+    w = W.mixed()
+    s = MlaDecodeStep(w, device=DEV)
+    s.populate(include_new=False)
+    s.layer_setup(2048)
+    s.layer_populate()
+    s.y.fill_(float("nan"))
+    _graph_replay(s.layer_step)
+    assert s.device_status()[0][0] == 0
+    assert L.mla_get_device_status(s.proj_ws)[0] == 0
+    li = s.layer
+    ql = np.diff(np.asarray(w.query_start_loc))
+    got = to_f64(s.y)
+
+    def ref_rows(b):
+        tr = w.token_range(b)
+        return O.mla_layer_naive(li.hidden[tr], w.kv_positions[tr], li.W_q, li.W_kv_a, w.W_uk,
+                                 w.W_uv, li.W_o, w.rms_weight, w.rms_eps, w.rope_base,
+                                 w.softmax_scale, num_new=int(ql[b]))
+
+    # a prefill chunk (512 rows), then eight decode sequences (one row each)
+    # under one bar, as the other full-size tests sample
+    assert_close(got[w.q_range(0)], ref_rows(0), "bf16", "layer mixed, prefill sequence 0")
+    dec = [10, 17, 24, 31, 38, 45, 52, 63]
+    assert all(ql[b] == 1 for b in dec)
+    rows = [w.q_range(b).start for b in dec]
+    assert_close(got[rows], np.concatenate([ref_rows(b) for b in dec]), "bf16",
+                 "layer mixed, 8 decode sequences")

@@ -74,7 +74,7 @@ def test_q_proj_vs_oracle(T, H):
     _check(to_f64(q_pe), rp, bound[..., 128:], "q_pe")
 
 
-@pytest.mark.parametrize("T", [1, 5, 64, 129, 2108])
+@pytest.mark.parametrize("T", [1, 5, 64, 129, 300, 2108])
 def test_kv_a_proj_vs_oracle(T):
     D = 2048
     rng = np.random.default_rng(200 + T)
@@ -93,7 +93,8 @@ def test_kv_a_proj_vs_oracle(T):
     _check(to_f64(k_pe), rk, bound[:, 512:], "k_pe")
 
 
-@pytest.mark.parametrize("T,H,D", [(1, 16, 2048), (64, 16, 2048), (33, 128, 1024), (700, 16, 512)])
+@pytest.mark.parametrize("T,H,D", [(1, 16, 2048), (64, 16, 2048), (33, 128, 1024), (700, 16, 512),
+                                   (2108, 16, 2048), (257, 32, 1024)])
 def test_o_proj_vs_oracle(T, H, D):
     rng = np.random.default_rng(300 + T + H)
     cfg = L.make_config(H, 64, "bf16")
