@@ -16,7 +16,7 @@
 // bf16 pairs (the A operand of the score MMAs). Per CTA (384 threads):
 //   warp 0 (TMA producer): 64-key stages of the head's rows (per page, 5 boxes
 //     of 64 columns x block_size rows: K_nope, K_nope, k_rot, V, V;
-//     SWIZZLE_128B) through a 4-stage ring; every block id is bounds-checked.
+//     SWIZZLE_128B) through a 5-stage ring; every block id is bounds-checked.
 //   warp 1 (score issuer; owns the TMEM allocation): S[j % 2] = Q K_j^T
 //     (12 tcgen05.mma, M 128, N 64, K 16, A from TMEM) as soon as the stage
 //     has landed and the buffer was read, up to two stages ahead.
@@ -50,7 +50,7 @@ constexpr int kPtKeys = 64;                        // keys per stage
 constexpr int kPtSlab = kPtKeys * 128;             // 64 rows x 64 bf16 = 8 KB
 constexpr int kPtStageSlabs = 5;                   // K_nope x2, k_rot, V x2
 constexpr int kPtStage = kPtStageSlabs * kPtSlab;  // 40 KB
-constexpr int kPtStages = 4;
+constexpr int kPtStages = 5;
 constexpr int kPtThreads = 384;
 constexpr int kPtSoft0 = 4;                        // warps 4-7, 8-11: softmax warpgroups
 constexpr int kPtBarWg0 = 1;                       // named barriers 1, 2: one warpgroup
@@ -60,8 +60,8 @@ constexpr float kPtRescaleLog2 = 8.f;
 constexpr int kNaiveRow = kDn + kDr + kDv;         // 320 values per (slot, head)
 
 enum {
-  kPtFull0 = 0,                    // [4] stage landed (TMA bytes)
-  kPtEmpty0 = kPtFull0 + kPtStages,  // [4] scores and products of the stage done
+  kPtFull0 = 0,                    // [5] stage landed (TMA bytes)
+  kPtEmpty0 = kPtFull0 + kPtStages,  // [5] scores and products of the stage done
   kPtSFull0 = kPtEmpty0 + kPtStages, // [2] S[b] computed
   kPtSFree0 = kPtSFull0 + 2,       // [2] S[b] read by its warpgroup (128 arrivals)
   kPtPFull0 = kPtSFree0 + 2,       // [2] P[b] stored (128 arrivals)
@@ -286,11 +286,15 @@ __global__ void __launch_bounds__(kPtThreads, 1)
       if (j >= 2 && !warp_wait(&bars[kPtSFree0 + sb], ((j - 2) >> 1) & 1)) { ok = false; break; }
       tc::fence_after_sync();
       if (leader) {
+        // descriptors advance by constant steps: 32 bytes (2 units) per K=16
+        // step inside a slab, kPtSlab between slabs
+        const uint64_t kd = kdesc + (uint64_t)((st * kPtStage) >> 4);
+        const uint32_t d = tmem + kTS + 64 * sb;
 #pragma unroll
         for (int kk = 0; kk < 12; ++kk)
-          tc::mma_bf16_tmem_a(tmem + kTS + 64 * sb, tmem + kTQ + 8 * kk,
-                              kdesc + (uint64_t)((st * kPtStage + (kk >> 2) * kPtSlab + (kk & 3) * 32) >> 4),
-                              kIdS, kk > 0);
+          tc::mma_bf16_tmem_a(d, tmem + kTQ + 8 * kk,
+                              kd + (uint64_t)((((kk >> 2) * kPtSlab) >> 4) + 2 * (kk & 3)), kIdS,
+                              kk > 0);
         tc::commit(&bars[kPtSFull0 + sb]);
       }
       __syncwarp();
