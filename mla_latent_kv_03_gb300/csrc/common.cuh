@@ -362,6 +362,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 // 2^x through the PTX approximate base-2 exponential (documented max relative
 // error about 2^-22); 2^-inf = 0.
+// max(a, b, c) in one instruction (the three-input form of max.f32; like
+// fmaxf, a NaN operand is ignored)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

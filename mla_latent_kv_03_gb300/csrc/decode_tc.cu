@@ -686,14 +686,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (!live) x[j] = -INFINITY;
           }
         }
-        float mx[16];
+        // the row maximum in 16 three-input maxima (32 -> 12 -> 4 -> 2 -> 1)
+        float m12[12];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) mx[j] = fmaxf(x[j], x[j + 16]);
-#pragma unroll
-        for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-          for (int j = 0; j < w; ++j) mx[j] = fmaxf(mx[j], mx[j + w]);
-        const float m_cand = mx[0] * scale;   // scale > 0
+        for (int j = 0; j < 10; ++j) m12[j] = fmax3(x[3 * j], x[3 * j + 1], x[3 * j + 2]);
+        m12[10] = x[30];
+        m12[11] = x[31];
+        const float mxr = fmaxf(fmax3(fmax3(m12[0], m12[1], m12[2]), fmax3(m12[3], m12[4], m12[5]), m12[6]),
+                                fmax3(fmax3(m12[7], m12[8], m12[9]), m12[10], m12[11]));
+        const float m_cand = mxr * scale;   // scale > 0
         float alpha = 1.f;
         bool rescale_o = false;
         if (m_cand > m_used + kRescaleLog2 || (m_used == -INFINITY && m_cand != -INFINITY)) {

@@ -456,14 +456,16 @@ __global__ void __launch_bounds__(kPtThreads, 1)
           if (!keep) x[c] = -INFINITY;
         }
       }
-      float mx[16];
+      // the row maximum in 32 three-input maxima (64 -> 22 -> 8 -> 3 -> 1)
+      float m22[22], m8[8];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) mx[c] = fmaxf(fmaxf(x[c], x[c + 16]), fmaxf(x[c + 32], x[c + 48]));
+      for (int c = 0; c < 21; ++c) m22[c] = fmax3(x[3 * c], x[3 * c + 1], x[3 * c + 2]);
+      m22[21] = x[63];
 #pragma unroll
-      for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-        for (int c = 0; c < w; ++c) mx[c] = fmaxf(mx[c], mx[c + w]);
-      const float m_cand = mx[0] * scale;             // scale > 0
+      for (int c = 0; c < 7; ++c) m8[c] = fmax3(m22[3 * c], m22[3 * c + 1], m22[3 * c + 2]);
+      m8[7] = m22[21];
+      const float mxr = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+      const float m_cand = mxr * scale;               // scale > 0
       const float m_prev = j > 0 ? wait_m(j - 1) : -INFINITY;
       if (m_prev != m_prev) fail = true;               // NaN: the wait gave up
       float m_new = m_prev, alpha = 1.f;
@@ -501,10 +503,6 @@ __global__ void __launch_bounds__(kPtThreads, 1)
           fail = true;
         }
       }
-      // P[j % 2] is free once the product of stage j - 2 is done
-      if (j >= 2 &&
-          !__all_sync(0xffffffffu, pt_wait(&bars[kPtPVDone0 + sb], ((j - 2) >> 1) & 1, abort_flag)))
-        fail = true;
       const float mneg = m_new == -INFINITY ? 0.f : -m_new;
       float ps = 0.f;
       {
@@ -516,6 +514,11 @@ __global__ void __launch_bounds__(kPtThreads, 1)
           ps += p0 + p1;
           pk[c] = pack_bf16(p0, p1);
         }
+        // P[j % 2] is free once the product of stage j - 2 is done
+        if (j >= 2 &&
+            !__all_sync(0xffffffffu, pt_wait(&bars[kPtPVDone0 + sb], ((j - 2) >> 1) & 1, abort_flag)))
+          fail = true;
+        tc::fence_after_sync();
         tc::st32(trow + kTP + 32 * sb, pk);
       }
       l += ps;
