@@ -725,21 +725,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
         const float mneg = m_used == -INFINITY ? 0.f : -m_used;
-        float p[32];
+        // exponentials in pairs: the scale on the packed fp32 pipe, the sum as
+        // packed partial sums
+        float2 p[16];
+        const float2 sc2 = make_float2(scale, scale), mn2 = make_float2(mneg, mneg);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) p[j] = fast_exp2(fmaf(x[j], scale, mneg));
+        for (int j = 0; j < 16; ++j) {
+          const float2 e = fma_f32x2(make_float2(x[2 * j], x[2 * j + 1]), sc2, mn2);
+          p[j] = make_float2(fast_exp2(e.x), fast_exp2(e.y));
+        }
         uint32_t pk[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) pk[j] = pack_bf16(p[2 * j], p[2 * j + 1]);
+        for (int j = 0; j < 16; ++j) pk[j] = pack_bf16(p[j].x, p[j].y);
         tc::st16(trow + kPCol + (uint32_t)b * 16, pk);
-        float ps[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) ps[j] = p[j] + p[j + 16];
 #pragma unroll
         for (int w = 8; w >= 1; w >>= 1)
 #pragma unroll
-          for (int j = 0; j < w; ++j) ps[j] += ps[j + w];
-        l += ps[0];
+          for (int j = 0; j < w; ++j) p[j] = add_f32x2(p[j], p[j + w]);
+        l += p[0].x + p[0].y;
         if (v < kTok || okmask != full_mask) {
           // cache rows past the sequence's last token or in a rejected block may
           // hold anything (NaN): zero the latent columns so P = 0 stays 0

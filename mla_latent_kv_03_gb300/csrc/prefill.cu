@@ -507,13 +507,16 @@ __global__ void __launch_bounds__(kPtThreads, 1)
       float ps = 0.f;
       {
         uint32_t pk[32];
+        float2 acc = make_float2(0.f, 0.f);
+        const float2 sc2 = make_float2(scale, scale), mn2 = make_float2(mneg, mneg);
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          const float p0 = fast_exp2(fmaf(x[2 * c], scale, mneg));
-          const float p1 = fast_exp2(fmaf(x[2 * c + 1], scale, mneg));
-          ps += p0 + p1;
-          pk[c] = pack_bf16(p0, p1);
+          const float2 e = fma_f32x2(make_float2(x[2 * c], x[2 * c + 1]), sc2, mn2);
+          const float2 p = make_float2(fast_exp2(e.x), fast_exp2(e.y));
+          acc = add_f32x2(acc, p);
+          pk[c] = pack_bf16(p.x, p.y);
         }
+        ps = acc.x + acc.y;
         // P[j % 2] is free once the product of stage j - 2 is done
         if (j >= 2 &&
             !__all_sync(0xffffffffu, pt_wait(&bars[kPtPVDone0 + sb], ((j - 2) >> 1) & 1, abort_flag)))
