@@ -53,8 +53,7 @@ constexpr int kPtStage = kPtStageSlabs * kPtSlab;  // 40 KB
 constexpr int kPtStages = 5;
 constexpr int kPtThreads = 384;
 constexpr int kPtSoft0 = 4;                        // warps 4-7, 8-11: softmax warpgroups
-constexpr int kPtBarWg0 = 1;                       // named barriers 1, 2: one warpgroup
-constexpr int kPtBarAll = 3;                       // named barrier 3: both warpgroups
+constexpr int kPtBarAll = 3;                       // named barrier 3: both softmax warpgroups
 constexpr uint32_t kTO = 0, kTS = 128, kTP = 256, kTQ = 320, kTCols = 512;
 constexpr float kPtRescaleLog2 = 8.f;
 constexpr int kNaiveRow = kDn + kDr + kDv;         // 320 values per (slot, head)
@@ -422,7 +421,9 @@ __global__ void __launch_bounds__(kPtThreads, 1)
     for (int j = wg; j < nk; j += 2) {
       const int st = j % kPtStages, sb = j & 1;
       const bool okw = pt_wait(&bars[kPtSFull0 + sb], (j >> 1) & 1, abort_flag);
-      if (bar_any(kPtBarWg0 + wg, 128, !okw || fail)) {
+      // a warp that gives up raises the abort flag; the other warps' bounded
+      // waits see it and leave too, and all meet at the barrier after the loop
+      if (__any_sync(0xffffffffu, !okw || fail)) {
         aborted = true;
         *abort_flag = 1;
         break;
