@@ -477,7 +477,8 @@ def run_ours(args, world, rank, local):
             s.hybrid_step(side)
             return
         if form == "layer":
-            s.layer_step()
+            # kv_a_proj and the cache write beside q_proj and the absorption
+            s.layer_step(side=side)
             return
         if form == "fp8":
             s.absorb()

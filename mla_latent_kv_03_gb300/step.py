@@ -179,6 +179,11 @@ class MlaDecodeStep:
             raise L.MlaError(L.MLA_OK + 2, "mla_proj_workspace_size")
         self.proj_ws = torch.empty(need, dtype=torch.uint8, device=dev)
         L.mla_workspace_init(self.proj_ws)
+        # a second projection workspace for kv_a_proj when it runs beside
+        # q_proj (calls that share a workspace must not overlap)
+        self.proj_ws_side = torch.empty(need, dtype=torch.uint8, device=dev)
+        L.mla_workspace_init(self.proj_ws_side)
+        self.ly_fork, self.ly_join = torch.cuda.Event(), torch.cuda.Event()
 
     def layer_populate(self) -> None:
         """kv_a_proj of every token, then the cache write of the old ones."""
@@ -188,15 +193,32 @@ class MlaDecodeStep:
         self.k_pe_new = self.k_pe[new].contiguous()
         self.populate(include_new=False)
 
-    def layer_step(self, stream=None) -> torch.Tensor:
+    def layer_step(self, stream=None, side=None) -> torch.Tensor:
         """One decode step of the whole layer: q_proj and kv_a_proj of the new
-        tokens, their cache write, absorb, decode + merge, out_proj, o_proj."""
-        L.mla_q_proj(self.cfg, self.hidden_new, self.W_q, self.q_nope, self.q_pe, self.proj_ws,
-                     stream=stream)
-        L.mla_kv_a_proj(self.cfg, self.hidden_new, self.W_kv_a, self.c_kv_new, self.k_pe_new,
-                        self.proj_ws, stream=stream)
-        self.write_new(stream=stream)
-        self.absorb(stream=stream)
+        tokens, their cache write, absorb, decode + merge, out_proj, o_proj.
+        With a `side` stream, kv_a_proj and the cache write run there,
+        concurrently with q_proj and the absorption on the current stream,
+        and the decode waits for both."""
+        if side is None:
+            L.mla_q_proj(self.cfg, self.hidden_new, self.W_q, self.q_nope, self.q_pe, self.proj_ws,
+                         stream=stream)
+            L.mla_kv_a_proj(self.cfg, self.hidden_new, self.W_kv_a, self.c_kv_new, self.k_pe_new,
+                            self.proj_ws, stream=stream)
+            self.write_new(stream=stream)
+            self.absorb(stream=stream)
+        else:
+            cur = torch.cuda.current_stream() if stream is None else stream
+            self.ly_fork.record(cur)
+            side.wait_event(self.ly_fork)
+            with torch.cuda.stream(side):
+                L.mla_kv_a_proj(self.cfg, self.hidden_new, self.W_kv_a, self.c_kv_new, self.k_pe_new,
+                                self.proj_ws_side)
+                self.write_new()
+                self.ly_join.record(side)
+            L.mla_q_proj(self.cfg, self.hidden_new, self.W_q, self.q_nope, self.q_pe, self.proj_ws,
+                         stream=stream)
+            self.absorb(stream=stream)
+            cur.wait_event(self.ly_join)
         self.decode_paged_combine(stream=stream)
         self.out_proj(stream=stream)
         L.mla_o_proj(self.cfg, self.out, self.W_o, self.y, self.proj_ws, stream=stream)

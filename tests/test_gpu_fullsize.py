@@ -203,9 +203,11 @@ def test_serving_layer_bench_step_graphed():
     s.layer_setup(2048)
     s.layer_populate()
     s.y.fill_(float("nan"))
-    _graph_replay(s.layer_step)
+    side = torch.cuda.Stream()
+    _graph_replay(lambda: s.layer_step(side=side))   # as the bench runs it
     assert s.device_status()[0][0] == 0
     assert L.mla_get_device_status(s.proj_ws)[0] == 0
+    assert L.mla_get_device_status(s.proj_ws_side)[0] == 0
     li = s.layer
     for b in (5, 62):
         tr, qr = w.token_range(b), w.q_range(b)
@@ -288,9 +290,11 @@ def test_mixed_layer_bench_step_graphed():
     s.layer_setup(2048)
     s.layer_populate()
     s.y.fill_(float("nan"))
-    _graph_replay(s.layer_step)
+    side = torch.cuda.Stream()
+    _graph_replay(lambda: s.layer_step(side=side))   # as the bench runs it
     assert s.device_status()[0][0] == 0
     assert L.mla_get_device_status(s.proj_ws)[0] == 0
+    assert L.mla_get_device_status(s.proj_ws_side)[0] == 0
     li = s.layer
     ql = np.diff(np.asarray(w.query_start_loc))
     got = to_f64(s.y)

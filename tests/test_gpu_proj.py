@@ -159,3 +159,12 @@ def test_whole_layer_vs_the_naive_oracle(name):
                                     w.W_uv, li.W_o, w.rms_weight, w.rms_eps, w.rope_base,
                                     w.softmax_scale, num_new=qr.stop - qr.start)
     assert_close(y, ref, "bf16", f"layer {name}")
+    # kv_a_proj and the cache write on a side stream beside q_proj and the
+    # absorption: the same kernels on the same inputs, bit for bit
+    first = s.y.clone()
+    s.y.fill_(float("nan"))
+    side = torch.cuda.Stream()
+    s.layer_step(side=side)
+    torch.cuda.synchronize()
+    assert L.mla_get_device_status(s.proj_ws_side)[0] == 0
+    assert torch.equal(s.y, first)
