@@ -59,12 +59,13 @@ PROFILES = {
         ["decode_bf16.cu", "common.cuh", "sched.cuh", "merge.cuh", "async_copy.cuh"]),
     ("decode_tc_kernel", "ragged_h128"): (
         "decode_tc_ragged_B32_H128.md",
-        ["decode_tc.cu", "common.cuh", "cluster.cuh", "tcgen05.cuh", "merge.cuh", "async_copy.cuh"]),
+        ["decode_tc.cu", "common.cuh", "cluster.cuh", "tcgen05.cuh", "merge.cuh", "async_copy.cuh",
+         "pair_math.cuh"]),
     ("expand_tc_kernel", "serving"): (
         "expand_tc_serving_B64_L4096.md", ["naive.cu", "common.cuh", "tcgen05.cuh", "async_copy.cuh"]),
     ("naive_prefill_tc_kernel", "mixed"): (
         "naive_prefill_tc_mixed_P4_D60.md",
-        ["prefill.cu", "common.cuh", "async_copy.cuh", "rope_pairs.cuh", "tcgen05.cuh"]),
+        ["prefill.cu", "common.cuh", "async_copy.cuh", "rope_pairs.cuh", "tcgen05.cuh", "pair_math.cuh"]),
     ("naive_decode_kernel", "serving"): (
         "naive_decode_serving_B64_L4096.md", ["naive.cu", "common.cuh", "tcgen05.cuh", "async_copy.cuh"]),
 }

@@ -53,6 +53,7 @@
 #include "cluster.cuh"
 #include "common.cuh"
 #include "internal.h"
+#include "pair_math.cuh"
 #include "merge.cuh"
 #include "tcgen05.cuh"
 

@@ -39,6 +39,7 @@
 #include "async_copy.cuh"
 #include "common.cuh"
 #include "internal.h"
+#include "pair_math.cuh"
 #include "rope_pairs.cuh"
 #include "tcgen05.cuh"
 
