@@ -63,7 +63,9 @@ PROFILES = {
          "pair_math.cuh"]),
     ("expand_tc_kernel", "serving"): (
         "expand_tc_serving_B64_L4096.md", ["naive.cu", "common.cuh", "tcgen05.cuh", "async_copy.cuh"]),
-    ("naive_prefill_tc_kernel", "mixed"): (
+    # the hybrid form's launch covers only the prefill chunks (the full_kv
+    # form runs the same kernel over every sequence: no summary of that launch)
+    ("naive_prefill_tc_kernel", "mixed:hybrid"): (
         "naive_prefill_tc_mixed_P4_D60.md",
         ["prefill.cu", "common.cuh", "async_copy.cuh", "rope_pairs.cuh", "tcgen05.cuh", "pair_math.cuh"]),
     ("naive_decode_kernel", "serving"): (
@@ -87,7 +89,7 @@ def parse_args(argv=None):
                         "window (fewer when K steps take long, at least 3)")
     p.add_argument("--flushed-steps", type=int, default=50,
                    help="single steps timed with L2 flushed before each")
-    p.add_argument("--code-hash", default=None, metavar="KERNEL:WORKLOAD",
+    p.add_argument("--code-hash", default=None, metavar="KERNEL:WORKLOAD[:FORM]",
                    help="print the code hash a profile summary of KERNEL on WORKLOAD records, "
                         "and exit")
     p.add_argument("--ref-seconds", type=float, default=120.0,
@@ -663,7 +665,7 @@ def run_ours(args, world, rank, local):
         tflops = flops / (kernel_ms * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": round(tflops, 1), "peak": tpeak,
                     "unit": "TFLOP/s", "frac": round(tflops / tpeak, 4),
-                    "traffic": profiled_traffic(kernel, args.workload), "kernel": kernel,
+                    "traffic": profiled_traffic(kernel, f"{args.workload}:{form}"), "kernel": kernel,
                     "kernel_us": round(kernel_ms * 1e3, 2), "algorithmic_flops": flops,
                     "absorbed_attention_flops": attn_flops,
                     "peak_kind": "measured bf16 dense (cuBLAS, burst)"}
@@ -950,7 +952,7 @@ def run_reference(args, world, rank):
 def main(argv=None):
     args = parse_args(argv)
     if args.code_hash:
-        kernel, workload = args.code_hash.split(":")
+        kernel, workload = args.code_hash.split(":", 1)
         print(code_hash(PROFILES[(kernel, workload)][1]))
         return
     world, rank, local = dist_setup()
