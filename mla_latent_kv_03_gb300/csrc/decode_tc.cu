@@ -193,7 +193,9 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
 }
 
 // Four barriers polled together (their latencies overlap); parity 2 means
-// "no wait". The first is waited with cluster-scope acquire.
+// "no wait". All are waited with the default CTA-scope acquire: the peer's
+// partial scores land by bulk copy with complete_tx on this CTA's own
+// barrier, whose phase completion makes the copied bytes visible here.
 __device__ __forceinline__ bool wait4_or_abort(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1,
                                                uint64_t* b2, uint32_t p2, uint64_t* b3, uint32_t p3,
                                                volatile int* abort_flag) {
@@ -201,7 +203,7 @@ __device__ __forceinline__ bool wait4_or_abort(uint64_t* b0, uint32_t p0, uint64
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred q0, q1, q2, q3;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 q0, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 q0, [%1], %2;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 q1, [%3], %4;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 q2, [%5], %6;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 q3, [%7], %8;\n\t"
