@@ -358,6 +358,24 @@ mla_status mla_latent_expand(const mla_config* cfg, const void* cache, int64_t n
                              void* stream);
 
 /*
+ * mla_latent_expand in two parts, for weights that stay fixed across steps:
+ * mla_latent_expand_prepare lays W_uk, W_uv [H, 512, 128] out in the
+ * workspace as the expansion's operand (what every mla_latent_expand and
+ * mla_naive_cache_write call does first); mla_latent_expand_prepared then
+ * expands with those prepared weights and is otherwise mla_latent_expand
+ * (same arguments but the weights, same checks and results, bit for bit).
+ * The prepared weights stay valid until a call with other weights prepares
+ * the same workspace; mla_naive_decode and mla_naive_prefill leave them. A
+ * workspace never prepared gives unspecified rows (no device fault).
+ */
+mla_status mla_latent_expand_prepare(const mla_config* cfg, const void* W_uk, const void* W_uv,
+                                     void* workspace, size_t ws_bytes, void* stream);
+mla_status mla_latent_expand_prepared(const mla_config* cfg, const void* cache, int64_t num_blocks,
+                                      const int32_t* block_table, int32_t max_blocks_per_seq,
+                                      const int32_t* seq_lens, int32_t batch, void* kv_cache,
+                                      void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * mla_naive_decode -- attention over the expanded rows:
  *   q[n,h]   = [q_nope[n,h] || RoPE(q_pe[n,h], q_positions[n])]
  *   out[n,h] = sum_t softmax_t(softmax_scale * q[n,h] . K[t,h]) V[t,h]

@@ -624,14 +624,20 @@ mla_status naive_common_checks(const mla_config* cfg) {
   return MLA_OK;
 }
 
-// Wt, then the expansion of the rows `src_map` views.
-cudaError_t expand(const mla_config& cfg, const void* W_uk, const void* W_uv, uint8_t* ws,
-                   const CUtensorMap& src_map, const ExArgs& ea, unsigned tiles, cudaStream_t st) {
+// Wt (the K-major B operand of the expansion) into the workspace.
+cudaError_t prep_wt(const mla_config& cfg, const void* W_uk, const void* W_uv, uint8_t* ws,
+                    cudaStream_t st) {
+  __nv_bfloat16* Wt = reinterpret_cast<__nv_bfloat16*>(ws + 256);
+  return launch_pdl(wt_prep_kernel, dim3(kDc / 32, 256 / 32, cfg.num_heads), dim3(32, 8), 0, st,
+                    (const __nv_bfloat16*)W_uk, (const __nv_bfloat16*)W_uv, Wt);
+}
+
+// The expansion of the rows `src_map` views with the workspace's Wt.
+cudaError_t expand_rows(const mla_config& cfg, uint8_t* ws, const CUtensorMap& src_map,
+                        const ExArgs& ea, unsigned tiles, cudaStream_t st) {
   const int H = cfg.num_heads;
   __nv_bfloat16* Wt = reinterpret_cast<__nv_bfloat16*>(ws + 256);
-  cudaError_t e = launch_pdl(wt_prep_kernel, dim3(kDc / 32, 256 / 32, H), dim3(32, 8), 0, st,
-                             (const __nv_bfloat16*)W_uk, (const __nv_bfloat16*)W_uv, Wt);
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
   CUtensorMap wt_map;
   if (!encode_map_2d(&wt_map, Wt, kDc, (uint64_t)H * 256, 64, 256)) return cudaErrorInvalidValue;
   e = cudaFuncSetAttribute(expand_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -647,6 +653,62 @@ cudaError_t expand(const mla_config& cfg, const void* W_uk, const void* W_uv, ui
                                                                     : (unsigned)sms;
   return launch_pdl(expand_tc_kernel, dim3(grid), dim3(kExThreads), ExSmem::alloc, st, src_map,
                     wt_map, args);
+}
+
+// Wt, then the expansion.
+cudaError_t expand(const mla_config& cfg, const void* W_uk, const void* W_uv, uint8_t* ws,
+                   const CUtensorMap& src_map, const ExArgs& ea, unsigned tiles, cudaStream_t st) {
+  cudaError_t e = prep_wt(cfg, W_uk, W_uv, ws, st);
+  if (e != cudaSuccess) return e;
+  return expand_rows(cfg, ws, src_map, ea, tiles, st);
+}
+
+// mla_latent_expand with (W_uk, W_uv) or, when both are null, with the
+// weights already prepared in the workspace.
+mla_status latent_expand(const mla_config* cfg, const void* cache, int64_t num_blocks,
+                         const int32_t* block_table, int32_t max_blocks_per_seq,
+                         const int32_t* seq_lens, int32_t batch, const void* W_uk,
+                         const void* W_uv, void* kv_cache, void* workspace, size_t ws_bytes,
+                         void* stream) {
+  const bool prepared = W_uk == nullptr && W_uv == nullptr;
+  mla_status s = naive_common_checks(cfg);
+  if (s != MLA_OK) return s;
+  if (num_blocks < 0 || max_blocks_per_seq < 0 || batch < 0) return MLA_ERR_INVALID_ARGUMENT;
+  if (num_blocks * cfg->block_size > ((int64_t)1 << 31) / cfg->num_heads)
+    return MLA_ERR_UNSUPPORTED;
+  if (!workspace || !is_aligned(workspace, 256)) return MLA_ERR_INVALID_ARGUMENT;
+  if (batch == 0 || max_blocks_per_seq == 0 || num_blocks == 0) return MLA_OK;
+  if (!cache || !block_table || !seq_lens || !kv_cache || (!prepared && (!W_uk || !W_uv)))
+    return MLA_ERR_INVALID_ARGUMENT;
+  if (!is_aligned(cache, 16) || (!prepared && (!is_aligned(W_uk, 16) || !is_aligned(W_uv, 16))) ||
+      !is_aligned(kv_cache, 16) || !is_aligned(block_table, 4) || !is_aligned(seq_lens, 4))
+    return MLA_ERR_INVALID_ARGUMENT;
+  const NaiveWs L = naive_ws(cfg->num_heads, 0, 0, 1);
+  if (ws_bytes < L.write_end) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  const int bs = cfg->block_size;
+  const int64_t max_len = (int64_t)max_blocks_per_seq * bs;
+  const int64_t tiles = (max_len + kExRows - 1) / kExRows;
+  if ((int64_t)batch * tiles * cfg->num_heads > 0x7fffffff) return MLA_ERR_UNSUPPORTED;
+  CUtensorMap src_map;
+  if (!encode_row_map(&src_map, cache, (uint64_t)num_blocks * bs, (uint32_t)bs)) return MLA_ERR_CUDA;
+  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+  ExArgs ea{};
+  ea.block_table = block_table;
+  ea.seq_lens = seq_lens;
+  ea.max_blocks_per_seq = max_blocks_per_seq;
+  ea.tiles_per_seq = (int32_t)tiles;
+  ea.num_blocks = num_blocks;
+  ea.block_size = bs;
+  ea.box_rows = bs;
+  ea.H = cfg->num_heads;
+  ea.mode = 1;
+  ea.src = reinterpret_cast<const __nv_bfloat16*>(cache);
+  ea.kv = reinterpret_cast<__nv_bfloat16*>(kv_cache);
+  ea.num_slots = num_blocks * bs;
+  ea.status = reinterpret_cast<uint32_t*>(ws);
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return cuda_status(prepared ? expand_rows(*cfg, ws, src_map, ea, (unsigned)(batch * tiles), st)
+                              : expand(*cfg, W_uk, W_uv, ws, src_map, ea, (unsigned)(batch * tiles), st));
 }
 
 }  // namespace
@@ -723,44 +785,31 @@ mla_status mla_latent_expand(const mla_config* cfg, const void* cache, int64_t n
                              const int32_t* seq_lens, int32_t batch, const void* W_uk,
                              const void* W_uv, void* kv_cache, void* workspace, size_t ws_bytes,
                              void* stream) {
+  if (!W_uk || !W_uv) return MLA_ERR_INVALID_ARGUMENT;
+  return latent_expand(cfg, cache, num_blocks, block_table, max_blocks_per_seq, seq_lens, batch,
+                       W_uk, W_uv, kv_cache, workspace, ws_bytes, stream);
+}
+
+mla_status mla_latent_expand_prepare(const mla_config* cfg, const void* W_uk, const void* W_uv,
+                                     void* workspace, size_t ws_bytes, void* stream) {
   mla_status s = naive_common_checks(cfg);
   if (s != MLA_OK) return s;
-  if (num_blocks < 0 || max_blocks_per_seq < 0 || batch < 0) return MLA_ERR_INVALID_ARGUMENT;
-  if (num_blocks * cfg->block_size > ((int64_t)1 << 31) / cfg->num_heads)
-    return MLA_ERR_UNSUPPORTED;
-  if (!workspace || !is_aligned(workspace, 256)) return MLA_ERR_INVALID_ARGUMENT;
-  if (batch == 0 || max_blocks_per_seq == 0 || num_blocks == 0) return MLA_OK;
-  if (!cache || !block_table || !seq_lens || !W_uk || !W_uv || !kv_cache)
+  if (!workspace || !is_aligned(workspace, 256) || !W_uk || !W_uv || !is_aligned(W_uk, 16) ||
+      !is_aligned(W_uv, 16))
     return MLA_ERR_INVALID_ARGUMENT;
-  if (!is_aligned(cache, 16) || !is_aligned(W_uk, 16) || !is_aligned(W_uv, 16) ||
-      !is_aligned(kv_cache, 16) || !is_aligned(block_table, 4) || !is_aligned(seq_lens, 4))
-    return MLA_ERR_INVALID_ARGUMENT;
-  const NaiveWs L = naive_ws(cfg->num_heads, 0, 0, 1);
-  if (ws_bytes < L.write_end) return MLA_ERR_WORKSPACE_TOO_SMALL;
-  const int bs = cfg->block_size;
-  const int64_t max_len = (int64_t)max_blocks_per_seq * bs;
-  const int64_t tiles = (max_len + kExRows - 1) / kExRows;
-  if ((int64_t)batch * tiles * cfg->num_heads > 0x7fffffff) return MLA_ERR_UNSUPPORTED;
-  CUtensorMap src_map;
-  if (!encode_row_map(&src_map, cache, (uint64_t)num_blocks * bs, (uint32_t)bs)) return MLA_ERR_CUDA;
-  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
-  ExArgs ea{};
-  ea.block_table = block_table;
-  ea.seq_lens = seq_lens;
-  ea.max_blocks_per_seq = max_blocks_per_seq;
-  ea.tiles_per_seq = (int32_t)tiles;
-  ea.num_blocks = num_blocks;
-  ea.block_size = bs;
-  ea.box_rows = bs;
-  ea.H = cfg->num_heads;
-  ea.mode = 1;
-  ea.src = reinterpret_cast<const __nv_bfloat16*>(cache);
-  ea.kv = reinterpret_cast<__nv_bfloat16*>(kv_cache);
-  ea.num_slots = num_blocks * bs;
-  ea.status = reinterpret_cast<uint32_t*>(ws);
-  return cuda_status(expand(*cfg, W_uk, W_uv, ws, src_map, ea, (unsigned)(batch * tiles),
-                            reinterpret_cast<cudaStream_t>(stream)));
+  if (ws_bytes < naive_ws(cfg->num_heads, 0, 0, 1).write_end) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  return cuda_status(prep_wt(*cfg, W_uk, W_uv, reinterpret_cast<uint8_t*>(workspace),
+                             reinterpret_cast<cudaStream_t>(stream)));
 }
+
+mla_status mla_latent_expand_prepared(const mla_config* cfg, const void* cache, int64_t num_blocks,
+                                      const int32_t* block_table, int32_t max_blocks_per_seq,
+                                      const int32_t* seq_lens, int32_t batch, void* kv_cache,
+                                      void* workspace, size_t ws_bytes, void* stream) {
+  return latent_expand(cfg, cache, num_blocks, block_table, max_blocks_per_seq, seq_lens, batch,
+                       nullptr, nullptr, kv_cache, workspace, ws_bytes, stream);
+}
+
 
 mla_status mla_naive_decode(const mla_config* cfg, const void* q_nope, const void* q_pe,
                             const int32_t* q_positions, const void* kv_cache, int64_t num_blocks,

@@ -34,7 +34,8 @@ EXPORTS = (
     "mla_decode_paged_combine_fp8",
     "mla_proj_workspace_size", "mla_q_proj", "mla_kv_a_proj", "mla_o_proj",
     "mla_naive_workspace_size", "mla_naive_cache_write",
-    "mla_latent_expand", "mla_naive_decode", "mla_naive_prefill",
+    "mla_latent_expand", "mla_latent_expand_prepare", "mla_latent_expand_prepared",
+    "mla_naive_decode", "mla_naive_prefill",
     "mla_combine", "mla_out_proj",
     "mla_get_device_status", "mla_selftest_wait_timeout", "mla_status_string", "mla_version",
 )
@@ -88,6 +89,9 @@ _SIGS = {
     "mla_naive_workspace_size": (_sz, [_cfgp, _i64, _i32, _i64]),
     "mla_naive_cache_write": (_i32, [_cfgp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _i64,
                                      _vp, _sz, _vp]),
+    "mla_latent_expand_prepare": (_i32, [_cfgp, _vp, _vp, _vp, _sz, _vp]),
+    "mla_latent_expand_prepared": (_i32, [_cfgp, _vp, _i64, _vp, _i32, _vp, _i32, _vp, _vp, _sz,
+                                          _vp]),
     "mla_latent_expand": (_i32, [_cfgp, _vp, _i64, _vp, _i32, _vp, _i32, _vp, _vp, _vp, _vp, _sz,
                                  _vp]),
     "mla_naive_decode": (_i32, [_cfgp, _vp, _vp, _vp, _vp, _i64, _vp, _i32, _vp, _vp, _i32, _i64,
@@ -333,6 +337,25 @@ def mla_latent_expand(cfg: MlaConfig, cache, block_table, seq_lens, W_uk, W_uv, 
         _ptr(W_uv, dt, "W_uv"), _ptr(kv_cache, dt, "kv_cache"),
         _ptr(workspace, None, "workspace"), _nbytes(workspace), _stream(stream)),
         "mla_latent_expand")
+
+
+def mla_latent_expand_prepare(cfg: MlaConfig, W_uk, W_uv, workspace, stream=None) -> None:
+    dt = _torch_dtype(cfg)
+    _check(load().mla_latent_expand_prepare(
+        ctypes.byref(cfg), _ptr(W_uk, dt, "W_uk"), _ptr(W_uv, dt, "W_uv"),
+        _ptr(workspace, None, "workspace"), _nbytes(workspace), _stream(stream)),
+        "mla_latent_expand_prepare")
+
+
+def mla_latent_expand_prepared(cfg: MlaConfig, cache, block_table, seq_lens, kv_cache, workspace,
+                               stream=None) -> None:
+    dt = _torch_dtype(cfg)
+    _check(load().mla_latent_expand_prepared(
+        ctypes.byref(cfg), _ptr(cache, dt, "cache"), cache.shape[0],
+        _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+        _ptr(seq_lens, torch.int32, "seq_lens"), seq_lens.shape[0], _ptr(kv_cache, dt, "kv_cache"),
+        _ptr(workspace, None, "workspace"), _nbytes(workspace), _stream(stream)),
+        "mla_latent_expand_prepared")
 
 
 def mla_naive_decode(cfg: MlaConfig, q_nope, q_pe, q_positions, kv_cache, block_table, seq_lens,

@@ -114,6 +114,13 @@ def test_naive_forms_are_bf16_only_and_check_their_workspace(lib):
     assert lib.mla_naive_decode(ctypes.byref(bf16), p, p, p, p, 16, p, 4, p, p, 4, 4, p,
                                 256, p, None) == 3
     assert lib.mla_latent_expand(ctypes.byref(bf16), p, 16, p, 4, p, 4, p, p, p, p, 256, None) == 3
+    # the two-part expansion: the same refusals, nothing launched
+    assert lib.mla_latent_expand_prepare(ctypes.byref(bf16), p, p, p, 256, None) == 3
+    assert lib.mla_latent_expand_prepare(ctypes.byref(f32), p, p, p, 1 << 30, None) == 2
+    assert lib.mla_latent_expand_prepare(ctypes.byref(bf16), None, p, p, 1 << 30, None) == 1
+    assert lib.mla_latent_expand_prepared(ctypes.byref(bf16), p, 16, p, 4, p, 4, p, p, 256, None) == 3
+    assert lib.mla_latent_expand_prepared(ctypes.byref(bf16), None, 16, p, 4, p, 4, p, p, 1 << 30,
+                                          None) == 1
 
 
 def test_rope_pairing_field_defaults_to_rotate_half_and_is_checked(lib):

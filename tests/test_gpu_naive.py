@@ -94,6 +94,17 @@ def test_latent_expand_equals_the_naive_cache_write(name):
     a = v1.view(torch.int16).reshape(-1, w.num_heads, 320)[torch.from_numpy(slots).to(DEV)]
     b = s.kv_naive.view(torch.int16).reshape(-1, w.num_heads, 320)[torch.from_numpy(slots).to(DEV)]
     assert torch.equal(a, b)
+    # the two-part form: weights prepared once (into a fresh workspace), then
+    # expanded twice with them -- the same rows, bit for bit
+    ws2 = torch.zeros_like(s.naive_ws)
+    L.mla_latent_expand_prepare(s.cfg, s.W_uk, s.W_uv, ws2)
+    for _ in range(2):
+        s.kv_naive.view(torch.int16).fill_(0x7FC1)
+        L.mla_latent_expand_prepared(s.cfg, s.cache, s.block_table, s.seq_lens, s.kv_naive, ws2)
+        torch.cuda.synchronize()
+        assert L.mla_get_device_status(ws2)[0] == 0
+        c = s.kv_naive.view(torch.int16).reshape(-1, w.num_heads, 320)[torch.from_numpy(slots).to(DEV)]
+        assert torch.equal(a, c)
 
 
 @pytest.mark.parametrize("name", sorted(CASES))
