@@ -64,7 +64,8 @@ __global__ void iota_kernel(int64_t* __restrict__ out, int64_t n) {
 // chunks of 64 columns.
 //   warp 0   producer: the X chunk (128 rows, TMA boxes of box_rows rows: pages
 //            of the latent cache, or slices of a dense buffer) and the Wt chunk
-//            (256 rows) into a 4-stage ring; a unit's box rows are looked up
+//            (256 rows) into a 4-stage ring, every copy of a chunk issued by one
+//            warp instruction (a lane per box); a unit's box rows are looked up
 //            one unit ahead
 //   warp 1   MMA: 4 tcgen05.mma (M 128, N 256, K 16) per chunk into one of two
 //            256-column TMEM accumulators, alternating by unit
@@ -214,9 +215,6 @@ __global__ void __launch_bounds__(kExThreads, 1) expand_tc_kernel(
     for (; ok && u < a.total_units; u += gridDim.x) {
       const int un = u + gridDim.x;  // look the next unit's boxes up now
       const int ynext = (un < a.total_units && lane < nbox) ? ex_box_row(a, un / H, lane) : 0;
-      int ys[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) ys[i] = __shfl_sync(0xffffffffu, ycur, i);
       const int h = u % H;
 #pragma unroll 1
       for (int kc = 0; kc < 8; ++kc, ++c) {
@@ -226,13 +224,15 @@ __global__ void __launch_bounds__(kExThreads, 1) expand_tc_kernel(
           ok = false;
           break;
         }
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&full[st], kExA + kExB);
-          uint8_t* da = sm + ExSmem::a + st * kExA;
-          for (int i = 0; i < nbox; ++i)
-            tma_load_2d(da + i * a.box_rows * 128, &src_map, 64 * kc, ys[i], &full[st]);
+        // one warp instruction issues every copy of the chunk: lane i < nbox
+        // the i-th box of source rows (its own looked-up row), lane nbox the
+        // weight chunk
+        if (lane == 0) mbar_arrive_expect_tx(&full[st], kExA + kExB);
+        if (lane < nbox)
+          tma_load_2d(sm + ExSmem::a + st * kExA + lane * a.box_rows * 128, &src_map, 64 * kc, ycur,
+                      &full[st]);
+        else if (lane == nbox)
           tma_load_2d(sm + ExSmem::b + st * kExB, &wt_map, 64 * kc, h * 256, &full[st]);
-        }
         last_fill[st] = c;
         __syncwarp();
       }
