@@ -482,7 +482,7 @@ __global__ void __maxnreg__(168)
         // lane (g, q) takes codes 64j + 16q + 0..15 of its two tokens per
         // 64-column slab j: pairs 2t and 2t+1 are its B registers of k-block t
         const uint8_t* k0p = stg + (16 * w + pig) * 128;
-#pragma unroll 2
+#pragma unroll
         for (int j = 0; j < 8; ++j) {
           const uint32_t off = (j >> 1) * kSlabBytes + (((4 * (j & 1) + q) ^ pig) << 4);
           const uint4 c0w = *reinterpret_cast<const uint4*>(k0p + off);
