@@ -236,3 +236,105 @@ def test_noalloc_with_no_rows_is_a_noop(lib):
     cfg = L.make_config(16, 64, "bf16")
     assert lib.mla_decode_paged_noalloc(ctypes.byref(cfg), None, None, 0, None, 0, None, None, 0, 0,
                                         None, None, None) == 0
+
+
+def test_workspace_init_checks_its_arguments(lib):
+    ws = ctypes.c_void_p(1 << 20)   # never dereferenced: every case below is refused first
+    assert lib.mla_workspace_init(None, 4096, None) == 1
+    assert lib.mla_workspace_init(ctypes.c_void_p((1 << 20) + 16), 4096, None) == 1   # not 256-aligned
+    assert lib.mla_workspace_init(ws, 8, None) == 1                                   # smaller than the header
+
+
+def test_plan_checks_its_arguments_on_the_host(lib):
+    cfg = L.make_config(16, 64, "bf16")
+    c = ctypes.byref(cfg)
+    ws, p = ctypes.c_void_p(1 << 20), ctypes.c_void_p(4096)
+    assert lib.mla_decode_plan(None, p, p, 1, 1, 4, ws, 1 << 30, None) == 1
+    assert lib.mla_decode_plan(c, p, p, 1, -1, 4, ws, 1 << 30, None) == 1
+    assert lib.mla_decode_plan(c, p, p, -1, 1, 4, ws, 1 << 30, None) == 1
+    assert lib.mla_decode_plan(c, p, p, 1, 1, -4, ws, 1 << 30, None) == 1
+    assert lib.mla_decode_plan(c, p, p, 1, 48 * 1024 + 1, 4, ws, 1 << 30, None) == 2   # rows beyond one plan
+    assert lib.mla_decode_plan(c, p, p, 1, 1, 4, None, 1 << 30, None) == 1
+    assert lib.mla_decode_plan(c, p, p, 1, 1, 4, ctypes.c_void_p((1 << 20) + 64), 1 << 30, None) == 1
+    assert lib.mla_decode_plan(c, None, p, 1, 1, 4, ws, 1 << 30, None) == 1
+    assert lib.mla_decode_plan(c, p, None, 1, 1, 4, ws, 1 << 30, None) == 1
+    assert lib.mla_decode_plan(c, p, p, 0, 1, 4, ws, 1 << 30, None) == 1               # rows without sequences
+    assert lib.mla_decode_plan(c, ctypes.c_void_p(4098), p, 1, 1, 4, ws, 1 << 30, None) == 1
+    # no rows: nothing to plan, nothing read
+    assert lib.mla_decode_plan(c, None, None, 0, 0, 0, ws, 0, None) == 0
+
+
+@pytest.mark.parametrize("call", ["mla_decode_planned", "mla_decode_combine"])
+def test_planned_decode_checks_its_arguments_on_the_host(lib, call):
+    cfg = L.make_config(16, 64, "bf16")
+    c = ctypes.byref(cfg)
+    ws, p, o = ctypes.c_void_p(1 << 20), ctypes.c_void_p(4096), ctypes.c_void_p(8192)
+    fn = getattr(lib, call)
+    extra = [o] if call == "mla_decode_combine" else []
+
+    def run(cfgp, q, cache, nblk, bt, mbps, batch, nq, w):
+        return fn(cfgp, q, cache, nblk, bt, mbps, batch, nq, w, 1 << 30, *extra, None)
+
+    assert run(None, p, p, 8, p, 4, 1, 1, ws) == 1
+    assert run(c, p, p, -1, p, 4, 1, 1, ws) == 1
+    assert run(c, p, p, 8, p, -4, 1, 1, ws) == 1
+    assert run(c, p, p, 8, p, 4, -1, 1, ws) == 1
+    assert run(c, p, p, 8, p, 4, 1, -1, ws) == 1
+    assert run(c, p, p, 8, p, 4, 1, 48 * 1024 + 1, ws) == 2
+    assert run(c, p, p, (1 << 31) // 64 + 1, p, 4, 1, 1, ws) == 2        # slots beyond 2^31
+    assert run(c, p, p, 8, p, 4, 1, 1, None) == 1
+    assert run(c, None, p, 8, p, 4, 1, 1, ws) == 1
+    assert run(c, p, None, 8, p, 4, 1, 1, ws) == 1
+    assert run(c, p, p, 8, None, 4, 1, 1, ws) == 1
+    assert run(c, ctypes.c_void_p(4104), p, 8, p, 4, 1, 1, ws) == 1      # q_abs not 16-byte aligned
+    assert run(c, p, p, 8, ctypes.c_void_p(4098), 4, 1, 1, ws) == 1      # block table not 4-byte aligned
+    assert run(c, None, None, 0, None, 0, 0, 0, ws) == 0                  # no rows
+    if call == "mla_decode_combine":
+        assert fn(c, p, p, 8, p, 4, 1, 1, ws, 1 << 30, None, None) == 1                  # no o_lat
+        assert fn(c, p, p, 8, p, 4, 1, 1, ws, 1 << 30, ctypes.c_void_p(8200), None) == 1  # o_lat misaligned
+
+
+def test_combine_calls_check_their_arguments_on_the_host(lib):
+    cfg = L.make_config(16, 64, "bf16")
+    c = ctypes.byref(cfg)
+    ws, o, w = ctypes.c_void_p(1 << 20), ctypes.c_void_p(8192), ctypes.c_void_p(16384)
+    assert lib.mla_combine(None, ws, 1 << 30, 1, 1, o, None) == 1
+    assert lib.mla_combine(c, ws, 1 << 30, -1, 1, o, None) == 1
+    assert lib.mla_combine(c, ws, 1 << 30, 1, -1, o, None) == 1
+    assert lib.mla_combine(c, ws, 1 << 30, 1, 48 * 1024 + 1, o, None) == 2
+    assert lib.mla_combine(c, None, 1 << 30, 1, 1, o, None) == 1
+    assert lib.mla_combine(c, ws, 1 << 30, 1, 1, None, None) == 1
+    assert lib.mla_combine(c, ws, 1 << 30, 1, 1, ctypes.c_void_p(8196), None) == 1
+    assert lib.mla_combine(c, None, 0, 0, 0, None, None) == 0
+    assert lib.mla_combine_out_proj(None, ws, 1 << 30, 1, 1, w, o, None) == 1
+    assert lib.mla_combine_out_proj(c, ws, 1 << 30, 1, -1, w, o, None) == 1
+    assert lib.mla_combine_out_proj(c, ws, 1 << 30, 1, 48 * 1024 + 1, w, o, None) == 2
+    assert lib.mla_combine_out_proj(c, None, 1 << 30, 1, 1, w, o, None) == 1
+    assert lib.mla_combine_out_proj(c, ws, 1 << 30, 1, 1, None, o, None) == 1
+    assert lib.mla_combine_out_proj(c, ws, 1 << 30, 1, 1, w, None, None) == 1
+    assert lib.mla_combine_out_proj(c, ws, 1 << 30, 1, 1, ctypes.c_void_p(16392), o, None) == 1
+    assert lib.mla_combine_out_proj(c, None, 0, 0, 0, None, None, None) == 0
+
+
+def test_naive_cache_write_checks_its_arguments_on_the_host(lib):
+    cfg = L.make_config(16, 64, "bf16")
+    c = ctypes.byref(cfg)
+    ws, p, s8 = ctypes.c_void_p(1 << 20), ctypes.c_void_p(4096), ctypes.c_void_p(8192)
+
+    def run(cfgp, ckv, kpe, pos, slots, n, rms, wuk, wuv, kv, nblk, w, wsb):
+        return lib.mla_naive_cache_write(cfgp, ckv, kpe, pos, slots, n, rms, wuk, wuv, kv, nblk, w, wsb, None)
+
+    assert run(None, p, p, p, s8, 4, p, p, p, p, 8, ws, 1 << 30) == 1
+    assert run(c, p, p, p, s8, -1, p, p, p, p, 8, ws, 1 << 30) == 1
+    assert run(c, p, p, p, s8, 4, p, p, p, p, -8, ws, 1 << 30) == 1
+    assert run(c, p, p, p, s8, (1 << 24) + 1, p, p, p, p, 8, ws, 1 << 30) == 1
+    assert run(c, p, p, p, s8, 4, p, p, p, p, 8, None, 1 << 30) == 1
+    assert run(c, None, p, p, s8, 4, p, p, p, p, 8, ws, 1 << 30) == 1
+    assert run(c, p, p, p, s8, 4, p, None, p, p, 8, ws, 1 << 30) == 1
+    assert run(c, p, p, p, s8, 4, p, p, p, None, 8, ws, 1 << 30) == 1
+    assert run(c, p, p, p, ctypes.c_void_p(8196), 4, p, p, p, p, 8, ws, 1 << 30) == 1   # slots not 8-byte aligned
+    assert run(c, p, p, p, s8, 4, p, ctypes.c_void_p(4100), p, p, 8, ws, 1 << 30) == 1  # W_uk misaligned
+    assert run(c, p, p, p, s8, 4, p, p, p, p, 8, ws, 64) == 3                          # workspace too small
+    assert run(c, None, None, None, None, 0, None, None, None, None, 0, ws, 0) == 0      # no tokens
+    f32 = L.make_config(16, 64, "f32")
+    assert run(ctypes.byref(f32), p, p, p, s8, 4, p, p, p, p, 8, ws, 1 << 30) == 2      # bf16 only
