@@ -338,3 +338,36 @@ def test_naive_cache_write_checks_its_arguments_on_the_host(lib):
     assert run(c, None, None, None, None, 0, None, None, None, None, 0, ws, 0) == 0      # no tokens
     f32 = L.make_config(16, 64, "f32")
     assert run(ctypes.byref(f32), p, p, p, s8, 4, p, p, p, p, 8, ws, 1 << 30) == 2      # bf16 only
+
+
+def test_paged_combine_checks_its_arguments_on_the_host(lib):
+    cfg = L.make_config(16, 64, "bf16")
+    c = ctypes.byref(cfg)
+    ws, p, o = ctypes.c_void_p(1 << 20), ctypes.c_void_p(4096), ctypes.c_void_p(8192)
+
+    def run(cfgp, q, cache, nblk, bt, mbps, sl, qsl, batch, nq, w, out):
+        return lib.mla_decode_paged_combine(cfgp, q, cache, nblk, bt, mbps, sl, qsl, batch, nq, w,
+                                            1 << 30, out, None)
+
+    assert run(None, p, p, 8, p, 4, p, p, 1, 1, ws, o) == 1
+    assert run(c, p, p, 8, p, 4, p, p, 1, -1, ws, o) == 1
+    assert run(c, p, p, 8, p, 4, p, p, 1, 48 * 1024 + 1, ws, o) == 2
+    assert run(c, p, p, (1 << 31) // 64 + 1, p, 4, p, p, 1, 1, ws, o) == 2
+    assert run(c, p, p, 8, p, 4, p, p, 1, 1, None, o) == 1
+    assert run(c, p, p, 8, p, 4, None, p, 1, 1, ws, o) == 1          # no seq_lens
+    assert run(c, p, p, 8, p, 4, p, None, 1, 1, ws, o) == 1          # no query_start_loc
+    assert run(c, p, p, 8, p, 4, p, p, 0, 1, ws, o) == 1             # rows without sequences
+    assert run(c, p, p, 8, p, 4, p, p, 1, 1, ws, None) == 1          # no o_lat
+    assert run(c, p, p, 8, p, 4, p, p, 1, 1, ws, ctypes.c_void_p(8200)) == 1
+    assert run(c, p, p, 8, p, 4, ctypes.c_void_p(4098), p, 1, 1, ws, o) == 1
+    assert run(c, None, None, 0, None, 0, None, None, 0, 0, ws, None) == 0
+
+
+def test_device_status_and_self_test_check_their_arguments(lib):
+    word = ctypes.c_uint32(0)
+    assert lib.mla_get_device_status(None, ctypes.byref(word), 0, None) == 1
+    assert lib.mla_get_device_status(ctypes.c_void_p(4098), ctypes.byref(word), 0, None) == 1
+    p = ctypes.c_void_p(4096)
+    assert lib.mla_selftest_wait_timeout(None, 1000, None) == 1
+    assert lib.mla_selftest_wait_timeout(p, 0, None) == 1
+    assert lib.mla_selftest_wait_timeout(p, 10_000_000_001, None) == 1   # limit above 10 s
