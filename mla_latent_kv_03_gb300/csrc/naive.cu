@@ -514,7 +514,7 @@ __global__ void __launch_bounds__(256) naive_decode_kernel(NdArgs a) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] *= alpha;
     m = mn;
-#pragma unroll 8
+#pragma unroll
     for (int j = 0; j < 32; ++j) {
       const float pj = __shfl_sync(0xffffffffu, p, j);
       const int sj = __shfl_sync(0xffffffffu, slot, j);
